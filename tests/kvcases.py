@@ -1,0 +1,34 @@
+"""Test helpers: turn a synthetic workload into oracle inputs (no codec arithmetic)."""
+import numpy as np
+import torch
+
+import oracle as O
+from kv_cache_page_gb300 import synth
+
+CODEC_IDS = {"none": O.NONE, "fp8_cast": O.FP8_CAST, "fp8_fixed": O.FP8_FIXED,
+             "fp8_dynamic": O.FP8_DYNAMIC, "tq3": O.TQ3, "tq4": O.TQ4, "uni3": O.UNI3,
+             "uni4": O.UNI4, "uni8": O.UNI8}
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    """Raw 16-bit patterns of a tensor as a contiguous uint16 numpy array."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16).reshape(-1).copy()
+
+
+def oracle_geom(case: synth.Case, arm: synth.Arm, reject_abs=448.0):
+    return O.make_geom(
+        dtype=O.FP16 if case.dtype == torch.float16 else O.BF16,
+        layout=O.SEPARATE if case.layout == "separate" else O.PACKED,
+        head_dim=case.head_dim, num_heads=case.num_heads, block_tokens=case.block_tokens,
+        num_layers=case.num_layers, num_blocks=case.num_blocks, strides=case.strides,
+        codecs=(CODEC_IDS[arm.k_codec], CODEC_IDS[arm.v_codec]), protect=arm.protect,
+        seed=case.seed, reject_abs=reject_abs,
+        fixed_amax=None if case.fixed_amax is None else case.fixed_amax.numpy())
+
+
+def oracle_descs(rows):
+    d = np.zeros(len(rows), dtype=O.DESC_DTYPE)
+    if rows:
+        a = np.array(rows, dtype=np.uint64)
+        d["layer"], d["block"], d["role"], d["enc_offset"] = a[:, 0], a[:, 1], a[:, 2], a[:, 3]
+    return d
