@@ -332,13 +332,16 @@ void kvo_tq_decode_vec(const uint8_t* codes, uint16_t norm16, int D, int bits,
 /* ======================================================================== */
 void kvo_uniform_encode_vec(const float* x, int D, int bits, uint8_t* codes,
                             uint16_t* m16, uint16_t* s16) {
-  /* minimum and maximum with -0 ordered below +0 (IEEE 754-2019 minimum /
-   * maximum), so the stored FP16 minimum of an all-zero vector is defined */
+  /* READING: the sign of a zero minimum or maximum carries no information for
+   * the step or the offset; a zero extreme is taken as +0 (x + 0 in FP32), so
+   * the stored FP16 minimum of a vector whose minimum is a zero is 0x0000 */
   float mn = x[0], mx = x[0];
   for (int i = 1; i < D; ++i) {
-    if (x[i] < mn || (x[i] == mn && signbit(x[i]) && !signbit(mn))) mn = x[i];
-    if (x[i] > mx || (x[i] == mx && !signbit(x[i]) && signbit(mx))) mx = x[i];
+    if (x[i] < mn) mn = x[i];
+    if (x[i] > mx) mx = x[i];
   }
+  mn = mn + 0.0f;
+  mx = mx + 0.0f;
   float levels = (float)((1 << bits) - 1);
   *m16 = kvo_f32_to_f16(mn);
   *s16 = kvo_f32_to_f16((mx - mn) / levels);

@@ -155,11 +155,17 @@ def test_uniform_constant_and_zero_vectors():
     assert np.all(codes == 0) and np.all(s16 == 0)
     dec = O.uniform_decode(codes, m16, s16)
     assert np.array_equal(dec, x)
-    # mixed signed zeros: the minimum is -0 (IEEE minimum), the maximum +0
-    z = np.zeros((1, 32), np.float32)
+    # zero extremes are stored as +0 whatever the signs of the zeros
+    z = np.zeros((2, 32), np.float32)
     z[0, 5] = -0.0
+    z[1, :] = -0.0
     _, mz, sz = O.uniform_encode(z, 8)
-    assert mz[0] == 0x8000 and sz[0] == 0
+    assert np.all(mz == 0x0000) and np.all(sz == 0)
+    w = np.full((1, 32), -0.0, np.float32)
+    w[0, 3] = -1.0                       # maximum is a (negative) zero
+    c, mw, sw = O.uniform_encode(w, 4)
+    assert mw[0] == O.f32_to_f16(np.array([-1.0], np.float32))[0]
+    assert sw[0] == O.f32_to_f16(np.array([1.0 / 15], np.float32))[0]
 
 
 # ---------------------------------------------------------------- packing
