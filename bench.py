@@ -1,0 +1,517 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 KV-page codec: encode + decode GB/s of raw KV and the
+HBM roofline fraction of the dominant kernel.
+
+One step = every codec arm of the workload, encode then decode, over the whole
+synthetic KV cache (resident in HBM; 4.8 GB of source pages, far larger than
+the 129 MB L2, so no flush is needed between steps).  Default workload:
+Qwen3-8B-shaped KV (36 layers, 8 KV heads, D=128, FP16, 4 x 8192 tokens in
+16-token pages) with the FP8 K16/V8 arm (V only) and the FP8 K8/V8 arm, both
+with dynamic per-token/head scales.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+N > 1 runs one process per GPU (torchrun): every rank codes its own copy of the
+workload (weak scaling, no data-path collective; a gloo barrier and a max of
+the timings are the only cross-rank operations).  `--impl reference` times the
+plain CPU oracle on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from kv_cache_page_gb300 import codec as K  # noqa: E402
+from kv_cache_page_gb300 import synth  # noqa: E402
+
+METRIC = "codec encode/decode GB/s of raw KV (1×GB300) and % of HBM roofline"
+UNIT = "GB/s"
+GB = 1e9
+DESC_BYTES = 24
+
+
+# ----------------------------------------------------------------------------- setup
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        return dist
+    return None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class Arm:
+    """One codec arm bound to device buffers: codec handle, descriptors,
+    encoded buffer, statuses and restore destinations."""
+
+    def __init__(self, case: synth.Case, arm: synth.Arm, dev_layers, device):
+        self.case, self.arm = case, arm
+        self.codec = K.Codec(dtype="fp16" if case.dtype == torch.float16 else "bf16",
+                             layout=case.layout, head_dim=case.head_dim,
+                             num_kv_heads=case.num_heads, block_tokens=case.block_tokens,
+                             num_layers=case.num_layers, num_blocks=case.num_blocks,
+                             strides=case.strides, k_codec=arm.k_codec, v_codec=arm.v_codec,
+                             protect=arm.protect, rotation_seed=case.seed,
+                             fixed_amax=None if case.fixed_amax is None else case.fixed_amax.numpy())
+        self.seg = [self.codec.segment_bytes(r)[0] for r in (0, 1)]
+        raw_seg = self.codec.segment_bytes(0)[1]
+        rows, self.total = synth.segment_list(case, arm, self.seg)
+        self.rows = rows
+        self.n = len(rows)
+        self.descs = K.descriptors(rows, device)
+        self.src = dev_layers
+        self.enc = torch.empty(self.total, dtype=torch.uint8, device=device)
+        self.status = torch.empty(self.n, dtype=torch.uint8, device=device)
+        self.dst = [None if t is None else torch.empty_like(t) for t in dev_layers]
+        # which layer tensors this arm touches (separate layout: K/V by role)
+        if case.layout == "separate":
+            used = {2 * l + r for l in range(case.num_layers) for r in arm.roles}
+        else:
+            used = set(range(case.num_layers))
+        self.used = sorted(used)
+        self.src_view = [t if i in used else None for i, t in enumerate(dev_layers)]
+        self.dst_view = [t if i in used else None for i, t in enumerate(self.dst)]
+        prot = [l for l in range(case.num_layers)
+                if l < arm.protect[0] or l >= case.num_layers - arm.protect[1]]
+        self.n_coded = sum(1 for r in rows if r[0] not in prot)  # segments actually transformed
+        self.raw_seg = raw_seg
+        self.raw_bytes = self.n_coded * raw_seg
+        nv = case.num_heads * case.block_tokens
+        self.alg_bytes_enc = sum(raw_seg + self.seg[r[2]] for r in rows if r[0] not in prot) + \
+            self.n * (DESC_BYTES + 1)
+        self.alg_bytes_dec = self.alg_bytes_enc
+        self.vectors = self.n_coded * nv
+        codecs = sorted({c for c, r in ((arm.k_codec, 0), (arm.v_codec, 1)) if r in arm.roles and c != "none"})
+        self.kname = "+".join(codecs)
+
+    def encode(self, stream=None):
+        self.codec.encode(self.src_view, self.descs, self.n, self.enc, self.total, self.status, stream)
+
+    def decode(self, stream=None):
+        self.codec.decode(self.dst_view, self.descs, self.n, self.enc, self.total, self.status, None,
+                          stream)
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.lines = []
+        target = None
+        try:
+            u = torch.cuda.get_device_properties(device_index).uuid
+            target = "GPU-" + str(u)
+        except Exception:
+            target = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if target:
+            cmd += ["-i", target]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- traffic record
+def recorded_traffic(kname, units):
+    """DRAM bytes per launch from the committed ncu summary, scaled by units,
+    when the kernel sources are unchanged since the capture; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        rec = json.load(open(p))
+        import hashlib
+        h = hashlib.sha256()
+        for f in sorted(rec["sources"]):
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        if h.hexdigest() != rec["sources_sha256"]:
+            return None
+        k = rec["kernels"].get(kname)
+        if not k:
+            return None
+        return k["dram_bytes_per_unit"] * units
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args, dist, world, rank, local):
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    case = synth.make_case(args.workload, device=device, seed=args.seed)
+    arms = [Arm(case, a, case.layers, device) for a in case.arms]
+    stream = torch.cuda.current_stream(device)
+
+    def step(events=None):
+        for a in arms:
+            for fn, tag in ((a.encode, "encode"), (a.decode, "decode")):
+                if events is not None:
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+                    events.append((f"{a.kname}_{tag}", a, tag, e0, e1))
+                else:
+                    fn()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    statuses = [a.status.cpu() for a in arms]
+    n_encoded = sum(int((s == K.SEG_ENCODED).sum()) for s in statuses)
+
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    events = []
+    barrier(dist)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(events)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    ms_total = max_over_ranks(dist, ms_total)
+    raw_per_step = sum(2 * a.raw_bytes for a in arms)       # encode + decode
+    value = sum_over_ranks(dist, raw_per_step * args.steps) / (ms_total / 1e3) / GB
+
+    # per-kernel live durations (CUDA events on the launching stream)
+    per = {}
+    for name, a, tag, e0, e1 in events:
+        d = per.setdefault(name, {"ms": [], "arm": a, "tag": tag})
+        d["ms"].append(e0.elapsed_time(e1))
+    kernels = {}
+    for name, d in per.items():
+        a = d["arm"]
+        avg = sum(d["ms"]) / len(d["ms"])
+        alg = a.alg_bytes_enc if d["tag"] == "encode" else a.alg_bytes_dec
+        kernels[name] = {"launches": len(d["ms"]), "avg_ms": avg, "total_ms": sum(d["ms"]),
+                         "alg_bytes": alg, "achieved_gbs": alg / (avg / 1e3) / GB,
+                         "raw_gbs": a.raw_bytes / (avg / 1e3) / GB, "vectors": a.vectors}
+    dom = max(kernels, key=lambda k: kernels[k]["total_ms"])
+    peak, peak_kind = load_peaks()
+    dk = kernels[dom]
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(dk["achieved_gbs"], 1),
+                "peak": peak, "unit": "GB/s", "frac": round(dk["achieved_gbs"] / peak, 4),
+                "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                "traffic": recorded_traffic(dom, dk["vectors"])}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, arms, stream, dist)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; see kv_cache_page_gb300/synth.py)",
+        "config": {"workload": args.workload, "arms": [a.arm.name for a in arms],
+                   "source_dtype": "fp16" if case.dtype == torch.float16 else "bf16",
+                   "layers": case.num_layers, "pages_per_layer": case.num_blocks,
+                   "kv_heads": case.num_heads, "head_dim": case.head_dim,
+                   "raw_kv_bytes_per_step": raw_per_step, "segments_encoded": n_encoded,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                    for k, v in kernels.items()},
+        "gpu_launches": len(events),
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if args.extra and world == 1:
+        result["other_workloads"] = run_extra(args, device)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args, case_name=args.workload, seconds=args.cpu_seconds)
+    for a in arms:
+        a.codec.close()
+    return result
+
+
+def run_e2e(args, arms, stream, dist):
+    """Same step through the C ABI with host buffers: raw pages H2D from pinned
+    memory, encode, encoded bytes + statuses D2H (offload); encoded bytes +
+    statuses H2D, decode, restored pages D2H (restore)."""
+    host = []
+    for a in arms:
+        src_h = [t.cpu().pin_memory() if i in a.used else None for i, t in enumerate(a.src)]
+        dst_h = [torch.empty_like(t, device="cpu").pin_memory() if i in a.used else None
+                 for i, t in enumerate(a.src)]
+        enc_h = torch.empty(a.total, dtype=torch.uint8).pin_memory()
+        st_h = torch.empty(a.n, dtype=torch.uint8).pin_memory()
+        host.append((src_h, dst_h, enc_h, st_h))
+    h2d = d2h = 0
+    for a, (src_h, dst_h, enc_h, st_h) in zip(arms, host):
+        for i in a.used:
+            h2d += src_h[i].numel() * 2
+            d2h += dst_h[i].numel() * 2
+        h2d += a.total + a.n
+        d2h += a.total + a.n
+
+    def step():
+        for a, (src_h, dst_h, enc_h, st_h) in zip(arms, host):
+            for i in a.used:
+                a.src[i].copy_(src_h[i], non_blocking=True)
+            a.encode()
+            enc_h.copy_(a.enc, non_blocking=True)
+            st_h.copy_(a.status, non_blocking=True)
+            a.enc.copy_(enc_h, non_blocking=True)
+            a.status.copy_(st_h, non_blocking=True)
+            a.decode()
+            for i in a.used:
+                dst_h[i].copy_(a.dst[i], non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        step()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, args.e2e_steps))
+    barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    sec = max_over_ranks(dist, time.perf_counter() - t0)
+    raw = sum(2 * a.raw_bytes for a in arms)
+    value = sum_over_ranks(dist, raw * steps) / sec / GB
+    return {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def run_extra(args, device):
+    """Per-arm encode / decode raw-KV GB/s on the other workloads (context lines;
+    the headline is the default workload)."""
+    out = {}
+    specs = [("tiny", {}), ("vllm_packed", {}), ("head_dim_sweep", {"head_dim": 32}),
+             ("head_dim_sweep", {"head_dim": 64}), ("head_dim_sweep", {"head_dim": 128}),
+             ("head_dim_sweep", {"head_dim": 256}), ("qwen25_7b_offload", {})]
+    for name, kw in specs:
+        if name == args.workload and not kw:
+            continue
+        case = synth.make_case(name, device=device, **kw)
+        label = name + (f"_d{kw['head_dim']}" if kw else "")
+        for arm in case.arms:
+            a = Arm(case, arm, case.layers, device)
+            for _ in range(3):
+                a.encode()
+                a.decode()
+            torch.cuda.synchronize()
+            res = {}
+            for tag, fn, alg in (("encode", a.encode, a.alg_bytes_enc), ("decode", a.decode, a.alg_bytes_dec)):
+                ts = []
+                for _ in range(max(5, args.steps)):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    fn()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    ts.append(e0.elapsed_time(e1))
+                ms = statistics.median(ts)
+                res[tag] = {"ms": round(ms, 4), "raw_gbs": round(a.raw_bytes / (ms / 1e3) / GB, 1),
+                            "hbm_gbs": round(alg / (ms / 1e3) / GB, 1)}
+            res["fits_in_l2"] = (a.raw_bytes + a.total) < 129e6
+            out[f"{label}:{arm.name}"] = res
+            a.codec.close()
+        del case
+        torch.cuda.empty_cache()
+    return out
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def _oracle_sample(case_name, blocks, layers):
+    """Host copies of a bounded sample of the workload + per-arm oracle inputs."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle as O
+    from kvcases import host_bits, oracle_descs, oracle_geom
+    case = synth.make_case(case_name, num_layers=layers, num_blocks=blocks)
+    bits = [host_bits(t) for t in case.layers]
+    work = []
+    for arm in case.arms:
+        g = oracle_geom(case, arm)
+        seg = [O.segment_enc_bytes(g, r) for r in (0, 1)]
+        rows, total = synth.segment_list(case, arm, seg)
+        work.append((g, rows, total, case.raw_segment_bytes))
+    return O, bits, work, oracle_descs
+
+
+def _oracle_pass(O, bits, work, oracle_descs, threads):
+    """Encode then decode every arm of the sample, segments split over threads
+    (ctypes releases the GIL).  Returns raw bytes processed (both directions)."""
+    done = 0
+
+    def one(g, rows, total):
+        enc, st = O.encode(g, bits, oracle_descs(rows), total)
+        outs = [b.copy() for b in bits]
+        O.decode(g, outs, oracle_descs(rows), enc, st)
+
+    jobs = []
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        for g, rows, total, raw_seg in work:
+            chunk = -(-len(rows) // threads)
+            for k in range(0, len(rows), chunk):
+                part = [(l, b, r, off) for (l, b, r, off) in rows[k:k + chunk]]
+                jobs.append(ex.submit(one, g, part, total))
+            done += 2 * len(rows) * raw_seg
+        for j in jobs:
+            j.result()
+    return done
+
+
+def cpu_baseline(args, case_name, seconds):
+    threads = os.cpu_count() or 1
+    blocks = max(threads * 2, 16)
+    O, bits, work, od = _oracle_sample(case_name, blocks, 1)
+    _oracle_pass(O, bits, work, od, threads)            # warm-up
+    t0 = time.perf_counter()
+    done, passes = 0, 0
+    while True:
+        done += _oracle_pass(O, bits, work, od, threads)
+        passes += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    sec = time.perf_counter() - t0
+    return {"value": round(done / sec / GB, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{case_name}: layer 0, pages 0..{blocks - 1}, every arm, encode+decode, "
+                      f"{passes} passes in {sec:.1f} s"}
+
+
+def run_reference(args):
+    threads = os.cpu_count() or 1
+    blocks = max(threads, 8)
+    O, bits, work, od = _oracle_sample(args.workload, blocks, 1)
+    for _ in range(args.warmup):
+        _oracle_pass(O, bits, work, od, threads)
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(args.steps):
+        done += _oracle_pass(O, bits, work, od, threads)
+    sec = time.perf_counter() - t0
+    value = done / sec / GB
+    sample = f"{args.workload}: layer 0, pages 0..{blocks - 1}, every arm, encode+decode per step"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(sec * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": args.workload, "sample": sample},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="qwen3_8b", choices=list(synth.CASES))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-extra", dest="extra", action="store_false")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    dist = init_dist(world)
+    res = run_gpu(args, dist, world, rank, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,195 @@
+/*
+ * kv_codec.h -- C ABI of the GB300 KV-cache page codec.
+ *
+ * The codec encodes KV-cache pages on the GPU before they are offloaded and
+ * restores them into the engine's native FP16/BF16 layout, as described by
+ * "KV precision and storage encoding" (OrbitKV docs), section "FP8 and
+ * TurboQuant", and "Asymmetric KV: methods and results" (knlp), section
+ * "Precision and scaling reference".
+ *
+ * Unit of work: a SEGMENT = all vectors of one role (K or V) of one page
+ * (block) of one layer, i.e. num_kv_heads * block_tokens vectors of head_dim
+ * elements.  The storage-format page attaches metadata and raw fallback per
+ * segment (section "Ownership, storage and GDS").
+ *
+ * Encoded segment slot (little endian):
+ *     [codes of vector 0 .. n-1][metadata of vector 0 .. n-1][zero padding]
+ * with vectors ordered v = token * num_kv_heads + head, padded to a multiple of
+ * 128 bytes (kv_codec_segment_bytes gives the size).  Codes per vector:
+ *     FP8 (all modes)     head_dim bytes, E4M3FN
+ *     TQ3 / TQ4           head_dim*bits/8 bytes, little-endian bit stream
+ *                         (code i in bits [bits*i, bits*i + bits))
+ *     UNIFORM3/4          head_dim*bits/8 bytes, same bit stream
+ *     UNIFORM8            head_dim bytes
+ * Metadata per vector:
+ *     FP8_DYNAMIC         FP32 scale (4 bytes)
+ *     FP8_CAST/FIXED      none
+ *     TQ3 / TQ4           FP16 norm of the source vector (2 bytes)
+ *     UNIFORM3/4/8        FP16 minimum, FP16 step (4 bytes)
+ * E.g. head_dim 128: TQ4 K 66, UNIFORM4 V 68, TQ3 K 50, UNIFORM3 V 52 bytes per
+ * vector (the storage-format page's payload sizes).
+ *
+ * Threading and streams: a handle is immutable after creation and may be used
+ * from several host threads.  Encode/decode only enqueue work on the caller's
+ * CUDA stream (no synchronisation, no allocation); all buffers belong to the
+ * caller and must stay valid until that work completes.
+ *
+ * All functions return KV_OK (0) or a negative KV_ERR_* code and never abort.
+ */
+#ifndef KV_CODEC_H
+#define KV_CODEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KV_CODEC_ABI_VERSION 1u
+#define KV_CODEC_MAX_LAYERS 512u
+
+/* ---- return codes ------------------------------------------------------ */
+#define KV_OK 0
+#define KV_ERR_INVALID_ARG -1          /* NULL pointer, zero size, bad enum value */
+#define KV_ERR_UNSUPPORTED_HEAD_DIM -2 /* head_dim not in {32, 64, 128, 256} */
+#define KV_ERR_LAYOUT_MISMATCH -3      /* strides overlap or do not fit the layout */
+#define KV_ERR_UNSUPPORTED_CODEC_FOR_ROLE -4 /* TQ3/TQ4 requested for V */
+#define KV_ERR_MISALIGNED -5           /* pointer or stride not 16-byte aligned */
+#define KV_ERR_CUDA -6                 /* a CUDA runtime call failed (launch, device query) */
+#define KV_ERR_ABI -7                  /* abi_version / struct_size mismatch */
+#define KV_ERR_TOO_MANY_LAYERS -8      /* num_layers = 0 or > KV_CODEC_MAX_LAYERS */
+
+/* ---- enums ------------------------------------------------------------- */
+#define KV_DT_FP16 1u
+#define KV_DT_BF16 2u
+
+#define KV_LAYOUT_SEPARATE 1u    /* K and V tensors, each [block, token, head, D] by strides */
+#define KV_LAYOUT_VLLM_PACKED 2u /* one tensor per layer, rows of 2*D: K = [0, D), V = [D, 2D) */
+
+#define KV_CODEC_NONE 0u        /* role is not encoded: its segments get KV_SEG_RAW_POLICY */
+#define KV_CODEC_FP8_CAST 1u    /* E4M3FN of x (scale 1) */
+#define KV_CODEC_FP8_FIXED 2u   /* E4M3FN of x / s, s per (layer, role) from calibration */
+#define KV_CODEC_FP8_DYNAMIC 3u /* E4M3FN of x / s, s per token/head vector, stored FP32 */
+#define KV_CODEC_TQ3 4u         /* TurboQuant K, 3-bit codes (K role only) */
+#define KV_CODEC_TQ4 5u         /* TurboQuant K, 4-bit codes (K role only) */
+#define KV_CODEC_UNIFORM3 6u    /* per-vector uniform, FP16 min and step */
+#define KV_CODEC_UNIFORM4 7u
+#define KV_CODEC_UNIFORM8 8u
+
+/* ---- per-segment status bytes (written by encode, read by decode) ------- */
+#define KV_SEG_ENCODED 1u       /* slot holds the encoding */
+#define KV_SEG_RAW_NONFINITE 2u /* an element is inf or NaN: keep raw */
+#define KV_SEG_RAW_RANGE 3u     /* an element has |x| > reject_abs: keep raw, no clipping */
+#define KV_SEG_RAW_PROTECTED 4u /* layer is in the protected first/last range */
+#define KV_SEG_RAW_POLICY 5u    /* the role's codec is KV_CODEC_NONE */
+#define KV_SEG_RAW_OVERSIZE 6u  /* source segment larger than 16 MiB */
+#define KV_SEG_RAW_NO_SAVING 7u /* aligned encoding saves less than 12.5% */
+#define KV_SEG_BAD_DESC 8u      /* descriptor invalid (see kv_segment_desc); nothing written */
+/* In every RAW_* / BAD_DESC case the segment's slot is not written (BAD_DESC)
+ * or holds unspecified bytes (RAW_*); the caller keeps the raw page. */
+
+/* ---- geometry ----------------------------------------------------------- */
+/* Registered once per engine KV cache ("Python only registers engine tensor
+ * geometry"; "quantization never infers head layout from byte count",
+ * storage-format page, "FP8 and TurboQuant").  Strides are in ELEMENTS, the
+ * element (head_dim) stride is 1, and for the 128-bit vector accesses every
+ * stride must be a multiple of 8 elements (16 bytes). */
+typedef struct kv_codec_geometry {
+  uint32_t abi_version;   /* KV_CODEC_ABI_VERSION */
+  uint32_t struct_size;   /* sizeof(kv_codec_geometry) */
+  uint32_t dtype;         /* KV_DT_FP16 | KV_DT_BF16 */
+  uint32_t layout;        /* KV_LAYOUT_SEPARATE | KV_LAYOUT_VLLM_PACKED */
+  uint32_t head_dim;      /* 32, 64, 128 or 256 */
+  uint32_t num_kv_heads;  /* H >= 1 */
+  uint32_t block_tokens;  /* tokens per page >= 1 (16 in the pages' engines) */
+  uint32_t num_layers;    /* 1 .. KV_CODEC_MAX_LAYERS */
+  uint64_t num_blocks;    /* pages per layer tensor; descriptors with block >= this are rejected */
+  int64_t stride_block;   /* elements between pages */
+  int64_t stride_token;   /* elements between tokens of a page */
+  int64_t stride_head;    /* elements between heads of a token */
+  uint32_t k_codec;       /* KV_CODEC_* for the K role */
+  uint32_t v_codec;       /* KV_CODEC_* for the V role (TQ kinds not allowed) */
+  uint32_t protect_first; /* layers [0, protect_first) stay raw */
+  uint32_t protect_last;  /* layers [num_layers - protect_last, num_layers) stay raw */
+  uint64_t rotation_seed; /* seed of the TurboQuant sign vector */
+  float reject_abs;       /* admission bound, 0 < reject_abs <= 448; 0 selects 448 */
+  uint32_t reserved0;     /* must be 0 */
+  const float* fixed_amax; /* host, [num_layers][2] (K, V) calibration absolute maxima,
+                              required iff a role uses FP8_FIXED; copied at create */
+} kv_codec_geometry;
+
+/* One segment to encode or decode.  Device-resident array, 24 bytes each.
+ * A descriptor is invalid (status KV_SEG_BAD_DESC, nothing read or written) when
+ * layer >= num_layers, block >= num_blocks, role > 1, the layer pointer for it is
+ * NULL, enc_offset is not a multiple of 16, or the slot does not fit in the
+ * encoded buffer (enc_offset + kv_codec_segment_bytes(role) > buffer bytes). */
+typedef struct kv_segment_desc {
+  uint32_t layer;
+  uint32_t block;
+  uint32_t role;          /* 0 = K, 1 = V */
+  uint32_t reserved;      /* ignored */
+  uint64_t enc_offset;    /* byte offset of the segment's slot in the encoded buffer */
+} kv_segment_desc;
+
+typedef struct kv_codec_s* kv_codec_t;
+
+/* Validate a geometry and build the handle: sign vector (SplitMix64 of
+ * rotation_seed), Lloyd-Max codebooks for TQ roles, FP8 fixed scales
+ * s = max(amax, 1e-12) * fl32(1/448) per (layer, role).  Host only: touches no
+ * GPU and allocates no device memory.  On error *out is set to NULL. */
+int kv_codec_create(const kv_codec_geometry* geometry, kv_codec_t* out);
+
+/* Release a handle (host memory only; no GPU work is pending on its behalf
+ * beyond what the caller enqueued, which does not reference the handle). */
+int kv_codec_destroy(kv_codec_t codec);
+
+/* Bytes of one encoded segment slot for `role` (multiple of 128; 0 if the role
+ * has no codec) and of one raw source segment (H * block_tokens * D * 2). */
+int kv_codec_segment_bytes(kv_codec_t codec, uint32_t role, uint64_t* enc_bytes,
+                           uint64_t* raw_bytes);
+
+/* Encode n_segments segments.
+ *   layer_ptrs   HOST array of DEVICE pointers, 16-byte aligned: separate layout
+ *                [K_0, V_0, K_1, V_1, ...] (2 * num_layers entries), packed layout
+ *                one per layer (num_layers entries).  NULL entries are allowed for
+ *                roles that no descriptor references.
+ *   n_layer_ptrs number of entries in layer_ptrs (must match the layout).
+ *   d_descs      DEVICE array of n_segments descriptors.
+ *   d_out        DEVICE encoded buffer of out_bytes bytes, 16-byte aligned.
+ *   d_status     DEVICE array of n_segments status bytes (written for every segment).
+ *   stream       cudaStream_t (NULL = legacy default stream).
+ * Segments are independent; descriptors may repeat a source page but must not
+ * overlap slots.  n_segments = 0 is a no-op. */
+int kv_codec_encode(kv_codec_t codec, const void* const* layer_ptrs, uint32_t n_layer_ptrs,
+                    const kv_segment_desc* d_descs, uint32_t n_segments, void* d_out,
+                    uint64_t out_bytes, uint8_t* d_status, void* stream);
+
+/* Restore every segment whose status is KV_SEG_ENCODED into the engine layout;
+ * all other segments are left untouched (the caller restores them from its raw
+ * copy).  d_result (optional DEVICE array of n_segments bytes) receives
+ * KV_SEG_ENCODED for restored segments, KV_SEG_BAD_DESC for invalid descriptors
+ * (or a role without codec), and the input status otherwise. */
+int kv_codec_decode(kv_codec_t codec, void* const* layer_ptrs, uint32_t n_layer_ptrs,
+                    const kv_segment_desc* d_descs, uint32_t n_segments, const void* d_in,
+                    uint64_t in_bytes, const uint8_t* d_status, uint8_t* d_result,
+                    void* stream);
+
+/* Static description of an error code. */
+const char* kv_codec_strerror(int code);
+
+/* The codebook the handle-independent TurboQuant path uses for (bits, head_dim):
+ * 2^bits centroids ascending and 2^bits - 1 boundaries, FP32, host memory.
+ * Gaussian Lloyd-Max levels scaled by 1/sqrt(head_dim). */
+int kv_codec_codebook(uint32_t bits, uint32_t head_dim, float* centroids, float* boundaries);
+
+/* The sign vector for (seed, head_dim): one byte per element, 1 = negate. */
+int kv_codec_signs(uint64_t seed, uint32_t head_dim, uint8_t* negate);
+
+/* ABI version compiled into the library. */
+uint32_t kv_codec_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KV_CODEC_H */

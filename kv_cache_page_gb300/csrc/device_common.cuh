@@ -1,0 +1,290 @@
+// device_common.cuh -- segment planning, streaming loads and number-format
+// helpers shared by the codec kernels.
+//
+// Thread mapping used by every kernel: a vector of D elements is held by
+// G = D/8 consecutive lanes, lane li holding the 8 contiguous elements
+// [8*li, 8*li + 8) (one 128-bit load of the 16-bit source).  A warp therefore
+// holds 32/G vectors at a time; each lane handles U such vectors per step so
+// that U independent 128-bit loads are in flight per thread.  A CTA owns one
+// segment at a time and walks the segment's vectors in token-major order
+// j = t*H + h, which is also the order of the encoded slot.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kv_internal.h"
+
+namespace kvc {
+
+constexpr int kE = 8;  // elements per lane per vector
+
+// ---------------------------------------------------------------- planning
+enum Action { kProcess = 0, kReport = 1, kSkip = 2 };
+
+struct Seg {
+  int action;
+  uint8_t status;        // kReport: the byte to write
+  uint32_t role;
+  uint32_t layer;
+  const uint16_t* page;  // first element of this role's vectors of the page
+  uint8_t* slot;         // encoded slot
+};
+
+// Decide what this CTA does with segment i.  Uniform across the CTA.
+__device__ __forceinline__ Seg plan_segment(const Params& p, uint32_t i, int dir) {
+  Seg s;
+  const kv_segment_desc* dp = p.descs + i;
+  const uint32_t layer = __ldg(&dp->layer), block = __ldg(&dp->block), role = __ldg(&dp->role);
+  const uint64_t off = __ldg(reinterpret_cast<const unsigned long long*>(&dp->enc_offset));
+  s.role = role;
+  s.layer = layer;
+  s.page = nullptr;
+  s.slot = nullptr;
+  s.status = 0;
+  bool ok = layer < p.L && role <= 1u && (uint64_t)block < p.num_blocks && (off & 15u) == 0;
+  const void* base = nullptr;
+  if (ok) {
+    base = p.layout == KV_LAYOUT_SEPARATE ? p.layer_ptr[2 * layer + role] : p.layer_ptr[layer];
+    const uint64_t need = p.seg_bytes[role];
+    ok = base != nullptr && off <= p.buf_bytes && need <= p.buf_bytes - off;
+  }
+  const uint8_t bad = (uint8_t)KV_SEG_BAD_DESC;
+  if (!ok) {
+    s.action = p.is_first ? kReport : kSkip;
+    s.status = bad;
+    return s;
+  }
+  if (p.codec[role] == KV_CODEC_NONE) {
+    s.action = p.is_first ? kReport : kSkip;
+    s.status = dir == kEncode ? (uint8_t)KV_SEG_RAW_POLICY : bad;
+    return s;
+  }
+  if (p.role_sel != 2u && role != p.role_sel) {
+    s.action = kSkip;
+    return s;
+  }
+  if (dir == kEncode) {
+    if (layer < p.protect_first || layer + p.protect_last >= p.L) {
+      s.action = kReport;
+      s.status = (uint8_t)KV_SEG_RAW_PROTECTED;
+      return s;
+    }
+    if (p.static_status[role]) {
+      s.action = kReport;
+      s.status = p.static_status[role];
+      return s;
+    }
+  } else {
+    const uint8_t st = __ldg(p.status + i);
+    if (st != (uint8_t)KV_SEG_ENCODED) {
+      s.action = kReport;
+      s.status = st;
+      return s;
+    }
+  }
+  int64_t e = (int64_t)block * p.sb;
+  if (p.layout == KV_LAYOUT_VLLM_PACKED) e += (int64_t)role * p.D;
+  s.page = reinterpret_cast<const uint16_t*>(base) + e;
+  s.slot = p.buf + off;
+  s.action = kProcess;
+  return s;
+}
+
+// Element offset of vector j (token-major) inside its page.
+__device__ __forceinline__ int64_t vec_off(const Params& p, uint32_t j) {
+  const uint32_t t = (uint32_t)(((uint64_t)j * p.h_magic) >> 32);
+  const uint32_t h = j - t * p.H;
+  return (int64_t)t * p.st + (int64_t)h * p.sh;
+}
+
+// ---------------------------------------------------------------- memory
+__device__ __forceinline__ uint4 ld_stream16(const void* ptr) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(ptr));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_nc8(const void* ptr) {
+  uint2 v;
+  asm("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(ptr));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_nc4(const void* ptr) {
+  uint32_t v;
+  asm("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(ptr));
+  return v;
+}
+__device__ __forceinline__ uint16_t ld_nc2(const void* ptr) {
+  uint16_t v;
+  asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(ptr));
+  return v;
+}
+__device__ __forceinline__ void st16(void* ptr, uint4 v) { *reinterpret_cast<uint4*>(ptr) = v; }
+__device__ __forceinline__ void st8(void* ptr, uint2 v) { *reinterpret_cast<uint2*>(ptr) = v; }
+__device__ __forceinline__ void st4(void* ptr, uint32_t v) { *reinterpret_cast<uint32_t*>(ptr) = v; }
+
+// Zero the alignment padding [used, seg_bytes) of a slot (whole CTA).
+__device__ __forceinline__ void zero_padding(uint8_t* slot, uint64_t used, uint64_t total) {
+  for (uint64_t k = used + threadIdx.x; k < total; k += blockDim.x) slot[k] = 0;
+}
+
+// ---------------------------------------------------------------- 16-bit formats
+// DT = 0: FP16, DT = 1: BF16.  Two elements per 32-bit word, element 2k in the
+// low half (little endian).
+template <int DT>
+__device__ __forceinline__ uint32_t min_nan2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if (DT == 0) asm("min.NaN.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <int DT>
+__device__ __forceinline__ uint32_t max_nan2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if (DT == 0) asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <int DT>
+__device__ __forceinline__ float lo_f32(uint32_t w) {
+  if (DT == 0) return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+  return __uint_as_float(w << 16);
+}
+template <int DT>
+__device__ __forceinline__ float hi_f32(uint32_t w) {
+  if (DT == 0) return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+  return __uint_as_float(w & 0xffff0000u);
+}
+// Round two floats to the 16-bit format (nearest-even), lo in the low half.
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  uint32_t d;
+  if (DT == 0) asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  else asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+template <int DT>
+__device__ __forceinline__ void unpack8(const uint4& w, float (&x)[8]) {
+  x[0] = lo_f32<DT>(w.x); x[1] = hi_f32<DT>(w.x);
+  x[2] = lo_f32<DT>(w.y); x[3] = hi_f32<DT>(w.y);
+  x[4] = lo_f32<DT>(w.z); x[5] = hi_f32<DT>(w.z);
+  x[6] = lo_f32<DT>(w.w); x[7] = hi_f32<DT>(w.w);
+}
+template <int DT>
+__device__ __forceinline__ uint4 pack8(const float (&y)[8]) {
+  return make_uint4(pack2<DT>(y[0], y[1]), pack2<DT>(y[2], y[3]), pack2<DT>(y[4], y[5]),
+                    pack2<DT>(y[6], y[7]));
+}
+
+// Minimum and maximum of the vector held by G lanes (8 elements each), NaN
+// propagating, returned as floats (exact: min/max of 16-bit values).
+template <int DT, int G>
+__device__ __forceinline__ void vec_minmax(const uint4& w, float& mn, float& mx) {
+  uint32_t a = min_nan2<DT>(min_nan2<DT>(w.x, w.y), min_nan2<DT>(w.z, w.w));
+  uint32_t b = max_nan2<DT>(max_nan2<DT>(w.x, w.y), max_nan2<DT>(w.z, w.w));
+#pragma unroll
+  for (int o = 1; o < G; o <<= 1) {
+    a = min_nan2<DT>(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = max_nan2<DT>(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
+  a = min_nan2<DT>(a, __byte_perm(a, 0, 0x1032));
+  b = max_nan2<DT>(b, __byte_perm(b, 0, 0x1032));
+  mn = lo_f32<DT>(a);
+  mx = lo_f32<DT>(b);
+}
+
+// Admission flags of one vector from its min/max: bit 0 nonfinite, bit 1 range.
+__device__ __forceinline__ uint32_t admission(float mn, float mx, float reject) {
+  const bool nonfinite = !(isfinite(mn) && isfinite(mx));
+  const bool range = (mn < -reject) || (mx > reject);
+  return nonfinite ? 1u : (range ? 2u : 0u);
+}
+
+// ---------------------------------------------------------------- arithmetic
+// Correctly rounded x / s from the correctly rounded reciprocal r = RN(1/s):
+// q0 = RN(x r), residual e = x - q0 s (exact by FMA), q = RN(q0 + e r) (one
+// Newton correction, Markstein 1990), sign copied from x so that -0 / s = -0.
+__device__ __forceinline__ float div_by(float x, float s, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float e = __fmaf_rn(-q0, s, x);
+  return copysignf(__fmaf_rn(e, r, q0), x);
+}
+
+// Pairwise sum over the vector (element order) held by G lanes of 8: an
+// in-thread tree over the 8 elements, then xor-shuffles with ascending lane
+// distance.  Every lane of the group ends with the same bits.
+template <int G>
+__device__ __forceinline__ float pairwise_sum8(const float (&a)[8]) {
+  const float b0 = __fadd_rn(a[0], a[1]), b1 = __fadd_rn(a[2], a[3]);
+  const float b2 = __fadd_rn(a[4], a[5]), b3 = __fadd_rn(a[6], a[7]);
+  float c = __fadd_rn(__fadd_rn(b0, b1), __fadd_rn(b2, b3));
+#pragma unroll
+  for (int o = 1; o < G; o <<= 1) c = __fadd_rn(c, __shfl_xor_sync(0xffffffffu, c, o));
+  return c;
+}
+
+// Walsh-Hadamard butterflies (no scale) over the vector held by G lanes, stride
+// h = 1, 2, 4 inside the thread, then h = 8, 16, ... across lanes (lane
+// distance h/8).  Pair (a_lo, a_hi) -> (a_lo + a_hi, a_lo - a_hi); across
+// lanes each side computes its own output as fma(mine, +-1, partner), which
+// is the single rounding of the same sum or difference.
+template <int G>
+__device__ __forceinline__ void wht_butterflies(float (&a)[8], uint32_t li) {
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i & h) continue;
+      const float u = a[i], v = a[i + h];
+      a[i] = __fadd_rn(u, v);
+      a[i + h] = __fsub_rn(u, v);
+    }
+  }
+#pragma unroll
+  for (int o = 1; o < G; o <<= 1) {
+    const float sgn = (li & (uint32_t)o) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float partner = __shfl_xor_sync(0xffffffffu, a[i], o);
+      a[i] = __fmaf_rn(a[i], sgn, partner);
+    }
+  }
+}
+
+// Lane-local 3-bit codes of 8 elements (24 bits) -> the 12-byte little-endian
+// stream chunk of lanes 4q..4q+3 stored as three words by lanes 4q..4q+2.
+// `dst` points at the vector's code bytes; li is the lane index in the vector.
+__device__ __forceinline__ void store_3bit(uint8_t* dst, uint32_t v24, uint32_t li, bool active) {
+  const uint32_t next = __shfl_down_sync(0xffffffffu, v24, 1);
+  const uint32_t k = li & 3u;
+  if (active && k < 3u) {
+    const uint32_t w = (v24 >> (8u * k)) | (next << (24u - 8u * k));
+    st4(dst + 12u * (li >> 2) + 4u * k, w);
+  }
+}
+
+// Inverse of store_3bit: the 24 bits of lane li from the vector's code bytes.
+__device__ __forceinline__ uint32_t load_3bit(const uint8_t* src, uint32_t li) {
+  const uint32_t bit = 24u * li;
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(src) + (bit >> 5);
+  const uint32_t lo = ld_nc4(w), hi = ld_nc4(w + 1);
+  return __funnelshift_r(lo, hi, bit & 31u) & 0xffffffu;
+}
+
+// Launch a codec kernel (signature void(Params)) on the caller's stream.
+template <typename K>
+inline int launch_codec_kernel(K kernel, const Params& p, void* stream) {
+  unsigned grid = 0;
+  const int rc = grid_for(reinterpret_cast<const void*>(kernel), p.n_segments, &grid);
+  if (rc != KV_OK || grid == 0) return rc;
+  void* args[] = {const_cast<Params*>(&p)};
+  const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(kernel), dim3(grid),
+                                         dim3(kThreads), args, 0, (cudaStream_t)stream);
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+}  // namespace kvc

@@ -1,0 +1,380 @@
+// kv_codec_host.cpp -- the C ABI: geometry validation, codec tables, launches.
+//
+// The handle is a validated copy of the registered geometry plus the tables
+// the kernels need (sign bits, Lloyd-Max codebook, FP8 fixed scales); it lives
+// in host memory and travels to every launch as the kernel parameter block.
+// "KV precision and storage encoding" (OrbitKV), section "FP8 and
+// TurboQuant": the manager validates dtype, head dimension, strides and K/V
+// roles for vLLM's packed [block, head, token, 2 x head_dim] layout and for
+// separate K/V tensors, and never infers the head layout from byte counts.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <utility>
+
+#include "kv_codec.h"
+#include "kv_internal.h"
+
+struct kv_codec_s {
+  kvc::Params p;  // geometry part filled at create; call part per call
+};
+
+namespace {
+
+using kvc::Params;
+
+bool valid_codec(uint32_t c) { return c <= KV_CODEC_UNIFORM8; }
+bool is_fp8(uint32_t c) { return c >= KV_CODEC_FP8_CAST && c <= KV_CODEC_FP8_DYNAMIC; }
+bool is_tq(uint32_t c) { return c == KV_CODEC_TQ3 || c == KV_CODEC_TQ4; }
+uint32_t codec_bits(uint32_t c) {
+  switch (c) {
+    case KV_CODEC_TQ3: case KV_CODEC_UNIFORM3: return 3;
+    case KV_CODEC_TQ4: case KV_CODEC_UNIFORM4: return 4;
+    case KV_CODEC_UNIFORM8: return 8;
+  }
+  return 0;
+}
+bool supported_dim(uint32_t d) { return d == 32 || d == 64 || d == 128 || d == 256; }
+
+// --- SplitMix64 (Steele, Lea & Flood, OOPSLA 2014): golden-gamma increment and
+// the variant-13 finalizer.  Bit i of the sign stream is bit (i mod 64) of the
+// (i div 64)-th output; 1 negates element i.
+uint64_t splitmix_next(uint64_t& state) {
+  state += 0x9E3779B97F4A7C15ull;
+  uint64_t z = state;
+  z ^= z >> 30;
+  z *= 0xBF58476D1CE4E5B9ull;
+  z ^= z >> 27;
+  z *= 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+void sign_words(uint64_t seed, uint32_t D, uint32_t* words /* D/32 */) {
+  uint64_t st = seed;
+  for (uint32_t k = 0; k < D / 64; ++k) {
+    const uint64_t w = splitmix_next(st);
+    words[2 * k] = (uint32_t)w;
+    words[2 * k + 1] = (uint32_t)(w >> 32);
+  }
+  if (D == 32) words[0] = (uint32_t)splitmix_next(st);
+}
+
+// --- Gaussian Lloyd-Max quantizer with K = 2^bits levels, solved on the
+// positive half-line (the density is symmetric and K is even): boundaries
+// t_0 = 0, t_k = (c_k + c_{k+1}) / 2, t_{K/2} = inf; centroid of (a, b) is
+// (pdf(a) - pdf(b)) / (Q(a) - Q(b)) with Q the upper tail.  Iterated in FP64
+// to its fixed point.  Returns the K/2 positive centroids, ascending.
+void lloyd_max_positive(uint32_t bits, double* c) {
+  const uint32_t half = (1u << bits) / 2;
+  const double inv_sqrt2pi = 0.39894228040143267794;
+  auto pdf = [&](double t) { return std::isinf(t) ? 0.0 : inv_sqrt2pi * std::exp(-0.5 * t * t); };
+  auto tail = [](double t) { return std::isinf(t) ? 0.0 : 0.5 * std::erfc(t / 1.41421356237309504880); };
+  for (uint32_t k = 0; k < half; ++k) c[k] = (k + 0.5) * 3.0 / half;
+  double t[130];
+  for (int it = 0; it < 200000; ++it) {
+    t[0] = 0.0;
+    for (uint32_t k = 1; k < half; ++k) t[k] = 0.5 * (c[k - 1] + c[k]);
+    t[half] = INFINITY;
+    double change = 0.0;
+    for (uint32_t k = 0; k < half; ++k) {
+      const double nc = (pdf(t[k]) - pdf(t[k + 1])) / (tail(t[k]) - tail(t[k + 1]));
+      change = std::max(change, std::fabs(nc - c[k]));
+      c[k] = nc;
+    }
+    if (change <= 4e-16) break;
+  }
+}
+
+void make_codebook(uint32_t bits, uint32_t D, float* cent, float* bnd) {
+  const uint32_t K = 1u << bits, half = K / 2;
+  double pos[64];
+  lloyd_max_positive(bits, pos);
+  double full[128];
+  for (uint32_t k = 0; k < half; ++k) {
+    full[half + k] = pos[k];
+    full[half - 1 - k] = -pos[k];
+  }
+  const double rs = std::sqrt((double)D);
+  for (uint32_t j = 0; j < K; ++j) cent[j] = (float)(full[j] / rs);
+  for (uint32_t j = 0; j + 1 < K; ++j) bnd[j] = (float)((0.5 * (full[j] + full[j + 1])) / rs);
+}
+
+// FP8 scale rule: max(amax, 1e-12) * fl32(1/448), in FP32.
+float fp8_scale(float amax) {
+  const float recip = 1.0f / 448.0f;
+  const float a = amax > 1e-12f ? amax : 1e-12f;
+  return a * recip;
+}
+
+// Non-overlap of the page layout: dims sorted by stride must each step over
+// the whole extent of the smaller ones (extent-1 dims do not matter).
+bool strides_fit(uint64_t row, int64_t sb, uint64_t nb, int64_t st, uint64_t nt, int64_t sh,
+                 uint64_t nh) {
+  std::pair<uint64_t, uint64_t> dims[3] = {{(uint64_t)sh, nh}, {(uint64_t)st, nt}, {(uint64_t)sb, nb}};
+  std::sort(dims, dims + 3);
+  uint64_t span = row;  // elements covered by the smaller dims
+  for (auto& d : dims) {
+    if (d.second <= 1) continue;
+    if (d.first < span) return false;
+    // span = stride * (extent - 1) + previous span, watching overflow
+    if (d.second - 1 > (uint64_t(1) << 62) / d.first) return false;
+    span = d.first * (d.second - 1) + span;
+    if (span > (uint64_t(1) << 62)) return false;
+  }
+  return true;
+}
+
+// --- launch bookkeeping: SM count per device, occupancy per (device, kernel)
+std::mutex g_mu;
+std::map<int, int> g_sms;
+std::map<std::pair<int, const void*>, int> g_occ;
+
+int launch_all(kv_codec_s* h, int dir, void* stream) {
+  Params& p = h->p;
+  const uint32_t kc = p.codec[0], vc = p.codec[1];
+  auto run = [&](uint32_t codec) -> int {
+    if (is_fp8(codec)) return kvc::launch_fp8(p, dir, codec, stream);
+    if (is_tq(codec)) return kvc::launch_turboquant(p, dir, codec, stream);
+    return kvc::launch_uniform(p, dir, codec, stream);
+  };
+  if (kc == vc) {
+    p.is_first = 1;
+    if (kc == KV_CODEC_NONE) {  // statuses only
+      p.role_sel = 3;
+      return kvc::launch_fp8(p, dir, KV_CODEC_FP8_CAST, stream);
+    }
+    p.role_sel = 2;
+    return run(kc);
+  }
+  int first = 1;
+  for (uint32_t r = 0; r < 2; ++r) {
+    const uint32_t c = p.codec[r];
+    if (c == KV_CODEC_NONE) continue;
+    p.role_sel = r;
+    p.is_first = (uint32_t)first;
+    first = 0;
+    const int rc = run(c);
+    if (rc != KV_OK) return rc;
+  }
+  return KV_OK;
+}
+
+int check_call(kv_codec_s* h, const void* const* layer_ptrs, uint32_t n_layer_ptrs,
+               const kv_segment_desc* d_descs, const void* buf, const void* status) {
+  const Params& p = h->p;
+  const uint32_t want = p.layout == KV_LAYOUT_SEPARATE ? 2 * p.L : p.L;
+  if (!layer_ptrs || n_layer_ptrs != want || !d_descs || !buf || !status) return KV_ERR_INVALID_ARG;
+  if (((uintptr_t)buf & 15u) || ((uintptr_t)d_descs & 7u)) return KV_ERR_MISALIGNED;
+  for (uint32_t k = 0; k < n_layer_ptrs; ++k)
+    if ((uintptr_t)layer_ptrs[k] & 15u) return KV_ERR_MISALIGNED;
+  return KV_OK;
+}
+
+}  // namespace
+
+namespace kvc {
+int grid_for(const void* kernel, uint32_t n_segments, unsigned* grid) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
+  int sms = 0, occ = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_sms.find(dev);
+    if (it != g_sms.end()) sms = it->second;
+    auto jt = g_occ.find({dev, kernel});
+    if (jt != g_occ.end()) occ = jt->second;
+  }
+  if (sms == 0) {
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KV_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_sms[dev] = sms;
+  }
+  if (occ == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess)
+      return KV_ERR_CUDA;
+    if (occ < 1) occ = 1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_occ[{dev, kernel}] = occ;
+  }
+  const uint64_t g = std::min<uint64_t>((uint64_t)sms * (uint64_t)occ, n_segments);
+  *grid = (unsigned)g;
+  return KV_OK;
+}
+}  // namespace kvc
+
+extern "C" {
+
+uint32_t kv_codec_abi_version(void) { return KV_CODEC_ABI_VERSION; }
+
+const char* kv_codec_strerror(int code) {
+  switch (code) {
+    case KV_OK: return "ok";
+    case KV_ERR_INVALID_ARG: return "invalid argument";
+    case KV_ERR_UNSUPPORTED_HEAD_DIM: return "head_dim must be 32, 64, 128 or 256";
+    case KV_ERR_LAYOUT_MISMATCH: return "strides overlap or do not fit the layout";
+    case KV_ERR_UNSUPPORTED_CODEC_FOR_ROLE: return "TurboQuant codecs are for the K role only";
+    case KV_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
+    case KV_ERR_CUDA: return "CUDA runtime error";
+    case KV_ERR_ABI: return "geometry ABI version or size mismatch";
+    case KV_ERR_TOO_MANY_LAYERS: return "num_layers must be 1..KV_CODEC_MAX_LAYERS";
+  }
+  return "unknown error";
+}
+
+int kv_codec_codebook(uint32_t bits, uint32_t head_dim, float* centroids, float* boundaries) {
+  if (bits < 1 || bits > 4 || !centroids || !boundaries) return KV_ERR_INVALID_ARG;
+  if (!supported_dim(head_dim)) return KV_ERR_UNSUPPORTED_HEAD_DIM;
+  make_codebook(bits, head_dim, centroids, boundaries);
+  return KV_OK;
+}
+
+int kv_codec_signs(uint64_t seed, uint32_t head_dim, uint8_t* negate) {
+  if (!negate) return KV_ERR_INVALID_ARG;
+  if (!supported_dim(head_dim)) return KV_ERR_UNSUPPORTED_HEAD_DIM;
+  uint32_t w[8] = {0};
+  sign_words(seed, head_dim, w);
+  for (uint32_t i = 0; i < head_dim; ++i) negate[i] = (uint8_t)((w[i >> 5] >> (i & 31)) & 1u);
+  return KV_OK;
+}
+
+int kv_codec_create(const kv_codec_geometry* g, kv_codec_t* out) {
+  if (!out) return KV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!g) return KV_ERR_INVALID_ARG;
+  if (g->abi_version != KV_CODEC_ABI_VERSION || g->struct_size != sizeof(kv_codec_geometry))
+    return KV_ERR_ABI;
+  if (g->dtype != KV_DT_FP16 && g->dtype != KV_DT_BF16) return KV_ERR_INVALID_ARG;
+  if (g->layout != KV_LAYOUT_SEPARATE && g->layout != KV_LAYOUT_VLLM_PACKED) return KV_ERR_INVALID_ARG;
+  if (!supported_dim(g->head_dim)) return KV_ERR_UNSUPPORTED_HEAD_DIM;
+  if (g->num_layers == 0 || g->num_layers > KV_CODEC_MAX_LAYERS) return KV_ERR_TOO_MANY_LAYERS;
+  if (g->num_kv_heads == 0 || g->block_tokens == 0 || g->num_blocks == 0 || g->reserved0 != 0)
+    return KV_ERR_INVALID_ARG;
+  const uint64_t nv = (uint64_t)g->num_kv_heads * g->block_tokens;
+  if (nv > (1u << 20) || g->num_kv_heads > 4096) return KV_ERR_INVALID_ARG;
+  if (!valid_codec(g->k_codec) || !valid_codec(g->v_codec)) return KV_ERR_INVALID_ARG;
+  if (is_tq(g->v_codec)) return KV_ERR_UNSUPPORTED_CODEC_FOR_ROLE;
+  float reject = g->reject_abs == 0.0f ? 448.0f : g->reject_abs;
+  if (!(reject > 0.0f && reject <= 448.0f)) return KV_ERR_INVALID_ARG;
+  if (g->stride_block <= 0 || g->stride_token <= 0 || g->stride_head <= 0) return KV_ERR_LAYOUT_MISMATCH;
+  if ((g->stride_block | g->stride_token | g->stride_head) & 7) return KV_ERR_MISALIGNED;
+  const uint64_t row = g->layout == KV_LAYOUT_SEPARATE ? g->head_dim : 2ull * g->head_dim;
+  if (!strides_fit(row, g->stride_block, g->num_blocks, g->stride_token, g->block_tokens,
+                   g->stride_head, g->num_kv_heads))
+    return KV_ERR_LAYOUT_MISMATCH;
+  const bool fixed = g->k_codec == KV_CODEC_FP8_FIXED || g->v_codec == KV_CODEC_FP8_FIXED;
+  if (fixed) {
+    if (!g->fixed_amax) return KV_ERR_INVALID_ARG;
+    for (uint32_t k = 0; k < 2 * g->num_layers; ++k)
+      if (!(std::isfinite(g->fixed_amax[k]) && g->fixed_amax[k] >= 0.0f)) return KV_ERR_INVALID_ARG;
+  }
+
+  kv_codec_s* h = new (std::nothrow) kv_codec_s;
+  if (!h) return KV_ERR_INVALID_ARG;
+  std::memset(h, 0, sizeof(*h));
+  Params& p = h->p;
+  p.dtype = g->dtype;
+  p.layout = g->layout;
+  p.D = g->head_dim;
+  p.H = g->num_kv_heads;
+  p.T = g->block_tokens;
+  p.L = g->num_layers;
+  p.nv = (uint32_t)nv;
+  p.n_layer_ptrs = g->layout == KV_LAYOUT_SEPARATE ? 2 * g->num_layers : g->num_layers;
+  p.num_blocks = g->num_blocks;
+  p.h_magic = ((1ull << 32) + p.H - 1) / p.H;
+  p.sb = g->stride_block;
+  p.st = g->stride_token;
+  p.sh = g->stride_head;
+  p.codec[0] = g->k_codec;
+  p.codec[1] = g->v_codec;
+  p.protect_first = g->protect_first;
+  p.protect_last = g->protect_last;
+  p.reject_abs = reject;
+  p.wht_scale = (float)(1.0 / std::sqrt((double)g->head_dim));
+  const uint64_t raw = nv * g->head_dim * 2;
+  for (int r = 0; r < 2; ++r) {
+    const uint32_t c = p.codec[r];
+    uint32_t cb = 0, mb = 0;
+    if (is_fp8(c)) {
+      cb = p.D;
+      mb = c == KV_CODEC_FP8_DYNAMIC ? 4 : 0;
+    } else if (c != KV_CODEC_NONE) {
+      cb = p.D * codec_bits(c) / 8;
+      mb = is_tq(c) ? 2 : 4;
+    }
+    p.code_bytes[r] = cb;
+    p.meta_bytes[r] = mb;
+    p.seg_bytes[r] = (nv * (cb + mb) + 127) / 128 * 128;
+    uint8_t st = 0;
+    if (c != KV_CODEC_NONE) {
+      if (raw > (16ull << 20)) st = KV_SEG_RAW_OVERSIZE;
+      else if (8 * p.seg_bytes[r] > 7 * raw) st = KV_SEG_RAW_NO_SAVING;
+    }
+    p.static_status[r] = st;
+  }
+  sign_words(g->rotation_seed, p.D, p.sign_words);
+  if (is_tq(g->k_codec)) make_codebook(codec_bits(g->k_codec), p.D, p.cent, p.bnd);
+  if (fixed)
+    for (uint32_t l = 0; l < p.L; ++l)
+      for (int r = 0; r < 2; ++r) p.fixed_scale[l][r] = fp8_scale(g->fixed_amax[2 * l + r]);
+  *out = h;
+  return KV_OK;
+}
+
+int kv_codec_destroy(kv_codec_t h) {
+  if (!h) return KV_ERR_INVALID_ARG;
+  delete h;
+  return KV_OK;
+}
+
+int kv_codec_segment_bytes(kv_codec_t h, uint32_t role, uint64_t* enc_bytes, uint64_t* raw_bytes) {
+  if (!h || role > 1) return KV_ERR_INVALID_ARG;
+  if (enc_bytes) *enc_bytes = h->p.codec[role] == KV_CODEC_NONE ? 0 : h->p.seg_bytes[role];
+  if (raw_bytes) *raw_bytes = (uint64_t)h->p.nv * h->p.D * 2;
+  return KV_OK;
+}
+
+int kv_codec_encode(kv_codec_t h, const void* const* layer_ptrs, uint32_t n_layer_ptrs,
+                    const kv_segment_desc* d_descs, uint32_t n_segments, void* d_out,
+                    uint64_t out_bytes, uint8_t* d_status, void* stream) {
+  if (!h) return KV_ERR_INVALID_ARG;
+  if (n_segments == 0) return KV_OK;
+  const int rc = check_call(h, layer_ptrs, n_layer_ptrs, d_descs, d_out, d_status);
+  if (rc != KV_OK) return rc;
+  kv_codec_s call = *h;  // per-call copy: the handle stays immutable
+  Params& p = call.p;
+  for (uint32_t k = 0; k < n_layer_ptrs; ++k) p.layer_ptr[k] = layer_ptrs[k];
+  p.descs = d_descs;
+  p.n_segments = n_segments;
+  p.buf = static_cast<uint8_t*>(d_out);
+  p.buf_bytes = out_bytes;
+  p.status = d_status;
+  p.result = nullptr;
+  return launch_all(&call, kvc::kEncode, stream);
+}
+
+int kv_codec_decode(kv_codec_t h, void* const* layer_ptrs, uint32_t n_layer_ptrs,
+                    const kv_segment_desc* d_descs, uint32_t n_segments, const void* d_in,
+                    uint64_t in_bytes, const uint8_t* d_status, uint8_t* d_result, void* stream) {
+  if (!h) return KV_ERR_INVALID_ARG;
+  if (n_segments == 0) return KV_OK;
+  const int rc = check_call(h, layer_ptrs, n_layer_ptrs, d_descs, d_in, d_status);
+  if (rc != KV_OK) return rc;
+  kv_codec_s call = *h;
+  Params& p = call.p;
+  for (uint32_t k = 0; k < n_layer_ptrs; ++k) p.layer_ptr[k] = layer_ptrs[k];
+  p.descs = d_descs;
+  p.n_segments = n_segments;
+  p.buf = const_cast<uint8_t*>(static_cast<const uint8_t*>(d_in));
+  p.buf_bytes = in_bytes;
+  p.status = const_cast<uint8_t*>(d_status);
+  p.result = d_result;
+  return launch_all(&call, kvc::kDecode, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// kv_internal.h -- launch parameters shared by the host library and the kernels.
+//
+// Everything a kernel needs travels in one __grid_constant__ parameter block
+// (about 13 KB: per-layer pointers, fixed FP8 scales, the TurboQuant codebook
+// and sign bits), so the codec holds no device memory and a launch needs no
+// host-to-device copy.
+#pragma once
+#include <stdint.h>
+
+#include "kv_codec.h"
+
+namespace kvc {
+
+constexpr int kMaxLayers = (int)KV_CODEC_MAX_LAYERS;
+constexpr int kThreads = 256;           // threads per CTA for every codec kernel
+
+struct Params {
+  // ---- registered geometry ----
+  uint32_t dtype;                       // KV_DT_*
+  uint32_t layout;                      // KV_LAYOUT_*
+  uint32_t D;                           // head_dim
+  uint32_t H;                           // num_kv_heads
+  uint32_t T;                           // block_tokens
+  uint32_t L;                           // num_layers
+  uint32_t nv;                          // vectors per segment = H * T
+  uint32_t n_layer_ptrs;
+  uint64_t num_blocks;
+  uint64_t h_magic;                     // ceil(2^32 / H): t = (j * h_magic) >> 32
+  int64_t sb, st, sh;                   // strides (elements)
+  uint32_t codec[2];                    // KV_CODEC_* per role
+  uint32_t protect_first, protect_last;
+  uint32_t code_bytes[2];               // per vector
+  uint32_t meta_bytes[2];               // per vector
+  uint64_t seg_bytes[2];                // encoded slot (multiple of 128)
+  uint8_t static_status[2];             // 0 = encodable, else KV_SEG_RAW_{POLICY,OVERSIZE,NO_SAVING}
+  uint8_t pad0[2];
+  float reject_abs;                     // admission bound
+  float wht_scale;                      // fl32(1/sqrt(D))
+  uint32_t sign_words[8];               // TurboQuant sign bits, bit i = negate element i
+  float cent[16];                       // TurboQuant centroids (K codec)
+  float bnd[16];                        // TurboQuant boundaries (K codec), bnd[15] unused
+  float fixed_scale[kMaxLayers][2];     // FP8_FIXED scale per (layer, role)
+  const void* layer_ptr[2 * kMaxLayers];
+  // ---- per call ----
+  const kv_segment_desc* descs;
+  uint32_t n_segments;
+  uint32_t role_sel;                    // 0 / 1: that role only; 2: both roles; 3: none
+  uint32_t is_first;                    // this launch reports segments no launch encodes
+  uint32_t pad1;
+  uint8_t* buf;                         // encode: slots written; decode: slots read
+  uint64_t buf_bytes;
+  uint8_t* status;                      // encode: written; decode: read
+  uint8_t* result;                      // decode: optional per-segment result
+};
+
+enum Dir { kEncode = 0, kDecode = 1 };
+
+// Kernel launchers (one per codec family), defined in the .cu files.  `codec`
+// is the KV_CODEC_* kind the launch runs; grid size is chosen from the device.
+int launch_fp8(const Params& p, int dir, uint32_t codec, void* stream);
+int launch_uniform(const Params& p, int dir, uint32_t codec, void* stream);
+int launch_turboquant(const Params& p, int dir, uint32_t codec, void* stream);
+
+// Grid size for a codec kernel over n segments: one CTA per segment up to the
+// number of CTAs the device keeps resident (SM count x occupancy, cached per
+// device and kernel).  Defined in the host library.
+int grid_for(const void* kernel, uint32_t n_segments, unsigned* grid);
+
+}  // namespace kvc

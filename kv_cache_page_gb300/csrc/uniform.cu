@@ -1,0 +1,198 @@
+// uniform.cu -- per-vector uniform quantization with FP16 minimum and step.
+//
+// "KV precision and storage encoding" (OrbitKV), section "FP8 and TurboQuant":
+// V uses per-vector uniform quantization with an FP16 minimum and scale.
+// Per vector: m = fp16(min x), s = fp16((max x - min x) / (2^b - 1)), codes
+// clamp(rint((x - m) / s), 0, 2^b - 1) against the stored (rounded) m and s,
+// code 0 when s == 0; restore code * s + m.  Codes are a little-endian bit
+// stream (b = 3, 4) or one byte each (b = 8); metadata is (m, s) as two FP16.
+#include "device_common.cuh"
+
+namespace kvc {
+namespace {
+
+// round to nearest-even integer and saturate to [0, 255]
+__device__ __forceinline__ uint32_t rint_sat_u8(float q) {
+  uint32_t d;
+  asm("cvt.rni.sat.u8.f32 %0, %1;" : "=r"(d) : "f"(q));
+  return d & 0xffu;
+}
+
+template <int DT, int D, int BITS>
+__global__ void __launch_bounds__(kThreads) uniform_encode_kernel(const __grid_constant__ Params p) {
+  constexpr int G = D / kE, VPW = 32 / G, U = 4, W = kThreads / 32;
+  constexpr int STEP = W * VPW * U;
+  constexpr uint32_t LEVELS = (1u << BITS) - 1u;
+  constexpr int CB = D * BITS / 8;  // code bytes per vector
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  const uint32_t grp = lane / G, li = lane % G;
+  __shared__ uint32_t s_flag[2];
+  if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
+  __syncthreads();
+  const uint32_t nv = p.nv;
+  int it = 0;
+  for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
+    const Seg s = plan_segment(p, i, kEncode);
+    if (s.action != kProcess) {
+      if (s.action == kReport && threadIdx.x == 0) p.status[i] = s.status;
+      continue;
+    }
+    if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
+    uint8_t* codes = s.slot;
+    uint8_t* meta = s.slot + (uint64_t)nv * CB;
+    uint32_t flags = 0;
+    for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
+      uint4 w[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t j = j0 + u * VPW + grp;
+        w[u] = j < nv ? ld_stream16(s.page + vec_off(p, j) + li * kE) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t j = j0 + u * VPW + grp;
+        float mn, mx;
+        vec_minmax<DT, G>(w[u], mn, mx);
+        flags |= admission(mn, mx, p.reject_abs);
+        mn = __fadd_rn(mn, 0.0f);  // a zero minimum / maximum is +0
+        mx = __fadd_rn(mx, 0.0f);
+        const __half m16 = __float2half_rn(mn);
+        const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), (float)LEVELS));
+        const float m = __half2float(m16), sc = __half2float(s16);
+        const float r = __frcp_rn(sc);
+        float x[8];
+        unpack8<DT>(w[u], x);
+        uint32_t c[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t q = rint_sat_u8(div_by(__fsub_rn(x[e], m), sc, r));
+          c[e] = sc == 0.0f ? 0u : (q < LEVELS ? q : LEVELS);
+        }
+        const bool in = j < nv;
+        uint8_t* vc = codes + (uint64_t)j * CB;
+        if (BITS == 8) {
+          const uint2 out = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
+                                       c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+          if (in) st8(vc + li * 8, out);
+        } else if (BITS == 4) {
+          uint32_t v = 0;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v |= c[e] << (4 * e);
+          if (in) st4(vc + li * 4, v);
+        } else {
+          uint32_t v = 0;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v |= c[e] << (3 * e);
+          store_3bit(vc, v, li, in);
+        }
+        if (in && li == 0)
+          st4(meta + (uint64_t)j * 4,
+              (uint32_t)__half_as_ushort(m16) | ((uint32_t)__half_as_ushort(s16) << 16));
+      }
+    }
+    flags = __reduce_or_sync(0xffffffffu, flags);
+    if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
+    zero_padding(s.slot, (uint64_t)nv * (CB + 4), p.seg_bytes[s.role]);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint32_t f = s_flag[it & 1];
+      p.status[i] = (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+    }
+    ++it;
+  }
+}
+
+// exact float of a small unsigned integer: 2^23 + c, minus 2^23
+__device__ __forceinline__ float small_u2f(uint32_t c) {
+  return __fsub_rn(__uint_as_float(0x4b000000u | c), 8388608.0f);
+}
+
+template <int DT, int D, int BITS>
+__global__ void __launch_bounds__(kThreads) uniform_decode_kernel(const __grid_constant__ Params p) {
+  constexpr int G = D / kE, VPW = 32 / G, U = 4, W = kThreads / 32;
+  constexpr int STEP = W * VPW * U;
+  constexpr int CB = D * BITS / 8;
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  const uint32_t grp = lane / G, li = lane % G;
+  const uint32_t nv = p.nv;
+  for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
+    const Seg s = plan_segment(p, i, kDecode);
+    if (s.action != kProcess) {
+      if (s.action == kReport && threadIdx.x == 0 && p.result) p.result[i] = s.status;
+      continue;
+    }
+    const uint8_t* codes = s.slot;
+    const uint8_t* meta = s.slot + (uint64_t)nv * CB;
+    uint16_t* page = const_cast<uint16_t*>(s.page);
+    for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
+      uint2 cw[U];
+      uint32_t mw[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t j = j0 + u * VPW + grp;
+        const bool in = j < nv;
+        const uint8_t* vc = codes + (uint64_t)j * CB;
+        cw[u] = make_uint2(0, 0);
+        if (in) {
+          if (BITS == 8) cw[u] = ld_nc8(vc + li * 8);
+          else if (BITS == 4) cw[u].x = ld_nc4(vc + li * 4);
+          else cw[u].x = load_3bit(vc, li);
+        }
+        mw[u] = in ? ld_nc4(meta + (uint64_t)j * 4) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t j = j0 + u * VPW + grp;
+        const float m = __half2float(__ushort_as_half((unsigned short)(mw[u] & 0xffffu)));
+        const float sc = __half2float(__ushort_as_half((unsigned short)(mw[u] >> 16)));
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          uint32_t c;
+          if (BITS == 8) c = ((e < 4 ? cw[u].x : cw[u].y) >> (8 * (e & 3))) & 0xffu;
+          else c = (cw[u].x >> (BITS * e)) & ((1u << BITS) - 1u);
+          y[e] = __fadd_rn(__fmul_rn(small_u2f(c), sc), m);
+        }
+        if (j < nv) st16(page + vec_off(p, j) + li * kE, pack8<DT>(y));
+      }
+    }
+    if (threadIdx.x == 0 && p.result) p.result[i] = KV_SEG_ENCODED;
+  }
+}
+
+template <int DT, int D>
+int dispatch_bits(const Params& p, int dir, uint32_t codec, void* stream) {
+  const bool enc = dir == kEncode;
+  switch (codec) {
+    case KV_CODEC_UNIFORM3:
+      return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 3>, p, stream)
+                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 3>, p, stream);
+    case KV_CODEC_UNIFORM4:
+      return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 4>, p, stream)
+                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 4>, p, stream);
+    case KV_CODEC_UNIFORM8:
+      return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 8>, p, stream)
+                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 8>, p, stream);
+  }
+  return KV_ERR_INVALID_ARG;
+}
+
+template <int DT>
+int dispatch_dim(const Params& p, int dir, uint32_t codec, void* stream) {
+  switch (p.D) {
+    case 32: return dispatch_bits<DT, 32>(p, dir, codec, stream);
+    case 64: return dispatch_bits<DT, 64>(p, dir, codec, stream);
+    case 128: return dispatch_bits<DT, 128>(p, dir, codec, stream);
+    case 256: return dispatch_bits<DT, 256>(p, dir, codec, stream);
+  }
+  return KV_ERR_UNSUPPORTED_HEAD_DIM;
+}
+
+}  // namespace
+
+int launch_uniform(const Params& p, int dir, uint32_t codec, void* stream) {
+  return p.dtype == KV_DT_FP16 ? dispatch_dim<0>(p, dir, codec, stream)
+                               : dispatch_dim<1>(p, dir, codec, stream);
+}
+
+}  // namespace kvc

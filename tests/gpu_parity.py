@@ -1,0 +1,103 @@
+"""Run a workload through the CUDA codec (via the C ABI) and through the oracle
+on the same bits, and compare.  Used by the GPU tests and the smoke check.
+
+Comparison rules: statuses bit-exact; ENCODED slots byte-exact (codes,
+metadata and zero padding); restored pages within one unit in the last place
+of the 16-bit format (+0 and -0 equal), which the kernels in fact meet
+exactly; restore results byte-exact.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as O
+from kv_cache_page_gb300 import codec as K
+from kv_cache_page_gb300 import synth
+from kvcases import host_bits, oracle_descs, oracle_geom
+
+SENTINEL_ENC = 0xAB
+SENTINEL_PAGE = 0x7BCD  # an ordinary finite value, never produced by chance in bulk
+
+
+def make_codec(case: synth.Case, arm: synth.Arm, reject_abs=448.0) -> K.Codec:
+    return K.Codec(dtype="fp16" if case.dtype == torch.float16 else "bf16", layout=case.layout,
+                   head_dim=case.head_dim, num_kv_heads=case.num_heads,
+                   block_tokens=case.block_tokens, num_layers=case.num_layers,
+                   num_blocks=case.num_blocks, strides=case.strides, k_codec=arm.k_codec,
+                   v_codec=arm.v_codec, protect=arm.protect, rotation_seed=case.seed,
+                   reject_abs=reject_abs,
+                   fixed_amax=None if case.fixed_amax is None else case.fixed_amax.numpy())
+
+
+def ulp_diff_16(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Distance in units of the last place between 16-bit float patterns
+    (sign-magnitude -> monotone integers; +0 and -0 both map to 0)."""
+    def key(x):
+        x = x.astype(np.int64)
+        mag = x & 0x7FFF
+        return np.where(x & 0x8000, -mag, mag)
+    return np.abs(key(a) - key(b))
+
+
+def compare_pages(got: np.ndarray, want: np.ndarray, what: str):
+    if np.array_equal(got, want):
+        return 0
+    d = ulp_diff_16(got, want)
+    bad = np.flatnonzero(d > 1)
+    assert bad.size == 0, (f"{what}: {bad.size} elements differ by > 1 ulp; first at {bad[:5]}: "
+                           f"got {got[bad[:5]]} want {want[bad[:5]]}")
+    return int(np.count_nonzero(d))
+
+
+def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="cuda",
+               reject_abs=448.0, check_decode=True):
+    """Encode + decode `case` with `arm` on the GPU and in the oracle; assert parity.
+    Returns (status array, number of restored elements off by one ulp)."""
+    codec = make_codec(case, arm, reject_abs)
+    g = oracle_geom(case, arm, reject_abs)
+    seg = [codec.segment_bytes(r)[0] for r in (0, 1)]
+    assert seg == [0 if c == "none" else O.segment_enc_bytes(g, r)
+                   for r, c in enumerate((arm.k_codec, arm.v_codec))]
+    if rows is None:
+        rows, total = synth.segment_list(case, arm, seg)
+    elif total is None:
+        total = max([r[3] + seg[r[2]] for r in rows if r[2] <= 1 and r[3] < (1 << 32)] + [16])
+    n = len(rows)
+    dev_layers = [t.to(device) for t in case.layers]
+    host_layers = [host_bits(t) for t in case.layers]
+    descs = K.descriptors(rows, device)
+    out = torch.full((max(total, 16),), SENTINEL_ENC, dtype=torch.uint8, device=device)
+    status = torch.full((max(n, 1),), 0xEE, dtype=torch.uint8, device=device)
+    codec.encode(dev_layers, descs, n, out, total, status)
+    torch.cuda.synchronize()
+    enc_ref, st_ref = O.encode(g, host_layers, oracle_descs(rows), total)
+    st_gpu = status[:n].cpu().numpy()
+    assert np.array_equal(st_gpu, st_ref), f"status mismatch at {np.flatnonzero(st_gpu != st_ref)[:10]}"
+    enc_gpu = out[:total].cpu().numpy()
+    for (layer, blk, role, off), s in zip(rows, st_ref):
+        if s == O.S_ENCODED:
+            a, b = enc_gpu[off:off + seg[role]], enc_ref[off:off + seg[role]]
+            if not np.array_equal(a, b):
+                bad = np.flatnonzero(a != b)
+                raise AssertionError(f"slot (layer {layer}, block {blk}, role {role}) differs at "
+                                     f"{bad.size} bytes, first {bad[:8]}: got {a[bad[:8]]} want {b[bad[:8]]}")
+        elif s == O.S_BAD_DESC:
+            pass
+    ulps = 0
+    if check_decode:
+        # decode the oracle's encoding on the GPU into sentinel-filled pages
+        dst_dev = [torch.full_like(t, 0).view(torch.int16).fill_(SENTINEL_PAGE).view(t.dtype)
+                   for t in dev_layers]
+        dst_host = [np.full_like(h, SENTINEL_PAGE) for h in host_layers]
+        enc_dev = torch.from_numpy(enc_ref).to(device)
+        st_dev = torch.from_numpy(st_ref).to(device)
+        result = torch.full((max(n, 1),), 0xEE, dtype=torch.uint8, device=device)
+        codec.decode(dst_dev, descs, n, enc_dev, total, st_dev, result)
+        torch.cuda.synchronize()
+        res_ref = O.decode(g, dst_host, oracle_descs(rows), enc_ref, st_ref)
+        assert np.array_equal(result[:n].cpu().numpy(), res_ref)
+        for k, (d_dev, d_host) in enumerate(zip(dst_dev, dst_host)):
+            ulps += compare_pages(host_bits(d_dev), d_host, f"layer tensor {k}")
+    codec.close()
+    return st_ref, ulps

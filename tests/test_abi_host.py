@@ -1,0 +1,151 @@
+"""Host-only checks of the C ABI (no GPU): the library loads, exports every
+declared symbol, validates geometries, and its size queries, codebooks and
+sign vectors equal the oracle's (each side computes its own).
+"""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+from kv_cache_page_gb300 import build as kbuild
+from kv_cache_page_gb300 import codec as K
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kv_codec.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    kbuild.build()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(kv_codec_\w+)\s*\(", text, re.M)))
+
+
+def test_exports_every_declared_symbol():
+    names = declared_functions()
+    assert set(names) == set(K.EXPORTS)
+    L = C.CDLL(K.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_abi_version_and_struct_size():
+    assert K.lib().kv_codec_abi_version() == K.ABI_VERSION
+    assert C.sizeof(K.Geometry) == 104
+
+
+def _kw(**over):
+    kw = dict(dtype="fp16", layout="separate", head_dim=128, num_kv_heads=8, block_tokens=16,
+              num_layers=4, num_blocks=16, strides=(16 * 8 * 128, 8 * 128, 128),
+              k_codec="tq4", v_codec="uni4", protect=(0, 0), rotation_seed=3)
+    kw.update(over)
+    return kw
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(head_dim=96), -2),
+    (dict(head_dim=512), -2),
+    (dict(dtype="fp16", geometry_overrides={"dtype": 7}), -1),
+    (dict(geometry_overrides={"layout": 9}), -1),
+    (dict(num_layers=0), -8),
+    (dict(num_layers=513), -8),
+    (dict(v_codec="tq3"), -4),
+    (dict(geometry_overrides={"k_codec": 9}), -1),
+    (dict(strides=(16 * 8 * 128, 8 * 128, 100)), -5),        # head stride not 16-byte aligned
+    (dict(strides=(16 * 8 * 128, 8 * 128, 64)), -3),         # heads overlap (64 < D)
+    (dict(strides=(8 * 128, 8 * 128, 128)), -3),             # pages overlap tokens
+    (dict(strides=(0, 8 * 128, 128)), -3),
+    (dict(layout="packed", strides=(8 * 16 * 256, 256, 16 * 128)), -3),  # packed rows are 2D
+    (dict(reject_abs=500.0), -1),
+    (dict(reject_abs=float("nan")), -1),
+    (dict(k_codec="fp8_fixed", v_codec="fp8_fixed"), -1),    # fixed scales missing
+    (dict(geometry_overrides={"abi_version": 2}), -7),
+    (dict(geometry_overrides={"struct_size": 96}), -7),
+    (dict(geometry_overrides={"reserved0": 1}), -1),
+    (dict(num_kv_heads=0), -1),
+    (dict(num_blocks=0), -1),
+])
+def test_geometry_rejections(over, code):
+    with pytest.raises(K.KvCodecError) as e:
+        K.Codec(**_kw(**over))
+    assert e.value.code == code
+
+
+def test_valid_geometries_and_layout_variants():
+    K.Codec(**_kw()).close()
+    # HND page layout [block, head, token, D] expressed by strides
+    K.Codec(**_kw(strides=(16 * 8 * 128, 128, 16 * 128))).close()
+    # vLLM packed [block, head, token, 2D]
+    K.Codec(**_kw(layout="packed", strides=(8 * 16 * 256, 256, 16 * 256))).close()
+    K.Codec(**_kw(k_codec="fp8_fixed", v_codec="none", fixed_amax=np.ones((4, 2)))).close()
+    K.Codec(**_kw(k_codec="none", v_codec="none")).close()
+    # a single page / single head: extent-1 strides do not matter
+    K.Codec(**_kw(num_blocks=1, num_kv_heads=1, strides=(8, 128, 8))).close()
+
+
+def _oracle_geom(k, v, D, H=8, T=16):
+    return O.make_geom(dtype=O.FP16, layout=O.SEPARATE, head_dim=D, num_heads=H, block_tokens=T,
+                       num_layers=2, num_blocks=2, strides=(T * H * D, H * D, D),
+                       codecs=(K.CODEC[k], K.CODEC[v]), fixed_amax=np.ones((2, 2), np.float32))
+
+
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+@pytest.mark.parametrize("kc,vc", [("fp8_cast", "fp8_fixed"), ("fp8_dynamic", "fp8_dynamic"),
+                                   ("tq3", "uni3"), ("tq4", "uni4"), ("uni8", "uni8"), ("none", "uni4")])
+@pytest.mark.parametrize("H,T", [(8, 16), (3, 5), (1, 1)])
+def test_segment_bytes_match_oracle(D, kc, vc, H, T):
+    c = K.Codec(**_kw(head_dim=D, num_kv_heads=H, block_tokens=T, num_layers=2, num_blocks=2,
+                      strides=(T * H * D, H * D, D), k_codec=kc, v_codec=vc, fixed_amax=np.ones((2, 2))))
+    g = _oracle_geom(kc, vc, D, H, T)
+    for role, name in ((0, kc), (1, vc)):
+        enc, raw = c.segment_bytes(role)
+        assert raw == O.segment_raw_bytes(g)
+        assert enc == (0 if name == "none" else O.segment_enc_bytes(g, role))
+    c.close()
+
+
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+def test_codebook_bitwise_equal_to_oracle(bits, D):
+    cent, bnd = K.codebook(bits, D)
+    ocent, obnd = O.codebook(bits, D)
+    assert np.array_equal(cent.view(np.uint32), ocent.view(np.uint32))
+    assert np.array_equal(bnd.view(np.uint32), obnd.view(np.uint32))
+
+
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+@pytest.mark.parametrize("seed", [0, 1, 12345, 2**64 - 1])
+def test_signs_equal_to_oracle(D, seed):
+    assert np.array_equal(K.signs(seed, D), O.signs(seed, D))
+
+
+def test_call_argument_checks_need_no_gpu():
+    c = K.Codec(**_kw())
+    buf = 16 * 1024
+    # n_segments == 0 is a no-op
+    c.encode([None] * 8, 0, 0, 0, 0, 0, stream=0)
+    with pytest.raises(K.KvCodecError) as e:     # wrong pointer count for the layout
+        c.encode([0x1000] * 7, 0x2000, 1, 0x3000, buf, 0x4000, stream=0)
+    assert e.value.code == -1
+    with pytest.raises(K.KvCodecError) as e:     # misaligned layer pointer
+        c.encode([0x1008] * 8, 0x2000, 1, 0x3000, buf, 0x4000, stream=0)
+    assert e.value.code == -5
+    with pytest.raises(K.KvCodecError) as e:     # misaligned encoded buffer
+        c.decode([0x1000] * 8, 0x2000, 1, 0x3004, buf, 0x4000, stream=0)
+    assert e.value.code == -5
+    with pytest.raises(K.KvCodecError) as e:     # missing status array
+        c.encode([0x1000] * 8, 0x2000, 1, 0x3000, buf, None, stream=0)
+    assert e.value.code == -1
+    c.close()
+
+
+def test_strerror_covers_codes():
+    for code in range(0, -9, -1):
+        assert K.strerror(code) != "unknown error"
+    assert K.strerror(-99) == "unknown error"

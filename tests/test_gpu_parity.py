@@ -1,0 +1,222 @@
+"""GPU parity: the CUDA codec (through the C ABI) against the oracle, element by
+element, on the same seeded inputs.
+
+Rules (from the benchmark spec's tolerances): FP8 codes and scales, TurboQuant and
+uniform codes, metadata, padding and every segment status bit-exact; restored
+pages within 1 ulp of the 16-bit format (+-0 equal).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from gpu_parity import run_parity
+from kv_cache_page_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU hosts, skipped there
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from kv_cache_page_gb300 import build
+    build.build()
+
+
+ALL_CODECS = [("fp8_cast", "fp8_cast"), ("fp8_fixed", "fp8_fixed"), ("fp8_dynamic", "fp8_dynamic"),
+              ("tq3", "uni3"), ("tq4", "uni4"), ("uni8", "uni8"), ("uni3", "uni4"), ("none", "fp8_dynamic"),
+              ("tq4", "none")]
+
+
+def custom_case(*, D, H, T, L, B, dtype, layout, values="normal", seed=0):
+    g = torch.Generator().manual_seed(seed)
+    tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
+
+    def draw(shape):
+        if values == "normal":
+            x = torch.randn(shape, generator=g) * torch.exp(torch.randn(shape[:-1] + (1,), generator=g))
+        elif values == "heavy":
+            z = torch.randn(shape, generator=g)
+            chi = sum(torch.randn(shape, generator=g) ** 2 for _ in range(4))
+            x = z / torch.sqrt(chi / 4)
+        return x.clamp(-440, 440).to(tdt)
+
+    if layout == "separate":
+        layers = []
+        for _ in range(L):
+            layers += [draw((B, T, H, D)), draw((B, T, H, D))]
+        strides = synth._separate_strides(T, H, D)
+    else:
+        layers = [draw((B, H, T, 2 * D)) for _ in range(L)]
+        strides = synth._packed_strides(T, H, D)
+    amax = torch.rand(L, 2, generator=g) * 8 + 0.5
+    return synth.Case("custom", tdt, layout, D, H, T, L, B, strides, layers, [], seed, amax)
+
+
+@pytest.mark.parametrize("name", ["tiny"])
+def test_tiny_full_config(name):
+    case = synth.make_case(name)
+    for arm in case.arms:
+        st, ulps = run_parity(case, arm)
+        assert np.all(st == O.S_ENCODED)
+        assert ulps == 0
+
+
+def test_qwen3_8b_shape_small():
+    case = synth.make_case("qwen3_8b", num_layers=2, num_blocks=24)
+    for arm in case.arms:
+        st, ulps = run_parity(case, arm)
+        assert np.all(st == O.S_ENCODED) and ulps == 0
+
+
+def test_vllm_packed_tq3_with_raw_segments():
+    case = synth.make_case("vllm_packed", num_layers=6, num_blocks=40)
+    st, ulps = run_parity(case, case.arms[0])
+    assert np.count_nonzero(st == O.S_RAW_PROTECTED) == 4 * 40 * 2
+    assert ulps == 0
+
+
+def test_vllm_packed_planted_nonfinite_and_range():
+    case = synth.make_case("vllm_packed", num_layers=5, num_blocks=6)
+    case.arms[0].protect = (0, 0)
+    L0 = case.layers[2]
+    L0[1, 3, 7, 5] = float("inf")            # K of block 1
+    L0[2, 0, 0, 128 + 9] = float("nan")      # V of block 2
+    L0[3, 7, 15, 2] = -600.0                 # K of block 3
+    L0[4, 4, 4, 200] = 448.0                 # on the bound: admitted
+    st, ulps = run_parity(case, case.arms[0])
+    rows = synth.segment_list(case, case.arms[0], [1, 1])[0]
+    want = {(2, 1, 0): O.S_RAW_NONFINITE, (2, 2, 1): O.S_RAW_NONFINITE, (2, 3, 0): O.S_RAW_RANGE}
+    for (l, b, r, _), s in zip(rows, st):
+        if (l, b, r) in want:
+            assert s == want[(l, b, r)]
+    assert ulps == 0
+
+
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+def test_head_dim_sweep(D):
+    case = synth.make_case("head_dim_sweep", head_dim=D, num_blocks=6)
+    for arm in case.arms:
+        st, ulps = run_parity(case, arm)
+        assert np.all(st == O.S_ENCODED) and ulps == 0
+
+
+def test_large_offload_shape_small():
+    case = synth.make_case("qwen25_7b_offload", num_layers=5, num_blocks=12)
+    st, ulps = run_parity(case, case.arms[0])
+    assert ulps == 0
+
+
+@pytest.mark.parametrize("kc,vc", ALL_CODECS)
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("layout", ["separate", "packed"])
+def test_codec_matrix(kc, vc, D, dtype, layout):
+    # ragged segment (H=3, T=5: 15 vectors, not a multiple of any warp tile)
+    case = custom_case(D=D, H=3, T=5, L=2, B=5, dtype=dtype, layout=layout,
+                       values="heavy" if dtype == "bf16" else "normal", seed=D)
+    arm = synth.Arm("m", kc, vc, (0, 1))
+    st, ulps = run_parity(case, arm)
+    assert ulps == 0
+
+
+@pytest.mark.parametrize("kc,vc", [("tq4", "fp8_dynamic"), ("tq3", "uni8")])
+def test_large_segments_many_steps(kc, vc):
+    case = custom_case(D=128, H=32, T=16, L=1, B=3, dtype="fp16", layout="separate")
+    st, ulps = run_parity(case, synth.Arm("big", kc, vc, (0, 1)))
+    assert np.all(st == O.S_ENCODED) and ulps == 0
+
+
+def _exhaustive_layers(dtype):
+    allp = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f = O.src_to_f32(allp, dtype)
+    ok = np.isfinite(f) & (np.abs(f) <= 448)
+    good, bad = allp[ok], allp[~ok]
+    per = 128 * 8 * 16
+    ng = -(-good.size // per)
+    buf = np.zeros((ng + bad.size) * per, np.uint16)
+    buf[: good.size] = good
+    for i, b in enumerate(bad):
+        buf[(ng + i) * per + 37] = b
+    return buf, ng + bad.size
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("codec", ["fp8_cast", "fp8_dynamic", "uni8", "tq4"])
+def test_every_16bit_pattern(dtype, codec):
+    """All 65,536 source patterns: in-range finite values fill admitted pages, each
+    nonfinite / out-of-range pattern sits alone in a page of its own."""
+    odt = O.FP16 if dtype == "fp16" else O.BF16
+    buf, B = _exhaustive_layers(odt)
+    tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
+    t = torch.from_numpy(buf.view(np.int16)).view(tdt).reshape(B, 16, 8, 128)
+    case = synth.Case("exh", tdt, "separate", 128, 8, 16, 1, B, synth._separate_strides(16, 8, 128),
+                      [t, t.clone()], [], 0)
+    vc = "uni4" if codec == "tq4" else codec
+    st, ulps = run_parity(case, synth.Arm("exh", codec, vc, (0,)))
+    f = O.src_to_f32(buf.reshape(B, -1), odt)
+    bad_page = ~np.all(np.isfinite(f) & (np.abs(f) <= 448), axis=1)
+    assert np.array_equal(st != O.S_ENCODED, bad_page)
+    assert ulps == 0
+
+
+def test_special_values():
+    """Zeros of both signs, constant vectors, FP16 subnormals, +-448 exactly."""
+    D, H, T = 64, 2, 16
+    x = torch.zeros(6, T, H, D, dtype=torch.float32)
+    x[1] = -0.0
+    x[2, :, :, ::2] = -0.0
+    x[3] = 1.375
+    x[4] = torch.tensor(2.0**-24) * torch.arange(D)            # subnormal ramp
+    x[5, :, 0, 0], x[5, :, 1, 1] = 448.0, -448.0
+    t = x.half()
+    case = synth.Case("special", torch.float16, "separate", D, H, T, 1, 6,
+                      synth._separate_strides(T, H, D), [t, t.clone()], [], 0, torch.ones(1, 2))
+    for kc, vc in ALL_CODECS[:6]:
+        st, ulps = run_parity(case, synth.Arm("s", kc, vc, (0, 1)))
+        assert np.all(st == O.S_ENCODED) and ulps == 0
+
+
+def test_descriptor_edge_cases():
+    case = custom_case(D=64, H=2, T=16, L=4, B=3, dtype="fp16", layout="separate")
+    arm = synth.Arm("e", "tq4", "uni4", (0, 1), protect=(1, 1))
+    # slots: K (TQ4) 32 x 34 = 1088 -> 1152 bytes, V (uniform-4) 32 x 36 = 1152 bytes
+    rows = [(1, 0, 0, 0), (1, 1, 1, 1152), (0, 0, 0, 2304),     # layer 0 protected
+            (3, 2, 1, 3456),                                      # layer 3 protected
+            (4, 0, 0, 4608),                                      # layer out of range
+            (2, 3, 0, 4608),                                      # block out of range
+            (2, 0, 2, 4608),                                      # bad role
+            (2, 0, 0, 4616),                                      # misaligned slot
+            (2, 0, 0, 1 << 40),                                   # slot past the buffer
+            (2, 2, 1, 4608)]
+    st, _ = run_parity(case, arm, rows=rows, total=5 * 1152)
+    assert list(st) == [O.S_ENCODED, O.S_ENCODED, O.S_RAW_PROTECTED, O.S_RAW_PROTECTED,
+                        O.S_BAD_DESC, O.S_BAD_DESC, O.S_BAD_DESC, O.S_BAD_DESC, O.S_BAD_DESC,
+                        O.S_ENCODED]
+
+
+def test_no_codec_for_either_role_reports_policy():
+    case = custom_case(D=32, H=2, T=4, L=2, B=2, dtype="bf16", layout="packed")
+    st, _ = run_parity(case, synth.Arm("n", "none", "none", (0, 1)))
+    assert np.all(st == O.S_RAW_POLICY)
+
+
+def test_empty_call_is_a_no_op():
+    from kv_cache_page_gb300 import codec as K
+    case = synth.make_case("tiny")
+    from gpu_parity import make_codec
+    c = make_codec(case, case.arms[0])
+    c.encode([t.cuda() for t in case.layers], 0, 0, 0, 0, 0)
+    c.decode([t.cuda() for t in case.layers], 0, 0, 0, 0, 0)
+    torch.cuda.synchronize()
+    c.close()
+
+
+def test_repeat_calls_are_deterministic():
+    case = synth.make_case("tiny")
+    for arm in case.arms:
+        a, _ = run_parity(case, arm)
+        b, _ = run_parity(case, arm)
+        assert np.array_equal(a, b)
