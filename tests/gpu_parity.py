@@ -90,7 +90,8 @@ def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="
         dst_dev = [torch.full_like(t, 0).view(torch.int16).fill_(SENTINEL_PAGE).view(t.dtype)
                    for t in dev_layers]
         dst_host = [np.full_like(h, SENTINEL_PAGE) for h in host_layers]
-        enc_dev = torch.from_numpy(enc_ref).to(device)
+        enc_dev = torch.zeros(max(total, 16), dtype=torch.uint8, device=device)
+        enc_dev[:total] = torch.from_numpy(enc_ref).to(device)
         st_dev = torch.from_numpy(st_ref).to(device)
         result = torch.full((max(n, 1),), 0xEE, dtype=torch.uint8, device=device)
         codec.decode(dst_dev, descs, n, enc_dev, total, st_dev, result)
