@@ -231,7 +231,7 @@ def run_gpu(args, dist, world, rank, local):
                     e0.record(stream)
                     fn()
                     e1.record(stream)
-                    events.append((f"{a.kname}_{tag}", a, tag, e0, e1))
+                    events.append((f"{a.arm.name}:{a.kname}_{tag}", a, tag, e0, e1))
                 else:
                     fn()
 
@@ -279,7 +279,7 @@ def run_gpu(args, dist, world, rank, local):
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(dk["achieved_gbs"], 1),
                 "peak": peak, "unit": "GB/s", "frac": round(dk["achieved_gbs"] / peak, 4),
                 "peak_source": f"{peak_kind} hbm_gbs (copy)",
-                "traffic": recorded_traffic(dom, dk["vectors"])}
+                "traffic": recorded_traffic(dom.split(":", 1)[1], dk["vectors"])}
 
     e2e = None
     if not args.no_e2e:
@@ -488,7 +488,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="qwen3_8b", choices=list(synth.CASES))

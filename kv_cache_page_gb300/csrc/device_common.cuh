@@ -94,6 +94,7 @@ __device__ __forceinline__ Seg plan_segment(const Params& p, uint32_t i, int dir
 
 // Element offset of vector j (token-major) inside its page.
 __device__ __forceinline__ int64_t vec_off(const Params& p, uint32_t j) {
+  if (p.heads_contig) return (int64_t)j * p.sh;
   const uint32_t t = (uint32_t)(((uint64_t)j * p.h_magic) >> 32);
   const uint32_t h = j - t * p.H;
   return (int64_t)t * p.st + (int64_t)h * p.sh;
@@ -103,6 +104,15 @@ __device__ __forceinline__ int64_t vec_off(const Params& p, uint32_t j) {
 __device__ __forceinline__ uint4 ld_stream16(const void* ptr) {
   uint4 v;
   asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(ptr));
+  return v;
+}
+// read-only 16-byte load that allocates in L1 (for lanes reading 64-byte
+// blocks, whose second half-sector is then served from L1)
+__device__ __forceinline__ uint4 ld_nc16(const void* ptr) {
+  uint4 v;
+  asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
       : "l"(ptr));
   return v;
@@ -180,12 +190,17 @@ __device__ __forceinline__ uint4 pack8(const float (&y)[8]) {
                     pack2<DT>(y[6], y[7]));
 }
 
-// Minimum and maximum of the vector held by G lanes (8 elements each), NaN
-// propagating, returned as floats (exact: min/max of 16-bit values).
-template <int DT, int G>
-__device__ __forceinline__ void vec_minmax(const uint4& w, float& mn, float& mx) {
-  uint32_t a = min_nan2<DT>(min_nan2<DT>(w.x, w.y), min_nan2<DT>(w.z, w.w));
-  uint32_t b = max_nan2<DT>(max_nan2<DT>(w.x, w.y), max_nan2<DT>(w.z, w.w));
+// Minimum and maximum of the vector held by G lanes (NC 8-element chunks
+// each), NaN propagating, returned as floats (exact: min/max of 16-bit values).
+template <int DT, int G, int NC>
+__device__ __forceinline__ void vec_minmax(const uint4 (&w)[NC], float& mn, float& mx) {
+  uint32_t a = min_nan2<DT>(min_nan2<DT>(w[0].x, w[0].y), min_nan2<DT>(w[0].z, w[0].w));
+  uint32_t b = max_nan2<DT>(max_nan2<DT>(w[0].x, w[0].y), max_nan2<DT>(w[0].z, w[0].w));
+#pragma unroll
+  for (int c = 1; c < NC; ++c) {
+    a = min_nan2<DT>(a, min_nan2<DT>(min_nan2<DT>(w[c].x, w[c].y), min_nan2<DT>(w[c].z, w[c].w)));
+    b = max_nan2<DT>(b, max_nan2<DT>(max_nan2<DT>(w[c].x, w[c].y), max_nan2<DT>(w[c].z, w[c].w)));
+  }
 #pragma unroll
   for (int o = 1; o < G; o <<= 1) {
     a = min_nan2<DT>(a, __shfl_xor_sync(0xffffffffu, a, o));
@@ -195,6 +210,51 @@ __device__ __forceinline__ void vec_minmax(const uint4& w, float& mn, float& mx)
   b = max_nan2<DT>(b, __byte_perm(b, 0, 0x1032));
   mn = lo_f32<DT>(a);
   mx = lo_f32<DT>(b);
+}
+
+// Chunk assignment for the order-free codecs (FP8, uniform): the vector's
+// 16-byte chunks c = 0 .. D/8-1 are dealt round-robin to its G lanes, lane li
+// holding chunks li, li + G, ... (NC of them), so one warp load instruction
+// reads G contiguous chunks of each of the warp's 32/G vectors.  G is a
+// multiple of 4 for every head dim (the 3-bit packer combines 4 chunks).
+template <int D>
+struct ChunkMap {
+  static constexpr int E = D == 32 ? 8 : 16;   // elements per lane
+  static constexpr int G = D / E;               // lanes per vector
+  static constexpr int NC = E / 8;              // chunks per lane
+  static constexpr int VPW = 32 / G;            // vectors per warp row
+};
+
+// ---------------------------------------------------------------- packed FP32x2
+// One instruction on two independent FP32 lanes, each rounded as its scalar
+// counterpart (sm_100+ packed FP32 arithmetic).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{ .reg .b64 ra, rb, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5};"
+      " mul.rn.f32x2 rd, ra, rb; mov.b64 {%0, %1}, rd; }"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{ .reg .b64 ra, rb, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5};"
+      " add.rn.f32x2 rd, ra, rb; mov.b64 {%0, %1}, rd; }"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 d;
+  asm("{ .reg .b64 ra, rb, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5};"
+      " sub.rn.f32x2 rd, ra, rb; mov.b64 {%0, %1}, rd; }"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{ .reg .b64 ra, rb, rc, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5};"
+      " mov.b64 rc, {%6, %7}; fma.rn.f32x2 rd, ra, rb, rc; mov.b64 {%0, %1}, rd; }"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
 }
 
 // Admission flags of one vector from its min/max: bit 0 nonfinite, bit 1 range.
@@ -255,21 +315,24 @@ __device__ __forceinline__ void wht_butterflies(float (&a)[8], uint32_t li) {
   }
 }
 
-// Lane-local 3-bit codes of 8 elements (24 bits) -> the 12-byte little-endian
-// stream chunk of lanes 4q..4q+3 stored as three words by lanes 4q..4q+2.
-// `dst` points at the vector's code bytes; li is the lane index in the vector.
-__device__ __forceinline__ void store_3bit(uint8_t* dst, uint32_t v24, uint32_t li, bool active) {
+// 3-bit codes of one 8-element chunk (24 bits, chunk index c of the vector)
+// -> the 12-byte little-endian stream of chunks 4q..4q+3, written as three
+// words by the lanes holding chunks 4q..4q+2 (the four chunks sit on four
+// consecutive lanes).  `dst` points at the vector's code bytes.
+__device__ __forceinline__ void store_3bit(uint8_t* dst, uint32_t v24, uint32_t c, bool active) {
   const uint32_t next = __shfl_down_sync(0xffffffffu, v24, 1);
-  const uint32_t k = li & 3u;
+  const uint32_t k = c & 3u;
   if (active && k < 3u) {
     const uint32_t w = (v24 >> (8u * k)) | (next << (24u - 8u * k));
-    st4(dst + 12u * (li >> 2) + 4u * k, w);
+    st4(dst + 12u * (c >> 2) + 4u * k, w);
   }
 }
 
-// Inverse of store_3bit: the 24 bits of lane li from the vector's code bytes.
-__device__ __forceinline__ uint32_t load_3bit(const uint8_t* src, uint32_t li) {
-  const uint32_t bit = 24u * li;
+// Inverse of store_3bit: the 24 bits of chunk c from the vector's code bytes.
+// Reads at most one word past the chunk, which stays inside the slot (the
+// metadata region follows the codes).
+__device__ __forceinline__ uint32_t load_3bit(const uint8_t* src, uint32_t c) {
+  const uint32_t bit = 24u * c;
   const uint32_t* w = reinterpret_cast<const uint32_t*>(src) + (bit >> 5);
   const uint32_t lo = ld_nc4(w), hi = ld_nc4(w + 1);
   return __funnelshift_r(lo, hi, bit & 31u) & 0xffffffu;

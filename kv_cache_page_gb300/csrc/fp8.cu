@@ -19,23 +19,52 @@ namespace {
 
 constexpr float kRecip448 = 1.0f / 448.0f;  // fl32(1/448)
 
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+// four floats -> four E4M3FN bytes (first element in the low byte), RNE,
+// saturating to +-448 (the clip); NaN stays NaN
+__device__ __forceinline__ uint32_t e4m3x4(float x0, float x1, float x2, float x3) {
   uint32_t d;
-  asm("{ .reg .b16 t; cvt.rn.satfinite.e4m3x2.f32 t, %1, %2; cvt.u32.u16 %0, t; }"
+  asm("{ .reg .b16 lo, hi; cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;"
+      " cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3; mov.b32 %0, {lo, hi}; }"
       : "=r"(d)
-      : "f"(hi), "f"(lo));
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
   return d;
 }
-// two E4M3 bytes (low byte = first element) -> f16x2 (exact)
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  uint32_t d;
-  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(d) : "r"(two));
-  return d;
+// four E4M3 bytes -> two f16x2 words (exact)
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& h01, uint32_t& h23) {
+  asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; cvt.rn.f16x2.e4m3x2 %0, lo;"
+      " cvt.rn.f16x2.e4m3x2 %1, hi; }"
+      : "=r"(h01), "=r"(h23)
+      : "r"(w));
+}
+
+// E4M3 codes of 8 elements.  CAST: code(x).  FIXED / DYNAMIC: code(x / s),
+// the quotient correctly rounded: with nr = -RN(1/s), qn = RN(x nr) = -RN(x/s)
+// approximately, e = RN(x + qn s) is the exact residual x - q0 s, and
+// RN(qn + e nr) = -RN(x / s) exactly; the codes of -q have the sign bits
+// flipped back.  Zero inputs keep their sign through every step.
+template <uint32_t CODEC>
+__device__ __forceinline__ uint2 fp8_codes8(const float (&x)[8], float s, float nr) {
+  if (CODEC == KV_CODEC_FP8_CAST)
+    return make_uint2(e4m3x4(x[0], x[1], x[2], x[3]), e4m3x4(x[4], x[5], x[6], x[7]));
+  const float2 s2 = make_float2(s, s), nr2 = make_float2(nr, nr);
+  float q[8];
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    const float2 xx = make_float2(x[e], x[e + 1]);
+    const float2 q0n = mul2(xx, nr2);
+    const float2 res = fma2(q0n, s2, xx);
+    const float2 qn = fma2(res, nr2, q0n);
+    q[e] = qn.x;
+    q[e + 1] = qn.y;
+  }
+  return make_uint2(e4m3x4(q[0], q[1], q[2], q[3]) ^ 0x80808080u,
+                    e4m3x4(q[4], q[5], q[6], q[7]) ^ 0x80808080u);
 }
 
 template <int DT, int D, uint32_t CODEC>
 __global__ void __launch_bounds__(kThreads) fp8_encode_kernel(const __grid_constant__ Params p) {
-  constexpr int G = D / kE, VPW = 32 / G, U = 4, W = kThreads / 32;
+  using M = ChunkMap<D>;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = 2, W = kThreads / 32;
   constexpr int STEP = W * VPW * U;
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
@@ -51,44 +80,43 @@ __global__ void __launch_bounds__(kThreads) fp8_encode_kernel(const __grid_const
       continue;
     }
     if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
-    float scale = 1.0f;
-    if (CODEC == KV_CODEC_FP8_FIXED) scale = p.fixed_scale[s.layer][s.role];
-    const float rscale = __frcp_rn(scale);
+    float fixed = 1.0f;
+    if (CODEC == KV_CODEC_FP8_FIXED) fixed = p.fixed_scale[s.layer][s.role];
+    const float fixed_nr = -__frcp_rn(fixed);
     uint8_t* codes = s.slot;
     uint8_t* meta = s.slot + (uint64_t)nv * D;
     uint32_t flags = 0;
     for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
-      uint4 w[U];
+      uint4 w[U][NC];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint32_t j = j0 + u * VPW + grp;
-        w[u] = j < nv ? ld_stream16(s.page + vec_off(p, j) + li * kE) : make_uint4(0, 0, 0, 0);
+        const uint16_t* src = s.page + (j < nv ? vec_off(p, j) : 0);
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          w[u][c] = j < nv ? ld_stream16(src + 8 * (li + G * c)) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint32_t j = j0 + u * VPW + grp;
         float mn, mx;
-        vec_minmax<DT, G>(w[u], mn, mx);
+        vec_minmax<DT, G, NC>(w[u], mn, mx);
         flags |= admission(mn, mx, p.reject_abs);
-        float x[8];
-        unpack8<DT>(w[u], x);
-        float sc = scale, r = rscale;
+        float sc = fixed, nr = fixed_nr;
         if (CODEC == KV_CODEC_FP8_DYNAMIC) {
-          const float amax = fmaxf(-mn, mx);
-          sc = __fmul_rn(fmaxf(amax, 1e-12f), kRecip448);
-          r = __frcp_rn(sc);
+          sc = __fmul_rn(fmaxf(fmaxf(-mn, mx), 1e-12f), kRecip448);
+          nr = -__frcp_rn(sc);
         }
-        if (CODEC != KV_CODEC_FP8_CAST) {
+        const bool in = j < nv;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = div_by(x[e], sc, r);
+        for (int c = 0; c < NC; ++c) {
+          float x[8];
+          unpack8<DT>(w[u][c], x);
+          const uint2 out = fp8_codes8<CODEC>(x, sc, nr);
+          if (in) st8(codes + (uint64_t)j * D + 8 * (li + G * c), out);
         }
-        const uint32_t b01 = e4m3x2(x[0], x[1]), b23 = e4m3x2(x[2], x[3]);
-        const uint32_t b45 = e4m3x2(x[4], x[5]), b67 = e4m3x2(x[6], x[7]);
-        const uint2 out = make_uint2(b01 | (b23 << 16), b45 | (b67 << 16));
-        if (j < nv) {
-          st8(codes + (uint64_t)j * D + li * kE, out);
-          if (CODEC == KV_CODEC_FP8_DYNAMIC && li == 0) st4(meta + (uint64_t)j * 4, __float_as_uint(sc));
-        }
+        if (CODEC == KV_CODEC_FP8_DYNAMIC && in && li == 0)
+          st4(meta + (uint64_t)j * 4, __float_as_uint(sc));
       }
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
@@ -106,7 +134,8 @@ __global__ void __launch_bounds__(kThreads) fp8_encode_kernel(const __grid_const
 
 template <int DT, int D, uint32_t CODEC>
 __global__ void __launch_bounds__(kThreads) fp8_decode_kernel(const __grid_constant__ Params p) {
-  constexpr int G = D / kE, VPW = 32 / G, U = 4, W = kThreads / 32;
+  using M = ChunkMap<D>;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = 2, W = kThreads / 32;
   constexpr int STEP = W * VPW * U;
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
@@ -117,34 +146,48 @@ __global__ void __launch_bounds__(kThreads) fp8_decode_kernel(const __grid_const
       if (s.action == kReport && threadIdx.x == 0 && p.result) p.result[i] = s.status;
       continue;
     }
-    float scale = 1.0f;
-    if (CODEC == KV_CODEC_FP8_FIXED) scale = p.fixed_scale[s.layer][s.role];
+    float fixed = 1.0f;
+    if (CODEC == KV_CODEC_FP8_FIXED) fixed = p.fixed_scale[s.layer][s.role];
     const uint8_t* codes = s.slot;
     const uint8_t* meta = s.slot + (uint64_t)nv * D;
     uint16_t* page = const_cast<uint16_t*>(s.page);
     for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
-      uint2 c[U];
+      uint2 cw[U][NC];
       float sc[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint32_t j = j0 + u * VPW + grp;
         const bool in = j < nv;
-        c[u] = in ? ld_nc8(codes + (uint64_t)j * D + li * kE) : make_uint2(0, 0);
-        sc[u] = scale;
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          cw[u][c] = in ? ld_nc8(codes + (uint64_t)j * D + 8 * (li + G * c)) : make_uint2(0, 0);
+        sc[u] = fixed;
         if (CODEC == KV_CODEC_FP8_DYNAMIC) sc[u] = in ? __uint_as_float(ld_nc4(meta + (uint64_t)j * 4)) : 0.0f;
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint32_t j = j0 + u * VPW + grp;
-        const uint32_t h[4] = {e4m3x2_to_f16x2(c[u].x & 0xffffu), e4m3x2_to_f16x2(c[u].x >> 16),
-                               e4m3x2_to_f16x2(c[u].y & 0xffffu), e4m3x2_to_f16x2(c[u].y >> 16)};
-        float y[8];
+        uint16_t* dst = page + (j < nv ? vec_off(p, j) : 0);
+        const float2 s2 = make_float2(sc[u], sc[u]);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          y[2 * k] = __fmul_rn(lo_f32<0>(h[k]), sc[u]);
-          y[2 * k + 1] = __fmul_rn(hi_f32<0>(h[k]), sc[u]);
+        for (int c = 0; c < NC; ++c) {
+          uint32_t h[4];
+          e4m3x4_to_f16(cw[u][c].x, h[0], h[1]);
+          e4m3x4_to_f16(cw[u][c].y, h[2], h[3]);
+          uint4 o;
+          if (DT == 0 && CODEC == KV_CODEC_FP8_CAST) {
+            o = make_uint4(h[0], h[1], h[2], h[3]);   // code value is already the FP16 result
+          } else {
+            uint32_t r[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 y = mul2(make_float2(lo_f32<0>(h[k]), hi_f32<0>(h[k])), s2);
+              r[k] = pack2<DT>(y.x, y.y);
+            }
+            o = make_uint4(r[0], r[1], r[2], r[3]);
+          }
+          if (j < nv) st16(dst + 8 * (li + G * c), o);
         }
-        if (j < nv) st16(page + vec_off(p, j) + li * kE, pack8<DT>(y));
       }
     }
     if (threadIdx.x == 0 && p.result) p.result[i] = KV_SEG_ENCODED;

@@ -104,6 +104,42 @@ void make_codebook(uint32_t bits, uint32_t D, float* cent, float* bnd) {
   for (uint32_t j = 0; j + 1 < K; ++j) bnd[j] = (float)((0.5 * (full[j] + full[j + 1])) / rs);
 }
 
+// Boundaries of the scaled domain moved to the unscaled WHT output:
+// W_j = max{w : RN(w * c) <= b_j}; RN(w * c) is monotone in w, so
+// RN(w * c) > b_j  <=>  w > W_j.
+float unscaled_threshold(float b, float c) {
+  volatile float cv = c;  // keep every product a single FP32 rounding
+  float w = (float)((double)b / (double)c);
+  auto prod = [&](float x) { volatile float y = x * cv; return (float)y; };
+  while (prod(w) > b) w = std::nextafterf(w, -INFINITY);
+  while (prod(std::nextafterf(w, INFINITY)) <= b) w = std::nextafterf(w, INFINITY);
+  return w;
+}
+
+// Cell table over c = rint(4 w) in [-kLutHalf, kLutHalf]: the code of every w
+// in the cell is lo + (w > thr), thr = the one threshold inside the cell or
+// +inf.  Returns false if a cell would hold two thresholds.
+bool build_index_table(const float* bnd, uint32_t nb, float c, float* thr, uint32_t* lo) {
+  float W[15];
+  for (uint32_t j = 0; j < nb; ++j) W[j] = unscaled_threshold(bnd[j], c);
+  for (int cell = -kvc::kLutHalf; cell <= kvc::kLutHalf; ++cell) {
+    // floats w with rint(4 w) == cell (4 w is exact; ties go to the even cell)
+    const float a = (float)((cell - 0.5) / 4.0), b = (float)((cell + 0.5) / 4.0);
+    const float wlo = (cell & 1) ? std::nextafterf(a, INFINITY) : a;
+    const float whi = (cell & 1) ? std::nextafterf(b, -INFINITY) : b;
+    uint32_t below = 0, inside = 0;
+    float t = INFINITY;
+    for (uint32_t j = 0; j < nb; ++j) {
+      if (W[j] < wlo) ++below;
+      else if (W[j] < whi) { ++inside; t = W[j]; }
+    }
+    if (inside > 1) return false;
+    thr[cell + kvc::kLutHalf] = t;
+    lo[cell + kvc::kLutHalf] = below;
+  }
+  return true;
+}
+
 // FP8 scale rule: max(amax, 1e-12) * fl32(1/448), in FP32.
 float fp8_scale(float amax) {
   const float recip = 1.0f / 448.0f;
@@ -287,6 +323,7 @@ int kv_codec_create(const kv_codec_geometry* g, kv_codec_t* out) {
   p.n_layer_ptrs = g->layout == KV_LAYOUT_SEPARATE ? 2 * g->num_layers : g->num_layers;
   p.num_blocks = g->num_blocks;
   p.h_magic = ((1ull << 32) + p.H - 1) / p.H;
+  p.heads_contig = (uint64_t)g->stride_token == (uint64_t)g->stride_head * g->num_kv_heads ? 1 : 0;
   p.sb = g->stride_block;
   p.st = g->stride_token;
   p.sh = g->stride_head;
@@ -318,7 +355,14 @@ int kv_codec_create(const kv_codec_geometry* g, kv_codec_t* out) {
     p.static_status[r] = st;
   }
   sign_words(g->rotation_seed, p.D, p.sign_words);
-  if (is_tq(g->k_codec)) make_codebook(codec_bits(g->k_codec), p.D, p.cent, p.bnd);
+  if (is_tq(g->k_codec)) {
+    const uint32_t bits = codec_bits(g->k_codec);
+    make_codebook(bits, p.D, p.cent, p.bnd);
+    if (!build_index_table(p.bnd, (1u << bits) - 1u, p.wht_scale, p.lut_thr, p.lut_lo)) {
+      delete h;
+      return KV_ERR_INVALID_ARG;
+    }
+  }
   if (fixed)
     for (uint32_t l = 0; l < p.L; ++l)
       for (int r = 0; r < 2; ++r) p.fixed_scale[l][r] = fp8_scale(g->fixed_amax[2 * l + r]);

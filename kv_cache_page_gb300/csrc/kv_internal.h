@@ -14,6 +14,11 @@ namespace kvc {
 constexpr int kMaxLayers = (int)KV_CODEC_MAX_LAYERS;
 constexpr int kThreads = 256;           // threads per CTA for every codec kernel
 
+// TurboQuant index table: cell c = rint(4 w) of the unscaled Walsh-Hadamard
+// output w (|w| <= sqrt(D) <= 16 for a unit vector), c in [-kLutHalf, kLutHalf].
+constexpr int kLutHalf = 68;
+constexpr int kLutCells = 2 * kLutHalf + 1;
+
 struct Params {
   // ---- registered geometry ----
   uint32_t dtype;                       // KV_DT_*
@@ -33,12 +38,18 @@ struct Params {
   uint32_t meta_bytes[2];               // per vector
   uint64_t seg_bytes[2];                // encoded slot (multiple of 128)
   uint8_t static_status[2];             // 0 = encodable, else KV_SEG_RAW_{POLICY,OVERSIZE,NO_SAVING}
-  uint8_t pad0[2];
+  uint8_t heads_contig;                 // st == H * sh: vector j of a page sits at j * sh
+  uint8_t pad0;
   float reject_abs;                     // admission bound
   float wht_scale;                      // fl32(1/sqrt(D))
   uint32_t sign_words[8];               // TurboQuant sign bits, bit i = negate element i
   float cent[16];                       // TurboQuant centroids (K codec)
   float bnd[16];                        // TurboQuant boundaries (K codec), bnd[15] unused
+  // Index table of the unscaled WHT output w: code(w) = lut_lo[c] + (w > lut_thr[c]),
+  // c = rint(4 w); built from the boundaries moved to the unscaled domain,
+  // W_j = max{w : RN(w * wht_scale) <= bnd[j]}, so that no scale multiply is needed.
+  float lut_thr[kLutCells];
+  uint32_t lut_lo[kLutCells];
   float fixed_scale[kMaxLayers][2];     // FP8_FIXED scale per (layer, role)
   const void* layer_ptr[2 * kMaxLayers];
   // ---- per call ----

@@ -11,6 +11,8 @@
 namespace kvc {
 namespace {
 
+#define LV(b) ((1u << (b)) - 1u)
+
 // round to nearest-even integer and saturate to [0, 255]
 __device__ __forceinline__ uint32_t rint_sat_u8(float q) {
   uint32_t d;
@@ -18,9 +20,28 @@ __device__ __forceinline__ uint32_t rint_sat_u8(float q) {
   return d & 0xffu;
 }
 
+// codes of 8 elements: clamp(rint((x - m) / s), 0, L), the quotient correctly
+// rounded (q0 = RN(d r), e = RN(d - q0 s) exact, q = RN(q0 + e r)); 0 if s == 0
+template <uint32_t LEVELS>
+__device__ __forceinline__ void uniform_codes8(const float (&x)[8], float m, float sc, float r,
+                                               uint32_t (&c)[8]) {
+  const float2 m2 = make_float2(m, m), ns2 = make_float2(-sc, -sc), r2 = make_float2(r, r);
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    const float2 d = sub2(make_float2(x[e], x[e + 1]), m2);
+    const float2 q0 = mul2(d, r2);
+    const float2 res = fma2(q0, ns2, d);
+    const float2 q = fma2(res, r2, q0);
+    const uint32_t a = rint_sat_u8(q.x), b = rint_sat_u8(q.y);
+    c[e] = sc == 0.0f ? 0u : (a < LEVELS ? a : LEVELS);
+    c[e + 1] = sc == 0.0f ? 0u : (b < LEVELS ? b : LEVELS);
+  }
+}
+
 template <int DT, int D, int BITS>
 __global__ void __launch_bounds__(kThreads) uniform_encode_kernel(const __grid_constant__ Params p) {
-  constexpr int G = D / kE, VPW = 32 / G, U = 4, W = kThreads / 32;
+  using M = ChunkMap<D>;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = 2, W = kThreads / 32;
   constexpr int STEP = W * VPW * U;
   constexpr uint32_t LEVELS = (1u << BITS) - 1u;
   constexpr int CB = D * BITS / 8;  // code bytes per vector
@@ -42,17 +63,20 @@ __global__ void __launch_bounds__(kThreads) uniform_encode_kernel(const __grid_c
     uint8_t* meta = s.slot + (uint64_t)nv * CB;
     uint32_t flags = 0;
     for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
-      uint4 w[U];
+      uint4 w[U][NC];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint32_t j = j0 + u * VPW + grp;
-        w[u] = j < nv ? ld_stream16(s.page + vec_off(p, j) + li * kE) : make_uint4(0, 0, 0, 0);
+        const uint16_t* src = s.page + (j < nv ? vec_off(p, j) : 0);
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          w[u][c] = j < nv ? ld_stream16(src + 8 * (li + G * c)) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint32_t j = j0 + u * VPW + grp;
         float mn, mx;
-        vec_minmax<DT, G>(w[u], mn, mx);
+        vec_minmax<DT, G, NC>(w[u], mn, mx);
         flags |= admission(mn, mx, p.reject_abs);
         mn = __fadd_rn(mn, 0.0f);  // a zero minimum / maximum is +0
         mx = __fadd_rn(mx, 0.0f);
@@ -60,30 +84,30 @@ __global__ void __launch_bounds__(kThreads) uniform_encode_kernel(const __grid_c
         const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), (float)LEVELS));
         const float m = __half2float(m16), sc = __half2float(s16);
         const float r = __frcp_rn(sc);
-        float x[8];
-        unpack8<DT>(w[u], x);
-        uint32_t c[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t q = rint_sat_u8(div_by(__fsub_rn(x[e], m), sc, r));
-          c[e] = sc == 0.0f ? 0u : (q < LEVELS ? q : LEVELS);
-        }
         const bool in = j < nv;
         uint8_t* vc = codes + (uint64_t)j * CB;
-        if (BITS == 8) {
-          const uint2 out = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
-                                       c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
-          if (in) st8(vc + li * 8, out);
-        } else if (BITS == 4) {
-          uint32_t v = 0;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) v |= c[e] << (4 * e);
-          if (in) st4(vc + li * 4, v);
-        } else {
-          uint32_t v = 0;
+        for (int ch = 0; ch < NC; ++ch) {
+          const uint32_t cidx = li + G * ch;
+          float x[8];
+          unpack8<DT>(w[u][ch], x);
+          uint32_t c[8];
+          uniform_codes8<LEVELS>(x, m, sc, r, c);
+          if (BITS == 8) {
+            const uint2 out = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
+                                         c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+            if (in) st8(vc + 8 * cidx, out);
+          } else if (BITS == 4) {
+            uint32_t v = 0;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) v |= c[e] << (3 * e);
-          store_3bit(vc, v, li, in);
+            for (int e = 0; e < 8; ++e) v |= c[e] << (4 * e);
+            if (in) st4(vc + 4 * cidx, v);
+          } else {
+            uint32_t v = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v |= c[e] << (3 * e);
+            store_3bit(vc, v, cidx, in);
+          }
         }
         if (in && li == 0)
           st4(meta + (uint64_t)j * 4,
@@ -102,14 +126,15 @@ __global__ void __launch_bounds__(kThreads) uniform_encode_kernel(const __grid_c
   }
 }
 
-// exact float of a small unsigned integer: 2^23 + c, minus 2^23
+// exact float of a small unsigned integer: (2^23 + c) - 2^23
 __device__ __forceinline__ float small_u2f(uint32_t c) {
   return __fsub_rn(__uint_as_float(0x4b000000u | c), 8388608.0f);
 }
 
 template <int DT, int D, int BITS>
 __global__ void __launch_bounds__(kThreads) uniform_decode_kernel(const __grid_constant__ Params p) {
-  constexpr int G = D / kE, VPW = 32 / G, U = 4, W = kThreads / 32;
+  using M = ChunkMap<D>;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = 2, W = kThreads / 32;
   constexpr int STEP = W * VPW * U;
   constexpr int CB = D * BITS / 8;
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
@@ -125,18 +150,22 @@ __global__ void __launch_bounds__(kThreads) uniform_decode_kernel(const __grid_c
     const uint8_t* meta = s.slot + (uint64_t)nv * CB;
     uint16_t* page = const_cast<uint16_t*>(s.page);
     for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
-      uint2 cw[U];
+      uint2 cw[U][NC];
       uint32_t mw[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint32_t j = j0 + u * VPW + grp;
         const bool in = j < nv;
         const uint8_t* vc = codes + (uint64_t)j * CB;
-        cw[u] = make_uint2(0, 0);
-        if (in) {
-          if (BITS == 8) cw[u] = ld_nc8(vc + li * 8);
-          else if (BITS == 4) cw[u].x = ld_nc4(vc + li * 4);
-          else cw[u].x = load_3bit(vc, li);
+#pragma unroll
+        for (int ch = 0; ch < NC; ++ch) {
+          const uint32_t cidx = li + G * ch;
+          cw[u][ch] = make_uint2(0, 0);
+          if (in) {
+            if (BITS == 8) cw[u][ch] = ld_nc8(vc + 8 * cidx);
+            else if (BITS == 4) cw[u][ch].x = ld_nc4(vc + 4 * cidx);
+            else cw[u][ch].x = load_3bit(vc, cidx);
+          }
         }
         mw[u] = in ? ld_nc4(meta + (uint64_t)j * 4) : 0u;
       }
@@ -145,15 +174,27 @@ __global__ void __launch_bounds__(kThreads) uniform_decode_kernel(const __grid_c
         const uint32_t j = j0 + u * VPW + grp;
         const float m = __half2float(__ushort_as_half((unsigned short)(mw[u] & 0xffffu)));
         const float sc = __half2float(__ushort_as_half((unsigned short)(mw[u] >> 16)));
-        float y[8];
+        const float2 m2 = make_float2(m, m), s2 = make_float2(sc, sc);
+        uint16_t* dst = page + (j < nv ? vec_off(p, j) : 0);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          uint32_t c;
-          if (BITS == 8) c = ((e < 4 ? cw[u].x : cw[u].y) >> (8 * (e & 3))) & 0xffu;
-          else c = (cw[u].x >> (BITS * e)) & ((1u << BITS) - 1u);
-          y[e] = __fadd_rn(__fmul_rn(small_u2f(c), sc), m);
+        for (int ch = 0; ch < NC; ++ch) {
+          uint32_t r[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint32_t c0, c1;
+            if (BITS == 8) {
+              const uint32_t wd = k < 2 ? cw[u][ch].x : cw[u][ch].y;
+              c0 = (wd >> (16 * (k & 1))) & 0xffu;
+              c1 = (wd >> (16 * (k & 1) + 8)) & 0xffu;
+            } else {
+              c0 = (cw[u][ch].x >> (BITS * 2 * k)) & LV(BITS);
+              c1 = (cw[u][ch].x >> (BITS * (2 * k + 1))) & LV(BITS);
+            }
+            const float2 y = add2(mul2(make_float2(small_u2f(c0), small_u2f(c1)), s2), m2);
+            r[k] = pack2<DT>(y.x, y.y);
+          }
+          if (j < nv) st16(dst + 8 * (li + G * ch), make_uint4(r[0], r[1], r[2], r[3]));
         }
-        if (j < nv) st16(page + vec_off(p, j) + li * kE, pack8<DT>(y));
       }
     }
     if (threadIdx.x == 0 && p.result) p.result[i] = KV_SEG_ENCODED;
