@@ -218,8 +218,10 @@ def recorded_traffic(kname, units):
 def run_gpu(args, dist, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    case = synth.make_case(args.workload, device=device, seed=args.seed)
-    arms = [Arm(case, a, case.layers, device) for a in case.arms]
+    case = synth.make_case(args.workload, device=device, seed=args.seed, num_layers=args.layers,
+                           num_blocks=args.pages, head_dim=args.head_dim)
+    arms = [Arm(case, a, case.layers, device) for a in case.arms
+            if args.arm is None or a.name == args.arm]
     stream = torch.cuda.current_stream(device)
 
     def step(events=None):
@@ -304,9 +306,12 @@ def run_gpu(args, dist, world, rank, local):
         "clocks": clk,
         "e2e": e2e,
     }
-    if args.extra and world == 1:
+    shrunk = args.layers is not None or args.pages is not None or args.arm is not None
+    if shrunk:
+        result["config"]["reduced"] = True
+    if args.extra and world == 1 and not shrunk:
         result["other_workloads"] = run_extra(args, device)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not shrunk:
         result["cpu_baseline"] = cpu_baseline(args, case_name=args.workload, seconds=args.cpu_seconds)
     for a in arms:
         a.codec.close()
@@ -493,6 +498,10 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="qwen3_8b", choices=list(synth.CASES))
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=None, help="shrink the workload (profiling)")
+    ap.add_argument("--pages", type=int, default=None, help="pages per layer (profiling)")
+    ap.add_argument("--head-dim", type=int, default=None, help="head_dim_sweep point")
+    ap.add_argument("--arm", default=None, help="run only this codec arm")
     ap.add_argument("--no-extra", dest="extra", action="store_false")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
