@@ -132,6 +132,19 @@ __device__ __forceinline__ uint16_t ld_nc2(const void* ptr) {
   asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(ptr));
   return v;
 }
+// asynchronous 16-byte global -> shared copy (bypasses L1), its commit and wait
+__device__ __forceinline__ void cp_async16(uint32_t smem, const void* gptr) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(gptr) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ uint4 lds16(uint32_t smem) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem));
+  return v;
+}
 __device__ __forceinline__ void st16(void* ptr, uint4 v) { *reinterpret_cast<uint4*>(ptr) = v; }
 __device__ __forceinline__ void st8(void* ptr, uint2 v) { *reinterpret_cast<uint2*>(ptr) = v; }
 __device__ __forceinline__ void st4(void* ptr, uint32_t v) { *reinterpret_cast<uint32_t*>(ptr) = v; }

@@ -237,7 +237,11 @@ int grid_for(const void* kernel, uint32_t n_segments, unsigned* grid) {
     std::lock_guard<std::mutex> lk(g_mu);
     g_occ[{dev, kernel}] = occ;
   }
-  const uint64_t g = std::min<uint64_t>((uint64_t)sms * (uint64_t)occ, n_segments);
+  uint64_t g = std::min<uint64_t>((uint64_t)sms * (uint64_t)occ, n_segments);
+  // An odd stride deals segments of both roles to every CTA when K and V
+  // segments alternate in the descriptor list (a launch that codes one role
+  // only skips the other role's segments).
+  if (g > 1 && g < n_segments && (g & 1) == 0) --g;
   *grid = (unsigned)g;
   return KV_OK;
 }

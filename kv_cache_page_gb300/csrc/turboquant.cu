@@ -30,21 +30,22 @@ constexpr int kTqE = 32;               // elements per lane
 constexpr float kCellMagic = 12582912.0f;  // 1.5 * 2^23: FFMA(w, 4, magic) has rint(4 w) in its low bits
 constexpr uint32_t kCellMagicBits = 0x4b400000u;
 
-// Sign masks of the lane's 16 packed words (elements 2m, 2m+1): bit 15 / 31.
-__device__ __forceinline__ void sign_masks(const Params& p, uint32_t li, uint32_t (&m)[16]) {
-  const uint32_t bits = p.sign_words[li];
-#pragma unroll
-  for (int k = 0; k < 16; ++k)
-    m[k] = (((bits >> (2 * k)) & 1u) << 15) | (((bits >> (2 * k + 1)) & 1u) << 31);
+// Sign mask word k (elements 2k, 2k+1 of a lane's 32) for sign word `bits`.
+__device__ __forceinline__ uint32_t sign_mask_word(uint32_t bits, int k) {
+  return (((bits >> (2 * k)) & 1u) << 15) | (((bits >> (2 * k + 1)) & 1u) << 31);
 }
 
-// Pairwise sum over the vector: in-thread tree over the lane's 32 elements
-// (pairs first), then xor-shuffles over the G lanes with ascending distance.
+// Pairwise sum of squares over the vector: squares of the lane's 32 elements
+// summed as an in-thread tree (pairs first), then xor-shuffles over the G
+// lanes with ascending distance.
 template <int G>
-__device__ __forceinline__ float vector_sum(const float2 (&a)[16]) {
+__device__ __forceinline__ float vector_sumsq(const float2 (&a)[16]) {
   float s[16];
 #pragma unroll
-  for (int m = 0; m < 16; ++m) s[m] = __fadd_rn(a[m].x, a[m].y);
+  for (int m = 0; m < 16; ++m) {
+    const float2 q = mul2(a[m], a[m]);
+    s[m] = __fadd_rn(q.x, q.y);
+  }
 #pragma unroll
   for (int w = 1; w < 16; w <<= 1)
 #pragma unroll
@@ -86,64 +87,110 @@ __device__ __forceinline__ void butterflies(float2 (&a)[16], uint32_t li) {
   }
 }
 
+// Shared tables of the TurboQuant kernels, built once per CTA.
+struct TqShared {
+  uint2 lut[kLutCells * 16];  // index cells, 16 copies: lanes of a half warp never share a bank
+  uint4 sign[8][5];           // sign masks per lane of a vector (row padded against bank conflicts)
+};
+
+__device__ __forceinline__ void tq_shared_init(const Params& p, TqShared& sh, bool lut) {
+  if (lut)
+    for (int k = threadIdx.x; k < kLutCells * 16; k += blockDim.x)
+      sh.lut[k] = make_uint2(__float_as_uint(p.lut_thr[k >> 4]), p.lut_lo[k >> 4]);
+  for (int t = threadIdx.x; t < 8 * 4; t += blockDim.x) {
+    const uint32_t bits = p.sign_words[t >> 2];
+    const int k = 4 * (t & 3);
+    sh.sign[t >> 2][t & 3] = make_uint4(sign_mask_word(bits, k), sign_mask_word(bits, k + 1),
+                                        sign_mask_word(bits, k + 2), sign_mask_word(bits, k + 3));
+  }
+}
+
+// Work of one warp: whole segments, warp w of the grid taking segments w,
+// w + (warps in grid), ...  Segments this launch does not code are reported
+// (lane 0 writes the status or result) or skipped on the way.
+template <int DIR>
+__device__ __forceinline__ uint32_t next_segment(const Params& p, uint32_t i, uint32_t stride,
+                                                 uint32_t lane, Seg& s) {
+  for (; i < p.n_segments; i += stride) {
+    s = plan_segment(p, i, DIR);
+    if (s.action == kProcess) return i;
+    if (s.action == kReport && lane == 0) {
+      if (DIR == kEncode) p.status[i] = s.status;
+      else if (p.result) p.result[i] = s.status;
+    }
+  }
+  return 0xffffffffu;
+}
+
 template <int DT, int D, int BITS>
 __global__ void __launch_bounds__(kThreads) tq_encode_kernel(const __grid_constant__ Params p) {
   constexpr int G = D / kTqE, VPW = 32 / G, W = kThreads / 32;
-  constexpr int STEP = W * VPW;
   constexpr int CB = D * BITS / 8;
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
-  // cell table, 16 copies so that the lanes of a half warp never share a bank
-  __shared__ uint2 s_lut[kLutCells * 16];
-  __shared__ uint32_t s_flag[2];
-  for (int k = threadIdx.x; k < kLutCells * 16; k += blockDim.x)
-    s_lut[k] = make_uint2(__float_as_uint(p.lut_thr[k >> 4]), p.lut_lo[k >> 4]);
-  if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
+  __shared__ TqShared sh;
+  // next vector of each lane: 64 bytes, chunk k at slot k ^ ((lane >> 1) & 3)
+  // so that the 8 lanes of a 128-bit shared access hit 8 different bank groups
+  __shared__ uint4 s_stage[W][32][4];
+  tq_shared_init(p, sh, true);
   __syncthreads();
-  uint32_t smask[16];
-  sign_masks(p, li, smask);
-  // byte address of cell c for this lane = bits(FFMA(w, 4, magic)) * 128 + lut_base
-  const uint32_t lut_base = (uint32_t)__cvta_generic_to_shared(s_lut) + (lane & 15u) * 8u +
+  const uint32_t lut_base = (uint32_t)__cvta_generic_to_shared(sh.lut) + (lane & 15u) * 8u +
                             (uint32_t)(kLutHalf * 128) - kCellMagicBits * 128u;
+  const uint32_t stage = (uint32_t)__cvta_generic_to_shared(&s_stage[warp][lane][0]);
+  const uint32_t swz = (lane >> 1) & 3u;
+  const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&sh.sign[li][0]);
   const uint32_t nv = p.nv;
-  int it = 0;
-  for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
-    const Seg s = plan_segment(p, i, kEncode);
-    if (s.action != kProcess) {
-      if (s.action == kReport && threadIdx.x == 0) p.status[i] = s.status;
-      continue;
+  const uint32_t stride = gridDim.x * W;
+
+  auto prefetch = [&](const Seg& s, uint32_t j) {
+    if (j < nv) {
+      const uint16_t* src = s.page + vec_off(p, j) + kTqE * li;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) cp_async16(stage + 16u * ((uint32_t)k ^ swz), src + 8 * k);
     }
-    if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
-    uint8_t* codes = s.slot;
-    uint8_t* meta = s.slot + (uint64_t)nv * CB;
+    cp_async_commit();
+  };
+
+  Seg cur;
+  uint32_t ci = next_segment<kEncode>(p, blockIdx.x * W + warp, stride, lane, cur);
+  if (ci != 0xffffffffu) prefetch(cur, grp);
+  while (ci != 0xffffffffu) {
+    uint8_t* codes = cur.slot;
+    uint8_t* meta = cur.slot + (uint64_t)nv * CB;
     uint32_t flags = 0;
-    for (uint32_t j0 = warp * VPW; j0 < nv; j0 += STEP) {
+    Seg nxt;
+    uint32_t ni = 0xffffffffu;
+    for (uint32_t j0 = 0; j0 < nv; j0 += VPW) {
       const uint32_t j = j0 + grp;
       const bool in = j < nv;
+      cp_async_wait_all();
       uint4 w[4];
-      const uint16_t* src = s.page + (in ? vec_off(p, j) : 0) + kTqE * li;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) w[c] = in ? ld_nc16(src + 8 * c) : make_uint4(0, 0, 0, 0);
+      for (int k = 0; k < 4; ++k) w[k] = in ? lds16(stage + 16u * ((uint32_t)k ^ swz)) : make_uint4(0, 0, 0, 0);
       float mn, mx;
       vec_minmax<DT, G, 4>(w, mn, mx);
+      // the staged data is in registers now: refill the stage with the next vector
+      if (j0 + VPW < nv) {
+        prefetch(cur, j0 + VPW + grp);
+      } else {
+        ni = next_segment<kEncode>(p, ci + stride, stride, lane, nxt);
+        if (ni != 0xffffffffu) prefetch(nxt, grp);
+      }
       const uint32_t vflags = admission(mn, mx, p.reject_abs);
       flags |= vflags;
       if (vflags) {  // keep NaN / inf out of the arithmetic (the segment stays raw)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) w[c] = make_uint4(0, 0, 0, 0);
+        for (int k = 0; k < 4; ++k) w[k] = make_uint4(0, 0, 0, 0);
       }
       float2 a[16];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const uint32_t ww[4] = {w[c].x ^ smask[4 * c], w[c].y ^ smask[4 * c + 1],
-                                w[c].z ^ smask[4 * c + 2], w[c].w ^ smask[4 * c + 3]};
+        const uint4 m = lds16(sign_addr + 16u * c);
+        const uint32_t ww[4] = {w[c].x ^ m.x, w[c].y ^ m.y, w[c].z ^ m.z, w[c].w ^ m.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) a[4 * c + k] = make_float2(lo_f32<DT>(ww[k]), hi_f32<DT>(ww[k]));
       }
-      float2 sq[16];
-#pragma unroll
-      for (int m = 0; m < 16; ++m) sq[m] = mul2(a[m], a[m]);
-      const float n = __fsqrt_rn(vector_sum<G>(sq));
+      const float n = __fsqrt_rn(vector_sumsq<G>(a));
       float r = __frcp_rn(n);
       if (!isfinite(r)) r = 0.0f;
       const float2 r2 = make_float2(r, r);
@@ -178,75 +225,83 @@ __global__ void __launch_bounds__(kThreads) tq_encode_kernel(const __grid_consta
         if (BITS == 4) {
           st16(vc + 16 * li, make_uint4(acc[0], acc[1], acc[2], acc[3]));
         } else {
-          const uint32_t w0 = acc[0] | (acc[1] << 24);
-          const uint32_t w1 = (acc[1] >> 8) | (acc[2] << 16);
-          const uint32_t w2 = (acc[2] >> 16) | (acc[3] << 8);
-          st4(vc + 12 * li, w0);
-          st4(vc + 12 * li + 4, w1);
-          st4(vc + 12 * li + 8, w2);
+          st4(vc + 12 * li, acc[0] | (acc[1] << 24));
+          st4(vc + 12 * li + 4, (acc[1] >> 8) | (acc[2] << 16));
+          st4(vc + 12 * li + 8, (acc[2] >> 16) | (acc[3] << 8));
         }
         if (li == 0)
           *reinterpret_cast<uint16_t*>(meta + (uint64_t)j * 2) = __half_as_ushort(__float2half_rn(n));
       }
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
-    if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
-    zero_padding(s.slot, (uint64_t)nv * (CB + 2), p.seg_bytes[s.role]);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const uint32_t f = s_flag[it & 1];
-      p.status[i] = (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
-    }
-    ++it;
+    for (uint64_t k = (uint64_t)nv * (CB + 2) + lane; k < p.seg_bytes[cur.role]; k += 32) cur.slot[k] = 0;
+    if (lane == 0)
+      p.status[ci] = (flags & 1u) ? KV_SEG_RAW_NONFINITE : (flags & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+    cur = nxt;
+    ci = ni;
   }
 }
 
 template <int DT, int D, int BITS>
 __global__ void __launch_bounds__(kThreads) tq_decode_kernel(const __grid_constant__ Params p) {
   constexpr int G = D / kTqE, VPW = 32 / G, W = kThreads / 32;
-  constexpr int STEP = W * VPW;
   constexpr int CB = D * BITS / 8;
   constexpr int NPAIR = BITS == 4 ? 256 : 64;  // table of two consecutive codes
+  constexpr int REP = BITS == 4 ? 8 : 16;       // copies (keeps the table within 48 KB of static smem)
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
-  // (centroid[lo code], centroid[hi code]) for every pair of codes, 16 copies
-  __shared__ float2 s_pair[NPAIR * 16];
-  for (int k = threadIdx.x; k < NPAIR * 16; k += blockDim.x) {
-    const int v = k >> 4;
+  __shared__ TqShared sh;
+  // (centroid[lo code], centroid[hi code]) for every pair of codes, REP copies
+  __shared__ float2 s_pair[NPAIR * REP];
+  tq_shared_init(p, sh, false);
+  for (int k = threadIdx.x; k < NPAIR * REP; k += blockDim.x) {
+    const int v = k / REP;
     s_pair[k] = make_float2(p.cent[v & ((1 << BITS) - 1)], p.cent[v >> BITS]);
   }
   __syncthreads();
-  uint32_t smask[16];
-  sign_masks(p, li, smask);
-  const uint32_t pair_base = (uint32_t)__cvta_generic_to_shared(s_pair) + (lane & 15u) * 8u;
+  const uint32_t pair_base = (uint32_t)__cvta_generic_to_shared(s_pair) + (lane % REP) * 8u;
+  const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&sh.sign[li][0]);
   const float cD = p.wht_scale;
   const float2 cD2 = make_float2(cD, cD);
   const uint32_t nv = p.nv;
-  for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
-    const Seg s = plan_segment(p, i, kDecode);
-    if (s.action != kProcess) {
-      if (s.action == kReport && threadIdx.x == 0 && p.result) p.result[i] = s.status;
-      continue;
+  const uint32_t stride = gridDim.x * W;
+
+  // codes and norm of vector j of segment s (registers; issued ahead of use)
+  auto fetch = [&](const Seg& s, uint32_t j, uint32_t (&cw)[4], uint16_t& n16) {
+    cw[0] = cw[1] = cw[2] = cw[3] = 0;
+    n16 = 0;
+    if (j < nv) {
+      const uint8_t* vc = s.slot + (uint64_t)j * CB;
+      if (BITS == 4) {
+        const uint4 t = ld_nc16(vc + 16 * li);
+        cw[0] = t.x; cw[1] = t.y; cw[2] = t.z; cw[3] = t.w;
+      } else {
+        cw[0] = ld_nc4(vc + 12 * li);
+        cw[1] = ld_nc4(vc + 12 * li + 4);
+        cw[2] = ld_nc4(vc + 12 * li + 8);
+      }
+      n16 = ld_nc2(s.slot + (uint64_t)nv * CB + (uint64_t)j * 2);
     }
-    const uint8_t* codes = s.slot;
-    const uint8_t* meta = s.slot + (uint64_t)nv * CB;
-    uint16_t* page = const_cast<uint16_t*>(s.page);
-    for (uint32_t j0 = warp * VPW; j0 < nv; j0 += STEP) {
+  };
+
+  Seg cur;
+  uint32_t ci = next_segment<kDecode>(p, blockIdx.x * W + warp, stride, lane, cur);
+  uint32_t cwn[4];
+  uint16_t nn;
+  if (ci != 0xffffffffu) fetch(cur, grp, cwn, nn);
+  while (ci != 0xffffffffu) {
+    uint16_t* page = const_cast<uint16_t*>(cur.page);
+    Seg nxt;
+    uint32_t ni = 0xffffffffu;
+    for (uint32_t j0 = 0; j0 < nv; j0 += VPW) {
       const uint32_t j = j0 + grp;
-      const bool in = j < nv;
-      const uint8_t* vc = codes + (uint64_t)j * CB;
-      uint32_t cw[4] = {0, 0, 0, 0};
-      uint16_t n16 = 0;
-      if (in) {
-        if (BITS == 4) {
-          const uint4 t = ld_nc16(vc + 16 * li);
-          cw[0] = t.x; cw[1] = t.y; cw[2] = t.z; cw[3] = t.w;
-        } else {
-          cw[0] = ld_nc4(vc + 12 * li);
-          cw[1] = ld_nc4(vc + 12 * li + 4);
-          cw[2] = ld_nc4(vc + 12 * li + 8);
-        }
-        n16 = ld_nc2(meta + (uint64_t)j * 2);
+      const uint32_t cw[4] = {cwn[0], cwn[1], cwn[2], cwn[3]};
+      const uint16_t n16 = nn;
+      if (j0 + VPW < nv) {
+        fetch(cur, j0 + VPW + grp, cwn, nn);
+      } else {
+        ni = next_segment<kDecode>(p, ci + stride, stride, lane, nxt);
+        if (ni != 0xffffffffu) fetch(nxt, grp, cwn, nn);
       }
       float2 a[16];
 #pragma unroll
@@ -258,28 +313,32 @@ __global__ void __launch_bounds__(kThreads) tq_decode_kernel(const __grid_consta
           const int bit = 6 * m;
           v = __funnelshift_r(cw[bit >> 5], cw[(bit >> 5) + 1], bit & 31) & 63u;
         }
-        asm("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(a[m].x), "=f"(a[m].y) : "r"(v * 128u + pair_base));
+        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(a[m].x), "=f"(a[m].y) : "r"(v * (8u * REP) + pair_base));
       }
-      float2 sq[16];
-#pragma unroll
-      for (int m = 0; m < 16; ++m) sq[m] = mul2(a[m], a[m]);
-      const float nc = __fsqrt_rn(vector_sum<G>(sq));
+      const float nc = __fsqrt_rn(vector_sumsq<G>(a));
       const float g = __fdiv_rn(__half2float(__ushort_as_half(n16)), nc);
       const float2 g2 = make_float2(g, g);
       butterflies<G>(a, li);
       uint32_t o[16];
 #pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const float2 t = mul2(mul2(a[m], cD2), g2);
-        o[m] = pack2<DT>(t.x, t.y) ^ smask[m];
+      for (int c = 0; c < 4; ++c) {
+        const uint4 m = lds16(sign_addr + 16u * c);
+        const uint32_t mk[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 t = mul2(mul2(a[4 * c + k], cD2), g2);
+          o[4 * c + k] = pack2<DT>(t.x, t.y) ^ mk[k];
+        }
       }
-      uint16_t* dst = page + (in ? vec_off(p, j) : 0) + kTqE * li;
-      if (in) {
+      if (j < nv) {
+        uint16_t* dst = page + vec_off(p, j) + kTqE * li;
 #pragma unroll
         for (int c = 0; c < 4; ++c) st16(dst + 8 * c, make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]));
       }
     }
-    if (threadIdx.x == 0 && p.result) p.result[i] = KV_SEG_ENCODED;
+    if (lane == 0 && p.result) p.result[ci] = KV_SEG_ENCODED;
+    cur = nxt;
+    ci = ni;
   }
 }
 
