@@ -105,16 +105,15 @@ __device__ __forceinline__ void tq_shared_init(const Params& p, TqShared& sh, bo
   }
 }
 
-// Work of one warp: whole segments, warp w of the grid taking segments w,
-// w + (warps in grid), ...  Segments this launch does not code are reported
-// (lane 0 writes the status or result) or skipped on the way.
+// The segments of one CTA are blockIdx.x, blockIdx.x + gridDim.x, ...  Finds
+// the next one this launch codes at or after i; segments it only reports get
+// their status (encode) or result (decode) from thread 0 on the way.
 template <int DIR>
-__device__ __forceinline__ uint32_t next_segment(const Params& p, uint32_t i, uint32_t stride,
-                                                 uint32_t lane, Seg& s) {
-  for (; i < p.n_segments; i += stride) {
+__device__ __forceinline__ uint32_t next_segment(const Params& p, uint32_t i, Seg& s) {
+  for (; i < p.n_segments; i += gridDim.x) {
     s = plan_segment(p, i, DIR);
     if (s.action == kProcess) return i;
-    if (s.action == kReport && lane == 0) {
+    if (s.action == kReport && threadIdx.x == 0) {
       if (DIR == kEncode) p.status[i] = s.status;
       else if (p.result) p.result[i] = s.status;
     }
@@ -122,17 +121,24 @@ __device__ __forceinline__ uint32_t next_segment(const Params& p, uint32_t i, ui
   return 0xffffffffu;
 }
 
+// A CTA codes one segment at a time; warp w takes vectors w*VPW + (0..VPW-1),
+// then + W*VPW, ...  Each warp keeps its next vector in flight while it
+// computes the current one (cp.async into a per-lane stage for encode,
+// register loads for decode), across segment boundaries too.
 template <int DT, int D, int BITS>
-__global__ void __launch_bounds__(kThreads) tq_encode_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, 3) tq_encode_kernel(const __grid_constant__ Params p) {
   constexpr int G = D / kTqE, VPW = 32 / G, W = kThreads / 32;
   constexpr int CB = D * BITS / 8;
+  constexpr uint32_t CSTEP = W * VPW;
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
   __shared__ TqShared sh;
   // next vector of each lane: 64 bytes, chunk k at slot k ^ ((lane >> 1) & 3)
   // so that the 8 lanes of a 128-bit shared access hit 8 different bank groups
   __shared__ uint4 s_stage[W][32][4];
+  __shared__ uint32_t s_flag[2];
   tq_shared_init(p, sh, true);
+  if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
   __syncthreads();
   const uint32_t lut_base = (uint32_t)__cvta_generic_to_shared(sh.lut) + (lane & 15u) * 8u +
                             (uint32_t)(kLutHalf * 128) - kCellMagicBits * 128u;
@@ -140,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) tq_encode_kernel(const __grid_consta
   const uint32_t swz = (lane >> 1) & 3u;
   const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&sh.sign[li][0]);
   const uint32_t nv = p.nv;
-  const uint32_t stride = gridDim.x * W;
+  const uint32_t jw = warp * VPW + grp;  // this lane's first vector in a segment
 
   auto prefetch = [&](const Seg& s, uint32_t j) {
     if (j < nv) {
@@ -152,15 +158,18 @@ __global__ void __launch_bounds__(kThreads) tq_encode_kernel(const __grid_consta
   };
 
   Seg cur;
-  uint32_t ci = next_segment<kEncode>(p, blockIdx.x * W + warp, stride, lane, cur);
-  if (ci != 0xffffffffu) prefetch(cur, grp);
+  uint32_t ci = next_segment<kEncode>(p, blockIdx.x, cur);
+  if (ci != 0xffffffffu) prefetch(cur, jw);
+  int it = 0;
   while (ci != 0xffffffffu) {
+    Seg nxt;
+    const uint32_t ni = next_segment<kEncode>(p, ci + gridDim.x, nxt);
+    if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
     uint8_t* codes = cur.slot;
     uint8_t* meta = cur.slot + (uint64_t)nv * CB;
     uint32_t flags = 0;
-    Seg nxt;
-    uint32_t ni = 0xffffffffu;
-    for (uint32_t j0 = 0; j0 < nv; j0 += VPW) {
+    if (warp * VPW >= nv && ni != 0xffffffffu) prefetch(nxt, jw);  // no work in this segment
+    for (uint32_t j0 = warp * VPW; j0 < nv; j0 += CSTEP) {
       const uint32_t j = j0 + grp;
       const bool in = j < nv;
       cp_async_wait_all();
@@ -170,12 +179,8 @@ __global__ void __launch_bounds__(kThreads) tq_encode_kernel(const __grid_consta
       float mn, mx;
       vec_minmax<DT, G, 4>(w, mn, mx);
       // the staged data is in registers now: refill the stage with the next vector
-      if (j0 + VPW < nv) {
-        prefetch(cur, j0 + VPW + grp);
-      } else {
-        ni = next_segment<kEncode>(p, ci + stride, stride, lane, nxt);
-        if (ni != 0xffffffffu) prefetch(nxt, grp);
-      }
+      if (j0 + CSTEP < nv) prefetch(cur, j + CSTEP);
+      else if (ni != 0xffffffffu) prefetch(nxt, jw);
       const uint32_t vflags = admission(mn, mx, p.reject_abs);
       flags |= vflags;
       if (vflags) {  // keep NaN / inf out of the arithmetic (the segment stays raw)
@@ -234,18 +239,24 @@ __global__ void __launch_bounds__(kThreads) tq_encode_kernel(const __grid_consta
       }
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
-    for (uint64_t k = (uint64_t)nv * (CB + 2) + lane; k < p.seg_bytes[cur.role]; k += 32) cur.slot[k] = 0;
-    if (lane == 0)
-      p.status[ci] = (flags & 1u) ? KV_SEG_RAW_NONFINITE : (flags & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+    if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
+    zero_padding(cur.slot, (uint64_t)nv * (CB + 2), p.seg_bytes[cur.role]);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint32_t f = s_flag[it & 1];
+      p.status[ci] = (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+    }
+    ++it;
     cur = nxt;
     ci = ni;
   }
 }
 
 template <int DT, int D, int BITS>
-__global__ void __launch_bounds__(kThreads) tq_decode_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_constant__ Params p) {
   constexpr int G = D / kTqE, VPW = 32 / G, W = kThreads / 32;
   constexpr int CB = D * BITS / 8;
+  constexpr uint32_t CSTEP = W * VPW;
   constexpr int NPAIR = BITS == 4 ? 256 : 64;  // table of two consecutive codes
   constexpr int REP = BITS == 4 ? 8 : 16;       // copies (keeps the table within 48 KB of static smem)
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
@@ -264,7 +275,7 @@ __global__ void __launch_bounds__(kThreads) tq_decode_kernel(const __grid_consta
   const float cD = p.wht_scale;
   const float2 cD2 = make_float2(cD, cD);
   const uint32_t nv = p.nv;
-  const uint32_t stride = gridDim.x * W;
+  const uint32_t jw = warp * VPW + grp;
 
   // codes and norm of vector j of segment s (registers; issued ahead of use)
   auto fetch = [&](const Seg& s, uint32_t j, uint32_t (&cw)[4], uint16_t& n16) {
@@ -285,24 +296,21 @@ __global__ void __launch_bounds__(kThreads) tq_decode_kernel(const __grid_consta
   };
 
   Seg cur;
-  uint32_t ci = next_segment<kDecode>(p, blockIdx.x * W + warp, stride, lane, cur);
-  uint32_t cwn[4];
-  uint16_t nn;
-  if (ci != 0xffffffffu) fetch(cur, grp, cwn, nn);
+  uint32_t ci = next_segment<kDecode>(p, blockIdx.x, cur);
+  uint32_t cwn[4] = {0, 0, 0, 0};
+  uint16_t nn = 0;
+  if (ci != 0xffffffffu) fetch(cur, jw, cwn, nn);
   while (ci != 0xffffffffu) {
-    uint16_t* page = const_cast<uint16_t*>(cur.page);
     Seg nxt;
-    uint32_t ni = 0xffffffffu;
-    for (uint32_t j0 = 0; j0 < nv; j0 += VPW) {
+    const uint32_t ni = next_segment<kDecode>(p, ci + gridDim.x, nxt);
+    uint16_t* page = const_cast<uint16_t*>(cur.page);
+    if (warp * VPW >= nv && ni != 0xffffffffu) fetch(nxt, jw, cwn, nn);
+    for (uint32_t j0 = warp * VPW; j0 < nv; j0 += CSTEP) {
       const uint32_t j = j0 + grp;
       const uint32_t cw[4] = {cwn[0], cwn[1], cwn[2], cwn[3]};
       const uint16_t n16 = nn;
-      if (j0 + VPW < nv) {
-        fetch(cur, j0 + VPW + grp, cwn, nn);
-      } else {
-        ni = next_segment<kDecode>(p, ci + stride, stride, lane, nxt);
-        if (ni != 0xffffffffu) fetch(nxt, grp, cwn, nn);
-      }
+      if (j0 + CSTEP < nv) fetch(cur, j + CSTEP, cwn, nn);
+      else if (ni != 0xffffffffu) fetch(nxt, jw, cwn, nn);
       float2 a[16];
 #pragma unroll
       for (int m = 0; m < 16; ++m) {
@@ -336,7 +344,7 @@ __global__ void __launch_bounds__(kThreads) tq_decode_kernel(const __grid_consta
         for (int c = 0; c < 4; ++c) st16(dst + 8 * c, make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]));
       }
     }
-    if (lane == 0 && p.result) p.result[ci] = KV_SEG_ENCODED;
+    if (threadIdx.x == 0 && p.result) p.result[ci] = KV_SEG_ENCODED;
     cur = nxt;
     ci = ni;
   }
