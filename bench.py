@@ -380,7 +380,15 @@ def run_extra(args, device):
             continue
         case = synth.make_case(name, device=device, **kw)
         label = name + (f"_d{kw['head_dim']}" if kw else "")
+        subs = []
         for arm in case.arms:
+            if arm.k_codec != arm.v_codec and len(arm.roles) == 2:
+                # one launch per role: time them apart
+                subs += [synth.Arm(f"{arm.name}.K", arm.k_codec, "none", (0,), arm.protect),
+                         synth.Arm(f"{arm.name}.V", "none", arm.v_codec, (1,), arm.protect)]
+            else:
+                subs.append(arm)
+        for arm in subs:
             a = Arm(case, arm, case.layers, device)
             for _ in range(3):
                 a.encode()
