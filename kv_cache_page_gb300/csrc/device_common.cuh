@@ -225,6 +225,30 @@ __device__ __forceinline__ void vec_minmax(const uint4 (&w)[NC], float& mn, floa
   mx = lo_f32<DT>(b);
 }
 
+// max(|a|, |b|) per half, NaN propagating (the sign of the result is the xor
+// of the input signs and is ignored by the callers)
+template <int DT>
+__device__ __forceinline__ uint32_t absmax_nan2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if (DT == 0) asm("max.NaN.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Largest |x| of the vector held by G lanes (NC chunks each), NaN propagating,
+// as a float (exact).
+template <int DT, int G, int NC>
+__device__ __forceinline__ float vec_absmax(const uint4 (&w)[NC]) {
+  uint32_t a = absmax_nan2<DT>(absmax_nan2<DT>(w[0].x, w[0].y), absmax_nan2<DT>(w[0].z, w[0].w));
+#pragma unroll
+  for (int c = 1; c < NC; ++c)
+    a = absmax_nan2<DT>(a, absmax_nan2<DT>(absmax_nan2<DT>(w[c].x, w[c].y), absmax_nan2<DT>(w[c].z, w[c].w)));
+#pragma unroll
+  for (int o = 1; o < G; o <<= 1) a = absmax_nan2<DT>(a, __shfl_xor_sync(0xffffffffu, a, o));
+  a = absmax_nan2<DT>(a, __byte_perm(a, 0, 0x1032));
+  return fabsf(lo_f32<DT>(a));
+}
+
 // Chunk assignment for the order-free codecs (FP8, uniform): the vector's
 // 16-byte chunks c = 0 .. D/8-1 are dealt round-robin to its G lanes, lane li
 // holding chunks li, li + G, ... (NC of them), so one warp load instruction
@@ -239,35 +263,16 @@ struct ChunkMap {
 };
 
 // ---------------------------------------------------------------- packed FP32x2
-// One instruction on two independent FP32 lanes, each rounded as its scalar
-// counterpart (sm_100+ packed FP32 arithmetic).
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  float2 d;
-  asm("{ .reg .b64 ra, rb, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5};"
-      " mul.rn.f32x2 rd, ra, rb; mov.b64 {%0, %1}, rd; }"
-      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  float2 d;
-  asm("{ .reg .b64 ra, rb, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5};"
-      " add.rn.f32x2 rd, ra, rb; mov.b64 {%0, %1}, rd; }"
-      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-  float2 d;
-  asm("{ .reg .b64 ra, rb, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5};"
-      " sub.rn.f32x2 rd, ra, rb; mov.b64 {%0, %1}, rd; }"
-      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{ .reg .b64 ra, rb, rc, rd; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5};"
-      " mov.b64 rc, {%6, %7}; fma.rn.f32x2 rd, ra, rb, rc; mov.b64 {%0, %1}, rd; }"
-      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
+// One instruction on two independent FP32 lanes, each rounded to nearest-even
+// as its scalar counterpart (sm_100+ packed FP32 arithmetic).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __fadd2_rn(a, make_float2(-b.x, -b.y)); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+// Admission flags of one vector from its largest |x|: bit 0 nonfinite, bit 1 range.
+__device__ __forceinline__ uint32_t admission_abs(float amax, float reject) {
+  return isfinite(amax) ? (amax > reject ? 2u : 0u) : 1u;
 }
 
 // Admission flags of one vector from its min/max: bit 0 nonfinite, bit 1 range.

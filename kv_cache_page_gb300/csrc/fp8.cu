@@ -99,12 +99,11 @@ __global__ void __launch_bounds__(kThreads) fp8_encode_kernel(const __grid_const
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint32_t j = j0 + u * VPW + grp;
-        float mn, mx;
-        vec_minmax<DT, G, NC>(w[u], mn, mx);
-        flags |= admission(mn, mx, p.reject_abs);
+        const float amax = vec_absmax<DT, G, NC>(w[u]);
+        flags |= admission_abs(amax, p.reject_abs);
         float sc = fixed, nr = fixed_nr;
         if (CODEC == KV_CODEC_FP8_DYNAMIC) {
-          sc = __fmul_rn(fmaxf(fmaxf(-mn, mx), 1e-12f), kRecip448);
+          sc = __fmul_rn(fmaxf(amax, 1e-12f), kRecip448);
           nr = -__frcp_rn(sc);
         }
         const bool in = j < nv;

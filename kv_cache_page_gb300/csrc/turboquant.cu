@@ -176,12 +176,11 @@ __global__ void __launch_bounds__(kThreads, 3) tq_encode_kernel(const __grid_con
       uint4 w[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) w[k] = in ? lds16(stage + 16u * ((uint32_t)k ^ swz)) : make_uint4(0, 0, 0, 0);
-      float mn, mx;
-      vec_minmax<DT, G, 4>(w, mn, mx);
+      const float amax = vec_absmax<DT, G, 4>(w);
       // the staged data is in registers now: refill the stage with the next vector
       if (j0 + CSTEP < nv) prefetch(cur, j + CSTEP);
       else if (ni != 0xffffffffu) prefetch(nxt, jw);
-      const uint32_t vflags = admission(mn, mx, p.reject_abs);
+      const uint32_t vflags = admission_abs(amax, p.reject_abs);
       flags |= vflags;
       if (vflags) {  // keep NaN / inf out of the arithmetic (the segment stays raw)
 #pragma unroll
