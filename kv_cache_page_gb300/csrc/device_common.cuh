@@ -33,16 +33,27 @@ struct Seg {
 };
 
 // Decide what this CTA does with segment i.  Uniform across the CTA.
+// Ownership: a launch that codes one role (role_sel 0 or 1) owns the
+// descriptors of that role; the first launch also owns descriptors with an
+// invalid role or a role without codec.  Descriptors of the other coded role
+// are skipped after reading just the role field.
 __device__ __forceinline__ Seg plan_segment(const Params& p, uint32_t i, int dir) {
   Seg s;
   const kv_segment_desc* dp = p.descs + i;
-  const uint32_t layer = __ldg(&dp->layer), block = __ldg(&dp->block), role = __ldg(&dp->role);
-  const uint64_t off = __ldg(reinterpret_cast<const unsigned long long*>(&dp->enc_offset));
+  const uint32_t role = __ldg(&dp->role);
   s.role = role;
-  s.layer = layer;
   s.page = nullptr;
   s.slot = nullptr;
   s.status = 0;
+  const bool coded_role = role <= 1u && p.codec[role] != KV_CODEC_NONE;
+  const bool owner = coded_role ? (p.role_sel == 2u || role == p.role_sel) : (p.is_first != 0u);
+  if (!owner) {
+    s.action = kSkip;
+    return s;
+  }
+  const uint32_t layer = __ldg(&dp->layer), block = __ldg(&dp->block);
+  const uint64_t off = __ldg(reinterpret_cast<const unsigned long long*>(&dp->enc_offset));
+  s.layer = layer;
   bool ok = layer < p.L && role <= 1u && (uint64_t)block < p.num_blocks && (off & 15u) == 0;
   const void* base = nullptr;
   if (ok) {
@@ -50,36 +61,27 @@ __device__ __forceinline__ Seg plan_segment(const Params& p, uint32_t i, int dir
     const uint64_t need = p.seg_bytes[role];
     ok = base != nullptr && off <= p.buf_bytes && need <= p.buf_bytes - off;
   }
-  const uint8_t bad = (uint8_t)KV_SEG_BAD_DESC;
+  s.action = kReport;
   if (!ok) {
-    s.action = p.is_first ? kReport : kSkip;
-    s.status = bad;
+    s.status = (uint8_t)KV_SEG_BAD_DESC;
     return s;
   }
-  if (p.codec[role] == KV_CODEC_NONE) {
-    s.action = p.is_first ? kReport : kSkip;
-    s.status = dir == kEncode ? (uint8_t)KV_SEG_RAW_POLICY : bad;
-    return s;
-  }
-  if (p.role_sel != 2u && role != p.role_sel) {
-    s.action = kSkip;
+  if (!coded_role) {
+    s.status = dir == kEncode ? (uint8_t)KV_SEG_RAW_POLICY : (uint8_t)KV_SEG_BAD_DESC;
     return s;
   }
   if (dir == kEncode) {
     if (layer < p.protect_first || layer + p.protect_last >= p.L) {
-      s.action = kReport;
       s.status = (uint8_t)KV_SEG_RAW_PROTECTED;
       return s;
     }
     if (p.static_status[role]) {
-      s.action = kReport;
       s.status = p.static_status[role];
       return s;
     }
   } else {
     const uint8_t st = __ldg(p.status + i);
     if (st != (uint8_t)KV_SEG_ENCODED) {
-      s.action = kReport;
       s.status = st;
       return s;
     }

@@ -35,22 +35,27 @@ __device__ __forceinline__ uint32_t sign_mask_word(uint32_t bits, int k) {
   return (((bits >> (2 * k)) & 1u) << 15) | (((bits >> (2 * k + 1)) & 1u) << 31);
 }
 
-// Pairwise sum of squares over the vector: squares of the lane's 32 elements
-// summed as an in-thread tree (pairs first), then xor-shuffles over the G
-// lanes with ascending distance.
+// Pairwise sum of the squares of pairs [M0, M0 + N) (2N elements), written
+// depth first so that few partial sums are live at a time.
+template <int M0, int N>
+struct PairSumSq {
+  static __device__ __forceinline__ float run(const float2 (&a)[16]) {
+    if constexpr (N == 1) {
+      const float2 q = mul2(a[M0], a[M0]);
+      return __fadd_rn(q.x, q.y);
+    } else {
+      const float lo = PairSumSq<M0, N / 2>::run(a);
+      const float hi = PairSumSq<M0 + N / 2, N / 2>::run(a);
+      return __fadd_rn(lo, hi);
+    }
+  }
+};
+
+// Pairwise sum of squares over the vector: the lane's 32 elements as an
+// in-thread tree, then xor-shuffles over the G lanes with ascending distance.
 template <int G>
 __device__ __forceinline__ float vector_sumsq(const float2 (&a)[16]) {
-  float s[16];
-#pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    const float2 q = mul2(a[m], a[m]);
-    s[m] = __fadd_rn(q.x, q.y);
-  }
-#pragma unroll
-  for (int w = 1; w < 16; w <<= 1)
-#pragma unroll
-    for (int m = 0; m < 16; m += 2 * w) s[m] = __fadd_rn(s[m], s[m + w]);
-  float c = s[0];
+  float c = PairSumSq<0, 16>::run(a);
 #pragma unroll
   for (int o = 1; o < G; o <<= 1) c = __fadd_rn(c, __shfl_xor_sync(0xffffffffu, c, o));
   return c;
