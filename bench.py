@@ -372,14 +372,19 @@ def run_extra(args, device):
     """Per-arm encode / decode raw-KV GB/s on the other workloads (context lines;
     the headline is the default workload)."""
     out = {}
-    specs = [("tiny", {}), ("vllm_packed", {}), ("head_dim_sweep", {"head_dim": 32}),
-             ("head_dim_sweep", {"head_dim": 64}), ("head_dim_sweep", {"head_dim": 128}),
-             ("head_dim_sweep", {"head_dim": 256}), ("qwen25_7b_offload", {})]
+    # the head-dim sweep is one layer in its parity form; for timing it is spread
+    # over 64 layers of the same law so that the data (0.5-4 GB) is far larger
+    # than the 129 MB L2
+    specs = [("tiny", {}), ("vllm_packed", {}),
+             ("head_dim_sweep", {"head_dim": 32, "num_layers": 64}),
+             ("head_dim_sweep", {"head_dim": 64, "num_layers": 64}),
+             ("head_dim_sweep", {"head_dim": 128, "num_layers": 64}),
+             ("head_dim_sweep", {"head_dim": 256, "num_layers": 64}), ("qwen25_7b_offload", {})]
     for name, kw in specs:
         if name == args.workload and not kw:
             continue
         case = synth.make_case(name, device=device, **kw)
-        label = name + (f"_d{kw['head_dim']}" if kw else "")
+        label = name + (f"_d{kw['head_dim']}_x{kw['num_layers']}" if kw else "")
         subs = []
         for arm in case.arms:
             if arm.k_codec != arm.v_codec and len(arm.roles) == 2:

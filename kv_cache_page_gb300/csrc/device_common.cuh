@@ -40,8 +40,11 @@ struct Seg {
 __device__ __forceinline__ Seg plan_segment(const Params& p, uint32_t i, int dir) {
   Seg s;
   const kv_segment_desc* dp = p.descs + i;
-  const uint32_t role = __ldg(&dp->role);
+  // all fields in one round trip
+  const uint32_t layer = __ldg(&dp->layer), block = __ldg(&dp->block), role = __ldg(&dp->role);
+  const uint64_t off = __ldg(reinterpret_cast<const unsigned long long*>(&dp->enc_offset));
   s.role = role;
+  s.layer = layer;
   s.page = nullptr;
   s.slot = nullptr;
   s.status = 0;
@@ -51,9 +54,6 @@ __device__ __forceinline__ Seg plan_segment(const Params& p, uint32_t i, int dir
     s.action = kSkip;
     return s;
   }
-  const uint32_t layer = __ldg(&dp->layer), block = __ldg(&dp->block);
-  const uint64_t off = __ldg(reinterpret_cast<const unsigned long long*>(&dp->enc_offset));
-  s.layer = layer;
   bool ok = layer < p.L && role <= 1u && (uint64_t)block < p.num_blocks && (off & 15u) == 0;
   const void* base = nullptr;
   if (ok) {
@@ -92,6 +92,48 @@ __device__ __forceinline__ Seg plan_segment(const Params& p, uint32_t i, int dir
   s.slot = p.buf + off;
   s.action = kProcess;
   return s;
+}
+
+// The segments of a CTA are blockIdx.x, blockIdx.x + gridDim.x, ...  A cursor
+// plans 32 upcoming candidates at once, one per lane (every warp of the CTA
+// holds the same cursor), writes the status (encode) or result (decode) of
+// those the launch only reports (warp 0 does the writing), and hands out the
+// ones it codes in order, re-planning each from its (now cached) descriptor.
+// The descriptor loads from memory are paid once per 32 segments.
+struct SegCursor {
+  uint32_t base;   // candidate index of lane 0
+  uint32_t mask;   // candidates of this batch still to hand out
+};
+
+__device__ __forceinline__ void cursor_init(SegCursor& c) {
+  c.base = blockIdx.x;
+  c.mask = 0;
+}
+
+// Next segment index to code (and its plan in s), or 0xffffffff when done.
+template <int DIR>
+__device__ __forceinline__ uint32_t cursor_next(const Params& p, SegCursor& c, Seg& s) {
+  while (c.mask == 0u) {
+    if (c.base >= p.n_segments) return 0xffffffffu;
+    const uint32_t i = c.base + (threadIdx.x & 31u) * gridDim.x;
+    bool go = false;
+    if (i < p.n_segments) {
+      const Seg m = plan_segment(p, i, DIR);
+      go = m.action == kProcess;
+      if (m.action == kReport && threadIdx.x < 32u) {
+        if (DIR == kEncode) p.status[i] = m.status;
+        else if (p.result) p.result[i] = m.status;
+      }
+    }
+    c.mask = __ballot_sync(0xffffffffu, go);
+    if (c.mask == 0u) c.base += 32u * gridDim.x;
+  }
+  const uint32_t k = (uint32_t)(__ffs(c.mask) - 1);
+  c.mask &= c.mask - 1u;
+  const uint32_t idx = c.base + k * gridDim.x;
+  if (c.mask == 0u) c.base += 32u * gridDim.x;
+  s = plan_segment(p, idx, DIR);
+  return idx;
 }
 
 // Element offset of vector j (token-major) inside its page.
@@ -358,11 +400,14 @@ __device__ __forceinline__ uint32_t load_3bit(const uint8_t* src, uint32_t c) {
   return __funnelshift_r(lo, hi, bit & 31u) & 0xffffffu;
 }
 
-// Launch a codec kernel (signature void(Params)) on the caller's stream.
+// Launch a codec kernel (signature void(Params)) on the caller's stream with
+// at most `max_per_sm` resident CTAs per SM.  The caps come from sweeps on a
+// GB300 (one CTA codes one segment): the write-heavy decodes stream best with
+// few CTAs per SM, the encodes with more.
 template <typename K>
-inline int launch_codec_kernel(K kernel, const Params& p, void* stream) {
+inline int launch_codec_kernel(K kernel, const Params& p, void* stream, int max_per_sm) {
   unsigned grid = 0;
-  const int rc = grid_for(reinterpret_cast<const void*>(kernel), p.n_segments, &grid);
+  const int rc = grid_for(reinterpret_cast<const void*>(kernel), p.n_segments, max_per_sm, &grid);
   if (rc != KV_OK || grid == 0) return rc;
   void* args[] = {const_cast<Params*>(&p)};
   const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(kernel), dim3(grid),

@@ -18,6 +18,8 @@ namespace kvc {
 namespace {
 
 constexpr float kRecip448 = 1.0f / 448.0f;  // fl32(1/448)
+constexpr int kEncodeCtas = 6;  // resident CTAs per SM (see launch_codec_kernel)
+constexpr int kDecodeCtas = 3;
 
 // four floats -> four E4M3FN bytes (first element in the low byte), RNE,
 // saturating to +-448 (the clip); NaN stays NaN
@@ -197,15 +199,15 @@ template <int DT, int D>
 int dispatch_mode(const Params& p, int dir, uint32_t codec, void* stream) {
   if (dir == kEncode) {
     switch (codec) {
-      case KV_CODEC_FP8_CAST: return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_CAST>, p, stream);
-      case KV_CODEC_FP8_FIXED: return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_FIXED>, p, stream);
-      case KV_CODEC_FP8_DYNAMIC: return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_DYNAMIC>, p, stream);
+      case KV_CODEC_FP8_CAST: return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_CAST>, p, stream, kEncodeCtas);
+      case KV_CODEC_FP8_FIXED: return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_FIXED>, p, stream, kEncodeCtas);
+      case KV_CODEC_FP8_DYNAMIC: return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_DYNAMIC>, p, stream, kEncodeCtas);
     }
   } else {
     switch (codec) {
-      case KV_CODEC_FP8_CAST: return launch_codec_kernel(fp8_decode_kernel<DT, D, KV_CODEC_FP8_CAST>, p, stream);
-      case KV_CODEC_FP8_FIXED: return launch_codec_kernel(fp8_decode_kernel<DT, D, KV_CODEC_FP8_FIXED>, p, stream);
-      case KV_CODEC_FP8_DYNAMIC: return launch_codec_kernel(fp8_decode_kernel<DT, D, KV_CODEC_FP8_DYNAMIC>, p, stream);
+      case KV_CODEC_FP8_CAST: return launch_codec_kernel(fp8_decode_kernel<DT, D, KV_CODEC_FP8_CAST>, p, stream, kDecodeCtas);
+      case KV_CODEC_FP8_FIXED: return launch_codec_kernel(fp8_decode_kernel<DT, D, KV_CODEC_FP8_FIXED>, p, stream, kDecodeCtas);
+      case KV_CODEC_FP8_DYNAMIC: return launch_codec_kernel(fp8_decode_kernel<DT, D, KV_CODEC_FP8_DYNAMIC>, p, stream, kDecodeCtas);
     }
   }
   return KV_ERR_INVALID_ARG;

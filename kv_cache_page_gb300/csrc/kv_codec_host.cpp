@@ -214,7 +214,7 @@ int check_call(kv_codec_s* h, const void* const* layer_ptrs, uint32_t n_layer_pt
 }  // namespace
 
 namespace kvc {
-int grid_for(const void* kernel, uint32_t n_segments, unsigned* grid) {
+int grid_for(const void* kernel, uint32_t n_segments, int max_per_sm, unsigned* grid) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
   int sms = 0, occ = 0;
@@ -237,7 +237,8 @@ int grid_for(const void* kernel, uint32_t n_segments, unsigned* grid) {
     std::lock_guard<std::mutex> lk(g_mu);
     g_occ[{dev, kernel}] = occ;
   }
-  uint64_t g = std::min<uint64_t>((uint64_t)sms * (uint64_t)occ, n_segments);
+  const int per_sm = std::max(1, std::min(occ, max_per_sm));
+  uint64_t g = std::min<uint64_t>((uint64_t)sms * (uint64_t)per_sm, n_segments);
   // An odd stride deals segments of both roles to every CTA when K and V
   // segments alternate in the descriptor list (a launch that codes one role
   // only skips the other role's segments).

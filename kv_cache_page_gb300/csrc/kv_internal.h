@@ -72,9 +72,9 @@ int launch_fp8(const Params& p, int dir, uint32_t codec, void* stream);
 int launch_uniform(const Params& p, int dir, uint32_t codec, void* stream);
 int launch_turboquant(const Params& p, int dir, uint32_t codec, void* stream);
 
-// Grid size for a codec kernel over n segments: one CTA per segment up to the
-// number of CTAs the device keeps resident (SM count x occupancy, cached per
-// device and kernel).  Defined in the host library.
-int grid_for(const void* kernel, uint32_t n_segments, unsigned* grid);
+// Grid size for a codec kernel over n segments: one CTA per segment up to
+// SM count x resident CTAs per SM, the latter the occupancy limit (cached per
+// device and kernel) capped at `max_per_sm`.  Defined in the host library.
+int grid_for(const void* kernel, uint32_t n_segments, int max_per_sm, unsigned* grid);
 
 }  // namespace kvc

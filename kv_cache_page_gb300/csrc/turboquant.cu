@@ -110,22 +110,6 @@ __device__ __forceinline__ void tq_shared_init(const Params& p, TqShared& sh, bo
   }
 }
 
-// The segments of one CTA are blockIdx.x, blockIdx.x + gridDim.x, ...  Finds
-// the next one this launch codes at or after i; segments it only reports get
-// their status (encode) or result (decode) from thread 0 on the way.
-template <int DIR>
-__device__ __forceinline__ uint32_t next_segment(const Params& p, uint32_t i, Seg& s) {
-  for (; i < p.n_segments; i += gridDim.x) {
-    s = plan_segment(p, i, DIR);
-    if (s.action == kProcess) return i;
-    if (s.action == kReport && threadIdx.x == 0) {
-      if (DIR == kEncode) p.status[i] = s.status;
-      else if (p.result) p.result[i] = s.status;
-    }
-  }
-  return 0xffffffffu;
-}
-
 // A CTA codes one segment at a time; warp w takes vectors w*VPW + (0..VPW-1),
 // then + W*VPW, ...  Each warp keeps its next vector in flight while it
 // computes the current one (cp.async into a per-lane stage for encode,
@@ -162,13 +146,15 @@ __global__ void __launch_bounds__(kThreads, 3) tq_encode_kernel(const __grid_con
     cp_async_commit();
   };
 
+  SegCursor cursor;
+  cursor_init(cursor);
   Seg cur;
-  uint32_t ci = next_segment<kEncode>(p, blockIdx.x, cur);
+  uint32_t ci = cursor_next<kEncode>(p, cursor, cur);
   if (ci != 0xffffffffu) prefetch(cur, jw);
   int it = 0;
   while (ci != 0xffffffffu) {
     Seg nxt;
-    const uint32_t ni = next_segment<kEncode>(p, ci + gridDim.x, nxt);
+    const uint32_t ni = cursor_next<kEncode>(p, cursor, nxt);
     if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
     uint8_t* codes = cur.slot;
     uint8_t* meta = cur.slot + (uint64_t)nv * CB;
@@ -299,14 +285,16 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
     }
   };
 
+  SegCursor cursor;
+  cursor_init(cursor);
   Seg cur;
-  uint32_t ci = next_segment<kDecode>(p, blockIdx.x, cur);
+  uint32_t ci = cursor_next<kDecode>(p, cursor, cur);
   uint32_t cwn[4] = {0, 0, 0, 0};
   uint16_t nn = 0;
   if (ci != 0xffffffffu) fetch(cur, jw, cwn, nn);
   while (ci != 0xffffffffu) {
     Seg nxt;
-    const uint32_t ni = next_segment<kDecode>(p, ci + gridDim.x, nxt);
+    const uint32_t ni = cursor_next<kDecode>(p, cursor, nxt);
     uint16_t* page = const_cast<uint16_t*>(cur.page);
     if (warp * VPW >= nv && ni != 0xffffffffu) fetch(nxt, jw, cwn, nn);
     for (uint32_t j0 = warp * VPW; j0 < nv; j0 += CSTEP) {
@@ -359,11 +347,11 @@ int dispatch_bits(const Params& p, int dir, uint32_t codec, void* stream) {
   const bool enc = dir == kEncode;
   switch (codec) {
     case KV_CODEC_TQ3:
-      return enc ? launch_codec_kernel(tq_encode_kernel<DT, D, 3>, p, stream)
-                 : launch_codec_kernel(tq_decode_kernel<DT, D, 3>, p, stream);
+      return enc ? launch_codec_kernel(tq_encode_kernel<DT, D, 3>, p, stream, 8)
+                 : launch_codec_kernel(tq_decode_kernel<DT, D, 3>, p, stream, 8);
     case KV_CODEC_TQ4:
-      return enc ? launch_codec_kernel(tq_encode_kernel<DT, D, 4>, p, stream)
-                 : launch_codec_kernel(tq_decode_kernel<DT, D, 4>, p, stream);
+      return enc ? launch_codec_kernel(tq_encode_kernel<DT, D, 4>, p, stream, 8)
+                 : launch_codec_kernel(tq_decode_kernel<DT, D, 4>, p, stream, 8);
   }
   return KV_ERR_INVALID_ARG;
 }

@@ -13,29 +13,42 @@ namespace {
 
 #define LV(b) ((1u << (b)) - 1u)
 
-// round to nearest-even integer and saturate to [0, 255]
-__device__ __forceinline__ uint32_t rint_sat_u8(float q) {
-  uint32_t d;
-  asm("cvt.rni.sat.u8.f32 %0, %1;" : "=r"(d) : "f"(q));
-  return d & 0xffu;
-}
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr int kEncodeCtas = 5;  // resident CTAs per SM (see launch_codec_kernel)
+constexpr int kDecodeCtas = 5;
 
-// codes of 8 elements: clamp(rint((x - m) / s), 0, L), the quotient correctly
-// rounded (q0 = RN(d r), e = RN(d - q0 s) exact, q = RN(q0 + e r)); 0 if s == 0
+// Codes of 8 elements: clamp(rint((x - m) / s), 0, L).  The quotient is
+// correctly rounded (q0 = RN(d r), e = RN(d - q0 s) exact, q = RN(q0 + e r));
+// clamping to [0, L] before rounding gives the same integer (0 and L are
+// integers), and RN(q + 1.5 * 2^23) holds rint(q) in its low byte.  The caller
+// passes r = 0 when s == 0, which makes every quotient 0.
 template <uint32_t LEVELS>
 __device__ __forceinline__ void uniform_codes8(const float (&x)[8], float m, float sc, float r,
                                                uint32_t (&c)[8]) {
   const float2 m2 = make_float2(m, m), ns2 = make_float2(-sc, -sc), r2 = make_float2(r, r);
+  const float2 mg2 = make_float2(kRoundMagic, kRoundMagic);
 #pragma unroll
   for (int e = 0; e < 8; e += 2) {
     const float2 d = sub2(make_float2(x[e], x[e + 1]), m2);
     const float2 q0 = mul2(d, r2);
     const float2 res = fma2(q0, ns2, d);
-    const float2 q = fma2(res, r2, q0);
-    const uint32_t a = rint_sat_u8(q.x), b = rint_sat_u8(q.y);
-    c[e] = sc == 0.0f ? 0u : (a < LEVELS ? a : LEVELS);
-    c[e + 1] = sc == 0.0f ? 0u : (b < LEVELS ? b : LEVELS);
+    float2 q = fma2(res, r2, q0);
+    q.x = fminf(fmaxf(q.x, 0.0f), (float)LEVELS);
+    q.y = fminf(fmaxf(q.y, 0.0f), (float)LEVELS);
+    const float2 t = add2(q, mg2);
+    c[e] = __float_as_uint(t.x) & 0xffu;
+    c[e + 1] = __float_as_uint(t.y) & 0xffu;
   }
+}
+
+// (max - min) / L correctly rounded, from the rounded reciprocal of L
+template <uint32_t LEVELS>
+__device__ __forceinline__ float div_levels(float range) {
+  constexpr float L = (float)LEVELS;
+  constexpr float rL = 1.0f / (float)LEVELS;
+  const float q0 = __fmul_rn(range, rL);
+  const float e = __fmaf_rn(-q0, L, range);
+  return __fmaf_rn(e, rL, q0);
 }
 
 template <int DT, int D, int BITS>
@@ -81,9 +94,9 @@ __global__ void __launch_bounds__(kThreads) uniform_encode_kernel(const __grid_c
         mn = __fadd_rn(mn, 0.0f);  // a zero minimum / maximum is +0
         mx = __fadd_rn(mx, 0.0f);
         const __half m16 = __float2half_rn(mn);
-        const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), (float)LEVELS));
+        const __half s16 = __float2half_rn(div_levels<LEVELS>(__fsub_rn(mx, mn)));
         const float m = __half2float(m16), sc = __half2float(s16);
-        const float r = __frcp_rn(sc);
+        const float r = sc == 0.0f ? 0.0f : __frcp_rn(sc);
         const bool in = j < nv;
         uint8_t* vc = codes + (uint64_t)j * CB;
 #pragma unroll
@@ -206,14 +219,14 @@ int dispatch_bits(const Params& p, int dir, uint32_t codec, void* stream) {
   const bool enc = dir == kEncode;
   switch (codec) {
     case KV_CODEC_UNIFORM3:
-      return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 3>, p, stream)
-                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 3>, p, stream);
+      return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 3>, p, stream, kEncodeCtas)
+                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 3>, p, stream, kDecodeCtas);
     case KV_CODEC_UNIFORM4:
-      return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 4>, p, stream)
-                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 4>, p, stream);
+      return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 4>, p, stream, kEncodeCtas)
+                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 4>, p, stream, kDecodeCtas);
     case KV_CODEC_UNIFORM8:
-      return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 8>, p, stream)
-                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 8>, p, stream);
+      return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 8>, p, stream, kEncodeCtas)
+                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 8>, p, stream, kDecodeCtas);
   }
   return KV_ERR_INVALID_ARG;
 }
