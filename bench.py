@@ -286,6 +286,9 @@ def run_gpu(args, dist, world, rank, local):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, arms, stream, dist)
+    host_link = None
+    if args.host_link and world == 1:
+        host_link = run_host_link(args, arms, stream)
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -305,6 +308,7 @@ def run_gpu(args, dist, world, rank, local):
         "gpu_launches": len(events),
         "clocks": clk,
         "e2e": e2e,
+        "host_link": host_link,
     }
     shrunk = args.layers is not None or args.pages is not None or args.arm is not None
     if shrunk:
@@ -366,6 +370,64 @@ def run_e2e(args, arms, stream, dist):
     value = sum_over_ranks(dist, raw * steps) / sec / GB
     return {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def run_host_link(args, arms, stream):
+    """Offload and restore with the encoded slots in pinned host memory, per arm:
+    zero-copy (the kernels store the slots and statuses into host memory, or load
+    them from there, through its device mapping: NVLink-C2C on GB300) against
+    staged (device slots + one cudaMemcpyAsync of the slot buffer each way).
+    Median of CUDA-event timings on the launching stream; GB/s of raw KV, and of
+    host-link bytes (slots + statuses)."""
+    out = {}
+    reps = max(3, min(args.steps, 10))
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    for a in arms:
+        enc_h = torch.empty(a.total, dtype=torch.uint8).pin_memory()
+        st_h = torch.empty(a.n, dtype=torch.uint8).pin_memory()
+        link = a.total + a.n
+
+        def off_zero():
+            a.codec.encode(a.src_view, a.descs, a.n, enc_h, a.total, st_h, stream)
+
+        def res_zero():
+            a.codec.decode(a.dst_view, a.descs, a.n, enc_h, a.total, st_h, None, stream)
+
+        def off_staged():
+            a.encode(stream)
+            enc_h.copy_(a.enc, non_blocking=True)
+            st_h.copy_(a.status, non_blocking=True)
+
+        def res_staged():
+            a.enc.copy_(enc_h, non_blocking=True)
+            a.status.copy_(st_h, non_blocking=True)
+            a.decode(stream)
+
+        res = {}
+        for tag, fn in (("offload_zero_copy", off_zero), ("restore_zero_copy", res_zero),
+                        ("offload_staged", off_staged), ("restore_staged", res_staged)):
+            ms = timed(fn)
+            res[tag] = {"ms": round(ms, 4), "raw_gbs": round(a.raw_bytes / (ms / 1e3) / GB, 1),
+                        "link_gbs": round(link / (ms / 1e3) / GB, 1)}
+        res["link_bytes"] = link
+        out[a.arm.name] = res
+        del enc_h, st_h
+    return out
 
 
 def run_extra(args, device):
@@ -518,6 +580,8 @@ def main(argv=None):
     ap.add_argument("--no-extra", dest="extra", action="store_false")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-host-link", dest="host_link", action="store_false",
+                    help="skip the host-resident slot offload/restore timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)

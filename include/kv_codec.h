@@ -34,6 +34,22 @@
  * CUDA stream (no synchronisation, no allocation); all buffers belong to the
  * caller and must stay valid until that work completes.
  *
+ * Host-resident slots (offload and restore without staging copies): the
+ * descriptor, slot, status and result buffers of encode/decode may each be
+ * device memory or PINNED host memory (cudaHostAlloc / cudaMallocHost /
+ * cudaHostRegister).  For pinned host memory the kernels load and store the
+ * bytes through its device mapping, i.e. over the CPU-GPU link (NVLink-C2C on
+ * GB300), so an encode writes its slots straight into host memory and a decode
+ * reads them from there and scatters the result into the engine pages.  This
+ * is the restore path of "Q4 KV cache for SGLang HiCache" (section "CPU to GPU:
+ * restoration": compressed copy, dequantization and scatter all enqueued on
+ * the transfer stream before the layer is marked ready) and the "upload encoded
+ * bytes and GPU decode" restore of the OrbitKV docs, with the copy folded into
+ * the kernel.  Stream order gives the ordering: the caller records an event on
+ * the stream it passes and makes the consuming stream wait on it.  Pageable
+ * host memory is refused (KV_ERR_NOT_ACCESSIBLE).  The engine pages
+ * (layer_ptrs) are device memory.
+ *
  * All functions return KV_OK (0) or a negative KV_ERR_* code and never abort.
  */
 #ifndef KV_CODEC_H
@@ -59,6 +75,7 @@ extern "C" {
 #define KV_ERR_CUDA -6                 /* a CUDA runtime call failed (launch, device query) */
 #define KV_ERR_ABI -7                  /* abi_version / struct_size mismatch */
 #define KV_ERR_TOO_MANY_LAYERS -8      /* num_layers = 0 or > KV_CODEC_MAX_LAYERS */
+#define KV_ERR_NOT_ACCESSIBLE -9       /* a buffer is pageable host memory (not pinned) */
 
 /* ---- enums ------------------------------------------------------------- */
 #define KV_DT_FP16 1u
@@ -155,9 +172,10 @@ int kv_codec_segment_bytes(kv_codec_t codec, uint32_t role, uint64_t* enc_bytes,
  *                one per layer (num_layers entries).  NULL entries are allowed for
  *                roles that no descriptor references.
  *   n_layer_ptrs number of entries in layer_ptrs (must match the layout).
- *   d_descs      DEVICE array of n_segments descriptors.
- *   d_out        DEVICE encoded buffer of out_bytes bytes, 16-byte aligned.
- *   d_status     DEVICE array of n_segments status bytes (written for every segment).
+ *   d_descs      array of n_segments descriptors, 8-byte aligned (device or pinned host).
+ *   d_out        encoded buffer of out_bytes bytes, 16-byte aligned (device or pinned host).
+ *   d_status     array of n_segments status bytes, written for every segment
+ *                (device or pinned host).
  *   stream       cudaStream_t (NULL = legacy default stream).
  * Segments are independent; descriptors may repeat a source page but must not
  * overlap slots.  n_segments = 0 is a no-op. */
@@ -167,7 +185,9 @@ int kv_codec_encode(kv_codec_t codec, const void* const* layer_ptrs, uint32_t n_
 
 /* Restore every segment whose status is KV_SEG_ENCODED into the engine layout;
  * all other segments are left untouched (the caller restores them from its raw
- * copy).  d_result (optional DEVICE array of n_segments bytes) receives
+ * copy).  d_descs, d_in (in_bytes bytes, 16-byte aligned), d_status and
+ * d_result may be device or pinned host memory, as for encode.  d_result
+ * (optional array of n_segments bytes) receives
  * KV_SEG_ENCODED for restored segments, KV_SEG_BAD_DESC for invalid descriptors
  * (or a role without codec), and the input status otherwise. */
 int kv_codec_decode(kv_codec_t codec, void* const* layer_ptrs, uint32_t n_layer_ptrs,

@@ -188,14 +188,20 @@ class Codec:
 
     def encode(self, layers, descs, n_segments: int, out, out_bytes: int, status, stream=None):
         """layers: list of device tensors (or pointers; separate: [K0, V0, ...], packed:
-        one per layer); descs: device uint8 tensor of descriptors; out / status: device
-        tensors.  Enqueues on `stream` (default: torch's current stream)."""
+        one per layer); descs: uint8 tensor of descriptors; out / status: tensors.
+        descs, out and status may be device or pinned host tensors (the kernel then
+        writes the slots and statuses straight into host memory).  Enqueues on
+        `stream` (default: torch's current stream)."""
         arr, n = self._layer_array(layers)
         _check(lib().kv_codec_encode(self._h, arr, n, _ptr(descs), n_segments, _ptr(out), out_bytes,
                                      _ptr(status), _stream_handle(stream)), "kv_codec_encode")
 
     def decode(self, layers, descs, n_segments: int, enc, enc_bytes: int, status, result=None,
                stream=None):
+        """Restore ENCODED segments into `layers` (device tensors).  descs, enc, status
+        and result may be device or pinned host tensors (the kernel then reads the slots
+        from host memory itself).  Enqueues on `stream` (default: torch's current
+        stream); make a consuming stream wait on an event recorded after it."""
         arr, n = self._layer_array(layers)
         _check(lib().kv_codec_decode(self._h, arr, n, _ptr(descs), n_segments, _ptr(enc), enc_bytes,
                                      _ptr(status), _ptr(result), _stream_handle(stream)),

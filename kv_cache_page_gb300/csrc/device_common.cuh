@@ -304,6 +304,7 @@ struct ChunkMap {
   static constexpr int G = D / E;               // lanes per vector
   static constexpr int NC = E / 8;              // chunks per lane
   static constexpr int VPW = 32 / G;            // vectors per warp row
+  static constexpr int U = NC == 1 ? 4 : 2;     // warp rows per step: 32 or 64 B of loads per lane
 };
 
 // ---------------------------------------------------------------- packed FP32x2

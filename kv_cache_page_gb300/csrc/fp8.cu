@@ -66,7 +66,7 @@ __device__ __forceinline__ uint2 fp8_codes8(const float (&x)[8], float s, float 
 template <int DT, int D, uint32_t CODEC>
 __global__ void __launch_bounds__(kThreads) fp8_encode_kernel(const __grid_constant__ Params p) {
   using M = ChunkMap<D>;
-  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = 2, W = kThreads / 32;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = kThreads / 32;
   constexpr int STEP = W * VPW * U;
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kThreads) fp8_encode_kernel(const __grid_const
 template <int DT, int D, uint32_t CODEC>
 __global__ void __launch_bounds__(kThreads) fp8_decode_kernel(const __grid_constant__ Params p) {
   using M = ChunkMap<D>;
-  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = 2, W = kThreads / 32;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = kThreads / 32;
   constexpr int STEP = W * VPW * U;
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;

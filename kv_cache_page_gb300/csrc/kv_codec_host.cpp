@@ -200,6 +200,50 @@ int launch_all(kv_codec_s* h, int dir, void* stream) {
   return KV_OK;
 }
 
+// Address under which the kernels reach a caller buffer: device and managed
+// memory as they are, pinned host memory through its device mapping (the
+// kernels then move its bytes over the CPU-GPU link themselves).  Pageable
+// host memory has no such address.
+int device_view(const void* ptr, const void** out) {
+  *out = nullptr;
+  if (!ptr) return KV_OK;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();  // clear the error this query left
+    return KV_ERR_CUDA;
+  }
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+      *out = ptr;
+      return KV_OK;
+    case cudaMemoryTypeHost:
+      if (!a.devicePointer) return KV_ERR_NOT_ACCESSIBLE;
+      *out = a.devicePointer;
+      return KV_OK;
+    default:
+      return KV_ERR_NOT_ACCESSIBLE;
+  }
+}
+
+// The device views of the descriptor, slot, status and result buffers of a call.
+int resolve_buffers(Params& p, const kv_segment_desc* descs, const void* buf, const void* status,
+                    const void* result) {
+  const void* v = nullptr;
+  int rc = device_view(descs, &v);
+  if (rc != KV_OK) return rc;
+  p.descs = static_cast<const kv_segment_desc*>(v);
+  if ((rc = device_view(buf, &v)) != KV_OK) return rc;
+  p.buf = const_cast<uint8_t*>(static_cast<const uint8_t*>(v));
+  if ((rc = device_view(status, &v)) != KV_OK) return rc;
+  p.status = const_cast<uint8_t*>(static_cast<const uint8_t*>(v));
+  if ((rc = device_view(result, &v)) != KV_OK) return rc;
+  p.result = const_cast<uint8_t*>(static_cast<const uint8_t*>(v));
+  // a mapping keeps the offset within the page, so the alignment checks on the
+  // caller's pointers hold for these addresses too
+  return KV_OK;
+}
+
 int check_call(kv_codec_s* h, const void* const* layer_ptrs, uint32_t n_layer_ptrs,
                const kv_segment_desc* d_descs, const void* buf, const void* status) {
   const Params& p = h->p;
@@ -260,6 +304,7 @@ const char* kv_codec_strerror(int code) {
     case KV_ERR_LAYOUT_MISMATCH: return "strides overlap or do not fit the layout";
     case KV_ERR_UNSUPPORTED_CODEC_FOR_ROLE: return "TurboQuant codecs are for the K role only";
     case KV_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
+    case KV_ERR_NOT_ACCESSIBLE: return "buffer is pageable host memory (pin it or use device memory)";
     case KV_ERR_CUDA: return "CUDA runtime error";
     case KV_ERR_ABI: return "geometry ABI version or size mismatch";
     case KV_ERR_TOO_MANY_LAYERS: return "num_layers must be 1..KV_CODEC_MAX_LAYERS";
@@ -398,12 +443,10 @@ int kv_codec_encode(kv_codec_t h, const void* const* layer_ptrs, uint32_t n_laye
   kv_codec_s call = *h;  // per-call copy: the handle stays immutable
   Params& p = call.p;
   for (uint32_t k = 0; k < n_layer_ptrs; ++k) p.layer_ptr[k] = layer_ptrs[k];
-  p.descs = d_descs;
+  const int rv = resolve_buffers(p, d_descs, d_out, d_status, nullptr);
+  if (rv != KV_OK) return rv;
   p.n_segments = n_segments;
-  p.buf = static_cast<uint8_t*>(d_out);
   p.buf_bytes = out_bytes;
-  p.status = d_status;
-  p.result = nullptr;
   return launch_all(&call, kvc::kEncode, stream);
 }
 
@@ -417,12 +460,10 @@ int kv_codec_decode(kv_codec_t h, void* const* layer_ptrs, uint32_t n_layer_ptrs
   kv_codec_s call = *h;
   Params& p = call.p;
   for (uint32_t k = 0; k < n_layer_ptrs; ++k) p.layer_ptr[k] = layer_ptrs[k];
-  p.descs = d_descs;
+  const int rv = resolve_buffers(p, d_descs, d_in, d_status, d_result);
+  if (rv != KV_OK) return rv;
   p.n_segments = n_segments;
-  p.buf = const_cast<uint8_t*>(static_cast<const uint8_t*>(d_in));
   p.buf_bytes = in_bytes;
-  p.status = const_cast<uint8_t*>(d_status);
-  p.result = d_result;
   return launch_all(&call, kvc::kDecode, stream);
 }
 

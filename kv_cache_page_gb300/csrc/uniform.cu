@@ -54,7 +54,7 @@ __device__ __forceinline__ float div_levels(float range) {
 template <int DT, int D, int BITS>
 __global__ void __launch_bounds__(kThreads) uniform_encode_kernel(const __grid_constant__ Params p) {
   using M = ChunkMap<D>;
-  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = 2, W = kThreads / 32;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = kThreads / 32;
   constexpr int STEP = W * VPW * U;
   constexpr uint32_t LEVELS = (1u << BITS) - 1u;
   constexpr int CB = D * BITS / 8;  // code bytes per vector
@@ -147,7 +147,7 @@ __device__ __forceinline__ float small_u2f(uint32_t c) {
 template <int DT, int D, int BITS>
 __global__ void __launch_bounds__(kThreads) uniform_decode_kernel(const __grid_constant__ Params p) {
   using M = ChunkMap<D>;
-  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = 2, W = kThreads / 32;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = kThreads / 32;
   constexpr int STEP = W * VPW * U;
   constexpr int CB = D * BITS / 8;
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;

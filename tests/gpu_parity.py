@@ -50,9 +50,19 @@ def compare_pages(got: np.ndarray, want: np.ndarray, what: str):
     return int(np.count_nonzero(d))
 
 
+def _buffer(t: torch.Tensor, where: str, device) -> torch.Tensor:
+    """`t` as a device tensor, or as a pinned host tensor that the kernels reach
+    through its device mapping."""
+    if where == "host":
+        return t.cpu().pin_memory()
+    return t.to(device)
+
+
 def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="cuda",
-               reject_abs=448.0, check_decode=True):
+               reject_abs=448.0, check_decode=True, buffers="device"):
     """Encode + decode `case` with `arm` on the GPU and in the oracle; assert parity.
+    buffers="host" keeps descriptors, slots, statuses and results in pinned host
+    memory (the kernels read and write them over the host link).
     Returns (status array, number of restored elements off by one ulp)."""
     codec = make_codec(case, arm, reject_abs)
     g = oracle_geom(case, arm, reject_abs)
@@ -66,9 +76,9 @@ def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="
     n = len(rows)
     dev_layers = [t.to(device) for t in case.layers]
     host_layers = [host_bits(t) for t in case.layers]
-    descs = K.descriptors(rows, device)
-    out = torch.full((max(total, 16),), SENTINEL_ENC, dtype=torch.uint8, device=device)
-    status = torch.full((max(n, 1),), 0xEE, dtype=torch.uint8, device=device)
+    descs = _buffer(K.descriptors(rows, "cpu"), buffers, device)
+    out = _buffer(torch.full((max(total, 16),), SENTINEL_ENC, dtype=torch.uint8), buffers, device)
+    status = _buffer(torch.full((max(n, 1),), 0xEE, dtype=torch.uint8), buffers, device)
     codec.encode(dev_layers, descs, n, out, total, status)
     torch.cuda.synchronize()
     enc_ref, st_ref = O.encode(g, host_layers, oracle_descs(rows), total)
@@ -90,10 +100,11 @@ def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="
         dst_dev = [torch.full_like(t, 0).view(torch.int16).fill_(SENTINEL_PAGE).view(t.dtype)
                    for t in dev_layers]
         dst_host = [np.full_like(h, SENTINEL_PAGE) for h in host_layers]
-        enc_dev = torch.zeros(max(total, 16), dtype=torch.uint8, device=device)
-        enc_dev[:total] = torch.from_numpy(enc_ref).to(device)
-        st_dev = torch.from_numpy(st_ref).to(device)
-        result = torch.full((max(n, 1),), 0xEE, dtype=torch.uint8, device=device)
+        enc_h = torch.zeros(max(total, 16), dtype=torch.uint8)
+        enc_h[:total] = torch.from_numpy(enc_ref)
+        enc_dev = _buffer(enc_h, buffers, device)
+        st_dev = _buffer(torch.from_numpy(st_ref), buffers, device)
+        result = _buffer(torch.full((max(n, 1),), 0xEE, dtype=torch.uint8), buffers, device)
         codec.decode(dst_dev, descs, n, enc_dev, total, st_dev, result)
         torch.cuda.synchronize()
         res_ref = O.decode(g, dst_host, oracle_descs(rows), enc_ref, st_ref)

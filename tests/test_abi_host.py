@@ -146,6 +146,11 @@ def test_call_argument_checks_need_no_gpu():
 
 
 def test_strerror_covers_codes():
-    for code in range(0, -9, -1):
-        assert K.strerror(code) != "unknown error"
+    import os
+    import re
+    hdr = open(os.path.join(os.path.dirname(__file__), "..", "include", "kv_codec.h")).read()
+    codes = [int(c) for c in re.findall(r"#define KV_ERR_\w+ (-\d+)", hdr)]
+    assert sorted(codes) == list(range(-len(codes), 0))
+    for code in [0] + codes:
+        assert K.strerror(code) != "unknown error", code
     assert K.strerror(-99) == "unknown error"
