@@ -27,7 +27,7 @@ _LIB = None
 # Interface numbers (written independently of the product's header).
 FP16, BF16 = 1, 2
 SEPARATE, PACKED = 1, 2
-NONE, FP8_CAST, FP8_FIXED, FP8_DYNAMIC, TQ3, TQ4, UNI3, UNI4, UNI8 = range(9)
+NONE, FP8_CAST, FP8_FIXED, FP8_DYNAMIC, TQ3, TQ4, UNI3, UNI4, UNI8, INT8 = range(10)
 (S_ENCODED, S_RAW_NONFINITE, S_RAW_RANGE, S_RAW_PROTECTED, S_RAW_POLICY,
  S_RAW_OVERSIZE, S_RAW_NO_SAVING, S_BAD_DESC) = range(1, 9)
 
@@ -63,6 +63,7 @@ _f32 = _P(np.float32, flags="C")
 _u16 = _P(np.uint16, flags="C")
 _u8 = _P(np.uint8, flags="C")
 _f64 = _P(np.float64, flags="C")
+_i8 = _P(np.int8, flags="C")
 
 
 def lib():
@@ -91,6 +92,10 @@ def lib():
             "kvo_uniform_encode_many": [_f32, C.c_int64, C.c_int, C.c_int, _u8, _u16, _u16],
             "kvo_uniform_decode_many": [_u8, _u16, _u16, C.c_int64, C.c_int, _f32],
             "kvo_tq_index_many": [_f32, C.c_int64, C.c_int, C.c_int, _u8],
+            "kvo_int8_scale": [C.c_float],
+            "kvo_int8_encode_many": [_f32, C.c_int64, C.c_int, _i8, _u16],
+            "kvo_int8_decode_many": [_i8, _u16, C.c_int64, C.c_int, _f32],
+            "kvo_int8_record_bytes": [C.c_int, C.c_int],
             "kvo_pack_bits": [_u8, C.c_int, C.c_int, _u8],
             "kvo_unpack_bits": [_u8, C.c_int, C.c_int, _u8],
             "kvo_segment_enc_bytes": [C.POINTER(Geom), C.c_int],
@@ -103,7 +108,8 @@ def lib():
         res = {"kvo_pairwise_sum": C.c_float, "kvo_fp8_scale_from_amax": C.c_float,
                "kvo_absmax": C.c_float, "kvo_wht_scale": C.c_float,
                "kvo_splitmix64_next": C.c_uint64, "kvo_segment_enc_bytes": C.c_int64,
-               "kvo_segment_raw_bytes": C.c_int64}
+               "kvo_segment_raw_bytes": C.c_int64, "kvo_int8_scale": C.c_uint16,
+               "kvo_int8_record_bytes": C.c_int64}
         for name, args in sig.items():
             f = getattr(L, name)
             f.argtypes = args
@@ -237,6 +243,35 @@ def uniform_decode(codes, m16, s16):
                                   np.ascontiguousarray(s16, dtype=np.uint16), nvec, D,
                                   out.reshape(-1))
     return out
+
+
+def int8_scale(amax) -> int:
+    """BF16 bits of the per-head INT8 scale for an absolute maximum."""
+    return int(lib().kvo_int8_scale(float(np.float32(amax))))
+
+
+def int8_encode(x):
+    """[HIQ "Building the INT8 codec"]: int8 codes and BF16 scale bits per row."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    nvec, D = x.shape
+    codes = np.empty((nvec, D), dtype=np.int8)
+    s16 = np.empty(nvec, dtype=np.uint16)
+    lib().kvo_int8_encode_many(x.reshape(-1), nvec, D, codes.reshape(-1), s16)
+    return codes, s16
+
+
+def int8_decode(codes, s16):
+    """code * scale in FP32 (exact); the caller rounds to BF16."""
+    codes = np.ascontiguousarray(codes, dtype=np.int8)
+    nvec, D = codes.shape
+    out = np.empty((nvec, D), dtype=np.float32)
+    lib().kvo_int8_decode_many(codes.reshape(-1), np.ascontiguousarray(s16, dtype=np.uint16),
+                               nvec, D, out.reshape(-1))
+    return out
+
+
+def int8_record_bytes(H, D) -> int:
+    return int(lib().kvo_int8_record_bytes(H, D))
 
 
 def pack_bits(codes, bits):

@@ -15,6 +15,8 @@
  *          sections "FP8 and TurboQuant" and "Ownership, storage and GDS".
  *   [ASYM] "Asymmetric KV: methods and results" (knlp), sections
  *          "Precision and scaling reference" and "Actual-worker comparison".
+ *   [HIQ]  "Building a quantized HiCache for SGLang", sections "Building the
+ *          INT8 codec" and "Why exactly 1,152 bytes?".
  * Readings taken where the pages are silent are marked READING and are listed
  * with their reasons in the design notes of the repository.
  *
@@ -36,7 +38,7 @@ enum { O_FP16 = 1, O_BF16 = 2 };
 enum { O_SEPARATE = 1, O_PACKED = 2 };
 enum {
   O_NONE = 0, O_FP8_CAST = 1, O_FP8_FIXED = 2, O_FP8_DYNAMIC = 3,
-  O_TQ3 = 4, O_TQ4 = 5, O_UNI3 = 6, O_UNI4 = 7, O_UNI8 = 8
+  O_TQ3 = 4, O_TQ4 = 5, O_UNI3 = 6, O_UNI4 = 7, O_UNI8 = 8, O_INT8 = 9
 };
 enum {
   S_ENCODED = 1, S_RAW_NONFINITE = 2, S_RAW_RANGE = 3, S_RAW_PROTECTED = 4,
@@ -362,6 +364,44 @@ void kvo_uniform_decode_vec(const uint8_t* codes, uint16_t m16, uint16_t s16, in
 }
 
 /* ======================================================================== */
+/* 5b. Symmetric per-head INT8 ([HIQ "Building the INT8 codec"]), BF16 KV.  */
+/* One scale per head vector (token, layer, K or V, head), in the page's     */
+/* order of operations on BF16 tensors:                                     */
+/*   amax  = max |x| raised to a floor (BF16 tensor: the floor is rounded to */
+/*           BF16 when it applies; READING: floor 1e-12, the FP8 rule's, as  */
+/*           the page names only "a small nonzero floor");                    */
+/*   scale = amax / 127, divided in FP32 and rounded to BF16 (BF16 tensor     */
+/*           divided by an integer);                                         */
+/*   code  = round half to even of FP32(x) / FP32(scale), clamped to          */
+/*           [-127, 127] (the rounded scale can push the quotient past 127);  */
+/*   restore = code * scale as BF16 tensors: the FP32 product (exact)         */
+/*           rounded to BF16.                                                  */
+/* ======================================================================== */
+static const float kInt8AmaxFloor = 1e-12f;
+
+uint16_t kvo_int8_scale(float amax) {
+  float a = amax < kInt8AmaxFloor ? kvo_bf16_to_f32(kvo_f32_to_bf16(kInt8AmaxFloor)) : amax;
+  float q = a / 127.0f;
+  return kvo_f32_to_bf16(q);
+}
+
+void kvo_int8_encode_vec(const float* x, int D, int8_t* codes, uint16_t* scale16) {
+  *scale16 = kvo_int8_scale(kvo_absmax(x, D));
+  float s = kvo_bf16_to_f32(*scale16);
+  for (int i = 0; i < D; ++i) {
+    float q = rintf(x[i] / s);   /* default rounding mode: nearest, ties to even */
+    if (q > 127.0f) q = 127.0f;
+    if (q < -127.0f) q = -127.0f;
+    codes[i] = (int8_t)q;
+  }
+}
+
+void kvo_int8_decode_vec(const int8_t* codes, uint16_t scale16, int D, float* out) {
+  float s = kvo_bf16_to_f32(scale16);
+  for (int i = 0; i < D; ++i) out[i] = (float)codes[i] * s;   /* exact; rounded by the caller */
+}
+
+/* ======================================================================== */
 /* 6. Code packing.  READING: little-endian bit stream, code i occupies bits */
 /* [b*i, b*i + b) (byte k, bit m is stream bit 8k + m); b = 8 is one byte    */
 /* per code.  Gives D*b/8 bytes per vector ([OKV]: 64 + 2 = 66 for 4-bit K). */
@@ -426,6 +466,15 @@ static int is_fp8(int c) { return c == O_FP8_CAST || c == O_FP8_FIXED || c == O_
 static int is_tq(int c) { return c == O_TQ3 || c == O_TQ4; }
 static int is_uni(int c) { return c == O_UNI3 || c == O_UNI4 || c == O_UNI8; }
 
+/* [HIQ "Why exactly 1,152 bytes?"]: the INT8 codec stores one record per
+ * token row of a role: the H heads' int8 codes (H*D bytes), then their H BF16
+ * scales, zero-padded to a multiple of 128 bytes (8 heads x 128: 1,040 ->
+ * 1,152).  A segment's slot is its block_tokens records in token order. */
+int64_t kvo_int8_record_bytes(int H, int D) {
+  int64_t b = (int64_t)H * (D + 2);
+  return (b + 127) / 128 * 128;
+}
+
 /* Bytes per vector: codes and metadata. */
 static void vec_bytes(int codec, int D, int* code_b, int* meta_b) {
   if (is_fp8(codec)) { *code_b = D; *meta_b = codec == O_FP8_DYNAMIC ? 4 : 0; }
@@ -435,6 +484,8 @@ static void vec_bytes(int codec, int D, int* code_b, int* meta_b) {
 }
 
 int64_t kvo_segment_enc_bytes(const kvo_geom* g, int role) {
+  if (g->codec[role] == O_INT8)
+    return (int64_t)g->block_tokens * kvo_int8_record_bytes(g->num_heads, g->head_dim);
   int cb, mb;
   vec_bytes(g->codec[role], g->head_dim, &cb, &mb);
   int64_t nv = (int64_t)g->num_heads * g->block_tokens;
@@ -516,13 +567,19 @@ void kvo_encode(const kvo_geom* g, void* const* ptrs, const kvo_desc* descs, uin
     int64_t seg_bytes = kvo_segment_enc_bytes(g, (int)d->role);
     memset(slot, 0, (size_t)seg_bytes);
     uint8_t* meta = slot + (size_t)nv * cbytes;
+    int64_t rec = kvo_int8_record_bytes(H, D);
     for (int t = 0; t < T; ++t)
       for (int h = 0; h < H; ++h) {
         int v = t * H + h;
         const uint16_t* p = vec_ptr(g, ptrs, d, t, h);
         for (int e = 0; e < D; ++e) x[e] = src_to_f32(p[e], g->dtype);
         uint8_t* vc = slot + (size_t)v * cbytes;
-        if (is_fp8(codec)) {
+        if (codec == O_INT8) {
+          uint8_t* r = slot + (size_t)(t * rec);
+          uint16_t s16;
+          kvo_int8_encode_vec(x, D, (int8_t*)(r + (size_t)h * D), &s16);
+          memcpy(r + (size_t)H * D + 2 * (size_t)h, &s16, 2);
+        } else if (is_fp8(codec)) {
           float s;
           if (codec == O_FP8_CAST) s = 1.0f;
           else if (codec == O_FP8_FIXED) s = kvo_fp8_scale_from_amax(g->fixed_amax[2 * d->layer + d->role]);
@@ -580,11 +637,17 @@ void kvo_decode(const kvo_geom* g, void* const* ptrs, const kvo_desc* descs, uin
     if (is_tq(codec) && cb_bits_done != bits) { kvo_codebook(bits, D, cent, bnd); cb_bits_done = bits; }
     const uint8_t* slot = in + d->enc_offset;
     const uint8_t* meta = slot + (size_t)nv * cbytes;
+    int64_t rec = kvo_int8_record_bytes(H, D);
     for (int t = 0; t < T; ++t)
       for (int h = 0; h < H; ++h) {
         int v = t * H + h;
         const uint8_t* vc = slot + (size_t)v * cbytes;
-        if (is_fp8(codec)) {
+        if (codec == O_INT8) {
+          const uint8_t* r = slot + (size_t)(t * rec);
+          uint16_t s16;
+          memcpy(&s16, r + (size_t)H * D + 2 * (size_t)h, 2);
+          kvo_int8_decode_vec((const int8_t*)(r + (size_t)h * D), s16, D, y);
+        } else if (is_fp8(codec)) {
           float s;
           if (codec == O_FP8_CAST) s = 1.0f;
           else if (codec == O_FP8_FIXED) s = kvo_fp8_scale_from_amax(g->fixed_amax[2 * d->layer + d->role]);
@@ -663,6 +726,13 @@ void kvo_uniform_decode_many(const uint8_t* codes, const uint16_t* m16, const ui
                              int64_t nvec, int D, float* out) {
   for (int64_t v = 0; v < nvec; ++v)
     kvo_uniform_decode_vec(codes + v * D, m16[v], s16[v], D, out + v * D);
+}
+void kvo_int8_encode_many(const float* x, int64_t nvec, int D, int8_t* codes, uint16_t* scale16) {
+  for (int64_t v = 0; v < nvec; ++v) kvo_int8_encode_vec(x + v * D, D, codes + v * D, scale16 + v);
+}
+void kvo_int8_decode_many(const int8_t* codes, const uint16_t* scale16, int64_t nvec, int D,
+                          float* out) {
+  for (int64_t v = 0; v < nvec; ++v) kvo_int8_decode_vec(codes + v * D, scale16[v], D, out + v * D);
 }
 void kvo_tq_index_many(const float* y, int64_t n, int bits, int D, uint8_t* codes) {
   float cent[16], bnd[16];
