@@ -441,7 +441,8 @@ def run_extra(args, device):
              ("head_dim_sweep", {"head_dim": 32, "num_layers": 64}),
              ("head_dim_sweep", {"head_dim": 64, "num_layers": 64}),
              ("head_dim_sweep", {"head_dim": 128, "num_layers": 64}),
-             ("head_dim_sweep", {"head_dim": 256, "num_layers": 64}), ("qwen25_7b_offload", {})]
+             ("head_dim_sweep", {"head_dim": 256, "num_layers": 64}), ("qwen25_7b_offload", {}),
+             ("hiq_qwen3_8b", {})]
     for name, kw in specs:
         if name == args.workload and not kw:
             continue

@@ -29,6 +29,17 @@
  * E.g. head_dim 128: TQ4 K 66, UNIFORM4 V 68, TQ3 K 50, UNIFORM3 V 52 bytes per
  * vector (the storage-format page's payload sizes).
  *
+ * INT8_HEAD slots follow instead the token-row record of "Building a quantized
+ * HiCache for SGLang" (section "Why exactly 1,152 bytes?"): one record per
+ * token of the page, in token order,
+ *     [int8 codes of head 0 .. H-1 (H*D bytes)][BF16 scale of head 0 .. H-1]
+ *     [zero padding to a multiple of 128 bytes]
+ * (8 heads x 128: 1,024 + 16 = 1,040 -> 1,152 bytes), so a slot is
+ * block_tokens records.  Per head vector (section "Building the INT8 codec"):
+ * amax = max|x| floored at 1e-12, scale = BF16(FP32(amax / 127)), code =
+ * round-half-even(FP32(x / scale)) clamped to [-127, 127]; restore =
+ * BF16(code * scale).  Defined for BF16 sources only.
+ *
  * Threading and streams: a handle is immutable after creation and may be used
  * from several host threads.  Encode/decode only enqueue work on the caller's
  * CUDA stream (no synchronisation, no allocation); all buffers belong to the
@@ -76,6 +87,7 @@ extern "C" {
 #define KV_ERR_ABI -7                  /* abi_version / struct_size mismatch */
 #define KV_ERR_TOO_MANY_LAYERS -8      /* num_layers = 0 or > KV_CODEC_MAX_LAYERS */
 #define KV_ERR_NOT_ACCESSIBLE -9       /* a buffer is pageable host memory (not pinned) */
+#define KV_ERR_UNSUPPORTED_DTYPE -10   /* codec not defined for the source dtype (INT8_HEAD: BF16) */
 
 /* ---- enums ------------------------------------------------------------- */
 #define KV_DT_FP16 1u
@@ -93,6 +105,7 @@ extern "C" {
 #define KV_CODEC_UNIFORM3 6u    /* per-vector uniform, FP16 min and step */
 #define KV_CODEC_UNIFORM4 7u
 #define KV_CODEC_UNIFORM8 8u
+#define KV_CODEC_INT8_HEAD 9u   /* symmetric per-head INT8, BF16 scale, token-row records (BF16 only) */
 
 /* ---- per-segment status bytes (written by encode, read by decode) ------- */
 #define KV_SEG_ENCODED 1u       /* slot holds the encoding */

@@ -1,0 +1,215 @@
+// int8.cu -- symmetric per-head INT8 encode / decode in token-row records.
+//
+// "Building a quantized HiCache for SGLang", section "Building the INT8
+// codec": one scale per KV head vector (token, layer, K or V, head); amax =
+// max|x| raised to a small floor, scale = amax / 127 (a BF16 tensor divided
+// by an integer: FP32 quotient rounded to BF16), code = round(FP32(x) /
+// FP32(scale)) clamped to [-127, 127]; restore = code * scale as BF16.
+// Section "Why exactly 1,152 bytes?": per token row of one role the H heads'
+// codes (H*D bytes) then their H BF16 scales, padded with zeros to a multiple
+// of 128 bytes; a segment's slot is its block_tokens records in token order.
+//
+// The source is BF16 (the page's KV dtype; the host refuses FP16).  Per
+// element the encoder does one correctly rounded division (reciprocal of the
+// scale + one FMA correction), a clamp and a magic-number rounding whose low
+// byte is the two's-complement code.
+#include "device_common.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int kEncodeCtas = 6;  // resident CTAs per SM (see launch_codec_kernel)
+constexpr int kDecodeCtas = 3;
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: RN(q + magic) holds rint(q) in its low byte
+constexpr float kAmaxFloor = 1e-12f;        // floor of the head maximum
+constexpr uint32_t kAmaxFloorBf16 = 0x2B8D0000u;  // BF16(1e-12f) as FP32 bits (the floored value)
+
+// Codes of 8 elements: clamp(rint(x / s), -127, 127) as 8 int8 bytes.  The
+// quotient is correctly rounded: q0 = RN(x r), e = RN(x - q0 s) is exact, q =
+// RN(q0 + e r).  Clamping before rounding gives the same integer (+-127 are
+// integers).
+__device__ __forceinline__ uint2 int8_codes8(const float (&x)[8], float s, float r) {
+  const float2 ns2 = make_float2(-s, -s), r2 = make_float2(r, r);
+  const float2 mg2 = make_float2(kRoundMagic, kRoundMagic);
+  uint32_t t[8];
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    const float2 xx = make_float2(x[e], x[e + 1]);
+    const float2 q0 = mul2(xx, r2);
+    const float2 res = fma2(q0, ns2, xx);
+    float2 q = fma2(res, r2, q0);
+    q.x = fminf(fmaxf(q.x, -127.0f), 127.0f);
+    q.y = fminf(fmaxf(q.y, -127.0f), 127.0f);
+    const float2 m = add2(q, mg2);
+    t[e] = __float_as_uint(m.x);
+    t[e + 1] = __float_as_uint(m.y);
+  }
+  // low bytes in element order
+  const uint32_t lo = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
+  const uint32_t hi = __byte_perm(__byte_perm(t[4], t[5], 0x0040), __byte_perm(t[6], t[7], 0x0040), 0x5410);
+  return make_uint2(lo, hi);
+}
+
+// Byte offset of vector j's codes and of its scale inside the slot.
+__device__ __forceinline__ void record_offsets(const Params& p, uint32_t j, uint32_t& code_off,
+                                               uint32_t& scale_off) {
+  const uint32_t t = (uint32_t)(((uint64_t)j * p.h_magic) >> 32);
+  const uint32_t h = j - t * p.H;
+  const uint32_t rec = t * p.rec_bytes;
+  code_off = rec + h * p.D;
+  scale_off = rec + p.H * p.D + 2u * h;
+}
+
+// Zero the padding of every record of a slot (whole CTA, 16-bit stores: the
+// used part H*(D+2) and the record size are even).
+__device__ __forceinline__ void zero_record_padding(const Params& p, uint8_t* slot) {
+  const uint32_t pad16 = (p.rec_bytes - p.rec_used) / 2u;
+  if (pad16 == 0) return;
+  const uint32_t total = p.T * pad16;
+  for (uint32_t k = threadIdx.x; k < total; k += blockDim.x) {
+    const uint32_t t = k / pad16, o = k - t * pad16;
+    *reinterpret_cast<uint16_t*>(slot + (uint64_t)t * p.rec_bytes + p.rec_used + 2u * o) = 0;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) int8_encode_kernel(const __grid_constant__ Params p) {
+  using M = ChunkMap<D>;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = kThreads / 32;
+  constexpr int STEP = W * VPW * U;
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  const uint32_t grp = lane / G, li = lane % G;
+  __shared__ uint32_t s_flag[2];
+  if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
+  __syncthreads();
+  const uint32_t nv = p.nv;
+  int it = 0;
+  for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
+    const Seg s = plan_segment(p, i, kEncode);
+    if (s.action != kProcess) {
+      if (s.action == kReport && threadIdx.x == 0) p.status[i] = s.status;
+      continue;
+    }
+    if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
+    uint32_t flags = 0;
+    for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
+      uint4 w[U][NC];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t j = j0 + u * VPW + grp;
+        const uint16_t* src = s.page + (j < nv ? vec_off(p, j) : 0);
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          w[u][c] = j < nv ? ld_stream16(src + 8 * (li + G * c)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t j = j0 + u * VPW + grp;
+        const float amax = vec_absmax<1, G, NC>(w[u]);
+        flags |= admission_abs(amax, p.reject_abs);
+        const float a = amax < kAmaxFloor ? __uint_as_float(kAmaxFloorBf16) : amax;
+        const __nv_bfloat16 s16 = __float2bfloat16_rn(__fdiv_rn(a, 127.0f));
+        const float sc = __bfloat162float(s16);
+        const float r = __frcp_rn(sc);
+        const bool in = j < nv;
+        uint32_t code_off = 0, scale_off = 0;
+        if (in) record_offsets(p, j, code_off, scale_off);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          float x[8];
+          unpack8<1>(w[u][c], x);
+          const uint2 out = int8_codes8(x, sc, r);
+          if (in) st8(s.slot + code_off + 8 * (li + G * c), out);
+        }
+        if (in && li == 0)
+          *reinterpret_cast<uint16_t*>(s.slot + scale_off) = __bfloat16_as_ushort(s16);
+      }
+    }
+    flags = __reduce_or_sync(0xffffffffu, flags);
+    if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
+    zero_record_padding(p, s.slot);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint32_t f = s_flag[it & 1];
+      p.status[i] = (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+    }
+    ++it;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) int8_decode_kernel(const __grid_constant__ Params p) {
+  using M = ChunkMap<D>;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = kThreads / 32;
+  constexpr int STEP = W * VPW * U;
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  const uint32_t grp = lane / G, li = lane % G;
+  const uint32_t nv = p.nv;
+  // float(c) for a two's-complement byte c: the word 0x4B0000(c ^ 0x80) is
+  // 2^23 + c + 128 exactly
+  const float2 bias2 = make_float2(-8388736.0f, -8388736.0f);
+  for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
+    const Seg s = plan_segment(p, i, kDecode);
+    if (s.action != kProcess) {
+      if (s.action == kReport && threadIdx.x == 0 && p.result) p.result[i] = s.status;
+      continue;
+    }
+    uint16_t* page = const_cast<uint16_t*>(s.page);
+    for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
+      uint2 cw[U][NC];
+      float sc[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t j = j0 + u * VPW + grp;
+        const bool in = j < nv;
+        uint32_t code_off = 0, scale_off = 0;
+        if (in) record_offsets(p, j, code_off, scale_off);
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+          cw[u][c] = in ? ld_nc8(s.slot + code_off + 8 * (li + G * c)) : make_uint2(0, 0);
+        sc[u] = in ? __uint_as_float((uint32_t)ld_nc2(s.slot + scale_off) << 16) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t j = j0 + u * VPW + grp;
+        uint16_t* dst = page + (j < nv ? vec_off(p, j) : 0);
+        const float2 s2 = make_float2(sc[u], sc[u]);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          uint32_t r[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t wd = (k < 2 ? cw[u][c].x : cw[u][c].y) ^ 0x80808080u;
+            const uint32_t b = 2u * (k & 1);
+            const float2 f = make_float2(__uint_as_float(__byte_perm(wd, 0x4B000000u, 0x7440u | b)),
+                                         __uint_as_float(__byte_perm(wd, 0x4B000000u, 0x7440u | (b + 1))));
+            const float2 y = mul2(add2(f, bias2), s2);
+            r[k] = pack2<1>(y.x, y.y);
+          }
+          if (j < nv) st16(dst + 8 * (li + G * c), make_uint4(r[0], r[1], r[2], r[3]));
+        }
+      }
+    }
+    if (threadIdx.x == 0 && p.result) p.result[i] = KV_SEG_ENCODED;
+  }
+}
+
+}  // namespace
+
+int launch_int8(const Params& p, int dir, uint32_t codec, void* stream) {
+  if (codec != KV_CODEC_INT8_HEAD || p.dtype != KV_DT_BF16) return KV_ERR_INVALID_ARG;
+  const bool enc = dir == kEncode;
+  switch (p.D) {
+    case 32: return enc ? launch_codec_kernel(int8_encode_kernel<32>, p, stream, kEncodeCtas)
+                        : launch_codec_kernel(int8_decode_kernel<32>, p, stream, kDecodeCtas);
+    case 64: return enc ? launch_codec_kernel(int8_encode_kernel<64>, p, stream, kEncodeCtas)
+                        : launch_codec_kernel(int8_decode_kernel<64>, p, stream, kDecodeCtas);
+    case 128: return enc ? launch_codec_kernel(int8_encode_kernel<128>, p, stream, kEncodeCtas)
+                         : launch_codec_kernel(int8_decode_kernel<128>, p, stream, kDecodeCtas);
+    case 256: return enc ? launch_codec_kernel(int8_encode_kernel<256>, p, stream, kEncodeCtas)
+                         : launch_codec_kernel(int8_decode_kernel<256>, p, stream, kDecodeCtas);
+  }
+  return KV_ERR_UNSUPPORTED_HEAD_DIM;
+}
+
+}  // namespace kvc

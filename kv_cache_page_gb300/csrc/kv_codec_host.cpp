@@ -28,7 +28,7 @@ namespace {
 
 using kvc::Params;
 
-bool valid_codec(uint32_t c) { return c <= KV_CODEC_UNIFORM8; }
+bool valid_codec(uint32_t c) { return c <= KV_CODEC_INT8_HEAD; }
 bool is_fp8(uint32_t c) { return c >= KV_CODEC_FP8_CAST && c <= KV_CODEC_FP8_DYNAMIC; }
 bool is_tq(uint32_t c) { return c == KV_CODEC_TQ3 || c == KV_CODEC_TQ4; }
 uint32_t codec_bits(uint32_t c) {
@@ -176,6 +176,7 @@ int launch_all(kv_codec_s* h, int dir, void* stream) {
   auto run = [&](uint32_t codec) -> int {
     if (is_fp8(codec)) return kvc::launch_fp8(p, dir, codec, stream);
     if (is_tq(codec)) return kvc::launch_turboquant(p, dir, codec, stream);
+    if (codec == KV_CODEC_INT8_HEAD) return kvc::launch_int8(p, dir, codec, stream);
     return kvc::launch_uniform(p, dir, codec, stream);
   };
   if (kc == vc) {
@@ -305,6 +306,7 @@ const char* kv_codec_strerror(int code) {
     case KV_ERR_UNSUPPORTED_CODEC_FOR_ROLE: return "TurboQuant codecs are for the K role only";
     case KV_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
     case KV_ERR_NOT_ACCESSIBLE: return "buffer is pageable host memory (pin it or use device memory)";
+    case KV_ERR_UNSUPPORTED_DTYPE: return "codec not defined for this source dtype (INT8_HEAD needs BF16)";
     case KV_ERR_CUDA: return "CUDA runtime error";
     case KV_ERR_ABI: return "geometry ABI version or size mismatch";
     case KV_ERR_TOO_MANY_LAYERS: return "num_layers must be 1..KV_CODEC_MAX_LAYERS";
@@ -344,6 +346,8 @@ int kv_codec_create(const kv_codec_geometry* g, kv_codec_t* out) {
   if (nv > (1u << 20) || g->num_kv_heads > 4096) return KV_ERR_INVALID_ARG;
   if (!valid_codec(g->k_codec) || !valid_codec(g->v_codec)) return KV_ERR_INVALID_ARG;
   if (is_tq(g->v_codec)) return KV_ERR_UNSUPPORTED_CODEC_FOR_ROLE;
+  if ((g->k_codec == KV_CODEC_INT8_HEAD || g->v_codec == KV_CODEC_INT8_HEAD) && g->dtype != KV_DT_BF16)
+    return KV_ERR_UNSUPPORTED_DTYPE;
   float reject = g->reject_abs == 0.0f ? 448.0f : g->reject_abs;
   if (!(reject > 0.0f && reject <= 448.0f)) return KV_ERR_INVALID_ARG;
   if (g->stride_block <= 0 || g->stride_token <= 0 || g->stride_head <= 0) return KV_ERR_LAYOUT_MISMATCH;
@@ -384,19 +388,26 @@ int kv_codec_create(const kv_codec_geometry* g, kv_codec_t* out) {
   p.reject_abs = reject;
   p.wht_scale = (float)(1.0 / std::sqrt((double)g->head_dim));
   const uint64_t raw = nv * g->head_dim * 2;
+  // INT8_HEAD token record: H int8 head vectors + H BF16 scales, 128-byte multiple
+  p.rec_used = p.H * (p.D + 2);
+  p.rec_bytes = (p.rec_used + 127) / 128 * 128;
   for (int r = 0; r < 2; ++r) {
     const uint32_t c = p.codec[r];
     uint32_t cb = 0, mb = 0;
     if (is_fp8(c)) {
       cb = p.D;
       mb = c == KV_CODEC_FP8_DYNAMIC ? 4 : 0;
+    } else if (c == KV_CODEC_INT8_HEAD) {
+      cb = p.D;
+      mb = 2;
     } else if (c != KV_CODEC_NONE) {
       cb = p.D * codec_bits(c) / 8;
       mb = is_tq(c) ? 2 : 4;
     }
     p.code_bytes[r] = cb;
     p.meta_bytes[r] = mb;
-    p.seg_bytes[r] = (nv * (cb + mb) + 127) / 128 * 128;
+    p.seg_bytes[r] = c == KV_CODEC_INT8_HEAD ? (uint64_t)p.T * p.rec_bytes
+                                             : (nv * (cb + mb) + 127) / 128 * 128;
     uint8_t st = 0;
     if (c != KV_CODEC_NONE) {
       if (raw > (16ull << 20)) st = KV_SEG_RAW_OVERSIZE;

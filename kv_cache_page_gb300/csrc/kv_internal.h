@@ -37,6 +37,8 @@ struct Params {
   uint32_t code_bytes[2];               // per vector
   uint32_t meta_bytes[2];               // per vector
   uint64_t seg_bytes[2];                // encoded slot (multiple of 128)
+  uint32_t rec_bytes;                   // INT8_HEAD token record: H * (D + 2) rounded up to 128
+  uint32_t rec_used;                    // H * (D + 2): codes and scales; zeros follow
   uint8_t static_status[2];             // 0 = encodable, else KV_SEG_RAW_{POLICY,OVERSIZE,NO_SAVING}
   uint8_t heads_contig;                 // st == H * sh: vector j of a page sits at j * sh
   uint8_t pad0;
@@ -71,6 +73,7 @@ enum Dir { kEncode = 0, kDecode = 1 };
 int launch_fp8(const Params& p, int dir, uint32_t codec, void* stream);
 int launch_uniform(const Params& p, int dir, uint32_t codec, void* stream);
 int launch_turboquant(const Params& p, int dir, uint32_t codec, void* stream);
+int launch_int8(const Params& p, int dir, uint32_t codec, void* stream);
 
 // Grid size for a codec kernel over n segments: one CTA per segment up to
 // SM count x resident CTAs per SM, the latter the occupancy limit (cached per

@@ -38,7 +38,7 @@ __all__ = ["Case", "make_case", "CASES"]
 class Arm:
     """One codec configuration run over a workload: codec per role ("none",
     "fp8_cast", "fp8_fixed", "fp8_dynamic", "tq3", "tq4", "uni3", "uni4",
-    "uni8") and the roles whose segments are submitted."""
+    "uni8", "int8") and the roles whose segments are submitted."""
     name: str
     k_codec: str
     v_codec: str
@@ -130,8 +130,11 @@ def make_case(name: str, *, device="cpu", num_layers: Optional[int] = None,
                     layers, [Arm("fp8_dynamic_k8v8", "fp8_dynamic", "fp8_dynamic", (0, 1)),
                              Arm("turboquant4", "tq4", "uni4", (0, 1))], seed)
 
-    if name == "qwen3_8b":
+    if name in ("qwen3_8b", "hiq_qwen3_8b"):
+        # the HiQCache page's model (Qwen3-8B, BF16 KV, symmetric per-head INT8
+        # host copy for K and V) on the same value law, in BF16
         L, B, H, D = num_layers or 36, num_blocks or 2048, 8, 128
+        dt = torch.float16 if name == "qwen3_8b" else torch.bfloat16
         g = _gen(device, seed)
         blocks_per_seq = 8192 // T
         pos = (torch.arange(B, device=device) % blocks_per_seq)[:, None] * T + \
@@ -142,10 +145,14 @@ def make_case(name: str, *, device="cpu", num_layers: Optional[int] = None,
             k = torch.randn(B, T, H, D, generator=g, device=device) * chan
             _rope_(k, pos)
             v = 0.5 * torch.randn(B, T, H, D, generator=g, device=device)
-            layers += [k.half(), v.half()]
-        return Case(name, torch.float16, "separate", D, H, T, L, B, _separate_strides(T, H, D),
-                    layers, [Arm("fp8_k16v8_dynamic", "none", "fp8_dynamic", (1,)),
-                             Arm("fp8_k8v8_dynamic", "fp8_dynamic", "fp8_dynamic", (0, 1))], seed)
+            layers += [k.to(dt), v.to(dt)]
+        if name == "hiq_qwen3_8b":
+            arms = [Arm("int8_head", "int8", "int8", (0, 1))]
+        else:
+            arms = [Arm("fp8_k16v8_dynamic", "none", "fp8_dynamic", (1,)),
+                    Arm("fp8_k8v8_dynamic", "fp8_dynamic", "fp8_dynamic", (0, 1))]
+        return Case(name, dt, "separate", D, H, T, L, B, _separate_strides(T, H, D), layers, arms,
+                    seed)
 
     if name == "vllm_packed":
         L, B, H, D = num_layers or 32, num_blocks or 4096, 8, 128
@@ -204,7 +211,7 @@ def make_case(name: str, *, device="cpu", num_layers: Optional[int] = None,
     raise ValueError(f"unknown workload {name!r}")
 
 
-CASES = ("tiny", "qwen3_8b", "vllm_packed", "head_dim_sweep", "qwen25_7b_offload")
+CASES = ("tiny", "qwen3_8b", "vllm_packed", "head_dim_sweep", "qwen25_7b_offload", "hiq_qwen3_8b")
 
 
 def segment_list(case: Case, arm: Arm, seg_bytes: Sequence[int], layers=None, blocks=None):

@@ -56,7 +56,7 @@ def _kw(**over):
     (dict(num_layers=0), -8),
     (dict(num_layers=513), -8),
     (dict(v_codec="tq3"), -4),
-    (dict(geometry_overrides={"k_codec": 9}), -1),
+    (dict(geometry_overrides={"k_codec": 10}), -1),
     (dict(strides=(16 * 8 * 128, 8 * 128, 100)), -5),        # head stride not 16-byte aligned
     (dict(strides=(16 * 8 * 128, 8 * 128, 64)), -3),         # heads overlap (64 < D)
     (dict(strides=(8 * 128, 8 * 128, 128)), -3),             # pages overlap tokens
@@ -108,6 +108,31 @@ def test_segment_bytes_match_oracle(D, kc, vc, H, T):
         assert raw == O.segment_raw_bytes(g)
         assert enc == (0 if name == "none" else O.segment_enc_bytes(g, role))
     c.close()
+
+
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+@pytest.mark.parametrize("kc,vc", [("int8", "int8"), ("int8", "fp8_dynamic"), ("none", "int8")])
+@pytest.mark.parametrize("H,T", [(8, 16), (3, 5), (1, 1), (32, 16)])
+def test_int8_record_segment_bytes_match_oracle(D, kc, vc, H, T):
+    c = K.Codec(**_kw(dtype="bf16", head_dim=D, num_kv_heads=H, block_tokens=T, num_layers=2,
+                      num_blocks=2, strides=(T * H * D, H * D, D), k_codec=kc, v_codec=vc))
+    g = O.make_geom(dtype=O.BF16, layout=O.SEPARATE, head_dim=D, num_heads=H, block_tokens=T,
+                    num_layers=2, num_blocks=2, strides=(T * H * D, H * D, D),
+                    codecs=(K.CODEC[kc], K.CODEC[vc]))
+    for role, name in ((0, kc), (1, vc)):
+        enc, raw = c.segment_bytes(role)
+        assert raw == O.segment_raw_bytes(g)
+        assert enc == (0 if name == "none" else O.segment_enc_bytes(g, role))
+        if name == "int8":
+            assert enc == T * O.int8_record_bytes(H, D)
+    c.close()
+
+
+def test_int8_needs_bf16_source():
+    for kc, vc in (("int8", "none"), ("fp8_dynamic", "int8")):
+        with pytest.raises(K.KvCodecError) as e:
+            K.Codec(**_kw(dtype="fp16", k_codec=kc, v_codec=vc))
+        assert e.value.code == -10
 
 
 @pytest.mark.parametrize("bits", [1, 2, 3, 4])

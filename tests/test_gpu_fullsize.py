@@ -93,7 +93,8 @@ def _check_arm(case, arm, n_random=40, seed=0):
                                      ("head_dim_sweep", {"head_dim": 64}),
                                      ("head_dim_sweep", {"head_dim": 128}),
                                      ("head_dim_sweep", {"head_dim": 256}),
-                                     ("qwen25_7b_offload", {}), ("tiny", {})])
+                                     ("qwen25_7b_offload", {}), ("hiq_qwen3_8b", {}),
+                                     ("tiny", {})])
 def test_full_size_sampled(name, kw):
     case = synth.make_case(name, device="cuda", **kw)
     for arm in case.arms:

@@ -45,6 +45,12 @@ def test_host_slots_qwen3_8b_shape(k, v):
     assert np.all(st[st != O.S_RAW_POLICY] == O.S_ENCODED)
 
 
+def test_host_slots_int8_records():
+    case = synth.make_case("hiq_qwen3_8b", num_layers=2, num_blocks=12)
+    st, ulps = run_parity(case, case.arms[0], buffers="host")
+    assert ulps == 0 and np.all(st == O.S_ENCODED)
+
+
 def test_host_slots_packed_layout_with_raw_segments():
     case = synth.make_case("vllm_packed", num_layers=6, num_blocks=24)
     st, ulps = run_parity(case, case.arms[0], buffers="host")

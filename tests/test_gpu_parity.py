@@ -122,6 +122,48 @@ def test_codec_matrix(kc, vc, D, dtype, layout):
     assert ulps == 0
 
 
+@pytest.mark.parametrize("kc,vc", [("int8", "int8"), ("int8", "fp8_dynamic"), ("tq4", "int8"),
+                                   ("none", "int8")])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+@pytest.mark.parametrize("H,T", [(3, 5), (8, 16), (1, 3)])
+@pytest.mark.parametrize("layout", ["separate", "packed"])
+def test_int8_head_matrix(kc, vc, D, H, T, layout):
+    """Symmetric per-head INT8 in token-row records (BF16 only), ragged and
+    page-shaped segments, both layouts, mixed with the other codecs."""
+    case = custom_case(D=D, H=H, T=T, L=2, B=4, dtype="bf16", layout=layout,
+                       values="heavy" if H == 3 else "normal", seed=D + H)
+    st, ulps = run_parity(case, synth.Arm("i8", kc, vc, (0, 1)))
+    assert ulps == 0
+
+
+def test_hiq_qwen3_8b_shape_small():
+    case = synth.make_case("hiq_qwen3_8b", num_layers=2, num_blocks=24)
+    for arm in case.arms:
+        st, ulps = run_parity(case, arm)
+        assert np.all(st == O.S_ENCODED) and ulps == 0
+
+
+def test_int8_special_values():
+    """BF16 zeros of both signs, an all-zero head (the maximum floor), heads
+    below the floor, powers of two, +-448 exactly, and a planted NaN and 452."""
+    D, H, T = 64, 2, 16
+    x = torch.zeros(8, T, H, D, dtype=torch.float32)
+    x[1] = -0.0
+    x[2, :, :, ::2] = -0.0
+    x[3] = 1e-14 * torch.arange(D)                                  # below the 1e-12 floor
+    x[4] = torch.tensor(2.0) ** torch.arange(-60, -60 + D).float()  # one octave per element
+    x[5, :, 0, 0], x[5, :, 1, 1] = 448.0, -448.0
+    x[6, 3, 1, 9] = float("nan")
+    x[7, 0, 0, 0] = 452.0                                           # BF16(449) is 448
+    t = x.bfloat16()
+    case = synth.Case("special8", torch.bfloat16, "separate", D, H, T, 1, 8,
+                      synth._separate_strides(T, H, D), [t, t.clone()], [], 0)
+    st, ulps = run_parity(case, synth.Arm("s", "int8", "int8", (0, 1)))
+    assert list(st[:12]) == [O.S_ENCODED] * 12
+    assert list(st[12:]) == [O.S_RAW_NONFINITE, O.S_RAW_NONFINITE, O.S_RAW_RANGE, O.S_RAW_RANGE]
+    assert ulps == 0
+
+
 @pytest.mark.parametrize("kc,vc", [("tq4", "fp8_dynamic"), ("tq3", "uni8")])
 def test_large_segments_many_steps(kc, vc):
     case = custom_case(D=128, H=32, T=16, L=1, B=3, dtype="fp16", layout="separate")
@@ -143,8 +185,9 @@ def _exhaustive_layers(dtype):
     return buf, ng + bad.size
 
 
-@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
-@pytest.mark.parametrize("codec", ["fp8_cast", "fp8_dynamic", "uni8", "tq4"])
+@pytest.mark.parametrize("dtype,codec", [(d, c) for d in ("fp16", "bf16")
+                                         for c in ("fp8_cast", "fp8_dynamic", "uni8", "tq4")]
+                         + [("bf16", "int8")])
 def test_every_16bit_pattern(dtype, codec):
     """All 65,536 source patterns: in-range finite values fill admitted pages, each
     nonfinite / out-of-range pattern sits alone in a page of its own."""
