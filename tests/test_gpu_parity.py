@@ -145,8 +145,9 @@ def test_hiq_qwen3_8b_shape_small():
 
 def test_int8_special_values():
     """BF16 zeros of both signs, an all-zero head (the maximum floor), heads
-    below the floor, powers of two, +-448 exactly, and a planted NaN and 452."""
-    D, H, T = 64, 2, 16
+    below the floor, powers of two, +-448 exactly, and a planted NaN and 452.
+    (H = 8: at H = 2 a 64-wide head's record pads to 256 bytes and saves nothing.)"""
+    D, H, T = 64, 8, 16
     x = torch.zeros(8, T, H, D, dtype=torch.float32)
     x[1] = -0.0
     x[2, :, :, ::2] = -0.0
