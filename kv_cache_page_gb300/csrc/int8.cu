@@ -11,8 +11,10 @@
 //
 // The source is BF16 (the page's KV dtype; the host refuses FP16).  Per
 // element the encoder does one correctly rounded division (reciprocal of the
-// scale + one FMA correction), a clamp and a magic-number rounding whose low
-// byte is the two's-complement code.
+// scale + one FMA correction) and a magic-number rounding whose low byte is
+// the two's-complement code.  The clamp to [-127, 127] is implied for BF16
+// sources: over every BF16 maximum a (floored), a / scale <= 127.33 < 127.5,
+// and |x| <= a, so every rounded quotient is already in range.
 #include "device_common.cuh"
 
 namespace kvc {
@@ -24,10 +26,9 @@ constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: RN(q + magic) holds r
 constexpr float kAmaxFloor = 1e-12f;        // floor of the head maximum
 constexpr uint32_t kAmaxFloorBf16 = 0x2B8D0000u;  // BF16(1e-12f) as FP32 bits (the floored value)
 
-// Codes of 8 elements: clamp(rint(x / s), -127, 127) as 8 int8 bytes.  The
-// quotient is correctly rounded: q0 = RN(x r), e = RN(x - q0 s) is exact, q =
-// RN(q0 + e r).  Clamping before rounding gives the same integer (+-127 are
-// integers).
+// Codes of 8 elements: rint(x / s) as 8 int8 bytes (|x / s| < 127.5, see
+// above).  The quotient is correctly rounded: q0 = RN(x r), e = RN(x - q0 s)
+// is exact, q = RN(q0 + e r).
 __device__ __forceinline__ uint2 int8_codes8(const float (&x)[8], float s, float r) {
   const float2 ns2 = make_float2(-s, -s), r2 = make_float2(r, r);
   const float2 mg2 = make_float2(kRoundMagic, kRoundMagic);
@@ -37,9 +38,7 @@ __device__ __forceinline__ uint2 int8_codes8(const float (&x)[8], float s, float
     const float2 xx = make_float2(x[e], x[e + 1]);
     const float2 q0 = mul2(xx, r2);
     const float2 res = fma2(q0, ns2, xx);
-    float2 q = fma2(res, r2, q0);
-    q.x = fminf(fmaxf(q.x, -127.0f), 127.0f);
-    q.y = fminf(fmaxf(q.y, -127.0f), 127.0f);
+    const float2 q = fma2(res, r2, q0);
     const float2 m = add2(q, mg2);
     t[e] = __float_as_uint(m.x);
     t[e + 1] = __float_as_uint(m.y);
@@ -48,6 +47,16 @@ __device__ __forceinline__ uint2 int8_codes8(const float (&x)[8], float s, float
   const uint32_t lo = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
   const uint32_t hi = __byte_perm(__byte_perm(t[4], t[5], 0x0040), __byte_perm(t[6], t[7], 0x0040), 0x5410);
   return make_uint2(lo, hi);
+}
+
+// a / 127 correctly rounded, for a BF16 maximum a >= the floor: q0 = RN(a
+// RN(1/127)), one FMA residual and correction (equal to the IEEE quotient for
+// every such a; checked exhaustively).
+__device__ __forceinline__ float div127(float a) {
+  constexpr float r = 1.0f / 127.0f;
+  const float q0 = __fmul_rn(a, r);
+  const float e = __fmaf_rn(-q0, 127.0f, a);
+  return __fmaf_rn(e, r, q0);
 }
 
 // Byte offset of vector j's codes and of its scale inside the slot.
@@ -108,7 +117,7 @@ __global__ void __launch_bounds__(kThreads) int8_encode_kernel(const __grid_cons
         const float amax = vec_absmax<1, G, NC>(w[u]);
         flags |= admission_abs(amax, p.reject_abs);
         const float a = amax < kAmaxFloor ? __uint_as_float(kAmaxFloorBf16) : amax;
-        const __nv_bfloat16 s16 = __float2bfloat16_rn(__fdiv_rn(a, 127.0f));
+        const __nv_bfloat16 s16 = __float2bfloat16_rn(div127(a));
         const float sc = __bfloat162float(s16);
         const float r = __frcp_rn(sc);
         const bool in = j < nv;

@@ -136,6 +136,27 @@ def test_int8_head_matrix(kc, vc, D, H, T, layout):
     assert ulps == 0
 
 
+def test_int8_every_bf16_maximum():
+    """Every positive BF16 value up to 448 as the maximum of its own head vector
+    (the rest of the vector spread below it): every scale the encoder can form
+    and the largest quotients, against the oracle."""
+    bits = np.arange(0x0001, 0x7F80, dtype=np.uint16)
+    a = O.bf16_to_f32(bits)
+    a = a[a <= 448.0]
+    D, H, T = 64, 8, 16
+    per = H * T
+    B = -(-a.size // per)
+    rng = np.random.default_rng(7)
+    x = np.zeros((B * per, D), np.float32)
+    x[:a.size, 0] = np.where(np.arange(a.size) % 2 == 0, a, -a)
+    x[:a.size, 1:] = a[:, None] * rng.uniform(-1, 1, (a.size, D - 1)).astype(np.float32)
+    t = torch.from_numpy(x.reshape(B, T, H, D)).bfloat16()
+    case = synth.Case("maxima", torch.bfloat16, "separate", D, H, T, 1, B,
+                      synth._separate_strides(T, H, D), [t, t.clone()], [], 0)
+    st, ulps = run_parity(case, synth.Arm("m", "int8", "int8", (0, 1)))
+    assert np.all(st == O.S_ENCODED) and ulps == 0
+
+
 def test_hiq_qwen3_8b_shape_small():
     case = synth.make_case("hiq_qwen3_8b", num_layers=2, num_blocks=24)
     for arm in case.arms:
