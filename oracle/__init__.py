@@ -29,7 +29,10 @@ FP16, BF16 = 1, 2
 SEPARATE, PACKED = 1, 2
 NONE, FP8_CAST, FP8_FIXED, FP8_DYNAMIC, TQ3, TQ4, UNI3, UNI4, UNI8, INT8 = range(10)
 (S_ENCODED, S_RAW_NONFINITE, S_RAW_RANGE, S_RAW_PROTECTED, S_RAW_POLICY,
- S_RAW_OVERSIZE, S_RAW_NO_SAVING, S_BAD_DESC) = range(1, 9)
+ S_RAW_OVERSIZE, S_RAW_NO_SAVING, S_BAD_DESC, S_CORRUPT) = range(1, 10)
+# segment header {u32 version, u32 format, u64 orig_bytes, u64 stored_bytes, u32 crc32, u32 status}
+HEADER_DTYPE = np.dtype([("version", "<u4"), ("format", "<u4"), ("orig_bytes", "<u8"),
+                         ("stored_bytes", "<u8"), ("crc32", "<u4"), ("status", "<u4")])
 
 
 def build(force: bool = False) -> str:
@@ -96,6 +99,11 @@ def lib():
             "kvo_int8_encode_many": [_f32, C.c_int64, C.c_int, _i8, _u16],
             "kvo_int8_decode_many": [_i8, _u16, C.c_int64, C.c_int, _f32],
             "kvo_int8_record_bytes": [C.c_int, C.c_int],
+            "kvo_crc32": [C.c_void_p, C.c_uint64],
+            "kvo_seal": [C.POINTER(Geom), C.c_void_p, C.c_uint32, C.c_void_p, C.c_uint64,
+                         C.c_void_p, C.c_void_p],
+            "kvo_verify": [C.POINTER(Geom), C.c_void_p, C.c_uint32, C.c_void_p, C.c_uint64,
+                           C.c_void_p, C.c_void_p],
             "kvo_pack_bits": [_u8, C.c_int, C.c_int, _u8],
             "kvo_unpack_bits": [_u8, C.c_int, C.c_int, _u8],
             "kvo_segment_enc_bytes": [C.POINTER(Geom), C.c_int],
@@ -109,7 +117,7 @@ def lib():
                "kvo_absmax": C.c_float, "kvo_wht_scale": C.c_float,
                "kvo_splitmix64_next": C.c_uint64, "kvo_segment_enc_bytes": C.c_int64,
                "kvo_segment_raw_bytes": C.c_int64, "kvo_int8_scale": C.c_uint16,
-               "kvo_int8_record_bytes": C.c_int64}
+               "kvo_int8_record_bytes": C.c_int64, "kvo_crc32": C.c_uint32}
         for name, args in sig.items():
             f = getattr(L, name)
             f.argtypes = args
@@ -347,3 +355,34 @@ def decode(g, layers, descs, enc, status):
     lib().kvo_decode(C.byref(g), _ptrs(layers), descs.ctypes.data, len(descs),
                      enc.ctypes.data, enc.size, status.ctypes.data, result.ctypes.data)
     return result
+
+
+# ---------------------------------------------------------------- headers
+def crc32(data) -> int:
+    """CRC-32 (reflected 0xEDB88320, preset and final complement), bit-serial."""
+    b = np.ascontiguousarray(np.frombuffer(bytes(data), np.uint8) if isinstance(data, (bytes, bytearray))
+                             else data, dtype=np.uint8).reshape(-1)
+    return int(lib().kvo_crc32(b.ctypes.data if b.size else None, b.size))
+
+
+def seal(g, descs, buf, status):
+    """Segment headers (HEADER_DTYPE[n]) for the slots in `buf`."""
+    descs = np.ascontiguousarray(descs, dtype=DESC_DTYPE)
+    buf = np.ascontiguousarray(buf, dtype=np.uint8)
+    status = np.ascontiguousarray(status, dtype=np.uint8)
+    out = np.zeros(len(descs), dtype=HEADER_DTYPE)
+    lib().kvo_seal(C.byref(g), descs.ctypes.data, len(descs), buf.ctypes.data, buf.size,
+                   status.ctypes.data, out.ctypes.data)
+    return out
+
+
+def verify(g, descs, buf, headers):
+    """Per-segment result: the header's status when header and checksum hold,
+    S_CORRUPT when not, S_BAD_DESC for an invalid descriptor."""
+    descs = np.ascontiguousarray(descs, dtype=DESC_DTYPE)
+    buf = np.ascontiguousarray(buf, dtype=np.uint8)
+    headers = np.ascontiguousarray(headers, dtype=HEADER_DTYPE)
+    out = np.zeros(len(descs), dtype=np.uint8)
+    lib().kvo_verify(C.byref(g), descs.ctypes.data, len(descs), buf.ctypes.data, buf.size,
+                     headers.ctypes.data, out.ctypes.data)
+    return out

@@ -42,7 +42,8 @@ enum {
 };
 enum {
   S_ENCODED = 1, S_RAW_NONFINITE = 2, S_RAW_RANGE = 3, S_RAW_PROTECTED = 4,
-  S_RAW_POLICY = 5, S_RAW_OVERSIZE = 6, S_RAW_NO_SAVING = 7, S_BAD_DESC = 8
+  S_RAW_POLICY = 5, S_RAW_OVERSIZE = 6, S_RAW_NO_SAVING = 7, S_BAD_DESC = 8,
+  S_CORRUPT = 9
 };
 
 /* ======================================================================== */
@@ -672,6 +673,93 @@ void kvo_decode(const kvo_geom* g, void* const* ptrs, const kvo_desc* descs, uin
   }
   free(y);
   free(codes);
+}
+
+/* ======================================================================== */
+/* 7b. Segment header and CRC-32 ([OKV "Ownership, storage and GDS"]: every  */
+/* encoded segment carries a version, its original length, its format, its  */
+/* stored length and a CRC32; checksums are validated before GPU decode and  */
+/* a damaged object becomes a miss).  READINGS: CRC-32 is the common IEEE    */
+/* 802.3 / zlib one (reflected polynomial 0xEDB88320, register preset to all */
+/* ones, result complemented) over the stored slot bytes; the header is      */
+/* {u32 version = 1, u32 format = codec | dtype << 8 | log2(head_dim) << 16, */
+/* u64 original bytes, u64 stored bytes (0 when the segment stayed raw),     */
+/* u32 crc32, u32 status}; a verified segment keeps status ENCODED, a header */
+/* or checksum mismatch gives CORRUPT, raw headers pass their status on.     */
+/* ======================================================================== */
+typedef struct {
+  uint32_t version, format;
+  uint64_t orig_bytes, stored_bytes;
+  uint32_t crc32, status;
+} kvo_header;
+
+/* Bit-serial CRC-32, one message bit at a time, straight from the definition
+ * of the reflected shift register. */
+uint32_t kvo_crc32(const uint8_t* p, uint64_t n) {
+  uint32_t r = 0xFFFFFFFFu;
+  for (uint64_t i = 0; i < n; ++i) {
+    r ^= p[i];
+    for (int k = 0; k < 8; ++k) r = (r & 1u) ? (r >> 1) ^ 0xEDB88320u : (r >> 1);
+  }
+  return ~r;
+}
+
+static uint32_t header_format(const kvo_geom* g, int role) {
+  int lg = 0;
+  while ((1 << lg) < g->head_dim) ++lg;
+  return (uint32_t)g->codec[role] | ((uint32_t)g->dtype << 8) | ((uint32_t)lg << 16);
+}
+
+/* Descriptor checks that need no layer pointers (sealing and verifying touch
+ * only the slot buffer). */
+static int slot_desc_ok(const kvo_geom* g, const kvo_desc* d, uint64_t buf_bytes) {
+  if (d->layer >= (uint32_t)g->num_layers || d->role > 1) return 0;
+  if ((int64_t)d->block >= g->num_blocks) return 0;
+  if (d->enc_offset % 16) return 0;
+  if (g->codec[d->role] == O_NONE) return 1;
+  uint64_t need = (uint64_t)kvo_segment_enc_bytes(g, (int)d->role);
+  if (d->enc_offset > buf_bytes || need > buf_bytes - d->enc_offset) return 0;
+  return 1;
+}
+
+void kvo_seal(const kvo_geom* g, const kvo_desc* descs, uint32_t n, const uint8_t* buf,
+              uint64_t buf_bytes, const uint8_t* status, kvo_header* out) {
+  for (uint32_t i = 0; i < n; ++i) {
+    const kvo_desc* d = &descs[i];
+    kvo_header h;
+    memset(&h, 0, sizeof h);
+    h.version = 1;
+    h.orig_bytes = (uint64_t)kvo_segment_raw_bytes(g);
+    if (!slot_desc_ok(g, d, buf_bytes)) {
+      h.status = S_BAD_DESC;
+    } else {
+      h.format = header_format(g, (int)d->role);
+      h.status = status[i];
+      if (status[i] == S_ENCODED && g->codec[d->role] != O_NONE) {
+        h.stored_bytes = (uint64_t)kvo_segment_enc_bytes(g, (int)d->role);
+        h.crc32 = kvo_crc32(buf + d->enc_offset, h.stored_bytes);
+      }
+    }
+    out[i] = h;
+  }
+}
+
+void kvo_verify(const kvo_geom* g, const kvo_desc* descs, uint32_t n, const uint8_t* buf,
+                uint64_t buf_bytes, const kvo_header* hdr, uint8_t* result) {
+  for (uint32_t i = 0; i < n; ++i) {
+    const kvo_desc* d = &descs[i];
+    const kvo_header* h = &hdr[i];
+    if (!slot_desc_ok(g, d, buf_bytes) || g->codec[d->role] == O_NONE) { result[i] = S_BAD_DESC; continue; }
+    int ok = h->version == 1 && h->format == header_format(g, (int)d->role) &&
+             h->orig_bytes == (uint64_t)kvo_segment_raw_bytes(g) &&
+             h->status >= S_ENCODED && h->status <= S_BAD_DESC;
+    if (ok && h->status == S_ENCODED)
+      ok = h->stored_bytes == (uint64_t)kvo_segment_enc_bytes(g, (int)d->role) &&
+           kvo_crc32(buf + d->enc_offset, h->stored_bytes) == h->crc32;
+    else if (ok)
+      ok = h->stored_bytes == 0;
+    result[i] = ok ? (uint8_t)h->status : (uint8_t)S_CORRUPT;
+  }
 }
 
 /* ======================================================================== */
