@@ -120,6 +120,7 @@ class Arm:
         self.dst_view = [t if i in used else None for i, t in enumerate(self.dst)]
         prot = [l for l in range(case.num_layers)
                 if l < arm.protect[0] or l >= case.num_layers - arm.protect[1]]
+        self.prot = set(prot)
         self.n_coded = sum(1 for r in rows if r[0] not in prot)  # segments actually transformed
         self.raw_seg = raw_seg
         self.raw_bytes = self.n_coded * raw_seg
@@ -289,6 +290,7 @@ def run_gpu(args, dist, world, rank, local):
     host_link = None
     if args.host_link and world == 1:
         host_link = run_host_link(args, arms, stream)
+    integrity = run_integrity(args, arms, stream, peak) if args.integrity else None
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -309,6 +311,7 @@ def run_gpu(args, dist, world, rank, local):
         "clocks": clk,
         "e2e": e2e,
         "host_link": host_link,
+        "integrity": integrity,
     }
     shrunk = args.layers is not None or args.pages is not None or args.arm is not None
     if shrunk:
@@ -427,6 +430,45 @@ def run_host_link(args, arms, stream):
         res["link_bytes"] = link
         out[a.arm.name] = res
         del enc_h, st_h
+    return out
+
+
+def run_integrity(args, arms, stream, peak):
+    """Segment headers (CRC-32 of every encoded slot): seal after encode and
+    verify before decode, per arm.  Median CUDA-event time on the launching
+    stream; GB/s of slot bytes checked and, against the HBM peak, of algorithmic
+    bytes (slots read + 32-byte headers written or read + descriptors)."""
+    out = {}
+    reps = max(3, min(args.steps, 20))
+    for a in arms:
+        hdr = torch.empty(a.n * 32, dtype=torch.uint8, device=a.enc.device)
+        res = torch.empty(a.n, dtype=torch.uint8, device=a.enc.device)
+        a.encode(stream)
+        slot_bytes = sum(a.seg[r[2]] for r in a.rows if r[0] not in a.prot)
+        alg = slot_bytes + a.n * (32 + DESC_BYTES + 1)
+        row = {}
+        for tag, fn in (("seal", lambda: a.codec.seal(a.descs, a.n, a.enc, a.total, a.status, hdr, stream)),
+                        ("verify", lambda: a.codec.verify(a.descs, a.n, a.enc, a.total, hdr, res, stream))):
+            for _ in range(2):
+                fn()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(reps):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            ms = statistics.median(ts)
+            row[tag] = {"ms": round(ms, 4), "slot_gbs": round(slot_bytes / (ms / 1e3) / GB, 1),
+                        "frac_of_hbm": round(alg / (ms / 1e3) / GB / peak, 4)}
+        ok = int((res == K.SEG_ENCODED).sum())
+        row["verified_encoded"] = ok
+        row["slot_bytes"] = slot_bytes
+        out[a.arm.name] = row
+        del hdr, res
     return out
 
 
@@ -583,6 +625,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-host-link", dest="host_link", action="store_false",
                     help="skip the host-resident slot offload/restore timings")
+    ap.add_argument("--no-integrity", dest="integrity", action="store_false",
+                    help="skip the segment header seal/verify timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)

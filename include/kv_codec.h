@@ -116,6 +116,7 @@ extern "C" {
 #define KV_SEG_RAW_OVERSIZE 6u  /* source segment larger than 16 MiB */
 #define KV_SEG_RAW_NO_SAVING 7u /* aligned encoding saves less than 12.5% */
 #define KV_SEG_BAD_DESC 8u      /* descriptor invalid (see kv_segment_desc); nothing written */
+#define KV_SEG_CORRUPT 9u       /* kv_codec_verify: header or CRC-32 mismatch; treat as a miss */
 /* In every RAW_* / BAD_DESC case the segment's slot is not written (BAD_DESC)
  * or holds unspecified bytes (RAW_*); the caller keeps the raw page. */
 
@@ -162,6 +163,21 @@ typedef struct kv_segment_desc {
   uint64_t enc_offset;    /* byte offset of the segment's slot in the encoded buffer */
 } kv_segment_desc;
 
+/* Segment header ("KV precision and storage encoding", OrbitKV docs, section
+ * "Ownership, storage and GDS": every encoded segment carries a version, its
+ * original length, its format, its stored length and a CRC32).  32 bytes,
+ * little endian, one per descriptor. */
+#define KV_SEGMENT_FORMAT_VERSION 1u
+typedef struct kv_segment_header {
+  uint32_t version;       /* KV_SEGMENT_FORMAT_VERSION */
+  uint32_t format;        /* codec kind | dtype << 8 | log2(head_dim) << 16 (0 for a bad descriptor) */
+  uint64_t orig_bytes;    /* source segment bytes: num_kv_heads * block_tokens * head_dim * 2 */
+  uint64_t stored_bytes;  /* encoded slot bytes; 0 when the segment stayed raw */
+  uint32_t crc32;         /* CRC-32 of the stored bytes: reflected polynomial 0xEDB88320,
+                             register preset to all ones, result complemented (zlib's) */
+  uint32_t status;        /* the segment's status when sealed */
+} kv_segment_header;
+
 typedef struct kv_codec_s* kv_codec_t;
 
 /* Validate a geometry and build the handle: sign vector (SplitMix64 of
@@ -207,6 +223,29 @@ int kv_codec_decode(kv_codec_t codec, void* const* layer_ptrs, uint32_t n_layer_
                     const kv_segment_desc* d_descs, uint32_t n_segments, const void* d_in,
                     uint64_t in_bytes, const uint8_t* d_status, uint8_t* d_result,
                     void* stream);
+
+/* Seal n_segments encoded slots: write one kv_segment_header per descriptor,
+ * with the CRC-32 of the slot for segments whose status is KV_SEG_ENCODED
+ * (stored_bytes 0 and crc32 0 for the others; status KV_SEG_BAD_DESC and
+ * format 0 for an invalid descriptor).  buf / buf_bytes: the encoded buffer
+ * (16-byte aligned); status: the statuses kv_codec_encode wrote; headers: n
+ * records, 8-byte aligned.  descs, buf, status and headers may be device or
+ * pinned host memory.  Stream-ordered like encode. */
+int kv_codec_seal(kv_codec_t codec, const kv_segment_desc* descs, uint32_t n_segments,
+                  const void* buf, uint64_t buf_bytes, const uint8_t* status,
+                  kv_segment_header* headers, void* stream);
+
+/* Check n_segments slots against their headers before decode (section
+ * "Ownership, storage and GDS": checksums are validated before GPU decode and a
+ * damaged object becomes a miss).  result[i] = the header's status when the
+ * header matches this geometry (version, format, original and stored length)
+ * and, for KV_SEG_ENCODED, the slot's CRC-32 matches; KV_SEG_CORRUPT otherwise;
+ * KV_SEG_BAD_DESC for an invalid descriptor or a role without codec.  Passing
+ * result as the status of kv_codec_decode restores exactly the verified
+ * segments.  Buffers as for kv_codec_seal; result: n bytes. */
+int kv_codec_verify(kv_codec_t codec, const kv_segment_desc* descs, uint32_t n_segments,
+                    const void* buf, uint64_t buf_bytes, const kv_segment_header* headers,
+                    uint8_t* result, void* stream);
 
 /* Static description of an error code. */
 const char* kv_codec_strerror(int code);

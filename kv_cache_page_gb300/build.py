@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 SRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvcodec.so")
-UNITS = ["fp8.cu", "uniform.cu", "turboquant.cu", "int8.cu", "kv_codec_host.cpp"]
+UNITS = ["fp8.cu", "uniform.cu", "turboquant.cu", "int8.cu", "crc.cu", "kv_codec_host.cpp"]
 HEADERS = ["kv_internal.h", "device_common.cuh"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -24,13 +24,17 @@ LAYOUT = {"separate": 1, "packed": 2}
 CODEC = {"none": 0, "fp8_cast": 1, "fp8_fixed": 2, "fp8_dynamic": 3, "tq3": 4, "tq4": 5,
          "uni3": 6, "uni4": 7, "uni8": 8, "int8": 9}
 SEG_ENCODED, SEG_RAW_NONFINITE, SEG_RAW_RANGE, SEG_RAW_PROTECTED = 1, 2, 3, 4
-SEG_RAW_POLICY, SEG_RAW_OVERSIZE, SEG_RAW_NO_SAVING, SEG_BAD_DESC = 5, 6, 7, 8
+SEG_RAW_POLICY, SEG_RAW_OVERSIZE, SEG_RAW_NO_SAVING, SEG_BAD_DESC, SEG_CORRUPT = 5, 6, 7, 8, 9
+# kv_segment_header
+HEADER_DTYPE = np.dtype([("version", "<u4"), ("format", "<u4"), ("orig_bytes", "<u8"),
+                         ("stored_bytes", "<u8"), ("crc32", "<u4"), ("status", "<u4")])
 
 DESC_DTYPE = np.dtype([("layer", "<u4"), ("block", "<u4"), ("role", "<u4"),
                        ("reserved", "<u4"), ("enc_offset", "<u8")])
 
 EXPORTS = ("kv_codec_create", "kv_codec_destroy", "kv_codec_segment_bytes", "kv_codec_encode",
-           "kv_codec_decode", "kv_codec_strerror", "kv_codec_codebook", "kv_codec_signs",
+           "kv_codec_decode", "kv_codec_seal", "kv_codec_verify", "kv_codec_strerror",
+           "kv_codec_codebook", "kv_codec_signs",
            "kv_codec_abi_version")
 
 
@@ -70,13 +74,16 @@ def lib():
         L.kv_codec_encode.argtypes = [vp, C.POINTER(vp), C.c_uint32, vp, C.c_uint32, vp, C.c_uint64, vp, vp]
         L.kv_codec_decode.argtypes = [vp, C.POINTER(vp), C.c_uint32, vp, C.c_uint32, vp, C.c_uint64, vp,
                                       vp, vp]
+        L.kv_codec_seal.argtypes = [vp, vp, C.c_uint32, vp, C.c_uint64, vp, vp, vp]
+        L.kv_codec_verify.argtypes = [vp, vp, C.c_uint32, vp, C.c_uint64, vp, vp, vp]
         L.kv_codec_strerror.argtypes = [C.c_int]
         L.kv_codec_strerror.restype = C.c_char_p
         L.kv_codec_codebook.argtypes = [C.c_uint32, C.c_uint32, C.POINTER(C.c_float), C.POINTER(C.c_float)]
         L.kv_codec_signs.argtypes = [C.c_uint64, C.c_uint32, C.POINTER(C.c_uint8)]
         L.kv_codec_abi_version.restype = C.c_uint32
         for f in ("kv_codec_create", "kv_codec_destroy", "kv_codec_segment_bytes", "kv_codec_encode",
-                  "kv_codec_decode", "kv_codec_codebook", "kv_codec_signs"):
+                  "kv_codec_decode", "kv_codec_seal", "kv_codec_verify", "kv_codec_codebook",
+                  "kv_codec_signs"):
             getattr(L, f).restype = C.c_int
         _LIB = L
     return _LIB
@@ -206,3 +213,17 @@ class Codec:
         _check(lib().kv_codec_decode(self._h, arr, n, _ptr(descs), n_segments, _ptr(enc), enc_bytes,
                                      _ptr(status), _ptr(result), _stream_handle(stream)),
                "kv_codec_decode")
+
+    def seal(self, descs, n_segments: int, buf, buf_bytes: int, status, headers, stream=None):
+        """One 32-byte kv_segment_header per descriptor into `headers` (a uint8 tensor
+        of 32 * n bytes, or HEADER_DTYPE memory), CRC-32 of every ENCODED slot.
+        Buffers: device or pinned host tensors."""
+        _check(lib().kv_codec_seal(self._h, _ptr(descs), n_segments, _ptr(buf), buf_bytes, _ptr(status),
+                                   _ptr(headers), _stream_handle(stream)), "kv_codec_seal")
+
+    def verify(self, descs, n_segments: int, buf, buf_bytes: int, headers, result, stream=None):
+        """Check slots against their headers: result[i] = the header's status, or
+        SEG_CORRUPT on a header or CRC-32 mismatch (a miss for decode)."""
+        _check(lib().kv_codec_verify(self._h, _ptr(descs), n_segments, _ptr(buf), buf_bytes,
+                                     _ptr(headers), _ptr(result), _stream_handle(stream)),
+               "kv_codec_verify")

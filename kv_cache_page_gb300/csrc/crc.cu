@@ -1,0 +1,163 @@
+// crc.cu -- segment headers: CRC-32 of encoded slots (seal) and their check
+// before decode (verify).
+//
+// "KV precision and storage encoding" (OrbitKV docs), section "Ownership,
+// storage and GDS": each encoded segment carries a version, its original
+// length, its format, its stored length and a CRC32; checksums are validated
+// before GPU decode, and a damaged object becomes a miss.
+//
+// CRC-32 here is zlib's (reflected polynomial 0xEDB88320, register preset to
+// all ones, result complemented).  One warp codes one slot.  With R(M) the
+// register of message M fed into a zero register and F_n the map "advance
+// the register through n zero bytes" (both GF(2)-linear):
+//   CRC(M) = R(M) ^ F_N(~0) ^ ~0,   R(A || B) = F_|B|(R(A)) ^ R(B),
+// and leading zero bytes leave R unchanged.  So the slot is front-padded to a
+// multiple of 512 bytes, lane l reads the 16-byte chunks l, l + 32, ... (one
+// coalesced 512-byte row per warp load), keeps s = F_512(s) ^ R(chunk), and
+// finally advances s by the 16 * (31 - l) bytes that follow its last chunk;
+// the xor of the lanes is R(M).  Every map is applied as 16-entry nibble
+// tables in shared memory (a table fills 16 distinct banks, so any indices
+// are conflict-free).
+#include "device_common.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int kCrcCtas = 8;              // resident CTAs per SM (8 warps, one slot each)
+constexpr int kWarps = kThreads / 32;
+constexpr int kRowUnroll = 4;            // rows of 16-byte chunks in flight per lane
+
+// A 32-bit GF(2)-linear map given as 8 nibble tables.
+__device__ __forceinline__ uint32_t apply8(const uint32_t (*t)[16], uint32_t r) {
+  const uint32_t a = t[0][r & 15u] ^ t[1][(r >> 4) & 15u] ^ t[2][(r >> 8) & 15u];
+  const uint32_t b = t[3][(r >> 12) & 15u] ^ t[4][(r >> 16) & 15u] ^ t[5][(r >> 20) & 15u];
+  return a ^ b ^ t[6][(r >> 24) & 15u] ^ t[7][r >> 28];
+}
+
+// R(chunk) of one 16-byte chunk: nibble i (byte i/2, low or high half) through
+// its own table.
+__device__ __forceinline__ uint32_t chunk_reg(const uint32_t (*t)[16], const uint4& c) {
+  return apply8(t, c.x) ^ apply8(t + 8, c.y) ^ apply8(t + 16, c.z) ^ apply8(t + 24, c.w);
+}
+
+// CRC-32 of the n-byte slot at `slot` (n a multiple of 16), computed by the
+// calling warp; every lane returns the same value.
+__device__ __forceinline__ uint32_t warp_crc(const CrcTables& T, const uint8_t* slot, uint32_t n,
+                                             uint32_t crc_k, uint32_t lane) {
+  const uint32_t pad = (512u - n % 512u) % 512u;
+  const uint32_t rows = (n + pad) / 512u;
+  uint32_t s = 0;
+  for (uint32_t m = 0; m < rows; m += kRowUnroll) {
+    uint4 c[kRowUnroll];
+#pragma unroll
+    for (int u = 0; u < kRowUnroll; ++u) {
+      const int64_t off = (int64_t)(m + u) * 512 + 16 * lane - pad;
+      c[u] = (m + u < rows && off >= 0) ? ld_nc16(slot + off) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kRowUnroll; ++u)
+      if (m + u < rows) s = apply8(T.row, s) ^ chunk_reg(T.chunk, c[u]);
+  }
+  const uint32_t after = 31u - lane;  // chunks of the last row after this lane's
+#pragma unroll
+  for (int b = 0; b < 5; ++b) {
+    const uint32_t t = apply8(T.fin[b], s);
+    s = ((after >> b) & 1u) ? t : s;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s ^= __shfl_xor_sync(0xffffffffu, s, o);
+  return s ^ crc_k;
+}
+
+__device__ __forceinline__ void load_tables(const CrcParams& p, CrcTables& t) {
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(&p.tab);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(&t);
+  for (uint32_t k = threadIdx.x; k < sizeof(CrcTables) / 4; k += blockDim.x) dst[k] = src[k];
+  __syncthreads();
+}
+
+// Descriptor checks that need no layer pointers.
+__device__ __forceinline__ bool slot_ok(const CrcParams& p, const kv_segment_desc* dp, uint32_t& role,
+                                        uint64_t& off) {
+  const uint32_t layer = __ldg(&dp->layer), block = __ldg(&dp->block);
+  role = __ldg(&dp->role);
+  off = __ldg(reinterpret_cast<const unsigned long long*>(&dp->enc_offset));
+  if (layer >= p.L || role > 1u || (uint64_t)block >= p.num_blocks || (off & 15u)) return false;
+  if (p.codec[role] == KV_CODEC_NONE) return true;
+  return off <= p.buf_bytes && p.seg_bytes[role] <= p.buf_bytes - off;
+}
+
+__device__ __forceinline__ void store_header(kv_segment_header* h, uint32_t format, uint64_t stored,
+                                             uint32_t crc, uint32_t status, uint64_t orig) {
+  uint64_t* w = reinterpret_cast<uint64_t*>(h);
+  w[0] = (uint64_t)KV_SEGMENT_FORMAT_VERSION | ((uint64_t)format << 32);
+  w[1] = orig;
+  w[2] = stored;
+  w[3] = (uint64_t)crc | ((uint64_t)status << 32);
+}
+
+__global__ void __launch_bounds__(kThreads) crc_seal_kernel(const __grid_constant__ CrcParams p) {
+  __shared__ CrcTables t;
+  load_tables(p, t);
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  for (uint32_t i = blockIdx.x * kWarps + warp; i < p.n_segments; i += gridDim.x * kWarps) {
+    uint32_t role;
+    uint64_t off;
+    if (!slot_ok(p, p.descs + i, role, off)) {
+      if (lane == 0) store_header(p.headers + i, 0, 0, 0, KV_SEG_BAD_DESC, p.orig_bytes);
+      continue;
+    }
+    const uint32_t st = p.status[i];
+    uint64_t stored = 0;
+    uint32_t crc = 0;
+    if (st == KV_SEG_ENCODED && p.codec[role] != KV_CODEC_NONE) {
+      stored = p.seg_bytes[role];
+      crc = warp_crc(t, p.buf + off, (uint32_t)stored, p.crc_k[role], lane);
+    }
+    if (lane == 0) store_header(p.headers + i, p.format[role], stored, crc, st, p.orig_bytes);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) crc_verify_kernel(const __grid_constant__ CrcParams p) {
+  __shared__ CrcTables t;
+  load_tables(p, t);
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  for (uint32_t i = blockIdx.x * kWarps + warp; i < p.n_segments; i += gridDim.x * kWarps) {
+    uint32_t role;
+    uint64_t off;
+    if (!slot_ok(p, p.descs + i, role, off) || p.codec[role] == KV_CODEC_NONE) {
+      if (lane == 0) p.result[i] = KV_SEG_BAD_DESC;
+      continue;
+    }
+    const uint64_t* w = reinterpret_cast<const uint64_t*>(p.headers + i);
+    const uint64_t w0 = __ldg(reinterpret_cast<const unsigned long long*>(w));
+    const uint64_t orig = __ldg(reinterpret_cast<const unsigned long long*>(w + 1));
+    const uint64_t stored = __ldg(reinterpret_cast<const unsigned long long*>(w + 2));
+    const uint64_t w3 = __ldg(reinterpret_cast<const unsigned long long*>(w + 3));
+    const uint32_t st = (uint32_t)(w3 >> 32);
+    bool ok = (uint32_t)w0 == KV_SEGMENT_FORMAT_VERSION && (uint32_t)(w0 >> 32) == p.format[role] &&
+              orig == p.orig_bytes && st >= KV_SEG_ENCODED && st <= KV_SEG_BAD_DESC;
+    if (ok && st == KV_SEG_ENCODED) {
+      ok = stored == p.seg_bytes[role];
+      if (ok) ok = warp_crc(t, p.buf + off, (uint32_t)stored, p.crc_k[role], lane) == (uint32_t)w3;
+    } else if (ok) {
+      ok = stored == 0;
+    }
+    if (lane == 0) p.result[i] = ok ? (uint8_t)st : (uint8_t)KV_SEG_CORRUPT;
+  }
+}
+
+}  // namespace
+
+int launch_crc(const CrcParams& p, int seal, void* stream) {
+  const void* k = seal ? reinterpret_cast<const void*>(crc_seal_kernel)
+                       : reinterpret_cast<const void*>(crc_verify_kernel);
+  unsigned grid = 0;
+  const int rc = grid_for(k, (p.n_segments + kWarps - 1) / kWarps, kCrcCtas, &grid);
+  if (rc != KV_OK || grid == 0) return rc;
+  void* args[] = {const_cast<CrcParams*>(&p)};
+  const cudaError_t e = cudaLaunchKernel(k, dim3(grid), dim3(kThreads), args, 0, (cudaStream_t)stream);
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+}  // namespace kvc

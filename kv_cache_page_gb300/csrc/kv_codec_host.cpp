@@ -21,7 +21,8 @@
 #include "kv_internal.h"
 
 struct kv_codec_s {
-  kvc::Params p;  // geometry part filled at create; call part per call
+  kvc::Params p;       // geometry part filled at create; call part per call
+  kvc::CrcParams crc;  // seal / verify: tables and per-role constants filled at create
 };
 
 namespace {
@@ -138,6 +139,68 @@ bool build_index_table(const float* bnd, uint32_t nb, float c, float* thr, uint3
     lo[cell + kvc::kLutHalf] = below;
   }
   return true;
+}
+
+// --- CRC-32 (zlib's: reflected polynomial 0xEDB88320) register maps.  A
+// GF(2)-linear map of the 32-bit register is kept as the images of its 32
+// unit vectors; powers of "advance by one zero byte" come by squaring.
+constexpr uint32_t kCrcPoly = 0xEDB88320u;
+
+struct Gf2Map {
+  uint32_t col[32];
+};
+
+uint32_t gf2_apply(const Gf2Map& m, uint32_t v) {
+  uint32_t r = 0;
+  for (int j = 0; v; ++j, v >>= 1)
+    if (v & 1u) r ^= m.col[j];
+  return r;
+}
+
+Gf2Map gf2_compose(const Gf2Map& a, const Gf2Map& b) {  // a after b
+  Gf2Map c;
+  for (int j = 0; j < 32; ++j) c.col[j] = gf2_apply(a, b.col[j]);
+  return c;
+}
+
+uint32_t crc_bit_steps(uint32_t r, int bits) {
+  for (int k = 0; k < bits; ++k) r = (r & 1u) ? (r >> 1) ^ kCrcPoly : (r >> 1);
+  return r;
+}
+
+// The register r advanced through n zero bytes.
+uint32_t crc_advance(uint32_t r, uint64_t n) {
+  Gf2Map step;
+  for (int j = 0; j < 32; ++j) step.col[j] = crc_bit_steps(1u << j, 8);
+  while (n) {
+    if (n & 1u) r = gf2_apply(step, r);
+    step = gf2_compose(step, step);
+    n >>= 1;
+  }
+  return r;
+}
+
+// Nibble tables of the kernels (see CrcTables).  Chunk nibble i = 8 w + k
+// sits in byte 4 w + k/2 of the chunk (low half for even k) and is followed by
+// 15 - that byte's index bytes of the chunk.
+void build_crc_tables(kvc::CrcTables& t) {
+  for (int i = 0; i < 32; ++i) {
+    const int byte = 4 * (i / 8) + (i % 8) / 2, shift = 4 * (i % 2);
+    for (uint32_t v = 0; v < 16; ++v)
+      t.chunk[i][v] = crc_advance(crc_bit_steps(v << shift, 8), (uint64_t)(15 - byte));
+  }
+  for (int k = 0; k < 8; ++k)
+    for (uint32_t v = 0; v < 16; ++v) {
+      t.row[k][v] = crc_advance(v << (4 * k), 512);
+      for (int b = 0; b < 5; ++b) t.fin[b][k][v] = crc_advance(v << (4 * k), 16ull << b);
+    }
+}
+
+const kvc::CrcTables& crc_tables() {
+  static kvc::CrcTables tab;
+  static std::once_flag once;
+  std::call_once(once, [] { build_crc_tables(tab); });
+  return tab;
 }
 
 // FP8 scale rule: max(amax, 1e-12) * fl32(1/448), in FP32.
@@ -427,6 +490,20 @@ int kv_codec_create(const kv_codec_geometry* g, kv_codec_t* out) {
   if (fixed)
     for (uint32_t l = 0; l < p.L; ++l)
       for (int r = 0; r < 2; ++r) p.fixed_scale[l][r] = fp8_scale(g->fixed_amax[2 * l + r]);
+  // seal / verify constants
+  kvc::CrcParams& c = h->crc;
+  c.tab = crc_tables();
+  c.L = p.L;
+  c.num_blocks = p.num_blocks;
+  c.orig_bytes = raw;
+  uint32_t lg = 0;
+  while ((1u << lg) < p.D) ++lg;
+  for (int r = 0; r < 2; ++r) {
+    c.codec[r] = p.codec[r];
+    c.format[r] = p.codec[r] | (p.dtype << 8) | (lg << 16);
+    c.seg_bytes[r] = p.seg_bytes[r];
+    c.crc_k[r] = crc_advance(0xFFFFFFFFu, p.seg_bytes[r]) ^ 0xFFFFFFFFu;
+  }
   *out = h;
   return KV_OK;
 }
@@ -459,6 +536,55 @@ int kv_codec_encode(kv_codec_t h, const void* const* layer_ptrs, uint32_t n_laye
   p.n_segments = n_segments;
   p.buf_bytes = out_bytes;
   return launch_all(&call, kvc::kEncode, stream);
+}
+
+int kv_codec_seal(kv_codec_t h, const kv_segment_desc* descs, uint32_t n_segments, const void* buf,
+                  uint64_t buf_bytes, const uint8_t* status, kv_segment_header* headers, void* stream) {
+  if (!h) return KV_ERR_INVALID_ARG;
+  if (n_segments == 0) return KV_OK;
+  if (!descs || !buf || !status || !headers) return KV_ERR_INVALID_ARG;
+  if (((uintptr_t)buf & 15u) || ((uintptr_t)descs & 7u) || ((uintptr_t)headers & 7u))
+    return KV_ERR_MISALIGNED;
+  kvc::CrcParams p = h->crc;
+  const void* v = nullptr;
+  int rc;
+  if ((rc = device_view(descs, &v)) != KV_OK) return rc;
+  p.descs = static_cast<const kv_segment_desc*>(v);
+  if ((rc = device_view(buf, &v)) != KV_OK) return rc;
+  p.buf = static_cast<const uint8_t*>(v);
+  if ((rc = device_view(status, &v)) != KV_OK) return rc;
+  p.status = static_cast<const uint8_t*>(v);
+  if ((rc = device_view(headers, &v)) != KV_OK) return rc;
+  p.headers = const_cast<kv_segment_header*>(static_cast<const kv_segment_header*>(v));
+  p.result = nullptr;
+  p.n_segments = n_segments;
+  p.buf_bytes = buf_bytes;
+  return kvc::launch_crc(p, 1, stream);
+}
+
+int kv_codec_verify(kv_codec_t h, const kv_segment_desc* descs, uint32_t n_segments, const void* buf,
+                    uint64_t buf_bytes, const kv_segment_header* headers, uint8_t* result,
+                    void* stream) {
+  if (!h) return KV_ERR_INVALID_ARG;
+  if (n_segments == 0) return KV_OK;
+  if (!descs || !buf || !headers || !result) return KV_ERR_INVALID_ARG;
+  if (((uintptr_t)buf & 15u) || ((uintptr_t)descs & 7u) || ((uintptr_t)headers & 7u))
+    return KV_ERR_MISALIGNED;
+  kvc::CrcParams p = h->crc;
+  const void* v = nullptr;
+  int rc;
+  if ((rc = device_view(descs, &v)) != KV_OK) return rc;
+  p.descs = static_cast<const kv_segment_desc*>(v);
+  if ((rc = device_view(buf, &v)) != KV_OK) return rc;
+  p.buf = static_cast<const uint8_t*>(v);
+  if ((rc = device_view(headers, &v)) != KV_OK) return rc;
+  p.headers = const_cast<kv_segment_header*>(static_cast<const kv_segment_header*>(v));
+  if ((rc = device_view(result, &v)) != KV_OK) return rc;
+  p.result = const_cast<uint8_t*>(static_cast<const uint8_t*>(v));
+  p.status = nullptr;
+  p.n_segments = n_segments;
+  p.buf_bytes = buf_bytes;
+  return kvc::launch_crc(p, 0, stream);
 }
 
 int kv_codec_decode(kv_codec_t h, void* const* layer_ptrs, uint32_t n_layer_ptrs,

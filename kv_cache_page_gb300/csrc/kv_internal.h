@@ -68,6 +68,39 @@ struct Params {
 
 enum Dir { kEncode = 0, kDecode = 1 };
 
+// Segment checksums (seal / verify).  CRC-32 over a slot is computed by one
+// warp: lane l reads the 16-byte chunks l, l + 32, ... of the slot (front
+// padded with zeros to a multiple of 512 bytes, which leaves a zero-preset CRC
+// unchanged) and keeps the zero-preset CRC register of its chunks, advanced by
+// 512 zero bytes per row; the lanes' registers are then advanced by the
+// 16 * (31 - l) bytes that follow their last chunk and xor-combined.  Every
+// step is a GF(2)-linear map of 32 bits, applied as 16-entry nibble tables.
+struct CrcTables {
+  uint32_t chunk[32][16];   // nibble i of a 16-byte chunk -> its share of the chunk's register
+  uint32_t row[8][16];      // register advanced by 512 zero bytes, per nibble
+  uint32_t fin[5][8][16];   // register advanced by 16 * 2^b zero bytes, b = 0..4
+};
+
+struct CrcParams {
+  CrcTables tab;
+  const kv_segment_desc* descs;
+  uint32_t n_segments;
+  uint32_t L;
+  uint64_t num_blocks;
+  uint32_t codec[2];
+  uint32_t format[2];                   // header format word per role
+  uint64_t seg_bytes[2];
+  uint32_t crc_k[2];                    // CRC of a zero slot of seg_bytes[role] (preset and complement)
+  uint64_t orig_bytes;
+  const uint8_t* buf;
+  uint64_t buf_bytes;
+  const uint8_t* status;                // seal: input statuses
+  kv_segment_header* headers;           // seal: written; verify: read
+  uint8_t* result;                      // verify: written
+};
+
+int launch_crc(const CrcParams& p, int seal, void* stream);
+
 // Kernel launchers (one per codec family), defined in the .cu files.  `codec`
 // is the KV_CODEC_* kind the launch runs; grid size is chosen from the device.
 int launch_fp8(const Params& p, int dir, uint32_t codec, void* stream);

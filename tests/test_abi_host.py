@@ -170,6 +170,26 @@ def test_call_argument_checks_need_no_gpu():
     c.close()
 
 
+def test_seal_verify_argument_checks_need_no_gpu():
+    c = K.Codec(**_kw())
+    with pytest.raises(K.KvCodecError) as e:
+        c.seal(0x2000, 1, None, 1024, 0x4000, 0x5000, stream=0)
+    assert e.value.code == -1
+    with pytest.raises(K.KvCodecError) as e:
+        c.seal(0x2000, 1, 0x3008, 1024, 0x4000, 0x5000, stream=0)      # slots not 16-aligned
+    assert e.value.code == -5
+    with pytest.raises(K.KvCodecError) as e:
+        c.verify(0x2000, 1, 0x3000, 1024, 0x5004, 0x6000, stream=0)    # headers not 8-aligned
+    assert e.value.code == -5
+    with pytest.raises(K.KvCodecError) as e:
+        c.verify(0x2000, 1, 0x3000, 1024, 0x5000, None, stream=0)
+    assert e.value.code == -1
+    c.seal(0, 0, 0, 0, 0, 0, stream=0)                                 # n = 0: no-op
+    c.verify(0, 0, 0, 0, 0, 0, stream=0)
+    assert K.HEADER_DTYPE.itemsize == 32 == O.HEADER_DTYPE.itemsize
+    c.close()
+
+
 def test_strerror_covers_codes():
     import os
     import re
