@@ -27,7 +27,7 @@ _LIB = None
 # Interface numbers (written independently of the product's header).
 FP16, BF16 = 1, 2
 SEPARATE, PACKED = 1, 2
-NONE, FP8_CAST, FP8_FIXED, FP8_DYNAMIC, TQ3, TQ4, UNI3, UNI4, UNI8, INT8 = range(10)
+NONE, FP8_CAST, FP8_FIXED, FP8_DYNAMIC, TQ3, TQ4, UNI3, UNI4, UNI8, INT8, TQ2, UNI2 = range(12)
 (S_ENCODED, S_RAW_NONFINITE, S_RAW_RANGE, S_RAW_PROTECTED, S_RAW_POLICY,
  S_RAW_OVERSIZE, S_RAW_NO_SAVING, S_BAD_DESC, S_CORRUPT) = range(1, 10)
 # segment header {u32 version, u32 format, u64 orig_bytes, u64 stored_bytes, u32 crc32, u32 status}

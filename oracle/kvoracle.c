@@ -38,7 +38,8 @@ enum { O_FP16 = 1, O_BF16 = 2 };
 enum { O_SEPARATE = 1, O_PACKED = 2 };
 enum {
   O_NONE = 0, O_FP8_CAST = 1, O_FP8_FIXED = 2, O_FP8_DYNAMIC = 3,
-  O_TQ3 = 4, O_TQ4 = 5, O_UNI3 = 6, O_UNI4 = 7, O_UNI8 = 8, O_INT8 = 9
+  O_TQ3 = 4, O_TQ4 = 5, O_UNI3 = 6, O_UNI4 = 7, O_UNI8 = 8, O_INT8 = 9,
+  O_TQ2 = 10, O_UNI2 = 11
 };
 enum {
   S_ENCODED = 1, S_RAW_NONFINITE = 2, S_RAW_RANGE = 3, S_RAW_PROTECTED = 4,
@@ -457,6 +458,7 @@ typedef struct {
 
 static int codec_bits(int codec) {
   switch (codec) {
+    case O_TQ2: case O_UNI2: return 2;
     case O_TQ3: case O_UNI3: return 3;
     case O_TQ4: case O_UNI4: return 4;
     case O_UNI8: return 8;
@@ -464,8 +466,8 @@ static int codec_bits(int codec) {
   }
 }
 static int is_fp8(int c) { return c == O_FP8_CAST || c == O_FP8_FIXED || c == O_FP8_DYNAMIC; }
-static int is_tq(int c) { return c == O_TQ3 || c == O_TQ4; }
-static int is_uni(int c) { return c == O_UNI3 || c == O_UNI4 || c == O_UNI8; }
+static int is_tq(int c) { return c == O_TQ2 || c == O_TQ3 || c == O_TQ4; }
+static int is_uni(int c) { return c == O_UNI2 || c == O_UNI3 || c == O_UNI4 || c == O_UNI8; }
 
 /* [HIQ "Why exactly 1,152 bytes?"]: the INT8 codec stores one record per
  * token row of a role: the H heads' int8 codes (H*D bytes), then their H BF16

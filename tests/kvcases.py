@@ -7,7 +7,7 @@ from kv_cache_page_gb300 import synth
 
 CODEC_IDS = {"none": O.NONE, "fp8_cast": O.FP8_CAST, "fp8_fixed": O.FP8_FIXED,
              "fp8_dynamic": O.FP8_DYNAMIC, "tq3": O.TQ3, "tq4": O.TQ4, "uni3": O.UNI3,
-             "uni4": O.UNI4, "uni8": O.UNI8, "int8": O.INT8}
+             "uni4": O.UNI4, "uni8": O.UNI8, "int8": O.INT8, "tq2": O.TQ2, "uni2": O.UNI2}
 
 
 def host_bits(t: torch.Tensor) -> np.ndarray:

@@ -175,7 +175,7 @@ def test_lloyd_max_matches_max_1960(bits):
     assert abs(mse - mse_tab) / mse_tab < 2e-3
 
 
-@pytest.mark.parametrize("bits", [3, 4])
+@pytest.mark.parametrize("bits", [2, 3, 4])
 def test_lloyd_max_centroid_condition_by_quadrature(bits):
     c = O.lloyd_max_gauss(bits)
     K = 1 << bits
@@ -186,7 +186,7 @@ def test_lloyd_max_centroid_condition_by_quadrature(bits):
         assert abs(m1 / m0 - c[j]) < 1e-9
 
 
-@pytest.mark.parametrize("bits", [3, 4])
+@pytest.mark.parametrize("bits", [2, 3, 4])
 @pytest.mark.parametrize("D", HEAD_DIMS)
 def test_codebook_scaling_and_symmetry(bits, D):
     cent, bnd = O.codebook(bits, D)

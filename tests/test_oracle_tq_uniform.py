@@ -22,7 +22,7 @@ def sylvester(D):
 
 
 # ---------------------------------------------------------------- centroid index
-@pytest.mark.parametrize("bits", [3, 4])
+@pytest.mark.parametrize("bits", [2, 3, 4])
 @pytest.mark.parametrize("D", HEAD_DIMS)
 def test_index_is_nearest_centroid_brute_force(bits, D):
     """Away from the boundaries the index is the nearest FP64 centroid; at each
@@ -45,7 +45,7 @@ def test_index_is_nearest_centroid_brute_force(bits, D):
 
 
 # ---------------------------------------------------------------- TQ encode
-@pytest.mark.parametrize("bits", [3, 4])
+@pytest.mark.parametrize("bits", [2, 3, 4])
 @pytest.mark.parametrize("D", HEAD_DIMS)
 def test_tq_recovers_planted_codes(bits, D):
     """Plant codes: y* = cent[c] / |cent[c]|, x = n * diag(signs) H y* / sqrt(D)
@@ -75,7 +75,7 @@ def test_tq_recovers_planted_codes(bits, D):
     assert np.all(np.abs(nf - n64) <= 2.0**-10 * n64)
 
 
-@pytest.mark.parametrize("bits", [3, 4])
+@pytest.mark.parametrize("bits", [2, 3, 4])
 @pytest.mark.parametrize("D", HEAD_DIMS)
 def test_tq_decode_matches_fp64_restatement(bits, D):
     """decode = n16 * diag(signs) H (c / |c|) / sqrt(D), c = centroids of the codes."""
@@ -96,7 +96,7 @@ def test_tq_decode_matches_fp64_restatement(bits, D):
         assert abs(np.linalg.norm(out[k]) / scale - 1) <= (2 * math.log2(D) + 8) * U32
 
 
-@pytest.mark.parametrize("bits,mse", [(3, 0.03455), (4, 0.009497)])
+@pytest.mark.parametrize("bits,mse", [(2, 0.1175), (3, 0.03455), (4, 0.009497)])
 def test_tq_relative_error_is_lloyd_max_distortion(bits, mse):
     """On Gaussian vectors the rotated coordinates are ~N(0, 1/D); the relative
     squared error after norm correction is close to the Lloyd-Max distortion."""
@@ -119,7 +119,7 @@ def test_tq_zero_vector():
 
 
 # ---------------------------------------------------------------- uniform
-@pytest.mark.parametrize("bits", [3, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 @pytest.mark.parametrize("D", HEAD_DIMS)
 def test_uniform_bound_and_extremes(bits, D):
     rng = np.random.default_rng(bits * 10 + D)
@@ -169,7 +169,7 @@ def test_uniform_constant_and_zero_vectors():
 
 
 # ---------------------------------------------------------------- packing
-@pytest.mark.parametrize("bits", [3, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 def test_pack_is_little_endian_bitstream(bits):
     rng = np.random.default_rng(bits)
     for n in (32, 64, 128, 256):
