@@ -17,15 +17,15 @@
  * with vectors ordered v = token * num_kv_heads + head, padded to a multiple of
  * 128 bytes (kv_codec_segment_bytes gives the size).  Codes per vector:
  *     FP8 (all modes)     head_dim bytes, E4M3FN
- *     TQ3 / TQ4           head_dim*bits/8 bytes, little-endian bit stream
+ *     TQ2 / TQ3 / TQ4     head_dim*bits/8 bytes, little-endian bit stream
  *                         (code i in bits [bits*i, bits*i + bits))
- *     UNIFORM3/4          head_dim*bits/8 bytes, same bit stream
+ *     UNIFORM2/3/4        head_dim*bits/8 bytes, same bit stream
  *     UNIFORM8            head_dim bytes
  * Metadata per vector:
  *     FP8_DYNAMIC         FP32 scale (4 bytes)
  *     FP8_CAST/FIXED      none
- *     TQ3 / TQ4           FP16 norm of the source vector (2 bytes)
- *     UNIFORM3/4/8        FP16 minimum, FP16 step (4 bytes)
+ *     TQ2 / TQ3 / TQ4     FP16 norm of the source vector (2 bytes)
+ *     UNIFORM2/3/4/8      FP16 minimum, FP16 step (4 bytes)
  * E.g. head_dim 128: TQ4 K 66, UNIFORM4 V 68, TQ3 K 50, UNIFORM3 V 52 bytes per
  * vector (the storage-format page's payload sizes).
  *
@@ -106,6 +106,8 @@ extern "C" {
 #define KV_CODEC_UNIFORM4 7u
 #define KV_CODEC_UNIFORM8 8u
 #define KV_CODEC_INT8_HEAD 9u   /* symmetric per-head INT8, BF16 scale, token-row records (BF16 only) */
+#define KV_CODEC_TQ2 10u        /* TurboQuant K, 2-bit codes (K role only) */
+#define KV_CODEC_UNIFORM2 11u   /* per-vector uniform, 2-bit codes */
 
 /* ---- per-segment status bytes (written by encode, read by decode) ------- */
 #define KV_SEG_ENCODED 1u       /* slot holds the encoding */

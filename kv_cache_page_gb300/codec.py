@@ -22,7 +22,7 @@ MAX_LAYERS = 512
 DT = {"fp16": 1, "bf16": 2}
 LAYOUT = {"separate": 1, "packed": 2}
 CODEC = {"none": 0, "fp8_cast": 1, "fp8_fixed": 2, "fp8_dynamic": 3, "tq3": 4, "tq4": 5,
-         "uni3": 6, "uni4": 7, "uni8": 8, "int8": 9}
+         "uni3": 6, "uni4": 7, "uni8": 8, "int8": 9, "tq2": 10, "uni2": 11}
 SEG_ENCODED, SEG_RAW_NONFINITE, SEG_RAW_RANGE, SEG_RAW_PROTECTED = 1, 2, 3, 4
 SEG_RAW_POLICY, SEG_RAW_OVERSIZE, SEG_RAW_NO_SAVING, SEG_BAD_DESC, SEG_CORRUPT = 5, 6, 7, 8, 9
 # kv_segment_header

@@ -29,11 +29,12 @@ namespace {
 
 using kvc::Params;
 
-bool valid_codec(uint32_t c) { return c <= KV_CODEC_INT8_HEAD; }
+bool valid_codec(uint32_t c) { return c <= KV_CODEC_UNIFORM2; }
 bool is_fp8(uint32_t c) { return c >= KV_CODEC_FP8_CAST && c <= KV_CODEC_FP8_DYNAMIC; }
-bool is_tq(uint32_t c) { return c == KV_CODEC_TQ3 || c == KV_CODEC_TQ4; }
+bool is_tq(uint32_t c) { return c == KV_CODEC_TQ2 || c == KV_CODEC_TQ3 || c == KV_CODEC_TQ4; }
 uint32_t codec_bits(uint32_t c) {
   switch (c) {
+    case KV_CODEC_TQ2: case KV_CODEC_UNIFORM2: return 2;
     case KV_CODEC_TQ3: case KV_CODEC_UNIFORM3: return 3;
     case KV_CODEC_TQ4: case KV_CODEC_UNIFORM4: return 4;
     case KV_CODEC_UNIFORM8: return 8;

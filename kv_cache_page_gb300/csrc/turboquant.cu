@@ -1,4 +1,4 @@
-// turboquant.cu -- TurboQuant-style K encode / decode kernels (3 and 4 bits).
+// turboquant.cu -- TurboQuant-style K encode / decode kernels (2, 3 and 4 bits).
 //
 // "KV precision and storage encoding" (OrbitKV), section "FP8 and
 // TurboQuant": normalize each head vector, apply deterministic random signs
@@ -219,6 +219,8 @@ __global__ void __launch_bounds__(kThreads, 3) tq_encode_kernel(const __grid_con
       if (in) {
         if (BITS == 4) {
           st16(vc + 16 * li, make_uint4(acc[0], acc[1], acc[2], acc[3]));
+        } else if (BITS == 2) {
+          st8(vc + 8 * li, make_uint2(acc[0] | (acc[1] << 16), acc[2] | (acc[3] << 16)));
         } else {
           st4(vc + 12 * li, acc[0] | (acc[1] << 24));
           st4(vc + 12 * li + 4, (acc[1] >> 8) | (acc[2] << 16));
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
   constexpr int G = D / kTqE, VPW = 32 / G, W = kThreads / 32;
   constexpr int CB = D * BITS / 8;
   constexpr uint32_t CSTEP = W * VPW;
-  constexpr int NPAIR = BITS == 4 ? 256 : 64;  // table of two consecutive codes
+  constexpr int NPAIR = 1 << (2 * BITS);        // table of two consecutive codes
   constexpr int REP = BITS == 4 ? 8 : 16;       // copies (keeps the table within 48 KB of static smem)
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
@@ -276,6 +278,9 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
       if (BITS == 4) {
         const uint4 t = ld_nc16(vc + 16 * li);
         cw[0] = t.x; cw[1] = t.y; cw[2] = t.z; cw[3] = t.w;
+      } else if (BITS == 2) {
+        const uint2 t = ld_nc8(vc + 8 * li);
+        cw[0] = t.x; cw[1] = t.y;
       } else {
         cw[0] = ld_nc4(vc + 12 * li);
         cw[1] = ld_nc4(vc + 12 * li + 4);
@@ -309,6 +314,8 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
         uint32_t v;
         if (BITS == 4) {
           v = __byte_perm(cw[m >> 2], 0, 0x4440 | (m & 3));
+        } else if (BITS == 2) {
+          v = (cw[m >> 3] >> (4 * (m & 7))) & 15u;
         } else {
           const int bit = 6 * m;
           v = __funnelshift_r(cw[bit >> 5], cw[(bit >> 5) + 1], bit & 31) & 63u;
@@ -346,6 +353,9 @@ template <int DT, int D>
 int dispatch_bits(const Params& p, int dir, uint32_t codec, void* stream) {
   const bool enc = dir == kEncode;
   switch (codec) {
+    case KV_CODEC_TQ2:
+      return enc ? launch_codec_kernel(tq_encode_kernel<DT, D, 2>, p, stream, 8)
+                 : launch_codec_kernel(tq_decode_kernel<DT, D, 2>, p, stream, 8);
     case KV_CODEC_TQ3:
       return enc ? launch_codec_kernel(tq_encode_kernel<DT, D, 3>, p, stream, 8)
                  : launch_codec_kernel(tq_decode_kernel<DT, D, 3>, p, stream, 8);

@@ -1,7 +1,8 @@
 // uniform.cu -- per-vector uniform quantization with FP16 minimum and step.
 //
 // "KV precision and storage encoding" (OrbitKV), section "FP8 and TurboQuant":
-// V uses per-vector uniform quantization with an FP16 minimum and scale.
+// V uses per-vector uniform quantization with an FP16 minimum and scale
+// (3 and 4 bits on the page; 2 and 8 bits here as well).
 // Per vector: m = fp16(min x), s = fp16((max x - min x) / (2^b - 1)), codes
 // clamp(rint((x - m) / s), 0, 2^b - 1) against the stored (rounded) m and s,
 // code 0 when s == 0; restore code * s + m.  Codes are a little-endian bit
@@ -115,6 +116,11 @@ __global__ void __launch_bounds__(kThreads) uniform_encode_kernel(const __grid_c
 #pragma unroll
             for (int e = 0; e < 8; ++e) v |= c[e] << (4 * e);
             if (in) st4(vc + 4 * cidx, v);
+          } else if (BITS == 2) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v |= c[e] << (2 * e);
+            if (in) *reinterpret_cast<uint16_t*>(vc + 2 * cidx) = (uint16_t)v;
           } else {
             uint32_t v = 0;
 #pragma unroll
@@ -177,6 +183,7 @@ __global__ void __launch_bounds__(kThreads) uniform_decode_kernel(const __grid_c
           if (in) {
             if (BITS == 8) cw[u][ch] = ld_nc8(vc + 8 * cidx);
             else if (BITS == 4) cw[u][ch].x = ld_nc4(vc + 4 * cidx);
+            else if (BITS == 2) cw[u][ch].x = ld_nc2(vc + 2 * cidx);
             else cw[u][ch].x = load_3bit(vc, cidx);
           }
         }
@@ -218,6 +225,9 @@ template <int DT, int D>
 int dispatch_bits(const Params& p, int dir, uint32_t codec, void* stream) {
   const bool enc = dir == kEncode;
   switch (codec) {
+    case KV_CODEC_UNIFORM2:
+      return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 2>, p, stream, kEncodeCtas)
+                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 2>, p, stream, kDecodeCtas);
     case KV_CODEC_UNIFORM3:
       return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 3>, p, stream, kEncodeCtas)
                  : launch_codec_kernel(uniform_decode_kernel<DT, D, 3>, p, stream, kDecodeCtas);

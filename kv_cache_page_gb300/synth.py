@@ -38,7 +38,7 @@ __all__ = ["Case", "make_case", "CASES"]
 class Arm:
     """One codec configuration run over a workload: codec per role ("none",
     "fp8_cast", "fp8_fixed", "fp8_dynamic", "tq3", "tq4", "uni3", "uni4",
-    "uni8", "int8") and the roles whose segments are submitted."""
+    "uni8", "int8", "tq2", "uni2") and the roles whose segments are submitted."""
     name: str
     k_codec: str
     v_codec: str
@@ -175,7 +175,8 @@ def make_case(name: str, *, device="cpu", num_layers: Optional[int] = None,
             val = [math.inf * s, math.nan, m * s, m * s][kd]
             layers[layer][blk, h, t, role * D + e] = val
         return Case(name, torch.bfloat16, "packed", D, H, T, L, B, _packed_strides(T, H, D),
-                    layers, [Arm("turboquant3", "tq3", "uni3", (0, 1), protect=(2, 2))], seed)
+                    layers, [Arm("turboquant3", "tq3", "uni3", (0, 1), protect=(2, 2)),
+                             Arm("turboquant2", "tq2", "uni2", (0, 1), protect=(2, 2))], seed)
 
     if name == "head_dim_sweep":
         L, B, H = num_layers or 1, num_blocks or 128, 32

@@ -56,7 +56,8 @@ def _kw(**over):
     (dict(num_layers=0), -8),
     (dict(num_layers=513), -8),
     (dict(v_codec="tq3"), -4),
-    (dict(geometry_overrides={"k_codec": 10}), -1),
+    (dict(v_codec="tq2"), -4),
+    (dict(geometry_overrides={"k_codec": 12}), -1),
     (dict(strides=(16 * 8 * 128, 8 * 128, 100)), -5),        # head stride not 16-byte aligned
     (dict(strides=(16 * 8 * 128, 8 * 128, 64)), -3),         # heads overlap (64 < D)
     (dict(strides=(8 * 128, 8 * 128, 128)), -3),             # pages overlap tokens
@@ -97,7 +98,8 @@ def _oracle_geom(k, v, D, H=8, T=16):
 
 @pytest.mark.parametrize("D", [32, 64, 128, 256])
 @pytest.mark.parametrize("kc,vc", [("fp8_cast", "fp8_fixed"), ("fp8_dynamic", "fp8_dynamic"),
-                                   ("tq3", "uni3"), ("tq4", "uni4"), ("uni8", "uni8"), ("none", "uni4")])
+                                   ("tq3", "uni3"), ("tq4", "uni4"), ("uni8", "uni8"), ("none", "uni4"),
+                                   ("tq2", "uni2")])
 @pytest.mark.parametrize("H,T", [(8, 16), (3, 5), (1, 1)])
 def test_segment_bytes_match_oracle(D, kc, vc, H, T):
     c = K.Codec(**_kw(head_dim=D, num_kv_heads=H, block_tokens=T, num_layers=2, num_blocks=2,

@@ -27,7 +27,7 @@ def built():
 
 ALL_CODECS = [("fp8_cast", "fp8_cast"), ("fp8_fixed", "fp8_fixed"), ("fp8_dynamic", "fp8_dynamic"),
               ("tq3", "uni3"), ("tq4", "uni4"), ("uni8", "uni8"), ("uni3", "uni4"), ("none", "fp8_dynamic"),
-              ("tq4", "none")]
+              ("tq4", "none"), ("tq2", "uni2"), ("uni2", "uni8")]
 
 
 def custom_case(*, D, H, T, L, B, dtype, layout, values="normal", seed=0):
@@ -208,7 +208,7 @@ def _exhaustive_layers(dtype):
 
 
 @pytest.mark.parametrize("dtype,codec", [(d, c) for d in ("fp16", "bf16")
-                                         for c in ("fp8_cast", "fp8_dynamic", "uni8", "tq4")]
+                                         for c in ("fp8_cast", "fp8_dynamic", "uni8", "tq4", "tq2")]
                          + [("bf16", "int8")])
 def test_every_16bit_pattern(dtype, codec):
     """All 65,536 source patterns: in-range finite values fill admitted pages, each
@@ -219,7 +219,7 @@ def test_every_16bit_pattern(dtype, codec):
     t = torch.from_numpy(buf.view(np.int16)).view(tdt).reshape(B, 16, 8, 128)
     case = synth.Case("exh", tdt, "separate", 128, 8, 16, 1, B, synth._separate_strides(16, 8, 128),
                       [t, t.clone()], [], 0)
-    vc = "uni4" if codec == "tq4" else codec
+    vc = {"tq4": "uni4", "tq2": "uni2"}.get(codec, codec)
     st, ulps = run_parity(case, synth.Arm("exh", codec, vc, (0,)))
     f = O.src_to_f32(buf.reshape(B, -1), odt)
     bad_page = ~np.all(np.isfinite(f) & (np.abs(f) <= 448), axis=1)

@@ -158,7 +158,7 @@ def _layout_restatement(case, arm, layers_bits, rows, enc):
         if codec == "fp8_dynamic":
             s = np.array([O.fp8_scale_from_amax(O.absmax(v)) for v in x], np.float32)
             body = np.concatenate([O.fp8_encode(x, s).reshape(-1), s.view(np.uint8)])
-        elif codec in ("tq3", "tq4"):
+        elif codec in ("tq2", "tq3", "tq4"):
             bits = int(codec[-1])
             c, n16 = O.tq_encode(x, bits, case.seed)
             body = np.concatenate([np.concatenate([O.pack_bits(r, bits) for r in c]), n16.view(np.uint8)])
