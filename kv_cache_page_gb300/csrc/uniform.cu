@@ -21,11 +21,12 @@ constexpr int kDecodeCtas = 5;
 // Codes of 8 elements: clamp(rint((x - m) / s), 0, L).  The quotient is
 // correctly rounded (q0 = RN(d r), e = RN(d - q0 s) exact, q = RN(q0 + e r));
 // clamping to [0, L] before rounding gives the same integer (0 and L are
-// integers), and RN(q + 1.5 * 2^23) holds rint(q) in its low byte.  The caller
-// passes r = 0 when s == 0, which makes every quotient 0.
+// integers), and RN(q + 1.5 * 2^23) holds rint(q) in its low byte, which is
+// what t[] returns (the higher bits are the magic's).  The caller passes r = 0
+// when s == 0, which makes every quotient 0.
 template <uint32_t LEVELS>
 __device__ __forceinline__ void uniform_codes8(const float (&x)[8], float m, float sc, float r,
-                                               uint32_t (&c)[8]) {
+                                               uint32_t (&t)[8]) {
   const float2 m2 = make_float2(m, m), ns2 = make_float2(-sc, -sc), r2 = make_float2(r, r);
   const float2 mg2 = make_float2(kRoundMagic, kRoundMagic);
 #pragma unroll
@@ -36,10 +37,27 @@ __device__ __forceinline__ void uniform_codes8(const float (&x)[8], float m, flo
     float2 q = fma2(res, r2, q0);
     q.x = fminf(fmaxf(q.x, 0.0f), (float)LEVELS);
     q.y = fminf(fmaxf(q.y, 0.0f), (float)LEVELS);
-    const float2 t = add2(q, mg2);
-    c[e] = __float_as_uint(t.x) & 0xffu;
-    c[e + 1] = __float_as_uint(t.y) & 0xffu;
+    const float2 v = add2(q, mg2);
+    t[e] = __float_as_uint(v.x);
+    t[e + 1] = __float_as_uint(v.y);
   }
+}
+
+// The low bytes of four words, in order, as one word (three byte permutes).
+__device__ __forceinline__ uint32_t low_bytes4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+
+// Codes of 8 elements (t[] from uniform_codes8) as the little-endian bit
+// stream of BITS-bit codes: 8 bytes (BITS = 8: byte permutes of the low
+// bytes) or the low 8 * BITS bits.
+template <int BITS>
+__device__ __forceinline__ uint2 pack_codes8(const uint32_t (&t)[8]) {
+  if (BITS == 8) return make_uint2(low_bytes4(t[0], t[1], t[2], t[3]), low_bytes4(t[4], t[5], t[6], t[7]));
+  uint32_t v = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) v |= (t[e] & ((1u << BITS) - 1u)) << (BITS * e);
+  return make_uint2(v, 0u);
 }
 
 // (max - min) / L correctly rounded, from the rounded reciprocal of L
@@ -105,27 +123,17 @@ __global__ void __launch_bounds__(kThreads) uniform_encode_kernel(const __grid_c
           const uint32_t cidx = li + G * ch;
           float x[8];
           unpack8<DT>(w[u][ch], x);
-          uint32_t c[8];
-          uniform_codes8<LEVELS>(x, m, sc, r, c);
+          uint32_t t[8];
+          uniform_codes8<LEVELS>(x, m, sc, r, t);
+          const uint2 v = pack_codes8<BITS>(t);
           if (BITS == 8) {
-            const uint2 out = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
-                                         c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
-            if (in) st8(vc + 8 * cidx, out);
+            if (in) st8(vc + 8 * cidx, v);
           } else if (BITS == 4) {
-            uint32_t v = 0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v |= c[e] << (4 * e);
-            if (in) st4(vc + 4 * cidx, v);
+            if (in) st4(vc + 4 * cidx, v.x);
           } else if (BITS == 2) {
-            uint32_t v = 0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v |= c[e] << (2 * e);
-            if (in) *reinterpret_cast<uint16_t*>(vc + 2 * cidx) = (uint16_t)v;
+            if (in) *reinterpret_cast<uint16_t*>(vc + 2 * cidx) = (uint16_t)v.x;
           } else {
-            uint32_t v = 0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v |= c[e] << (3 * e);
-            store_3bit(vc, v, cidx, in);
+            store_3bit(vc, v.x, cidx, in);
           }
         }
         if (in && li == 0)
