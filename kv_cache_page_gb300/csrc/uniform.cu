@@ -6,7 +6,7 @@
 // Per vector: m = fp16(min x), s = fp16((max x - min x) / (2^b - 1)), codes
 // clamp(rint((x - m) / s), 0, 2^b - 1) against the stored (rounded) m and s,
 // code 0 when s == 0; restore code * s + m.  Codes are a little-endian bit
-// stream (b = 3, 4) or one byte each (b = 8); metadata is (m, s) as two FP16.
+// stream (b = 2, 3, 4) or one byte each (b = 8); metadata is (m, s) as two FP16.
 #include "device_common.cuh"
 
 namespace kvc {
@@ -70,6 +70,35 @@ __device__ __forceinline__ float div_levels(float range) {
   return __fmaf_rn(e, rL, q0);
 }
 
+// Thread mapping (as for TurboQuant): lane li of a vector's G = D/32 lanes owns
+// its 32 contiguous elements [32 li, 32 li + 32) as four 16-byte chunks, so the
+// per-vector work (minimum / maximum over G lanes, the FP16 metadata, the
+// step's reciprocal) is shared by few lanes and every lane packs and stores its
+// own 32 codes (4 * BITS bytes) in one piece.
+constexpr int kUniE = 32;
+
+// Little-endian stream of a lane's 32 codes (four chunks of 8), stored at
+// `dst` (4 * BITS bytes, aligned to that size for BITS = 2, 4, 8 and to 4
+// bytes for BITS = 3).
+template <int BITS>
+__device__ __forceinline__ void store_codes32(uint8_t* dst, const uint2 (&v)[4]) {
+  if (BITS == 8) {
+    st16(dst, make_uint4(v[0].x, v[0].y, v[1].x, v[1].y));
+    st16(dst + 16, make_uint4(v[2].x, v[2].y, v[3].x, v[3].y));
+  } else if (BITS == 4) {
+    st16(dst, make_uint4(v[0].x, v[1].x, v[2].x, v[3].x));
+  } else if (BITS == 2) {
+    st8(dst, make_uint2(v[0].x | (v[1].x << 16), v[2].x | (v[3].x << 16)));
+  } else {  // 4 x 24 bits -> three words
+    st4(dst, v[0].x | (v[1].x << 24));
+    st4(dst + 4, (v[1].x >> 8) | (v[2].x << 16));
+    st4(dst + 8, (v[2].x >> 16) | (v[3].x << 8));
+  }
+}
+
+// 8-bit codes: the chunk layout of the FP8 kernels (G lanes of a vector take
+// its 16-byte chunks round-robin), so each lane's 8-byte code stores and each
+// warp's loads stay coalesced.
 template <int DT, int D, int BITS>
 __global__ void __launch_bounds__(kThreads) uniform_encode_kernel(const __grid_constant__ Params p) {
   using M = ChunkMap<D>;
@@ -139,6 +168,83 @@ __global__ void __launch_bounds__(kThreads) uniform_encode_kernel(const __grid_c
         if (in && li == 0)
           st4(meta + (uint64_t)j * 4,
               (uint32_t)__half_as_ushort(m16) | ((uint32_t)__half_as_ushort(s16) << 16));
+      }
+    }
+    flags = __reduce_or_sync(0xffffffffu, flags);
+    if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
+    zero_padding(s.slot, (uint64_t)nv * (CB + 4), p.seg_bytes[s.role]);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint32_t f = s_flag[it & 1];
+      p.status[i] = (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+    }
+    ++it;
+  }
+}
+
+// 2-, 3- and 4-bit codes: each lane codes its own 32 elements (see kUniE), so
+// the per-vector work is shared by D/32 lanes and the lane's codes (8, 12 or
+// 16 bytes) go out in one store, adjacent to its neighbours'.
+template <int DT, int D, int BITS>
+__global__ void __launch_bounds__(kThreads) uniform_encode_lanes_kernel(const __grid_constant__ Params p) {
+  constexpr int G = D / kUniE, VPW = 32 / G, U = 2, W = kThreads / 32;
+  constexpr int STEP = W * VPW * U;
+  constexpr uint32_t LEVELS = (1u << BITS) - 1u;
+  constexpr int CB = D * BITS / 8;        // code bytes per vector
+  constexpr int LB = kUniE * BITS / 8;    // code bytes per lane
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  const uint32_t grp = lane / G, li = lane % G;
+  __shared__ uint32_t s_flag[2];
+  if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
+  __syncthreads();
+  const uint32_t nv = p.nv;
+  int it = 0;
+  for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
+    const Seg s = plan_segment(p, i, kEncode);
+    if (s.action != kProcess) {
+      if (s.action == kReport && threadIdx.x == 0) p.status[i] = s.status;
+      continue;
+    }
+    if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
+    uint8_t* codes = s.slot;
+    uint8_t* meta = s.slot + (uint64_t)nv * CB;
+    uint32_t flags = 0;
+    for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
+      uint4 w[U][4];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t j = j0 + u * VPW + grp;
+        const uint16_t* src = s.page + (j < nv ? vec_off(p, j) : 0) + kUniE * li;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) w[u][c] = j < nv ? ld_nc16(src + 8 * c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t j = j0 + u * VPW + grp;
+        float mn, mx;
+        vec_minmax<DT, G, 4>(w[u], mn, mx);
+        flags |= admission(mn, mx, p.reject_abs);
+        mn = __fadd_rn(mn, 0.0f);  // a zero minimum / maximum is +0
+        mx = __fadd_rn(mx, 0.0f);
+        const __half m16 = __float2half_rn(mn);
+        const __half s16 = __float2half_rn(div_levels<LEVELS>(__fsub_rn(mx, mn)));
+        const float m = __half2float(m16), sc = __half2float(s16);
+        const float r = sc == 0.0f ? 0.0f : __frcp_rn(sc);
+        uint2 v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float x[8];
+          unpack8<DT>(w[u][c], x);
+          uint32_t t[8];
+          uniform_codes8<LEVELS>(x, m, sc, r, t);
+          v[c] = pack_codes8<BITS>(t);
+        }
+        if (j < nv) {
+          store_codes32<BITS>(codes + (uint64_t)j * CB + LB * li, v);
+          if (li == 0)
+            st4(meta + (uint64_t)j * 4,
+                (uint32_t)__half_as_ushort(m16) | ((uint32_t)__half_as_ushort(s16) << 16));
+        }
       }
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
@@ -234,13 +340,13 @@ int dispatch_bits(const Params& p, int dir, uint32_t codec, void* stream) {
   const bool enc = dir == kEncode;
   switch (codec) {
     case KV_CODEC_UNIFORM2:
-      return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 2>, p, stream, kEncodeCtas)
+      return enc ? launch_codec_kernel(uniform_encode_lanes_kernel<DT, D, 2>, p, stream, kEncodeCtas)
                  : launch_codec_kernel(uniform_decode_kernel<DT, D, 2>, p, stream, kDecodeCtas);
     case KV_CODEC_UNIFORM3:
-      return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 3>, p, stream, kEncodeCtas)
+      return enc ? launch_codec_kernel(uniform_encode_lanes_kernel<DT, D, 3>, p, stream, kEncodeCtas)
                  : launch_codec_kernel(uniform_decode_kernel<DT, D, 3>, p, stream, kDecodeCtas);
     case KV_CODEC_UNIFORM4:
-      return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 4>, p, stream, kEncodeCtas)
+      return enc ? launch_codec_kernel(uniform_encode_lanes_kernel<DT, D, 4>, p, stream, kEncodeCtas)
                  : launch_codec_kernel(uniform_decode_kernel<DT, D, 4>, p, stream, kDecodeCtas);
     case KV_CODEC_UNIFORM8:
       return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 8>, p, stream, kEncodeCtas)
