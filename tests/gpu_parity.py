@@ -113,3 +113,30 @@ def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="
             ulps += compare_pages(host_bits(d_dev), d_host, f"layer tensor {k}")
     codec.close()
     return st_ref, ulps
+
+
+def run_seal_parity(case: synth.Case, arm: synth.Arm, device="cuda"):
+    """Encode on the GPU, seal the slots (CRC-32 headers) and verify them; the
+    headers must equal the oracle's bit for bit and verify must pass every
+    segment's status through.  Returns the number of sealed ENCODED slots."""
+    codec = make_codec(case, arm)
+    seg = [codec.segment_bytes(r)[0] for r in (0, 1)]
+    rows, total = synth.segment_list(case, arm, seg)
+    n = len(rows)
+    layers = [t.to(device) for t in case.layers]
+    descs = K.descriptors(rows, device)
+    enc = torch.zeros(max(total, 16), dtype=torch.uint8, device=device)
+    st = torch.zeros(max(n, 1), dtype=torch.uint8, device=device)
+    hdr = torch.zeros(max(n, 1) * 32, dtype=torch.uint8, device=device)
+    res = torch.zeros(max(n, 1), dtype=torch.uint8, device=device)
+    codec.encode(layers, descs, n, enc, total, st)
+    codec.seal(descs, n, enc, total, st, hdr)
+    codec.verify(descs, n, enc, total, hdr, res)
+    torch.cuda.synchronize()
+    g = oracle_geom(case, arm)
+    st_h = st.cpu().numpy()[:n]
+    want = O.seal(g, oracle_descs(rows), enc.cpu().numpy()[:total], st_h)
+    assert np.array_equal(hdr.cpu().numpy()[:32 * n], want.view(np.uint8)), "headers differ"
+    assert np.array_equal(res.cpu().numpy()[:n], st_h), "verify rejected a sealed slot"
+    codec.close()
+    return int(np.count_nonzero(st_h == O.S_ENCODED))
