@@ -195,20 +195,20 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- traffic record
 def recorded_traffic(kname, units):
     """DRAM bytes per launch from the committed ncu summary, scaled by units,
-    when the kernel sources are unchanged since the capture; else None."""
+    when the files the kernel is compiled from are unchanged since the
+    capture; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
-        rec = json.load(open(p))
         import hashlib
-        h = hashlib.sha256()
-        for f in sorted(rec["sources"]):
-            h.update(open(os.path.join(ROOT, f), "rb").read())
-        if h.hexdigest() != rec["sources_sha256"]:
-            return None
-        k = rec["kernels"].get(kname)
+        k = json.load(open(p))["kernels"].get(kname)
         if not k:
+            return None
+        h = hashlib.sha256()
+        for f in sorted(k["sources"]):
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        if h.hexdigest() != k["sources_sha256"]:
             return None
         return k["dram_bytes_per_unit"] * units
     except Exception:
