@@ -506,16 +506,19 @@ def run_extra(args, device):
             torch.cuda.synchronize()
             res = {}
             for tag, fn, alg in (("encode", a.encode, a.alg_bytes_enc), ("decode", a.decode, a.alg_bytes_dec)):
-                ts = []
-                for _ in range(max(5, args.steps)):
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record()
+                # back-to-back launches between two events on the launching
+                # stream, as in the headline loop (a host sync per launch would
+                # add the host's call latency to every short kernel)
+                reps = max(5, args.steps)
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(reps):
                     fn()
-                    e1.record()
-                    torch.cuda.synchronize()
-                    ts.append(e0.elapsed_time(e1))
-                ms = statistics.median(ts)
+                e1.record()
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / reps
                 res[tag] = {"ms": round(ms, 4), "raw_gbs": round(a.raw_bytes / (ms / 1e3) / GB, 1),
                             "hbm_gbs": round(alg / (ms / 1e3) / GB, 1)}
             res["fits_in_l2"] = (a.raw_bytes + a.total) < 129e6

@@ -18,7 +18,11 @@ namespace kvc {
 namespace {
 
 constexpr float kRecip448 = 1.0f / 448.0f;  // fl32(1/448)
-constexpr int kEncodeCtas = 6;  // resident CTAs per SM (see launch_codec_kernel)
+// Resident CTAs per SM (see launch_codec_kernel), from sweeps of 2-8 on the
+// GB300: the dynamic-scale encoder (more work per vector) and the head_dim 32
+// encoders want 6, the fixed-scale / cast encoders 4; the decoders 3.
+template <uint32_t CODEC, int D>
+constexpr int encode_ctas() { return (CODEC == KV_CODEC_FP8_DYNAMIC || D == 32) ? 6 : 4; }
 constexpr int kDecodeCtas = 3;
 
 // four floats -> four E4M3FN bytes (first element in the low byte), RNE,
@@ -199,9 +203,15 @@ template <int DT, int D>
 int dispatch_mode(const Params& p, int dir, uint32_t codec, void* stream) {
   if (dir == kEncode) {
     switch (codec) {
-      case KV_CODEC_FP8_CAST: return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_CAST>, p, stream, kEncodeCtas);
-      case KV_CODEC_FP8_FIXED: return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_FIXED>, p, stream, kEncodeCtas);
-      case KV_CODEC_FP8_DYNAMIC: return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_DYNAMIC>, p, stream, kEncodeCtas);
+      case KV_CODEC_FP8_CAST:
+        return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_CAST>, p, stream,
+                                   encode_ctas<KV_CODEC_FP8_CAST, D>());
+      case KV_CODEC_FP8_FIXED:
+        return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_FIXED>, p, stream,
+                                   encode_ctas<KV_CODEC_FP8_FIXED, D>());
+      case KV_CODEC_FP8_DYNAMIC:
+        return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_DYNAMIC>, p, stream,
+                                   encode_ctas<KV_CODEC_FP8_DYNAMIC, D>());
     }
   } else {
     switch (codec) {

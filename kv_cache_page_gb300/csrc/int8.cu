@@ -21,7 +21,7 @@ namespace kvc {
 namespace {
 
 constexpr int kEncodeCtas = 6;  // resident CTAs per SM (see launch_codec_kernel)
-constexpr int kDecodeCtas = 3;
+constexpr int kDecodeCtas = 4;
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23: RN(q + magic) holds rint(q) in its low byte
 constexpr float kAmaxFloor = 1e-12f;        // floor of the head maximum
 constexpr uint32_t kAmaxFloorBf16 = 0x2B8D0000u;  // BF16(1e-12f) as FP32 bits (the floored value)
