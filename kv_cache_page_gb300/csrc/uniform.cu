@@ -16,10 +16,7 @@ namespace {
 
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
 constexpr int kEncodeCtas = 5;  // resident CTAs per SM (see launch_codec_kernel)
-// decoders: 5 at head_dim 32 (short vectors, more rows in flight), 4 above
-// (sweeps of 2-8 on the GB300)
-template <int D>
-constexpr int decode_ctas() { return D == 32 ? 5 : 4; }
+constexpr int kDecodeCtas = 5;
 
 // Codes of 8 elements: clamp(rint((x - m) / s), 0, L).  The quotient is
 // correctly rounded (q0 = RN(d r), e = RN(d - q0 s) exact, q = RN(q0 + e r));
@@ -344,16 +341,16 @@ int dispatch_bits(const Params& p, int dir, uint32_t codec, void* stream) {
   switch (codec) {
     case KV_CODEC_UNIFORM2:
       return enc ? launch_codec_kernel(uniform_encode_lanes_kernel<DT, D, 2>, p, stream, kEncodeCtas)
-                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 2>, p, stream, decode_ctas<D>());
+                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 2>, p, stream, kDecodeCtas);
     case KV_CODEC_UNIFORM3:
       return enc ? launch_codec_kernel(uniform_encode_lanes_kernel<DT, D, 3>, p, stream, kEncodeCtas)
-                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 3>, p, stream, decode_ctas<D>());
+                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 3>, p, stream, kDecodeCtas);
     case KV_CODEC_UNIFORM4:
       return enc ? launch_codec_kernel(uniform_encode_lanes_kernel<DT, D, 4>, p, stream, kEncodeCtas)
-                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 4>, p, stream, decode_ctas<D>());
+                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 4>, p, stream, kDecodeCtas);
     case KV_CODEC_UNIFORM8:
       return enc ? launch_codec_kernel(uniform_encode_kernel<DT, D, 8>, p, stream, kEncodeCtas)
-                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 8>, p, stream, decode_ctas<D>());
+                 : launch_codec_kernel(uniform_decode_kernel<DT, D, 8>, p, stream, kDecodeCtas);
   }
   return KV_ERR_INVALID_ARG;
 }
