@@ -193,6 +193,16 @@ def test_large_segments_many_steps(kc, vc):
     assert np.all(st == O.S_ENCODED) and ulps == 0
 
 
+@pytest.mark.parametrize("T,coded", [(512, True), (513, False)])
+def test_maximum_segment_size(T, coded):
+    """A segment of exactly 16 MiB of source (64 heads x 512 tokens x 256 dims,
+    FP16) is coded; one token more and it stays raw (OVERSIZE), for both roles."""
+    case = custom_case(D=256, H=64, T=T, L=1, B=1, dtype="fp16", layout="separate")
+    st, ulps = run_parity(case, synth.Arm("max", "fp8_dynamic", "uni8", (0, 1)))
+    want = O.S_ENCODED if coded else O.S_RAW_OVERSIZE
+    assert list(st) == [want, want] and ulps == 0
+
+
 def _exhaustive_layers(dtype):
     allp = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     f = O.src_to_f32(allp, dtype)
