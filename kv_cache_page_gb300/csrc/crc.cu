@@ -27,11 +27,22 @@ constexpr int kCrcCtas = 8;              // resident CTAs per SM (8 warps, one s
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowUnroll = 4;            // rows of 16-byte chunks in flight per lane
 
-// A 32-bit GF(2)-linear map given as 8 nibble tables.
+// Entry at byte offset `off` of nibble table q.
+__device__ __forceinline__ uint32_t entry(const uint32_t (*t)[16], int q, uint32_t off) {
+  return *reinterpret_cast<const uint32_t*>(reinterpret_cast<const char*>(t[q]) + off);
+}
+
+// A 32-bit GF(2)-linear map given as 8 nibble tables.  The even and the odd
+// nibbles of r, each times 4 (a table offset), are spread over the bytes of
+// two words with one shift and mask each; a byte permute then picks each.
 __device__ __forceinline__ uint32_t apply8(const uint32_t (*t)[16], uint32_t r) {
-  const uint32_t a = t[0][r & 15u] ^ t[1][(r >> 4) & 15u] ^ t[2][(r >> 8) & 15u];
-  const uint32_t b = t[3][(r >> 12) & 15u] ^ t[4][(r >> 16) & 15u] ^ t[5][(r >> 20) & 15u];
-  return a ^ b ^ t[6][(r >> 24) & 15u] ^ t[7][r >> 28];
+  const uint32_t ev = (r << 2) & 0x3C3C3C3Cu;   // byte k: 4 * nibble 2k
+  const uint32_t od = (r >> 2) & 0x3C3C3C3Cu;   // byte k: 4 * nibble 2k + 1
+  const uint32_t a = entry(t, 0, __byte_perm(ev, 0, 0x4440)) ^ entry(t, 1, __byte_perm(od, 0, 0x4440)) ^
+                     entry(t, 2, __byte_perm(ev, 0, 0x4441));
+  const uint32_t b = entry(t, 3, __byte_perm(od, 0, 0x4441)) ^ entry(t, 4, __byte_perm(ev, 0, 0x4442)) ^
+                     entry(t, 5, __byte_perm(od, 0, 0x4442));
+  return a ^ b ^ entry(t, 6, __byte_perm(ev, 0, 0x4443)) ^ entry(t, 7, __byte_perm(od, 0, 0x4443));
 }
 
 // R(chunk) of one 16-byte chunk: nibble i (byte i/2, low or high half) through
