@@ -92,22 +92,28 @@ __device__ __forceinline__ void butterflies(float2 (&a)[16], uint32_t li) {
   }
 }
 
-// Shared tables of the TurboQuant kernels, built once per CTA.
+// Shared tables of the TurboQuant kernels, built once per CTA: the encoder's
+// index cells, 16 copies (lanes of a half warp never share a bank), and the
+// sign masks per lane of a vector (rows padded against bank conflicts).
 struct TqShared {
-  uint2 lut[kLutCells * 16];  // index cells, 16 copies: lanes of a half warp never share a bank
-  uint4 sign[8][5];           // sign masks per lane of a vector (row padded against bank conflicts)
+  uint2 lut[kLutCells * 16];
+  uint4 sign[8][5];
 };
+
+__device__ __forceinline__ void tq_sign_init(const Params& p, uint4 (&sign)[8][5]) {
+  for (int t = threadIdx.x; t < 8 * 4; t += blockDim.x) {
+    const uint32_t bits = p.sign_words[t >> 2];
+    const int k = 4 * (t & 3);
+    sign[t >> 2][t & 3] = make_uint4(sign_mask_word(bits, k), sign_mask_word(bits, k + 1),
+                                     sign_mask_word(bits, k + 2), sign_mask_word(bits, k + 3));
+  }
+}
 
 __device__ __forceinline__ void tq_shared_init(const Params& p, TqShared& sh, bool lut) {
   if (lut)
     for (int k = threadIdx.x; k < kLutCells * 16; k += blockDim.x)
       sh.lut[k] = make_uint2(__float_as_uint(p.lut_thr[k >> 4]), p.lut_lo[k >> 4]);
-  for (int t = threadIdx.x; t < 8 * 4; t += blockDim.x) {
-    const uint32_t bits = p.sign_words[t >> 2];
-    const int k = 4 * (t & 3);
-    sh.sign[t >> 2][t & 3] = make_uint4(sign_mask_word(bits, k), sign_mask_word(bits, k + 1),
-                                        sign_mask_word(bits, k + 2), sign_mask_word(bits, k + 3));
-  }
+  tq_sign_init(p, sh.sign);
 }
 
 // A CTA codes one segment at a time; warp w takes vectors w*VPW + (0..VPW-1),
@@ -250,20 +256,20 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
   constexpr int CB = D * BITS / 8;
   constexpr uint32_t CSTEP = W * VPW;
   constexpr int NPAIR = 1 << (2 * BITS);        // table of two consecutive codes
-  constexpr int REP = BITS == 4 ? 8 : 16;       // copies (keeps the table within 48 KB of static smem)
+  constexpr int REP = 16;                       // copies: each lane of a half warp has its own banks
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
-  __shared__ TqShared sh;
+  __shared__ uint4 s_sign[8][5];
   // (centroid[lo code], centroid[hi code]) for every pair of codes, REP copies
   __shared__ float2 s_pair[NPAIR * REP];
-  tq_shared_init(p, sh, false);
+  tq_sign_init(p, s_sign);
   for (int k = threadIdx.x; k < NPAIR * REP; k += blockDim.x) {
     const int v = k / REP;
     s_pair[k] = make_float2(p.cent[v & ((1 << BITS) - 1)], p.cent[v >> BITS]);
   }
   __syncthreads();
   const uint32_t pair_base = (uint32_t)__cvta_generic_to_shared(s_pair) + (lane % REP) * 8u;
-  const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&sh.sign[li][0]);
+  const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&s_sign[li][0]);
   const float cD = p.wht_scale;
   const float2 cD2 = make_float2(cD, cD);
   const uint32_t nv = p.nv;

@@ -272,6 +272,48 @@ def test_descriptor_edge_cases():
                         O.S_ENCODED]
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_descriptor_fuzz(seed):
+    """Seeded random descriptor lists: shuffled order, a source page coded into
+    several slots, and invalid entries (layer, block, role, misaligned or
+    out-of-range offsets) mixed in.  Statuses, slots and restores against the
+    oracle; an invalid descriptor must not disturb its neighbours."""
+    rng = np.random.default_rng(seed)
+    kc, vc = [("fp8_dynamic", "uni4"), ("tq3", "fp8_cast"), ("uni8", "uni3"), ("tq4", "none"),
+              ("fp8_fixed", "fp8_dynamic"), ("uni2", "tq2_k_only")][seed]
+    if vc == "tq2_k_only":
+        kc, vc = "tq2", "uni2"
+    case = custom_case(D=int(rng.choice([32, 64, 128])), H=int(rng.integers(1, 9)), T=16, L=3, B=4,
+                       dtype="bf16" if seed % 2 else "fp16", layout="packed" if seed % 3 == 0 else "separate",
+                       values="heavy" if seed % 2 else "normal", seed=seed)
+    arm = synth.Arm("fz", kc, vc, (0, 1), (1, 0) if seed % 2 else (0, 0))
+    from gpu_parity import make_codec
+    c = make_codec(case, arm)
+    seg = [c.segment_bytes(r)[0] for r in (0, 1)]
+    c.close()
+    slot = max(seg + [128])
+    n = 40
+    rows = []
+    for k in range(n):
+        layer, blk, role = int(rng.integers(0, 3)), int(rng.integers(0, 4)), int(rng.integers(0, 2))
+        off = k * slot
+        kind = rng.random()
+        if kind < 0.08:
+            layer = 3 + int(rng.integers(0, 5))          # layer out of range
+        elif kind < 0.14:
+            blk = 4 + int(rng.integers(0, 3))            # block out of range
+        elif kind < 0.18:
+            role = 2                                     # bad role
+        elif kind < 0.22:
+            off += 8                                     # misaligned slot
+        elif kind < 0.26:
+            off = (n + 5) * slot                         # slot past the buffer
+        rows.append((layer, blk, role, off))
+    st, ulps = run_parity(case, arm, rows=rows, total=n * slot)
+    assert ulps == 0
+    assert np.any(st == O.S_BAD_DESC) and np.any(st == O.S_ENCODED)
+
+
 def test_no_codec_for_either_role_reports_policy():
     case = custom_case(D=32, H=2, T=4, L=2, B=2, dtype="bf16", layout="packed")
     st, _ = run_parity(case, synth.Arm("n", "none", "none", (0, 1)))
