@@ -92,6 +92,56 @@ __device__ __forceinline__ void butterflies(float2 (&a)[16], uint32_t li) {
   }
 }
 
+// Walsh-Hadamard butterflies of the decoder.  Strides 1 .. 16 as in
+// butterflies<G>; a cross-lane stage (lanes l and l ^ o, stride 32 o) is split
+// between the two lanes instead of doubled: the lower lane computes the sums
+// and differences of slots 0..15, the upper lane those of slots 16..31, so
+// each sends only the half the other needs (16 shuffles per stage, not 32).
+// Sums land in slots 0..15 and differences in 16..31 of both lanes.  After the
+// J = log2(G) stages, slot s of lane l holds element
+//   (s & 15) | (l << 4) | ((s >> 4) << (4 + J))
+// (the half bit of the slot and the lane bits have traded places).  Each sum
+// and difference is the single rounding of the same operands as in the
+// ascending-stride transform.
+template <int G>
+__device__ __forceinline__ void butterflies_split(float2 (&a)[16], uint32_t li) {
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {  // stride 1: inside each pair
+    const float u = a[m].x, v = a[m].y;
+    a[m] = make_float2(__fadd_rn(u, v), __fsub_rn(u, v));
+  }
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {  // strides 2, 4, 8, 16
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      if (m & h) continue;
+      const float2 u = a[m], v = a[m + h];
+      a[m] = add2(u, v);
+      a[m + h] = sub2(u, v);
+    }
+  }
+#pragma unroll
+  for (int o = 1; o < G; o <<= 1) {  // strides 32 o: across lanes, split
+    const bool low = (li & (uint32_t)o) == 0;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const float2 send = low ? a[8 + m] : a[m];
+      const float2 r = make_float2(__shfl_xor_sync(0xffffffffu, send.x, o),
+                                   __shfl_xor_sync(0xffffffffu, send.y, o));
+      const float2 u = low ? a[m] : r, v = low ? r : a[8 + m];
+      a[m] = add2(u, v);
+      a[8 + m] = sub2(u, v);
+    }
+  }
+}
+
+// First element of the 8 slots 8c .. 8c + 7 of lane li after butterflies_split.
+template <int G>
+__device__ __forceinline__ uint32_t split_group_start(uint32_t li, int c) {
+  constexpr int J = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+  return (uint32_t)((8 * c) & 15) | (li << 4) | ((uint32_t)(c >> 1) << (4 + J));
+}
+
 // Shared tables of the TurboQuant kernels, built once per CTA: the encoder's
 // index cells, 16 copies (lanes of a half warp never share a bank), and the
 // sign masks per lane of a vector (rows padded against bank conflicts).
@@ -104,6 +154,19 @@ __device__ __forceinline__ void tq_sign_init(const Params& p, uint4 (&sign)[8][5
   for (int t = threadIdx.x; t < 8 * 4; t += blockDim.x) {
     const uint32_t bits = p.sign_words[t >> 2];
     const int k = 4 * (t & 3);
+    sign[t >> 2][t & 3] = make_uint4(sign_mask_word(bits, k), sign_mask_word(bits, k + 1),
+                                     sign_mask_word(bits, k + 2), sign_mask_word(bits, k + 3));
+  }
+}
+
+// Sign masks of the decoder's output layout: row li, group c covers the 8
+// elements from split_group_start<G>(li, c).
+template <int G>
+__device__ __forceinline__ void tq_sign_init_split(const Params& p, uint4 (&sign)[8][5]) {
+  for (int t = threadIdx.x; t < 8 * 4; t += blockDim.x) {
+    const uint32_t e0 = split_group_start<G>((uint32_t)(t >> 2), t & 3);
+    const uint32_t bits = e0 < p.D ? p.sign_words[e0 >> 5] : 0u;
+    const int k = (int)((e0 & 31u) >> 1);
     sign[t >> 2][t & 3] = make_uint4(sign_mask_word(bits, k), sign_mask_word(bits, k + 1),
                                      sign_mask_word(bits, k + 2), sign_mask_word(bits, k + 3));
   }
@@ -262,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
   __shared__ uint4 s_sign[8][5];
   // (centroid[lo code], centroid[hi code]) for every pair of codes, REP copies
   __shared__ float2 s_pair[NPAIR * REP];
-  tq_sign_init(p, s_sign);
+  tq_sign_init_split<G>(p, s_sign);
   for (int k = threadIdx.x; k < NPAIR * REP; k += blockDim.x) {
     const int v = k / REP;
     s_pair[k] = make_float2(p.cent[v & ((1 << BITS) - 1)], p.cent[v >> BITS]);
@@ -331,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
       const float nc = __fsqrt_rn(vector_sumsq<G>(a));
       const float g = __fdiv_rn(__half2float(__ushort_as_half(n16)), nc);
       const float2 g2 = make_float2(g, g);
-      butterflies<G>(a, li);
+      butterflies_split<G>(a, li);
       uint32_t o[16];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -344,9 +407,10 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
         }
       }
       if (j < nv) {
-        uint16_t* dst = page + vec_off(p, j) + kTqE * li;
+        uint16_t* dst = page + vec_off(p, j);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) st16(dst + 8 * c, make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]));
+        for (int c = 0; c < 4; ++c)
+          st16(dst + split_group_start<G>(li, c), make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]));
       }
     }
     if (threadIdx.x == 0 && p.result) p.result[ci] = KV_SEG_ENCODED;
