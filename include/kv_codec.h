@@ -81,7 +81,7 @@ extern "C" {
 #define KV_ERR_INVALID_ARG -1          /* NULL pointer, zero size, bad enum value */
 #define KV_ERR_UNSUPPORTED_HEAD_DIM -2 /* head_dim not in {32, 64, 128, 256} */
 #define KV_ERR_LAYOUT_MISMATCH -3      /* strides overlap or do not fit the layout */
-#define KV_ERR_UNSUPPORTED_CODEC_FOR_ROLE -4 /* TQ3/TQ4 requested for V */
+#define KV_ERR_UNSUPPORTED_CODEC_FOR_ROLE -4 /* a TurboQuant kind (TQ2/TQ3/TQ4) requested for V */
 #define KV_ERR_MISALIGNED -5           /* pointer or stride not 16-byte aligned */
 #define KV_ERR_CUDA -6                 /* a CUDA runtime call failed (launch, device query) */
 #define KV_ERR_ABI -7                  /* abi_version / struct_size mismatch */

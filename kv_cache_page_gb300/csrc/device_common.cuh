@@ -1,13 +1,16 @@
 // device_common.cuh -- segment planning, streaming loads and number-format
 // helpers shared by the codec kernels.
 //
-// Thread mapping used by every kernel: a vector of D elements is held by
-// G = D/8 consecutive lanes, lane li holding the 8 contiguous elements
-// [8*li, 8*li + 8) (one 128-bit load of the 16-bit source).  A warp therefore
-// holds 32/G vectors at a time; each lane handles U such vectors per step so
-// that U independent 128-bit loads are in flight per thread.  A CTA owns one
-// segment at a time and walks the segment's vectors in token-major order
-// j = t*H + h, which is also the order of the encoded slot.
+// Thread mapping: a vector of D elements is held by G consecutive lanes.  The
+// streaming codecs (FP8, INT8, uniform-8 encode, every uniform decode) use
+// ChunkMap below: the vector's 16-byte chunks dealt round-robin to its lanes,
+// so each warp load and store covers whole contiguous runs.  TurboQuant and
+// the 2/3/4-bit uniform encoders give each lane 32 contiguous elements
+// (G = D/32).  A warp holds 32/G vectors at a time and each lane handles U
+// such vectors per step, so that several independent 128-bit loads are in
+// flight per thread.  A CTA owns one segment at a time and walks the
+// segment's vectors in token-major order j = t*H + h, which is also the order
+// of the encoded slot.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -17,8 +20,6 @@
 #include "kv_internal.h"
 
 namespace kvc {
-
-constexpr int kE = 8;  // elements per lane per vector
 
 // ---------------------------------------------------------------- planning
 enum Action { kProcess = 0, kReport = 1, kSkip = 2 };
