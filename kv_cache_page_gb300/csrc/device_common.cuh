@@ -403,17 +403,19 @@ __device__ __forceinline__ uint32_t load_3bit(const uint8_t* src, uint32_t c) {
 }
 
 // Launch a codec kernel (signature void(Params)) on the caller's stream with
-// at most `max_per_sm` resident CTAs per SM.  The caps come from sweeps on a
-// GB300 (one CTA codes one segment): the write-heavy decodes stream best with
-// few CTAs per SM, the encodes with more.
+// `threads` threads per CTA and at most `max_per_sm` resident CTAs per SM.
+// The caps come from sweeps on a GB300 (one CTA codes one segment): the
+// write-heavy decodes stream best with few CTAs per SM, the encodes with more.
 template <typename K>
-inline int launch_codec_kernel(K kernel, const Params& p, void* stream, int max_per_sm) {
+inline int launch_codec_kernel(K kernel, const Params& p, void* stream, int max_per_sm,
+                               int threads = kThreads) {
   unsigned grid = 0;
-  const int rc = grid_for(reinterpret_cast<const void*>(kernel), p.n_segments, max_per_sm, &grid);
+  const int rc = grid_for_threads(reinterpret_cast<const void*>(kernel), p.n_segments, max_per_sm,
+                                  threads, &grid);
   if (rc != KV_OK || grid == 0) return rc;
   void* args[] = {const_cast<Params*>(&p)};
   const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(kernel), dim3(grid),
-                                         dim3(kThreads), args, 0, (cudaStream_t)stream);
+                                         dim3(threads), args, 0, (cudaStream_t)stream);
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 

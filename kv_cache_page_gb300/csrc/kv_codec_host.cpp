@@ -324,6 +324,10 @@ int check_call(kv_codec_s* h, const void* const* layer_ptrs, uint32_t n_layer_pt
 
 namespace kvc {
 int grid_for(const void* kernel, uint32_t n_segments, int max_per_sm, unsigned* grid) {
+  return grid_for_threads(kernel, n_segments, max_per_sm, kThreads, grid);
+}
+
+int grid_for_threads(const void* kernel, uint32_t n_segments, int max_per_sm, int threads, unsigned* grid) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
   int sms = 0, occ = 0;
@@ -340,7 +344,7 @@ int grid_for(const void* kernel, uint32_t n_segments, int max_per_sm, unsigned* 
     g_sms[dev] = sms;
   }
   if (occ == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, 0) != cudaSuccess)
       return KV_ERR_CUDA;
     if (occ < 1) occ = 1;
     std::lock_guard<std::mutex> lk(g_mu);

@@ -112,5 +112,7 @@ int launch_int8(const Params& p, int dir, uint32_t codec, void* stream);
 // SM count x resident CTAs per SM, the latter the occupancy limit (cached per
 // device and kernel) capped at `max_per_sm`.  Defined in the host library.
 int grid_for(const void* kernel, uint32_t n_segments, int max_per_sm, unsigned* grid);
+// The same for a kernel launched with `threads` threads per CTA.
+int grid_for_threads(const void* kernel, uint32_t n_segments, int max_per_sm, int threads, unsigned* grid);
 
 }  // namespace kvc
