@@ -191,6 +191,12 @@ __device__ __forceinline__ uint4 lds16(uint32_t smem) {
   return v;
 }
 __device__ __forceinline__ void st16(void* ptr, uint4 v) { *reinterpret_cast<uint4*>(ptr) = v; }
+// 32-byte store (sm_100+); ptr must be 32-byte aligned
+__device__ __forceinline__ void st32(void* ptr, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(a.x), "r"(a.y),
+               "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
 __device__ __forceinline__ void st8(void* ptr, uint2 v) { *reinterpret_cast<uint2*>(ptr) = v; }
 __device__ __forceinline__ void st4(void* ptr, uint32_t v) { *reinterpret_cast<uint32_t*>(ptr) = v; }
 

@@ -526,6 +526,16 @@ int kv_codec_segment_bytes(kv_codec_t h, uint32_t role, uint64_t* enc_bytes, uin
   return KV_OK;
 }
 
+// Every vector of every page starts on a 32-byte boundary: the layer
+// pointers are 32-byte aligned and every stride is a multiple of 16
+// elements (the packed layout's V half starts D elements in, D >= 32).
+uint8_t vectors_32b_aligned(const kvc::Params& p) {
+  if ((p.sb | p.st | p.sh) & 15) return 0;
+  for (uint32_t k = 0; k < p.n_layer_ptrs; ++k)
+    if ((uintptr_t)p.layer_ptr[k] & 31u) return 0;
+  return 1;
+}
+
 int kv_codec_encode(kv_codec_t h, const void* const* layer_ptrs, uint32_t n_layer_ptrs,
                     const kv_segment_desc* d_descs, uint32_t n_segments, void* d_out,
                     uint64_t out_bytes, uint8_t* d_status, void* stream) {
@@ -536,6 +546,7 @@ int kv_codec_encode(kv_codec_t h, const void* const* layer_ptrs, uint32_t n_laye
   kv_codec_s call = *h;  // per-call copy: the handle stays immutable
   Params& p = call.p;
   for (uint32_t k = 0; k < n_layer_ptrs; ++k) p.layer_ptr[k] = layer_ptrs[k];
+  p.vec32 = vectors_32b_aligned(p);
   const int rv = resolve_buffers(p, d_descs, d_out, d_status, nullptr);
   if (rv != KV_OK) return rv;
   p.n_segments = n_segments;
@@ -602,6 +613,7 @@ int kv_codec_decode(kv_codec_t h, void* const* layer_ptrs, uint32_t n_layer_ptrs
   kv_codec_s call = *h;
   Params& p = call.p;
   for (uint32_t k = 0; k < n_layer_ptrs; ++k) p.layer_ptr[k] = layer_ptrs[k];
+  p.vec32 = vectors_32b_aligned(p);
   const int rv = resolve_buffers(p, d_descs, d_in, d_status, d_result);
   if (rv != KV_OK) return rv;
   p.n_segments = n_segments;

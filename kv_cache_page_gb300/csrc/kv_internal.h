@@ -41,7 +41,7 @@ struct Params {
   uint32_t rec_used;                    // H * (D + 2): codes and scales; zeros follow
   uint8_t static_status[2];             // 0 = encodable, else KV_SEG_RAW_{POLICY,OVERSIZE,NO_SAVING}
   uint8_t heads_contig;                 // st == H * sh: vector j of a page sits at j * sh
-  uint8_t pad0;
+  uint8_t vec32;                        // per call: every vector starts on a 32-byte boundary
   float reject_abs;                     // admission bound
   float wht_scale;                      // fl32(1/sqrt(D))
   uint32_t sign_words[8];               // TurboQuant sign bits, bit i = negate element i

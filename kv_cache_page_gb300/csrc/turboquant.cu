@@ -16,11 +16,12 @@
 // Decode: c_i = centroid[code_i], g = f32(n16) / sqrt(pairwise sum c_i^2),
 // out_i = +-(RN(RN(WHT(c)_i * 1/sqrt(D)) * g)).
 //
-// Thread mapping: each lane owns 32 contiguous elements of a vector (64
-// bytes of FP16/BF16), G = D/32 lanes per vector, held as 16 FP32 pairs
-// (element 2m, 2m+1).  Butterflies with stride 2..16 are packed FP32x2 ops
-// between pairs, stride 1 is inside a pair, and strides >= 32 are warp
-// shuffles across the vector's lanes.
+// Thread mapping: a lane owns 64 contiguous elements of a vector when the
+// encoder has D >= 64 or the decoder D >= 128 (the "64 elements per lane"
+// kernels below), else 32 (64 bytes of FP16/BF16), G = D/32 lanes per
+// vector, held as 16 FP32 pairs (element 2m, 2m+1).  Butterflies with stride
+// 2..16 are packed FP32x2 ops between pairs, stride 1 is inside a pair, and
+// strides >= 32 are warp shuffles across the vector's lanes.
 #include "device_common.cuh"
 
 namespace kvc {
@@ -39,7 +40,8 @@ __device__ __forceinline__ uint32_t sign_mask_word(uint32_t bits, int k) {
 // depth first so that few partial sums are live at a time.
 template <int M0, int N>
 struct PairSumSq {
-  static __device__ __forceinline__ float run(const float2 (&a)[16]) {
+  template <int P>
+  static __device__ __forceinline__ float run(const float2 (&a)[P]) {
     if constexpr (N == 1) {
       const float2 q = mul2(a[M0], a[M0]);
       return __fadd_rn(q.x, q.y);
@@ -51,11 +53,12 @@ struct PairSumSq {
   }
 };
 
-// Pairwise sum of squares over the vector: the lane's 32 elements as an
-// in-thread tree, then xor-shuffles over the G lanes with ascending distance.
-template <int G>
-__device__ __forceinline__ float vector_sumsq(const float2 (&a)[16]) {
-  float c = PairSumSq<0, 16>::run(a);
+// Pairwise sum of squares over the vector: the lane's 2P contiguous elements
+// as an in-thread tree, then xor-shuffles over the G lanes with ascending
+// distance.
+template <int G, int P>
+__device__ __forceinline__ float vector_sumsq(const float2 (&a)[P]) {
+  float c = PairSumSq<0, P>::run(a);
 #pragma unroll
   for (int o = 1; o < G; o <<= 1) c = __fadd_rn(c, __shfl_xor_sync(0xffffffffu, c, o));
   return c;
@@ -313,6 +316,387 @@ __global__ void __launch_bounds__(kThreads, 3) tq_encode_kernel(const __grid_con
   }
 }
 
+// ---------------------------------------------------------------- 64 elements per lane
+// For D >= 64 a lane owns 64 contiguous elements (G = D/64 lanes per vector):
+// the 64-point transform inside the lane needs no shuffles, and D = 128 has
+// a single cross-lane stage.  That stage is split between the two partner
+// lanes without any lane-dependent selects:
+//  * the odd lane negates its inputs 32..63 (folded into its sign masks, so
+//    free).  Negating the upper half of a transform's inputs swaps the two
+//    halves of its outputs, so after the in-lane stages its register s holds
+//    in-lane coefficient s ^ 32, exactly (each sum or difference is the
+//    single rounding of the same operands, up to sign);
+//  * both lanes keep registers 0..31 and send 32..63, and both compute
+//    X = keep + recv, Y = keep - recv.  The even lane gets the sums of
+//    elements 0..31 and the differences of elements 0..31 of the stage
+//    (vector elements A + s and A + 64 + s), the odd lane the sums and the
+//    negated differences of elements 32..63, negated once more afterwards.
+// Lane li ends with elements A + s (registers 0..31) and B + s (32..63):
+// A = 128 (li >> 1) + 32 (li & 1), B = A + 64 for G >= 2; A = 0, B = 32 for
+// G = 1.  Further stages (D = 256) pair lanes li and li ^ 2, which hold the
+// same elements of their halves with the same signs, and run unsplit.
+constexpr int kTq64Threads = 128;
+
+__device__ __forceinline__ uint4 xor4(const uint4& a, uint32_t m) {
+  return make_uint4(a.x ^ m, a.y ^ m, a.z ^ m, a.w ^ m);
+}
+
+template <int G, bool FIX>
+__device__ __forceinline__ void butterflies64(float2 (&a)[32], uint32_t li) {
+#pragma unroll
+  for (int m = 0; m < 32; ++m) {  // stride 1: inside each pair
+    const float u = a[m].x, v = a[m].y;
+    a[m] = make_float2(__fadd_rn(u, v), __fsub_rn(u, v));
+  }
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {  // strides 2 .. 32: pair m with pair m + h
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
+      if (m & h) continue;
+      const float2 u = a[m], v = a[m + h];
+      a[m] = add2(u, v);
+      a[m + h] = sub2(u, v);
+    }
+  }
+  if constexpr (G >= 2) {  // stride 64: lanes li, li ^ 1, split (see above)
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float2 r = make_float2(__shfl_xor_sync(0xffffffffu, a[16 + m].x, 1),
+                                   __shfl_xor_sync(0xffffffffu, a[16 + m].y, 1));
+      const float2 k = a[m];
+      a[m] = add2(k, r);
+      a[16 + m] = sub2(k, r);
+    }
+  }
+#pragma unroll
+  for (int o = 2; o < G; o <<= 1) {  // strides 128 o / 2: lanes li, li ^ o
+    const float sg = (li & (uint32_t)o) ? -1.0f : 1.0f;
+    const float2 sg2 = make_float2(sg, sg);
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
+      const float2 partner = make_float2(__shfl_xor_sync(0xffffffffu, a[m].x, o),
+                                         __shfl_xor_sync(0xffffffffu, a[m].y, o));
+      a[m] = fma2(a[m], sg2, partner);  // low lane: mine + partner; high lane: partner - mine
+    }
+  }
+  if constexpr (G >= 2 && FIX) {  // the odd lane's differences of the split stage
+    const float f = (li & 1u) ? -1.0f : 1.0f;
+    const float2 f2 = make_float2(f, f);
+#pragma unroll
+    for (int m = 16; m < 32; ++m) a[m] = mul2(a[m], f2);
+  }
+}
+
+// Codes of 32 consecutive elements held in pairs a[P0 .. P0 + 15], element 0
+// in the lowest bits of w[0]; BITS * 32 / 32 words.
+template <int BITS, int P0, int P>
+__device__ __forceinline__ void tq_codes32(const float2 (&a)[P], uint32_t lut_base, uint32_t (&acc)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int e = 7; e >= 0; --e) {
+      const float x = (e & 1) ? a[P0 + 4 * q + e / 2].y : a[P0 + 4 * q + e / 2].x;
+      const uint32_t cell = __float_as_uint(__fmaf_rn(x, 4.0f, kCellMagic));
+      uint2 ent;
+      asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(ent.x), "=r"(ent.y) : "r"(cell * 128u + lut_base));
+      v = (v << BITS) + ent.y + (x > __uint_as_float(ent.x) ? 1u : 0u);
+    }
+    acc[q] = v;
+  }
+}
+
+// Store the codes of 32 consecutive elements (acc as from tq_codes32) at
+// byte `dst` (the element index of the first times BITS / 8).
+template <int BITS>
+__device__ __forceinline__ void tq_store32(uint8_t* dst, const uint32_t (&acc)[4]) {
+  if (BITS == 4) {
+    st16(dst, make_uint4(acc[0], acc[1], acc[2], acc[3]));
+  } else if (BITS == 2) {
+    st8(dst, make_uint2(acc[0] | (acc[1] << 16), acc[2] | (acc[3] << 16)));
+  } else {
+    st4(dst, acc[0] | (acc[1] << 24));
+    st4(dst + 4, (acc[1] >> 8) | (acc[2] << 16));
+    st4(dst + 8, (acc[2] >> 16) | (acc[3] << 8));
+  }
+}
+
+template <int DT, int D, int BITS>
+__global__ void __launch_bounds__(kTq64Threads, 4) tq_encode64_kernel(const __grid_constant__ Params p) {
+  constexpr int E = 64, NCH = E / 8, G = D / E, VPW = 32 / G, W = kTq64Threads / 32;
+  constexpr int CB = D * BITS / 8;
+  constexpr uint32_t CSTEP = W * VPW;
+  static_assert(G >= 1 && G <= 4, "head dim 64 .. 256");
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  const uint32_t grp = lane / G, li = lane % G;
+  __shared__ uint2 s_lut[kLutCells * 16];
+  __shared__ uint4 s_sign[4][NCH + 1];
+  // next vector of each lane: 128 bytes, chunk k at slot k ^ (lane & 7) so
+  // that the 8 lanes of a 128-bit shared access hit 8 different bank groups
+  __shared__ uint4 s_stage[W][32][NCH];
+  __shared__ uint32_t s_flag[2];
+  for (int k = threadIdx.x; k < kLutCells * 16; k += blockDim.x)
+    s_lut[k] = make_uint2(__float_as_uint(p.lut_thr[k >> 4]), p.lut_lo[k >> 4]);
+  for (int t = threadIdx.x; t < G * NCH; t += blockDim.x) {
+    const uint32_t l = (uint32_t)t / NCH, c = (uint32_t)t % NCH;
+    const uint32_t e0 = l * E + 8u * c;
+    const uint32_t bits = p.sign_words[e0 >> 5];
+    const int k = (int)((e0 & 31u) >> 1);
+    uint4 m = make_uint4(sign_mask_word(bits, k), sign_mask_word(bits, k + 1), sign_mask_word(bits, k + 2),
+                         sign_mask_word(bits, k + 3));
+    if (G >= 2 && (l & 1u) && c >= NCH / 2) m = xor4(m, 0x80008000u);  // the odd lane's upper half
+    s_sign[l][c] = m;
+  }
+  if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
+  __syncthreads();
+  const uint32_t lut_base = (uint32_t)__cvta_generic_to_shared(s_lut) + (lane & 15u) * 8u +
+                            (uint32_t)(kLutHalf * 128) - kCellMagicBits * 128u;
+  const uint32_t stage = (uint32_t)__cvta_generic_to_shared(&s_stage[warp][lane][0]);
+  const uint32_t swz = lane & 7u;
+  const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&s_sign[li][0]);
+  const uint32_t run_a = G == 1 ? 0u : 128u * (li >> 1) + 32u * (li & 1u);
+  const uint32_t run_b = run_a + (G == 1 ? 32u : 64u);
+  const uint32_t nv = p.nv;
+  const uint32_t jw = warp * VPW + grp;
+
+  auto prefetch = [&](const Seg& s, uint32_t j) {
+    if (j < nv) {
+      const uint16_t* src = s.page + vec_off(p, j) + E * li;
+#pragma unroll
+      for (int k = 0; k < NCH; ++k) cp_async16(stage + 16u * ((uint32_t)k ^ swz), src + 8 * k);
+    }
+    cp_async_commit();
+  };
+
+  SegCursor cursor;
+  cursor_init(cursor);
+  Seg cur;
+  uint32_t ci = cursor_next<kEncode>(p, cursor, cur);
+  if (ci != 0xffffffffu) prefetch(cur, jw);
+  int it = 0;
+  while (ci != 0xffffffffu) {
+    Seg nxt;
+    const uint32_t ni = cursor_next<kEncode>(p, cursor, nxt);
+    if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
+    uint8_t* codes = cur.slot;
+    uint8_t* meta = cur.slot + (uint64_t)nv * CB;
+    uint32_t flags = 0;
+    if (warp * VPW >= nv && ni != 0xffffffffu) prefetch(nxt, jw);  // no work in this segment
+    for (uint32_t j0 = warp * VPW; j0 < nv; j0 += CSTEP) {
+      const uint32_t j = j0 + grp;
+      const bool in = j < nv;
+      cp_async_wait_all();
+      uint4 w[NCH];
+#pragma unroll
+      for (int k = 0; k < NCH; ++k)
+        w[k] = in ? lds16(stage + 16u * ((uint32_t)k ^ swz)) : make_uint4(0, 0, 0, 0);
+      const float amax = vec_absmax<DT, G, NCH>(w);
+      // the staged data is in registers now: refill the stage with the next vector
+      if (j0 + CSTEP < nv) prefetch(cur, j + CSTEP);
+      else if (ni != 0xffffffffu) prefetch(nxt, jw);
+      const uint32_t vflags = admission_abs(amax, p.reject_abs);
+      flags |= vflags;
+      if (vflags) {  // keep NaN / inf out of the arithmetic (the segment stays raw)
+#pragma unroll
+        for (int k = 0; k < NCH; ++k) w[k] = make_uint4(0, 0, 0, 0);
+      }
+      float2 a[32];
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        const uint4 m = lds16(sign_addr + 16u * c);
+        const uint32_t ww[4] = {w[c].x ^ m.x, w[c].y ^ m.y, w[c].z ^ m.z, w[c].w ^ m.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) a[4 * c + k] = make_float2(lo_f32<DT>(ww[k]), hi_f32<DT>(ww[k]));
+      }
+      const float n = __fsqrt_rn(vector_sumsq<G>(a));
+      float r = __frcp_rn(n);
+      if (!isfinite(r)) r = 0.0f;
+      const float2 r2 = make_float2(r, r);
+#pragma unroll
+      for (int m = 0; m < 32; ++m) a[m] = mul2(a[m], r2);
+      butterflies64<G, true>(a, li);
+      if (n < 0x1p-62f) {
+        // Norms this small may come from squares that underflowed, so |w|
+        // can exceed sqrt(D); clamp into the table (beyond +-17 every code
+        // is already the first or the last).
+#pragma unroll
+        for (int m = 0; m < 32; ++m)
+          a[m] = make_float2(fminf(fmaxf(a[m].x, -17.0f), 17.0f), fminf(fmaxf(a[m].y, -17.0f), 17.0f));
+      }
+      uint32_t acc_a[4], acc_b[4];
+      tq_codes32<BITS, 0>(a, lut_base, acc_a);
+      tq_codes32<BITS, 16>(a, lut_base, acc_b);
+      if (in) {
+        uint8_t* vc = codes + (uint64_t)j * CB;
+        tq_store32<BITS>(vc + run_a * BITS / 8, acc_a);
+        tq_store32<BITS>(vc + run_b * BITS / 8, acc_b);
+        if (li == 0)
+          *reinterpret_cast<uint16_t*>(meta + (uint64_t)j * 2) = __half_as_ushort(__float2half_rn(n));
+      }
+    }
+    flags = __reduce_or_sync(0xffffffffu, flags);
+    if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
+    zero_padding(cur.slot, (uint64_t)nv * (CB + 2), p.seg_bytes[cur.role]);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint32_t f = s_flag[it & 1];
+      p.status[ci] = (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+    }
+    ++it;
+    cur = nxt;
+    ci = ni;
+  }
+}
+
+// Decoder for D >= 64, the same lane layout as tq_encode64_kernel.  Lane li
+// reads the codes of elements 64 li .. 64 li + 63.  The odd lane's inputs
+// 32..63 are negated by complementing their codes (the codebook is symmetric:
+// centroid[c] = -centroid[2^b - 1 - c], exactly), and its negated
+// differences are corrected by its output sign masks.
+template <int DT, int D, int BITS>
+__global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __grid_constant__ Params p) {
+  constexpr int E = 64, G = D / E, VPW = 32 / G, W = kTq64Threads / 32;
+  constexpr int CB = D * BITS / 8;
+  constexpr int NW = 2 * BITS;                  // code words of a lane (64 codes)
+  constexpr uint32_t CSTEP = W * VPW;
+  constexpr int NPAIR = 1 << (2 * BITS);        // table of two consecutive codes
+  constexpr int REP = 16;                       // copies: each lane of a half warp has its own banks
+  static_assert(G >= 1 && G <= 4, "head dim 64 .. 256");
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  const uint32_t grp = lane / G, li = lane % G;
+  __shared__ uint4 s_sign[4][9];
+  // (centroid[lo code], centroid[hi code]) for every pair of codes, REP copies
+  __shared__ float2 s_pair[NPAIR * REP];
+  for (int t = threadIdx.x; t < G * 8; t += blockDim.x) {
+    // output chunk c of lane l: elements A + 8c (c < 4) or B + 8(c - 4)
+    const uint32_t l = (uint32_t)t / 8, c = (uint32_t)t % 8;
+    const uint32_t ra = G == 1 ? 0u : 128u * (l >> 1) + 32u * (l & 1u);
+    const uint32_t e0 = (c < 4 ? ra : ra + (G == 1 ? 32u : 64u)) + 8u * (c & 3u);
+    const uint32_t bits = p.sign_words[e0 >> 5];
+    const int k = (int)((e0 & 31u) >> 1);
+    uint4 m = make_uint4(sign_mask_word(bits, k), sign_mask_word(bits, k + 1), sign_mask_word(bits, k + 2),
+                         sign_mask_word(bits, k + 3));
+    if (G >= 2 && (l & 1u) && c >= 4) m = xor4(m, 0x80008000u);  // the odd lane's differences
+    s_sign[l][c] = m;
+  }
+  for (int k = threadIdx.x; k < NPAIR * REP; k += blockDim.x) {
+    const int v = k / REP;
+    s_pair[k] = make_float2(p.cent[v & ((1 << BITS) - 1)], p.cent[v >> BITS]);
+  }
+  __syncthreads();
+  const uint32_t pair_base = (uint32_t)__cvta_generic_to_shared(s_pair) + (lane % REP) * 8u;
+  const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&s_sign[li][0]);
+  const uint32_t run_a = G == 1 ? 0u : 128u * (li >> 1) + 32u * (li & 1u);
+  const uint32_t run_b = run_a + (G == 1 ? 32u : 64u);
+  const uint32_t cmask = (G >= 2 && (li & 1u)) ? 0xffffffffu : 0u;  // complement the upper codes
+  const bool vec32 = p.vec32 != 0;
+  const float cD = p.wht_scale;
+  const float2 cD2 = make_float2(cD, cD);
+  const uint32_t nv = p.nv;
+  const uint32_t jw = warp * VPW + grp;
+
+  // codes and norm of vector j of segment s (registers; issued ahead of use)
+  auto fetch = [&](const Seg& s, uint32_t j, uint32_t (&cw)[NW], uint16_t& n16) {
+#pragma unroll
+    for (int k = 0; k < NW; ++k) cw[k] = 0;
+    n16 = 0;
+    if (j < nv) {
+      const uint8_t* vc = s.slot + (uint64_t)j * CB + 8 * BITS * li;
+      if (BITS == 3) {
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+          const uint2 t = ld_nc8(vc + 8 * k);
+          cw[2 * k] = t.x;
+          cw[2 * k + 1] = t.y;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < NW / 4; ++k) {
+          const uint4 t = ld_nc16(vc + 16 * k);
+          cw[4 * k] = t.x; cw[4 * k + 1] = t.y; cw[4 * k + 2] = t.z; cw[4 * k + 3] = t.w;
+        }
+      }
+      n16 = ld_nc2(s.slot + (uint64_t)nv * CB + (uint64_t)j * 2);
+    }
+  };
+
+  SegCursor cursor;
+  cursor_init(cursor);
+  Seg cur;
+  uint32_t ci = cursor_next<kDecode>(p, cursor, cur);
+  uint32_t cwn[NW];
+  uint16_t nn = 0;
+#pragma unroll
+  for (int k = 0; k < NW; ++k) cwn[k] = 0;
+  if (ci != 0xffffffffu) fetch(cur, jw, cwn, nn);
+  while (ci != 0xffffffffu) {
+    Seg nxt;
+    const uint32_t ni = cursor_next<kDecode>(p, cursor, nxt);
+    uint16_t* page = const_cast<uint16_t*>(cur.page);
+    if (warp * VPW >= nv && ni != 0xffffffffu) fetch(nxt, jw, cwn, nn);
+    for (uint32_t j0 = warp * VPW; j0 < nv; j0 += CSTEP) {
+      const uint32_t j = j0 + grp;
+      uint32_t cw[NW];
+#pragma unroll
+      for (int k = 0; k < NW; ++k) cw[k] = k < NW / 2 ? cwn[k] : cwn[k] ^ cmask;
+      const uint16_t n16 = nn;
+      if (j0 + CSTEP < nv) fetch(cur, j + CSTEP, cwn, nn);
+      else if (ni != 0xffffffffu) fetch(nxt, jw, cwn, nn);
+      float2 a[32];
+#pragma unroll
+      for (int m = 0; m < 32; ++m) {
+        uint32_t v;
+        if (BITS == 4) {
+          v = __byte_perm(cw[m >> 2], 0, 0x4440 | (m & 3));
+        } else if (BITS == 2) {
+          v = (cw[m >> 3] >> (4 * (m & 7))) & 15u;
+        } else {
+          const int bit = 6 * m;
+          v = (bit & 31) <= 26 ? (cw[bit >> 5] >> (bit & 31)) & 63u
+                               : __funnelshift_r(cw[bit >> 5], cw[(bit >> 5) + 1], bit & 31) & 63u;
+        }
+        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(a[m].x), "=f"(a[m].y) : "r"(v * (8u * REP) + pair_base));
+      }
+      const float nc = __fsqrt_rn(vector_sumsq<G>(a));
+      const float g = __fdiv_rn(__half2float(__ushort_as_half(n16)), nc);
+      const float2 g2 = make_float2(g, g);
+      butterflies64<G, false>(a, li);
+      uint32_t o[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 m = lds16(sign_addr + 16u * c);
+        const uint32_t mk[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 t = mul2(mul2(a[4 * c + k], cD2), g2);
+          o[4 * c + k] = pack2<DT>(t.x, t.y) ^ mk[k];
+        }
+      }
+      if (j < nv) {
+        uint16_t* dst = page + vec_off(p, j);
+        if (vec32) {  // 32 bytes per store: twice the bytes per line of each warp store
+#pragma unroll
+          for (int c = 0; c < 4; c += 2) {
+            st32(dst + run_a + 8 * c, make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]),
+                 make_uint4(o[4 * c + 4], o[4 * c + 5], o[4 * c + 6], o[4 * c + 7]));
+            st32(dst + run_b + 8 * c, make_uint4(o[16 + 4 * c], o[17 + 4 * c], o[18 + 4 * c], o[19 + 4 * c]),
+                 make_uint4(o[20 + 4 * c], o[21 + 4 * c], o[22 + 4 * c], o[23 + 4 * c]));
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            st16(dst + run_a + 8 * c, make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]));
+            st16(dst + run_b + 8 * c, make_uint4(o[16 + 4 * c], o[17 + 4 * c], o[18 + 4 * c], o[19 + 4 * c]));
+          }
+        }
+      }
+    }
+    if (threadIdx.x == 0 && p.result) p.result[ci] = KV_SEG_ENCODED;
+    cur = nxt;
+    ci = ni;
+  }
+}
+
 template <int DT, int D, int BITS>
 __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_constant__ Params p) {
   constexpr int G = D / kTqE, VPW = 32 / G, W = kThreads / 32;
@@ -337,6 +721,7 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
   const float2 cD2 = make_float2(cD, cD);
   const uint32_t nv = p.nv;
   const uint32_t jw = warp * VPW + grp;
+  const bool vec32 = p.vec32 != 0;
 
   // codes and norm of vector j of segment s (registers; issued ahead of use)
   auto fetch = [&](const Seg& s, uint32_t j, uint32_t (&cw)[4], uint16_t& n16) {
@@ -408,9 +793,16 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
       }
       if (j < nv) {
         uint16_t* dst = page + vec_off(p, j);
+        if (vec32) {  // groups 2c, 2c + 1 are 16 consecutive elements starting on a 16-element boundary
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          st16(dst + split_group_start<G>(li, c), make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]));
+          for (int c = 0; c < 4; c += 2)
+            st32(dst + split_group_start<G>(li, c), make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]),
+                 make_uint4(o[4 * c + 4], o[4 * c + 5], o[4 * c + 6], o[4 * c + 7]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            st16(dst + split_group_start<G>(li, c), make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]));
+        }
       }
     }
     if (threadIdx.x == 0 && p.result) p.result[ci] = KV_SEG_ENCODED;
@@ -419,19 +811,35 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
   }
 }
 
+template <int DT, int D, int BITS>
+int encode(const Params& p, void* stream) {
+  if constexpr (D >= 64)
+    return launch_codec_kernel(tq_encode64_kernel<DT, D, BITS>, p, stream, 8, kTq64Threads);
+  else
+    return launch_codec_kernel(tq_encode_kernel<DT, D, BITS>, p, stream, 8);
+}
+
+// D = 64 decodes with 32 elements per lane: with one lane per vector each
+// 16-byte store would touch 32 different lines (0.50 against 0.57 of HBM
+// bandwidth on a GB300 for 4-bit codes).
+template <int DT, int D, int BITS>
+int decode(const Params& p, void* stream) {
+  if constexpr (D >= 128)
+    return launch_codec_kernel(tq_decode64_kernel<DT, D, BITS>, p, stream, 8, kTq64Threads);
+  else
+    return launch_codec_kernel(tq_decode_kernel<DT, D, BITS>, p, stream, 8);
+}
+
 template <int DT, int D>
 int dispatch_bits(const Params& p, int dir, uint32_t codec, void* stream) {
   const bool enc = dir == kEncode;
   switch (codec) {
     case KV_CODEC_TQ2:
-      return enc ? launch_codec_kernel(tq_encode_kernel<DT, D, 2>, p, stream, 8)
-                 : launch_codec_kernel(tq_decode_kernel<DT, D, 2>, p, stream, 8);
+      return enc ? encode<DT, D, 2>(p, stream) : decode<DT, D, 2>(p, stream);
     case KV_CODEC_TQ3:
-      return enc ? launch_codec_kernel(tq_encode_kernel<DT, D, 3>, p, stream, 8)
-                 : launch_codec_kernel(tq_decode_kernel<DT, D, 3>, p, stream, 8);
+      return enc ? encode<DT, D, 3>(p, stream) : decode<DT, D, 3>(p, stream);
     case KV_CODEC_TQ4:
-      return enc ? launch_codec_kernel(tq_encode_kernel<DT, D, 4>, p, stream, 8)
-                 : launch_codec_kernel(tq_decode_kernel<DT, D, 4>, p, stream, 8);
+      return enc ? encode<DT, D, 4>(p, stream) : decode<DT, D, 4>(p, stream);
   }
   return KV_ERR_INVALID_ARG;
 }

@@ -58,11 +58,27 @@ def _buffer(t: torch.Tensor, where: str, device) -> torch.Tensor:
     return t.to(device)
 
 
+def _offset_layer(t: torch.Tensor, device, offset_bytes: int) -> torch.Tensor:
+    """A device copy of the contiguous tensor `t` whose first element sits
+    `offset_bytes` past the start of its allocation (which is 256-byte aligned)."""
+    if offset_bytes == 0:
+        return t.to(device)
+    assert t.is_contiguous() and offset_bytes % t.element_size() == 0
+    k = offset_bytes // t.element_size()
+    base = torch.empty(t.numel() + k, dtype=t.dtype, device=device)
+    v = base[k:].view(t.shape)
+    v.copy_(t.to(device))
+    assert v.data_ptr() % 32 == offset_bytes % 32
+    return v
+
+
 def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="cuda",
-               reject_abs=448.0, check_decode=True, buffers="device"):
+               reject_abs=448.0, check_decode=True, buffers="device", layer_offset=0):
     """Encode + decode `case` with `arm` on the GPU and in the oracle; assert parity.
     buffers="host" keeps descriptors, slots, statuses and results in pinned host
-    memory (the kernels read and write them over the host link).
+    memory (the kernels read and write them over the host link).  layer_offset
+    places the source and restored layer tensors that many bytes past an aligned
+    allocation (16: the 16-byte alignment the library requires, not 32).
     Returns (status array, number of restored elements off by one ulp)."""
     codec = make_codec(case, arm, reject_abs)
     g = oracle_geom(case, arm, reject_abs)
@@ -74,7 +90,7 @@ def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="
     elif total is None:
         total = max([r[3] + seg[r[2]] for r in rows if r[2] <= 1 and r[3] < (1 << 32)] + [16])
     n = len(rows)
-    dev_layers = [t.to(device) for t in case.layers]
+    dev_layers = [_offset_layer(t, device, layer_offset) for t in case.layers]
     host_layers = [host_bits(t) for t in case.layers]
     descs = _buffer(K.descriptors(rows, "cpu"), buffers, device)
     out = _buffer(torch.full((max(total, 16),), SENTINEL_ENC, dtype=torch.uint8), buffers, device)
@@ -97,8 +113,9 @@ def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="
     ulps = 0
     if check_decode:
         # decode the oracle's encoding on the GPU into sentinel-filled pages
-        dst_dev = [torch.full_like(t, 0).view(torch.int16).fill_(SENTINEL_PAGE).view(t.dtype)
-                   for t in dev_layers]
+        dst_dev = [_offset_layer(t, device, layer_offset) for t in case.layers]
+        for t in dst_dev:
+            t.view(torch.int16).fill_(SENTINEL_PAGE)
         dst_host = [np.full_like(h, SENTINEL_PAGE) for h in host_layers]
         enc_h = torch.zeros(max(total, 16), dtype=torch.uint8)
         enc_h[:total] = torch.from_numpy(enc_ref)

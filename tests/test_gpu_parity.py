@@ -122,6 +122,20 @@ def test_codec_matrix(kc, vc, D, dtype, layout):
     assert ulps == 0
 
 
+@pytest.mark.parametrize("kc,vc", [("tq4", "uni4"), ("tq3", "uni3"), ("tq2", "uni2"),
+                                   ("fp8_dynamic", "uni8"), ("int8", "int8")])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+@pytest.mark.parametrize("layout", ["separate", "packed"])
+@pytest.mark.parametrize("offset", [16, 32])
+def test_layer_pointers_16_and_32_byte_aligned(kc, vc, D, layout, offset):
+    """Layer tensors 16 bytes past a 32-byte boundary (the library requires
+    16-byte alignment; kernels that move 32 bytes per access take their
+    16-byte path) and 32 bytes past a 256-byte one (the 32-byte path)."""
+    case = custom_case(D=D, H=8, T=16, L=2, B=4, dtype="bf16", layout=layout, seed=D + offset)
+    st, ulps = run_parity(case, synth.Arm("a", kc, vc, (0, 1)), layer_offset=offset)
+    assert ulps == 0 and np.all(st == O.S_ENCODED)
+
+
 @pytest.mark.parametrize("kc,vc", [("int8", "int8"), ("int8", "fp8_dynamic"), ("tq4", "int8"),
                                    ("none", "int8")])
 @pytest.mark.parametrize("D", [32, 64, 128, 256])
