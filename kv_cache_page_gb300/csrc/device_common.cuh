@@ -162,6 +162,12 @@ __device__ __forceinline__ uint4 ld_nc16(const void* ptr) {
       : "l"(ptr));
   return v;
 }
+// read-only 32-byte load (sm_100+); ptr must be 32-byte aligned
+__device__ __forceinline__ void ld_nc32(const void* ptr, uint4& a, uint4& b) {
+  asm("ld.global.nc.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+      : "l"(ptr));
+}
 __device__ __forceinline__ uint2 ld_nc8(const void* ptr) {
   uint2 v;
   asm("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(ptr));

@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(NT) uniform_encode_lanes_kernel(const __grid_c
   if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
   __syncthreads();
   const uint32_t nv = p.nv;
+  const bool vec32 = p.vec32 != 0;
   int it = 0;
   for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
     const Seg s = plan_segment(p, i, kEncode);
@@ -215,8 +216,16 @@ __global__ void __launch_bounds__(NT) uniform_encode_lanes_kernel(const __grid_c
       for (int u = 0; u < U; ++u) {
         const uint32_t j = j0 + u * VPW + grp;
         const uint16_t* src = s.page + (j < nv ? vec_off(p, j) : 0) + kUniE * li;
+        if (j >= nv) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) w[u][c] = j < nv ? ld_nc16(src + 8 * c) : make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < 4; ++c) w[u][c] = make_uint4(0, 0, 0, 0);
+        } else if (D >= 64 && vec32) {  // two 32-byte loads: a whole sector each (1% slower at D = 32)
+          ld_nc32(src, w[u][0], w[u][1]);
+          ld_nc32(src + 16, w[u][2], w[u][3]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) w[u][c] = ld_nc16(src + 8 * c);
+        }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
