@@ -16,10 +16,10 @@
 // Decode: c_i = centroid[code_i], g = f32(n16) / sqrt(pairwise sum c_i^2),
 // out_i = +-(RN(RN(WHT(c)_i * 1/sqrt(D)) * g)).
 //
-// Thread mapping: a lane owns 64 contiguous elements of a vector when the
-// encoder has D >= 64 or the decoder D >= 128 (the "64 elements per lane"
-// kernels below), else 32 (64 bytes of FP16/BF16), G = D/32 lanes per
-// vector, held as 16 FP32 pairs (element 2m, 2m+1).  Butterflies with stride
+// Thread mapping: a lane owns 64 contiguous elements of a vector when
+// D >= 64 (the "64 elements per lane" kernels below), else 32 (64 bytes of
+// FP16/BF16), G = D/32 lanes per vector, held as 16 FP32 pairs (element 2m,
+// 2m+1).  Butterflies with stride
 // 2..16 are packed FP32x2 ops between pairs, stride 1 is inside a pair, and
 // strides >= 32 are warp shuffles across the vector's lanes.
 #include "device_common.cuh"
@@ -819,12 +819,9 @@ int encode(const Params& p, void* stream) {
     return launch_codec_kernel(tq_encode_kernel<DT, D, BITS>, p, stream, 8);
 }
 
-// D = 64 decodes with 32 elements per lane: with one lane per vector each
-// 16-byte store would touch 32 different lines (0.50 against 0.57 of HBM
-// bandwidth on a GB300 for 4-bit codes).
 template <int DT, int D, int BITS>
 int decode(const Params& p, void* stream) {
-  if constexpr (D >= 128)
+  if constexpr (D >= 64)
     return launch_codec_kernel(tq_decode64_kernel<DT, D, BITS>, p, stream, 8, kTq64Threads);
   else
     return launch_codec_kernel(tq_decode_kernel<DT, D, BITS>, p, stream, 8);
