@@ -116,6 +116,7 @@ class Arm:
         else:
             used = set(range(case.num_layers))
         self.used = sorted(used)
+        self.layout = case.layout
         self.src_view = [t if i in used else None for i, t in enumerate(dev_layers)]
         self.dst_view = [t if i in used else None for i, t in enumerate(self.dst)]
         prot = [l for l in range(case.num_layers)
@@ -325,13 +326,22 @@ def run_gpu(args, dist, world, rank, local):
     return result
 
 
+
+
 def run_e2e(args, arms, stream, dist):
     """Same step through the C ABI with host buffers: raw pages H2D from pinned
     memory, encode with the slots and statuses written straight into pinned
     host memory (offload), decode reading them from there into the engine
     pages (restore), restored pages D2H.  The slot bytes cross the host link
     inside the kernels; they count as the step's D2H (offload) and H2D
-    (restore) traffic."""
+    (restore) traffic.
+
+    The step runs in chunks of args.e2e_chunk_layers layers, chunk c on stream
+    c % args.e2e_streams (each chunk: its pages H2D, encode and decode of its
+    segments, its restored pages D2H), so that one chunk's H2D copies, another's
+    kernels and a third's D2H copies share the full-duplex host link.  A
+    chunk's descriptors and statuses are a contiguous slice (the segment list
+    is layer-major) and its slots sit at their absolute offsets."""
     host = []
     for a in arms:
         src_h = [t.cpu().pin_memory() if i in a.used else None for i, t in enumerate(a.src)]
@@ -348,14 +358,32 @@ def run_e2e(args, arms, stream, dist):
         h2d += a.total + a.n
         d2h += a.total + a.n
 
+    chunks = []
+    for a, (src_h, dst_h, enc_h, st_h) in zip(arms, host):
+        layers = [r[0] for r in a.rows]
+        assert layers == sorted(layers), "segment list must be layer-major"
+        order = sorted(set(layers))
+        for c0 in range(0, len(order), args.e2e_chunk_layers):
+            group = set(order[c0:c0 + args.e2e_chunk_layers])
+            d0 = layers.index(min(group))
+            d1 = len(layers) - layers[::-1].index(max(group))
+            idx = [i for i in a.used if (i // 2 if a.layout == "separate" else i) in group]
+            chunks.append((a, idx, d0, d1, src_h, dst_h, enc_h, st_h))
+    streams = [torch.cuda.Stream(device=stream.device) for _ in range(args.e2e_streams)]
+    for s in streams:
+        s.wait_stream(stream)
+
     def step():
-        for a, (src_h, dst_h, enc_h, st_h) in zip(arms, host):
-            for i in a.used:
-                a.src[i].copy_(src_h[i], non_blocking=True)
-            a.codec.encode(a.src_view, a.descs, a.n, enc_h, a.total, st_h, stream)
-            a.codec.decode(a.dst_view, a.descs, a.n, enc_h, a.total, st_h, None, stream)
-            for i in a.used:
-                dst_h[i].copy_(a.dst[i], non_blocking=True)
+        for k, (a, idx, d0, d1, src_h, dst_h, enc_h, st_h) in enumerate(chunks):
+            s = streams[k % len(streams)]
+            descs = a.descs[d0 * DESC_BYTES:d1 * DESC_BYTES]
+            with torch.cuda.stream(s):
+                for i in idx:
+                    a.src[i].copy_(src_h[i], non_blocking=True)
+                a.codec.encode(a.src_view, descs, d1 - d0, enc_h, a.total, st_h[d0:d1], s)
+                a.codec.decode(a.dst_view, descs, d1 - d0, enc_h, a.total, st_h[d0:d1], None, s)
+                for i in idx:
+                    dst_h[i].copy_(a.dst[i], non_blocking=True)
 
     for _ in range(max(1, min(args.warmup, 2))):
         step()
@@ -373,7 +401,8 @@ def run_e2e(args, arms, stream, dist):
     return {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "path": "pages copied H2D/D2H from pinned memory; slots and statuses in pinned host "
-                    "memory, moved by the kernels"}
+                    f"memory, moved by the kernels; chunks of {args.e2e_chunk_layers} layers "
+                    f"pipelined over {args.e2e_streams} streams"}
 
 
 def run_host_link(args, arms, stream):
@@ -627,6 +656,10 @@ def main(argv=None):
     ap.add_argument("--no-extra", dest="extra", action="store_false")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-chunk-layers", type=int, default=4,
+                    help="layers per chunk of the pipelined end-to-end step")
+    ap.add_argument("--e2e-streams", type=int, default=3,
+                    help="streams the end-to-end chunks rotate over")
     ap.add_argument("--no-host-link", dest="host_link", action="store_false",
                     help="skip the host-resident slot offload/restore timings")
     ap.add_argument("--no-integrity", dest="integrity", action="store_false",

@@ -134,3 +134,53 @@ def test_restore_on_transfer_stream_orders_before_consumer():
         sums = [(d.float() - r.float()).abs().sum() for d, r in zip(dst, ref)]
         assert all(float(s) == 0.0 for s in sums), trial
     codec.close()
+
+
+def test_layer_chunks_pipelined_over_streams_match_one_call():
+    """Offload + restore in chunks of layers, chunk c on stream c % 3 (pages
+    H2D, encode into pinned host slots, decode from them, pages D2H), as a
+    pipelined offload path would run it: slots, statuses and restored pages
+    equal those of one call over all segments."""
+    case = synth.make_case("qwen3_8b", num_layers=7, num_blocks=10)
+    arm = case.arms[1]
+    codec = make_codec(case, arm)
+    seg = [codec.segment_bytes(r)[0] for r in (0, 1)]
+    rows, total = synth.segment_list(case, arm, seg)
+    n = len(rows)
+    layers = [t.cuda() for t in case.layers]
+    # one call, device buffers
+    descs = K.descriptors(rows, "cuda")
+    enc1 = torch.zeros(total, dtype=torch.uint8, device="cuda")
+    st1 = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    out1 = [torch.zeros_like(t) for t in layers]
+    codec.encode(layers, descs, n, enc1, total, st1)
+    codec.decode(out1, descs, n, enc1, total, st1)
+    torch.cuda.synchronize()
+    # chunks of 3 layers on 3 streams, pages staged through pinned host memory
+    src_h = [t.cpu().pin_memory() for t in case.layers]
+    dst_h = [torch.zeros_like(t).pin_memory() for t in case.layers]
+    src_d = [torch.zeros_like(t) for t in layers]
+    dst_d = [torch.zeros_like(t) for t in layers]
+    enc_h = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    st_h = torch.zeros(n, dtype=torch.uint8).pin_memory()
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    torch.cuda.synchronize()
+    lay = [r[0] for r in rows]
+    for c, l0 in enumerate(range(0, case.num_layers, 3)):
+        group = range(l0, min(l0 + 3, case.num_layers))
+        d0, d1 = lay.index(group[0]), len(lay) - lay[::-1].index(group[-1])
+        idx = [2 * l + r for l in group for r in (0, 1)]
+        s = streams[c % 3]
+        with torch.cuda.stream(s):
+            for i in idx:
+                src_d[i].copy_(src_h[i], non_blocking=True)
+            codec.encode(src_d, descs[d0 * 24:d1 * 24], d1 - d0, enc_h, total, st_h[d0:d1], stream=s)
+            codec.decode(dst_d, descs[d0 * 24:d1 * 24], d1 - d0, enc_h, total, st_h[d0:d1], stream=s)
+            for i in idx:
+                dst_h[i].copy_(dst_d[i], non_blocking=True)
+    torch.cuda.synchronize()
+    assert torch.equal(st_h, st1.cpu())
+    assert torch.equal(enc_h, enc1.cpu())
+    for a, b in zip(dst_h, out1):
+        assert torch.equal(a.view(torch.int16), b.cpu().view(torch.int16))
+    codec.close()
