@@ -393,16 +393,19 @@ template <int BITS, int P0, int P>
 __device__ __forceinline__ void tq_codes32(const float2 (&a)[P], uint32_t lut_base, uint32_t (&acc)[4]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    uint32_t v = 0;
+    uint32_t c[8];
 #pragma unroll
-    for (int e = 7; e >= 0; --e) {
+    for (int e = 0; e < 8; ++e) {
       const float x = (e & 1) ? a[P0 + 4 * q + e / 2].y : a[P0 + 4 * q + e / 2].x;
       const uint32_t cell = __float_as_uint(__fmaf_rn(x, 4.0f, kCellMagic));
       uint2 ent;
       asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(ent.x), "=r"(ent.y) : "r"(cell * 128u + lut_base));
-      v = (v << BITS) + ent.y + (x > __uint_as_float(ent.x) ? 1u : 0u);
+      c[e] = ent.y + (x > __uint_as_float(ent.x) ? 1u : 0u);
     }
-    acc[q] = v;
+    // element 0 in the lowest bits, combined as a tree (depth 3, not 8)
+    const uint32_t p0 = c[0] + (c[1] << BITS), p1 = c[2] + (c[3] << BITS);
+    const uint32_t p2 = c[4] + (c[5] << BITS), p3 = c[6] + (c[7] << BITS);
+    acc[q] = (p0 + (p1 << (2 * BITS))) + ((p2 + (p3 << (2 * BITS))) << (4 * BITS));
   }
 }
 
@@ -458,6 +461,7 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_encode64_kernel(const __gr
   const uint32_t run_b = run_a + (G == 1 ? 32u : 64u);
   const uint32_t nv = p.nv;
   const uint32_t jw = warp * VPW + grp;
+  const float admit_ss = p.reject_abs * p.reject_abs * 0.99609375f;
 
   auto prefetch = [&](const Seg& s, uint32_t j) {
     if (j < nv) {
@@ -490,16 +494,9 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_encode64_kernel(const __gr
 #pragma unroll
       for (int k = 0; k < NCH; ++k)
         w[k] = in ? lds16(stage + 16u * ((uint32_t)k ^ swz)) : make_uint4(0, 0, 0, 0);
-      const float amax = vec_absmax<DT, G, NCH>(w);
       // the staged data is in registers now: refill the stage with the next vector
       if (j0 + CSTEP < nv) prefetch(cur, j + CSTEP);
       else if (ni != 0xffffffffu) prefetch(nxt, jw);
-      const uint32_t vflags = admission_abs(amax, p.reject_abs);
-      flags |= vflags;
-      if (vflags) {  // keep NaN / inf out of the arithmetic (the segment stays raw)
-#pragma unroll
-        for (int k = 0; k < NCH; ++k) w[k] = make_uint4(0, 0, 0, 0);
-      }
       float2 a[32];
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
@@ -508,7 +505,32 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_encode64_kernel(const __gr
 #pragma unroll
         for (int k = 0; k < 4; ++k) a[4 * c + k] = make_float2(lo_f32<DT>(ww[k]), hi_f32<DT>(ww[k]));
       }
-      const float n = __fsqrt_rn(vector_sumsq<G>(a));
+      const float ss = vector_sumsq<G>(a);
+      // Admission.  ss is within 2^-20 (relative) of the exact sum of
+      // squares, so ss <= 0.996 reject^2 shows every |x| <= reject; a
+      // nonfinite element makes ss NaN or inf.  Otherwise the warp takes the
+      // exact maximum of every vector.
+      if (__any_sync(0xffffffffu, !(ss <= admit_ss))) {
+        float amax = 0.0f;
+        uint32_t nonfinite = 0;
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+          nonfinite |= !isfinite(a[m].x) | !isfinite(a[m].y);
+          amax = fmaxf(amax, fmaxf(fabsf(a[m].x), fabsf(a[m].y)));
+        }
+#pragma unroll
+        for (int o = 1; o < G; o <<= 1) {
+          nonfinite |= __shfl_xor_sync(0xffffffffu, nonfinite, o);
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        }
+        const uint32_t vflags = nonfinite ? 1u : (amax > p.reject_abs ? 2u : 0u);
+        flags |= vflags;
+        if (vflags) {  // keep NaN / inf out of the arithmetic (the segment stays raw)
+#pragma unroll
+          for (int m = 0; m < 32; ++m) a[m] = make_float2(0.0f, 0.0f);
+        }
+      }
+      const float n = __fsqrt_rn(ss);
       float r = __frcp_rn(n);
       if (!isfinite(r)) r = 0.0f;
       const float2 r2 = make_float2(r, r);

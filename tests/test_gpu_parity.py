@@ -251,6 +251,28 @@ def test_every_16bit_pattern(dtype, codec):
     assert ulps == 0
 
 
+@pytest.mark.parametrize("reject", [1.5, 3.0, 448.0])
+def test_admission_at_the_bound(reject):
+    """Every block holds a vector whose largest |x| is exactly reject_abs
+    (admitted); odd blocks also hold one element at the next BF16 value above
+    it (raw, out of range).  The vectors' norms exceed the bound, so the
+    encoders' exact check runs on admitted and rejected vectors alike."""
+    D, H, T, B = 128, 8, 16, 6
+    g = torch.Generator().manual_seed(int(reject * 16))
+    x = ((torch.rand(B, T, H, D, generator=g) * 2 - 1) * reject).bfloat16().float()
+    x[:, 0, 0, 0] = reject
+    x[:, 2, 5, 1] = -reject
+    above = torch.tensor([reject], dtype=torch.bfloat16).view(torch.int16) + 1
+    x[1::2, 5, 3, 7] = above.view(torch.bfloat16).float().item()
+    t = x.bfloat16()
+    case = synth.Case("bound", torch.bfloat16, "separate", D, H, T, 1, B,
+                      synth._separate_strides(T, H, D), [t, t.clone()], [], 0)
+    for kc, vc in [("tq4", "uni4"), ("tq3", "uni3"), ("tq2", "uni2"), ("fp8_dynamic", "int8")]:
+        st, ulps = run_parity(case, synth.Arm("b", kc, vc, (0, 1)), reject_abs=reject)
+        want = [O.S_RAW_RANGE if b % 2 else O.S_ENCODED for b in range(B) for _ in (0, 1)]
+        assert list(st) == want and ulps == 0, (kc, vc)
+
+
 def test_special_values():
     """Zeros of both signs, constant vectors, FP16 subnormals, +-448 exactly."""
     D, H, T = 64, 2, 16
