@@ -331,14 +331,31 @@ __global__ void __launch_bounds__(kThreads, 3) tq_encode_kernel(const __grid_con
 //    elements 0..31 and the differences of elements 0..31 of the stage
 //    (vector elements A + s and A + 64 + s), the odd lane the sums and the
 //    negated differences of elements 32..63, negated once more afterwards.
-// Lane li ends with elements A + s (registers 0..31) and B + s (32..63):
-// A = 128 (li >> 1) + 32 (li & 1), B = A + 64 for G >= 2; A = 0, B = 32 for
-// G = 1.  Further stages (D = 256) pair lanes li and li ^ 2, which hold the
-// same elements of their halves with the same signs, and run unsplit.
+// D = 256 splits its second stage (lanes li, li ^ 2) the same way, after
+// the first one has put the upper lanes' sums and differences in swapped
+// registers (butterflies64).  Lane li ends with elements 32 li + s
+// (registers 0..31) and 32 G + 32 li + s (32..63); tq64_run_negated names
+// the runs that come out negated.
 constexpr int kTq64Threads = 128;
 
 __device__ __forceinline__ uint4 xor4(const uint4& a, uint32_t m) {
   return make_uint4(a.x ^ m, a.y ^ m, a.z ^ m, a.w ^ m);
+}
+
+// After butterflies64 (without the fix), run R (0: registers 0..31, 1:
+// 32..63) of lane li holds the negated elements: lane 1's second run at
+// G = 2; lane 3's first and lane 2's second at G = 4.
+template <int G>
+__device__ __forceinline__ bool tq64_run_negated(uint32_t li, int run) {
+  if constexpr (G == 2) return run == 1 && li == 1u;
+  if constexpr (G == 4) return run == 0 ? li == 3u : li == 2u;
+  return false;
+}
+
+// Elements of run R of lane li: 32 li + s (R = 0) and 32 G + 32 li + s (R = 1).
+template <int G>
+__device__ __forceinline__ uint32_t tq64_run_start(uint32_t li, int run) {
+  return 32u * li + (run ? 32u * G : 0u);
 }
 
 template <int G, bool FIX>
@@ -358,7 +375,7 @@ __device__ __forceinline__ void butterflies64(float2 (&a)[32], uint32_t li) {
       a[m + h] = sub2(u, v);
     }
   }
-  if constexpr (G >= 2) {  // stride 64: lanes li, li ^ 1, split (see above)
+  if constexpr (G == 2) {  // stride 64: lanes li, li ^ 1, split (see above)
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
       const float2 r = make_float2(__shfl_xor_sync(0xffffffffu, a[16 + m].x, 1),
@@ -368,22 +385,41 @@ __device__ __forceinline__ void butterflies64(float2 (&a)[32], uint32_t li) {
       a[16 + m] = sub2(k, r);
     }
   }
+  if constexpr (G == 4) {
+    // stride 64 (lanes li, li ^ 1) as above, except that lanes 2 and 3 put
+    // the differences in registers 0..31 and the sums in 32..63: r * t + k
+    // with t = -1 is the single rounding of k - r.  Stride 128 (lanes li,
+    // li ^ 2) then pairs registers 0..31 of the lower lane with 32..63 of the
+    // upper one and splits the same way.
+    const float t = (li & 2u) ? -1.0f : 1.0f;
+    const float2 t2 = make_float2(t, t), nt2 = make_float2(-t, -t);
 #pragma unroll
-  for (int o = 2; o < G; o <<= 1) {  // strides 128 o / 2: lanes li, li ^ o
-    const float sg = (li & (uint32_t)o) ? -1.0f : 1.0f;
-    const float2 sg2 = make_float2(sg, sg);
+    for (int m = 0; m < 16; ++m) {
+      const float2 r = make_float2(__shfl_xor_sync(0xffffffffu, a[16 + m].x, 1),
+                                   __shfl_xor_sync(0xffffffffu, a[16 + m].y, 1));
+      const float2 k = a[m];
+      a[m] = fma2(r, t2, k);
+      a[16 + m] = fma2(r, nt2, k);
+    }
 #pragma unroll
-    for (int m = 0; m < 32; ++m) {
-      const float2 partner = make_float2(__shfl_xor_sync(0xffffffffu, a[m].x, o),
-                                         __shfl_xor_sync(0xffffffffu, a[m].y, o));
-      a[m] = fma2(a[m], sg2, partner);  // low lane: mine + partner; high lane: partner - mine
+    for (int m = 0; m < 16; ++m) {
+      const float2 r = make_float2(__shfl_xor_sync(0xffffffffu, a[16 + m].x, 2),
+                                   __shfl_xor_sync(0xffffffffu, a[16 + m].y, 2));
+      const float2 k = a[m];
+      a[m] = add2(k, r);
+      a[16 + m] = sub2(k, r);
     }
   }
-  if constexpr (G >= 2 && FIX) {  // the odd lane's differences of the split stage
-    const float f = (li & 1u) ? -1.0f : 1.0f;
-    const float2 f2 = make_float2(f, f);
+  if constexpr (G >= 2 && FIX) {  // the negated runs (see tq64_run_negated)
+    const float fa = tq64_run_negated<G>(li, 0) ? -1.0f : 1.0f;
+    const float fb = tq64_run_negated<G>(li, 1) ? -1.0f : 1.0f;
+    const float2 fa2 = make_float2(fa, fa), fb2 = make_float2(fb, fb);
+    if constexpr (G == 4) {
 #pragma unroll
-    for (int m = 16; m < 32; ++m) a[m] = mul2(a[m], f2);
+      for (int m = 0; m < 16; ++m) a[m] = mul2(a[m], fa2);
+    }
+#pragma unroll
+    for (int m = 16; m < 32; ++m) a[m] = mul2(a[m], fb2);
   }
 }
 
@@ -457,8 +493,7 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_encode64_kernel(const __gr
   const uint32_t stage = (uint32_t)__cvta_generic_to_shared(&s_stage[warp][lane][0]);
   const uint32_t swz = lane & 7u;
   const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&s_sign[li][0]);
-  const uint32_t run_a = G == 1 ? 0u : 128u * (li >> 1) + 32u * (li & 1u);
-  const uint32_t run_b = run_a + (G == 1 ? 32u : 64u);
+  const uint32_t run_a = tq64_run_start<G>(li, 0), run_b = tq64_run_start<G>(li, 1);
   const uint32_t nv = p.nv;
   const uint32_t jw = warp * VPW + grp;
   const float admit_ss = p.reject_abs * p.reject_abs * 0.99609375f;
@@ -592,13 +627,12 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
   for (int t = threadIdx.x; t < G * 8; t += blockDim.x) {
     // output chunk c of lane l: elements A + 8c (c < 4) or B + 8(c - 4)
     const uint32_t l = (uint32_t)t / 8, c = (uint32_t)t % 8;
-    const uint32_t ra = G == 1 ? 0u : 128u * (l >> 1) + 32u * (l & 1u);
-    const uint32_t e0 = (c < 4 ? ra : ra + (G == 1 ? 32u : 64u)) + 8u * (c & 3u);
+    const uint32_t e0 = tq64_run_start<G>(l, c < 4 ? 0 : 1) + 8u * (c & 3u);
     const uint32_t bits = p.sign_words[e0 >> 5];
     const int k = (int)((e0 & 31u) >> 1);
     uint4 m = make_uint4(sign_mask_word(bits, k), sign_mask_word(bits, k + 1), sign_mask_word(bits, k + 2),
                          sign_mask_word(bits, k + 3));
-    if (G >= 2 && (l & 1u) && c >= 4) m = xor4(m, 0x80008000u);  // the odd lane's differences
+    if (tq64_run_negated<G>(l, c < 4 ? 0 : 1)) m = xor4(m, 0x80008000u);  // negated runs
     s_sign[l][c] = m;
   }
   for (int k = threadIdx.x; k < NPAIR * REP; k += blockDim.x) {
@@ -608,8 +642,7 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
   __syncthreads();
   const uint32_t pair_base = (uint32_t)__cvta_generic_to_shared(s_pair) + (lane % REP) * 8u;
   const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&s_sign[li][0]);
-  const uint32_t run_a = G == 1 ? 0u : 128u * (li >> 1) + 32u * (li & 1u);
-  const uint32_t run_b = run_a + (G == 1 ? 32u : 64u);
+  const uint32_t run_a = tq64_run_start<G>(li, 0), run_b = tq64_run_start<G>(li, 1);
   const uint32_t cmask = (G >= 2 && (li & 1u)) ? 0xffffffffu : 0u;  // complement the upper codes
   const bool vec32 = p.vec32 != 0;
   const float cD = p.wht_scale;
