@@ -353,7 +353,11 @@ void kvo_uniform_encode_vec(const float* x, int D, int bits, uint8_t* codes,
   for (int i = 0; i < D; ++i) {
     if (s == 0.0f) { codes[i] = 0; continue; }
     float q = rintf((x[i] - m) / s);
-    if (q < 0.0f) q = 0.0f;
+    /* READING: a quotient that is not a number takes the lower clamp.  It
+     * arises only when the FP16 minimum and step overflow (m = -inf and
+     * s = inf), i.e. when an admission bound above the FP16 range lets BF16
+     * values beyond +-65504 through. */
+    if (!(q >= 0.0f)) q = 0.0f;
     if (q > levels) q = levels;
     codes[i] = (uint8_t)q;
   }
@@ -571,6 +575,11 @@ void kvo_encode(const kvo_geom* g, void* const* ptrs, const kvo_desc* descs, uin
     memset(slot, 0, (size_t)seg_bytes);
     uint8_t* meta = slot + (size_t)nv * cbytes;
     int64_t rec = kvo_int8_record_bytes(H, D);
+    /* READING: FP16 metadata that overflows (a TurboQuant norm, a uniform
+     * minimum or step beyond +-65504) cannot be stored, so the segment stays
+     * raw as out of range.  Under the default bound (448) this never happens;
+     * it needs an admission bound above the FP16 range and BF16 sources. */
+    int meta_overflow = 0;
     for (int t = 0; t < T; ++t)
       for (int h = 0; h < H; ++h) {
         int v = t * H + h;
@@ -594,17 +603,19 @@ void kvo_encode(const kvo_geom* g, void* const* ptrs, const kvo_desc* descs, uin
         } else if (is_tq(codec)) {
           uint16_t n16;
           kvo_tq_encode_vec(x, D, bits, neg, bnd, codes, &n16);
+          if ((n16 & 0x7FFFu) >= 0x7C00u) meta_overflow = 1;
           kvo_pack_bits(codes, D, bits, vc);
           memcpy(meta + (size_t)v * 2, &n16, 2);
         } else {
           uint16_t mm[2];
           kvo_uniform_encode_vec(x, D, bits, codes, &mm[0], &mm[1]);
+          if ((mm[0] & 0x7FFFu) >= 0x7C00u || (mm[1] & 0x7FFFu) >= 0x7C00u) meta_overflow = 1;
           if (bits == 8) memcpy(vc, codes, (size_t)D);
           else kvo_pack_bits(codes, D, bits, vc);
           memcpy(meta + (size_t)v * 4, mm, 4);
         }
       }
-    status[i] = S_ENCODED;
+    status[i] = meta_overflow ? S_RAW_RANGE : S_ENCODED;
   }
   free(x);
   free(codes);
@@ -641,6 +652,11 @@ void kvo_decode(const kvo_geom* g, void* const* ptrs, const kvo_desc* descs, uin
     const uint8_t* slot = in + d->enc_offset;
     const uint8_t* meta = slot + (size_t)nv * cbytes;
     int64_t rec = kvo_int8_record_bytes(H, D);
+    /* READING: FP16 metadata that overflows (a TurboQuant norm, a uniform
+     * minimum or step beyond +-65504) cannot be stored, so the segment stays
+     * raw as out of range.  Under the default bound (448) this never happens;
+     * it needs an admission bound above the FP16 range and BF16 sources. */
+    int meta_overflow = 0;
     for (int t = 0; t < T; ++t)
       for (int h = 0; h < H; ++h) {
         int v = t * H + h;

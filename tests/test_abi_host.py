@@ -64,6 +64,8 @@ def _kw(**over):
     (dict(strides=(0, 8 * 128, 128)), -3),
     (dict(layout="packed", strides=(8 * 16 * 256, 256, 16 * 128)), -3),  # packed rows are 2D
     (dict(reject_abs=500.0), -1),
+    (dict(reject_abs=float("inf")), -1),   # bounds above 448 could let FP16 metadata overflow
+    (dict(reject_abs=-1.0), -1),
     (dict(reject_abs=float("nan")), -1),
     (dict(k_codec="fp8_fixed", v_codec="fp8_fixed"), -1),    # fixed scales missing
     (dict(geometry_overrides={"abi_version": 2}), -7),

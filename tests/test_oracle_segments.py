@@ -268,3 +268,33 @@ def test_fp8_cast_exhaustive_table(dtype):
     src = O.src_to_f32(good, dtype)
     ref = torch.from_numpy(src).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert np.array_equal(codes, ref)
+
+
+@pytest.mark.parametrize("codecs,want_k,want_v", [
+    ((O.TQ4, O.UNI4), ["E", "R", "E", "R"], ["E", "R", "E", "E"]),
+    ((O.UNI8, O.UNI8), ["E", "R", "E", "E"], ["E", "R", "E", "E"]),
+    ((O.FP8_DYNAMIC, O.INT8), ["E"] * 4, ["E"] * 4)])
+def test_fp16_metadata_overflow_stays_raw(codecs, want_k, want_v):
+    """Under an admission bound above the FP16 range (here +inf) with BF16
+    sources, a TurboQuant norm or a uniform minimum / step beyond +-65504
+    cannot be stored: the segment stays raw as out of range.  FP8 (FP32
+    scale) and INT8 (BF16 scale) still code it."""
+    D, H, T, B = 64, 8, 16, 4                # (H = 8: at H = 2 an INT8 record saves nothing)
+    k = np.random.default_rng(3).standard_normal((B, T, H, D)).astype(np.float32)
+    k[1, 0, 0, :] = 1e5                                            # norm 8e5, minimum 1e5
+    k[2, 3, 1, :] = np.where(np.arange(D) % 2, 6000.0, -6000.0)   # norm 48,000: fits
+    k[3, 5, 0, 9] = 70000.0                                        # norm > 65504, step fits
+    kb = O.f32_to_bf16(k).reshape(-1)
+    g = O.make_geom(dtype=O.BF16, layout=O.SEPARATE, head_dim=D, num_heads=H, block_tokens=T,
+                    num_layers=1, num_blocks=B, strides=(T * H * D, H * D, D), codecs=codecs,
+                    seed=1, reject_abs=np.inf)
+    seg = [O.segment_enc_bytes(g, r) for r in (0, 1)]
+    rows, off = [], 0
+    for b in range(B):
+        for r in (0, 1):
+            rows.append((0, b, r, off))
+            off += seg[r]
+    _, st = O.encode(g, [kb, kb.copy()], oracle_descs(rows), off)
+    code = {"E": O.S_ENCODED, "R": O.S_RAW_RANGE}
+    assert list(st[0::2]) == [code[c] for c in want_k]
+    assert list(st[1::2]) == [code[c] for c in want_v]

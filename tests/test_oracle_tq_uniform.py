@@ -185,3 +185,18 @@ def test_pack_is_little_endian_bitstream(bits):
     if bits == 3:
         # codes 0..7 -> bits 000 100 010 110 001 101 011 111 (LSB first)
         assert list(O.pack_bits(np.arange(8, dtype=np.uint8), 3)) == [0x88, 0xC6, 0xFA]
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+def test_uniform_fp16_metadata_overflow(bits):
+    """Values beyond the FP16 range (only admitted under a bound above 65504):
+    the FP16 minimum overflows to -inf.  With a finite step every quotient is
+    +inf and codes as the top level; when the step overflows too, inf / inf
+    is not a number and codes as the lower clamp, 0."""
+    top = (1 << bits) - 1
+    x = np.array([[-1e5 + i for i in range(32)],          # m = -inf, s finite
+                  [-1e7 if i % 2 else 1e7 for i in range(32)]], dtype=np.float32)  # s = inf
+    codes, m16, s16 = O.uniform_encode(x, bits)
+    assert list(m16) == [0xFC00, 0xFC00]
+    assert s16[0] not in (0x7C00, 0) and s16[1] == 0x7C00
+    assert np.all(codes[0] == top) and np.all(codes[1] == 0)
