@@ -15,6 +15,7 @@ namespace {
 #define LV(b) ((1u << (b)) - 1u)
 
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr uint32_t kRoundMagicBits = 0x4b400000u;
 constexpr int kEncodeCtas = 5;  // resident CTAs per SM (see launch_codec_kernel)
 constexpr int kDecodeCtas = 5;
 
@@ -24,7 +25,14 @@ constexpr int kDecodeCtas = 5;
 // integers), and RN(q + 1.5 * 2^23) holds rint(q) in its low byte, which is
 // what t[] returns (the higher bits are the magic's).  The caller passes r = 0
 // when s == 0, which makes every quotient 0.
-template <uint32_t LEVELS>
+//
+// SAT (2, 4 and 8 bits): t[] is rint(q) itself, unclamped, as a signed
+// integer, and the saturating packs (pack_codes8) clamp it.  Admitted vectors
+// have |x| <= 448, so |m - min| <= 0.125 (half the FP16 spacing below 512)
+// and s >= 2^-24 whenever s != 0; hence |q| <= 0.125 * 2^24 + 1.5 L < 2^22,
+// the range in which RN(q + 1.5 * 2^23) - 1.5 * 2^23 is rint(q).  (Codes of
+// vectors that fail admission are never used: their segment stays raw.)
+template <uint32_t LEVELS, bool SAT>
 __device__ __forceinline__ void uniform_codes8(const float (&x)[8], float m, float sc, float r,
                                                uint32_t (&t)[8]) {
   const float2 m2 = make_float2(m, m), ns2 = make_float2(-sc, -sc), r2 = make_float2(r, r);
@@ -35,25 +43,42 @@ __device__ __forceinline__ void uniform_codes8(const float (&x)[8], float m, flo
     const float2 q0 = mul2(d, r2);
     const float2 res = fma2(q0, ns2, d);
     float2 q = fma2(res, r2, q0);
-    q.x = fminf(fmaxf(q.x, 0.0f), (float)LEVELS);
-    q.y = fminf(fmaxf(q.y, 0.0f), (float)LEVELS);
+    if (!SAT) {
+      q.x = fminf(fmaxf(q.x, 0.0f), (float)LEVELS);
+      q.y = fminf(fmaxf(q.y, 0.0f), (float)LEVELS);
+    }
     const float2 v = add2(q, mg2);
-    t[e] = __float_as_uint(v.x);
-    t[e + 1] = __float_as_uint(v.y);
+    t[e] = __float_as_uint(v.x) - (SAT ? kRoundMagicBits : 0u);
+    t[e + 1] = __float_as_uint(v.y) - (SAT ? kRoundMagicBits : 0u);
   }
 }
 
-// The low bytes of four words, in order, as one word (three byte permutes).
-__device__ __forceinline__ uint32_t low_bytes4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+// (c << 2 BITS) | (sat(a) << BITS) | sat(b), with a and b signed and sat the
+// clamp to [0, 2^BITS - 1]
+template <int BITS>
+__device__ __forceinline__ uint32_t pack_sat(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  if (BITS == 8) asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  else if (BITS == 4) asm("cvt.pack.sat.u4.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  else asm("cvt.pack.sat.u2.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 
 // Codes of 8 elements (t[] from uniform_codes8) as the little-endian bit
-// stream of BITS-bit codes: 8 bytes (BITS = 8: byte permutes of the low
-// bytes) or the low 8 * BITS bits.
+// stream of BITS-bit codes: 8 bytes (BITS = 8) or the low 8 * BITS bits.
+// 2, 4 and 8 bits: saturating packs, two codes each; 3 bits: the clamped
+// codes' low bits shifted into place.
 template <int BITS>
 __device__ __forceinline__ uint2 pack_codes8(const uint32_t (&t)[8]) {
-  if (BITS == 8) return make_uint2(low_bytes4(t[0], t[1], t[2], t[3]), low_bytes4(t[4], t[5], t[6], t[7]));
+  if (BITS == 8)
+    return make_uint2(pack_sat<8>(t[1], t[0], pack_sat<8>(t[3], t[2], 0u)),
+                      pack_sat<8>(t[5], t[4], pack_sat<8>(t[7], t[6], 0u)));
+  if (BITS == 4 || BITS == 2) {
+    uint32_t v = pack_sat<BITS>(t[7], t[6], 0u);
+    v = pack_sat<BITS>(t[5], t[4], v);
+    v = pack_sat<BITS>(t[3], t[2], v);
+    return make_uint2(pack_sat<BITS>(t[1], t[0], v), 0u);
+  }
   uint32_t v = 0;
 #pragma unroll
   for (int e = 0; e < 8; ++e) v |= (t[e] & ((1u << BITS) - 1u)) << (BITS * e);
@@ -153,7 +178,7 @@ __global__ void __launch_bounds__(NT) uniform_encode_kernel(const __grid_constan
           float x[8];
           unpack8<DT>(w[u][ch], x);
           uint32_t t[8];
-          uniform_codes8<LEVELS>(x, m, sc, r, t);
+          uniform_codes8<LEVELS, BITS != 3>(x, m, sc, r, t);
           const uint2 v = pack_codes8<BITS>(t);
           if (BITS == 8) {
             if (in) st8(vc + 8 * cidx, v);
@@ -245,7 +270,7 @@ __global__ void __launch_bounds__(NT) uniform_encode_lanes_kernel(const __grid_c
           float x[8];
           unpack8<DT>(w[u][c], x);
           uint32_t t[8];
-          uniform_codes8<LEVELS>(x, m, sc, r, t);
+          uniform_codes8<LEVELS, BITS != 3>(x, m, sc, r, t);
           v[c] = pack_codes8<BITS>(t);
         }
         if (j < nv) {
