@@ -423,6 +423,16 @@ __device__ __forceinline__ void butterflies64(float2 (&a)[32], uint32_t li) {
   }
 }
 
+// (c << 2 BITS) | (a << BITS) | b for codes a, b < 2^BITS (BITS = 2 or 4):
+// one saturating pack, which leaves in-range codes unchanged
+template <int BITS>
+__device__ __forceinline__ uint32_t tq_pack2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  if (BITS == 4) asm("cvt.pack.sat.u4.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  else asm("cvt.pack.sat.u2.s32.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 // Codes of 32 consecutive elements held in pairs a[P0 .. P0 + 15], element 0
 // in the lowest bits of w[0]; BITS * 32 / 32 words.
 template <int BITS, int P0, int P>
@@ -438,10 +448,16 @@ __device__ __forceinline__ void tq_codes32(const float2 (&a)[P], uint32_t lut_ba
       asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(ent.x), "=r"(ent.y) : "r"(cell * 128u + lut_base));
       c[e] = ent.y + (x > __uint_as_float(ent.x) ? 1u : 0u);
     }
-    // element 0 in the lowest bits, combined as a tree (depth 3, not 8)
-    const uint32_t p0 = c[0] + (c[1] << BITS), p1 = c[2] + (c[3] << BITS);
-    const uint32_t p2 = c[4] + (c[5] << BITS), p3 = c[6] + (c[7] << BITS);
-    acc[q] = (p0 + (p1 << (2 * BITS))) + ((p2 + (p3 << (2 * BITS))) << (4 * BITS));
+    if (BITS == 4 || BITS == 2) {  // element 0 in the lowest bits, two codes per pack
+      uint32_t v = tq_pack2<BITS>(c[7], c[6], 0u);
+      v = tq_pack2<BITS>(c[5], c[4], v);
+      v = tq_pack2<BITS>(c[3], c[2], v);
+      acc[q] = tq_pack2<BITS>(c[1], c[0], v);
+    } else {  // element 0 in the lowest bits, combined as a tree (depth 3, not 8)
+      const uint32_t p0 = c[0] + (c[1] << BITS), p1 = c[2] + (c[3] << BITS);
+      const uint32_t p2 = c[4] + (c[5] << BITS), p3 = c[6] + (c[7] << BITS);
+      acc[q] = (p0 + (p1 << (2 * BITS))) + ((p2 + (p3 << (2 * BITS))) << (4 * BITS));
+    }
   }
 }
 
