@@ -731,6 +731,12 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
       const float nc = __fsqrt_rn(vector_sumsq<G>(a));
       const float g = __fdiv_rn(__half2float(__ushort_as_half(n16)), nc);
       const float2 g2 = make_float2(g, g);
+      // D = 64, 256: 1/sqrt(D) is a power of two, and neither t * (1/sqrt(D))
+      // (|t| >= 2^-30 or 0: sums of centroids) nor (1/sqrt(D)) * g
+      // (g >= 2^-26) leaves the normal range, so both products are exact and
+      // RN(RN(t / sqrt(D)) * g) = RN(t * (g / sqrt(D))): one multiply.
+      constexpr bool kPow2Scale = D == 64 || D == 256;
+      const float2 gc2 = make_float2(__fmul_rn(g, cD), __fmul_rn(g, cD));
       butterflies64<G, false>(a, li);
       uint32_t o[32];
 #pragma unroll
@@ -739,7 +745,7 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
         const uint32_t mk[4] = {m.x, m.y, m.z, m.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float2 t = mul2(mul2(a[4 * c + k], cD2), g2);
+          const float2 t = kPow2Scale ? mul2(a[4 * c + k], gc2) : mul2(mul2(a[4 * c + k], cD2), g2);
           o[4 * c + k] = pack2<DT>(t.x, t.y) ^ mk[k];
         }
       }
