@@ -12,20 +12,32 @@
 // the register through n zero bytes" (both GF(2)-linear):
 //   CRC(M) = R(M) ^ F_N(~0) ^ ~0,   R(A || B) = F_|B|(R(A)) ^ R(B),
 // and leading zero bytes leave R unchanged.  So the slot is front-padded to a
-// multiple of 512 bytes, lane l reads the 16-byte chunks l, l + 32, ... (one
-// coalesced 512-byte row per warp load), keeps s = F_512(s) ^ R(chunk), and
-// finally advances s by the 16 * (31 - l) bytes that follow its last chunk;
-// the xor of the lanes is R(M).  Every map is applied as 16-entry nibble
-// tables in shared memory (a table fills 16 distinct banks, so any indices
-// are conflict-free).
+// multiple of kCrcRow (2 KB) bytes.  Lane l takes the 64-byte blocks l,
+// l + 32, ... (one row of 32 blocks per step), folds each block from a zero
+// register a word at a time with four byte tables (slicing by 4), and keeps
+// s = F_2048(s) ^ R(block).  Finally it advances s by the 64 * (31 - l) bytes
+// that follow its last block; the xor of the lanes is R(M).
+//
+// The byte tables sit in shared memory in 32 copies, entry e of copy l in bank
+// l, so the 32 lookups of a warp never conflict: 4 x 256 x 32 words (128 KB),
+// one 1024-thread CTA per SM.  The advance maps are 16-entry nibble tables
+// (a table fills 16 distinct banks, so any indices are conflict-free).
 #include "device_common.cuh"
 
 namespace kvc {
 namespace {
 
-constexpr int kCrcCtas = 8;              // resident CTAs per SM (8 warps, one slot each)
-constexpr int kWarps = kThreads / 32;
-constexpr int kRowUnroll = 4;            // rows of 16-byte chunks in flight per lane
+constexpr int kCrcThreads = 1024;       // one CTA per SM (the tables take 128 KB)
+constexpr int kWarps = kCrcThreads / 32;
+constexpr uint32_t kByteTabBytes = 4u * 256u * 32u * 4u;   // 128 KB
+constexpr uint32_t kTabAlign = 32768u;  // each byte table on a 32 KB boundary
+struct NibbleTables {
+  uint32_t row[8][16];
+  uint32_t fin[5][8][16];
+};
+// dynamic shared memory: the nibble tables, then the byte tables at the next
+// 32 KB boundary of the shared window
+constexpr uint32_t kCrcSmem = (uint32_t)sizeof(NibbleTables) + kTabAlign + kByteTabBytes;
 
 // Entry at byte offset `off` of nibble table q.
 __device__ __forceinline__ uint32_t entry(const uint32_t (*t)[16], int q, uint32_t off) {
@@ -45,31 +57,50 @@ __device__ __forceinline__ uint32_t apply8(const uint32_t (*t)[16], uint32_t r) 
   return a ^ b ^ entry(t, 6, __byte_perm(ev, 0, 0x4443)) ^ entry(t, 7, __byte_perm(od, 0, 0x4443));
 }
 
-// R(chunk) of one 16-byte chunk: nibble i (byte i/2, low or high half) through
-// its own table.
-__device__ __forceinline__ uint32_t chunk_reg(const uint32_t (*t)[16], const uint4& c) {
-  return apply8(t, c.x) ^ apply8(t + 8, c.y) ^ apply8(t + 16, c.z) ^ apply8(t + 24, c.w);
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
 }
 
-// CRC-32 of the n-byte slot at `slot` (n a multiple of 16), computed by the
-// calling warp; every lane returns the same value.
-__device__ __forceinline__ uint32_t warp_crc(const CrcTables& T, const uint8_t* slot, uint32_t n,
-                                             uint32_t crc_k, uint32_t lane) {
-  const uint32_t pad = (512u - n % 512u) % 512u;
-  const uint32_t rows = (n + pad) / 512u;
+// R of one 64-byte block (16 little-endian words) from a zero register.
+// tb = the shared address of this lane's copy of byte table 0: table k copy l
+// entry e is at tb + k * 32 KB + e * 128, and bits 7..14 of tb + k * 32 KB
+// are zero, so the byte shifted to bit 7 is OR-ed in.
+__device__ __forceinline__ uint32_t fold_block(uint32_t tb, const uint4 (&c)[4]) {
   uint32_t s = 0;
-  for (uint32_t m = 0; m < rows; m += kRowUnroll) {
-    uint4 c[kRowUnroll];
 #pragma unroll
-    for (int u = 0; u < kRowUnroll; ++u) {
-      const int64_t off = (int64_t)(m + u) * 512 + 16 * lane - pad;
-      c[u] = (m + u < rows && off >= 0) ? ld_nc16(slot + off) : make_uint4(0, 0, 0, 0);
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t w[4] = {c[q].x, c[q].y, c[q].z, c[q].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      s ^= w[k];
+      s = lds32(((s << 7) & 0x7f80u) | (tb + 3u * kTabAlign)) ^ lds32(((s >> 1) & 0x7f80u) | (tb + 2u * kTabAlign)) ^
+          lds32(((s >> 9) & 0x7f80u) | (tb + kTabAlign)) ^ lds32(((s >> 17) & 0x7f80u) | tb);
     }
-#pragma unroll
-    for (int u = 0; u < kRowUnroll; ++u)
-      if (m + u < rows) s = apply8(T.row, s) ^ chunk_reg(T.chunk, c[u]);
   }
-  const uint32_t after = 31u - lane;  // chunks of the last row after this lane's
+  return s;
+}
+
+// CRC-32 of the n-byte slot at `slot` (n a multiple of 128), computed by the
+// calling warp; every lane returns the same value.
+__device__ __forceinline__ uint32_t warp_crc(const NibbleTables& T, uint32_t tb, const uint8_t* slot,
+                                             uint32_t n, uint32_t crc_k, uint32_t lane) {
+  const uint32_t pad = (kCrcRow - n % kCrcRow) % kCrcRow;
+  const uint32_t rows = (n + pad) / kCrcRow;
+  uint32_t s = 0;
+  for (uint32_t m = 0; m < rows; ++m) {
+    const int64_t off = (int64_t)m * kCrcRow + kCrcBlock * lane - pad;
+    uint32_t r = 0;
+    if (off >= 0) {  // blocks of the front padding are zeros: R = 0
+      uint4 c[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) c[q] = ld_nc16(slot + off + 16 * q);
+      r = fold_block(tb, c);
+    }
+    s = apply8(T.row, s) ^ r;
+  }
+  const uint32_t after = 31u - lane;  // blocks of the last row after this lane's
 #pragma unroll
   for (int b = 0; b < 5; ++b) {
     const uint32_t t = apply8(T.fin[b], s);
@@ -80,11 +111,21 @@ __device__ __forceinline__ uint32_t warp_crc(const CrcTables& T, const uint8_t* 
   return s ^ crc_k;
 }
 
-__device__ __forceinline__ void load_tables(const CrcParams& p, CrcTables& t) {
-  const uint32_t* src = reinterpret_cast<const uint32_t*>(&p.tab);
-  uint32_t* dst = reinterpret_cast<uint32_t*>(&t);
-  for (uint32_t k = threadIdx.x; k < sizeof(CrcTables) / 4; k += blockDim.x) dst[k] = src[k];
+// Fill the shared tables; returns the shared address of this lane's copy of
+// byte table 0.
+__device__ __forceinline__ uint32_t load_tables(const CrcParams& p, NibbleTables*& nt) {
+  extern __shared__ __align__(16) uint8_t crc_smem[];
+  nt = reinterpret_cast<NibbleTables*>(crc_smem);
+  const uint32_t base = (uint32_t)__cvta_generic_to_shared(crc_smem);
+  const uint32_t tab = (base + (uint32_t)sizeof(NibbleTables) + kTabAlign - 1u) & ~(kTabAlign - 1u);
+  uint32_t* byte_tab = reinterpret_cast<uint32_t*>(crc_smem + (tab - base));
+  const uint32_t* src = &p.tab.row[0][0];
+  uint32_t* dst = &nt->row[0][0];
+  for (uint32_t k = threadIdx.x; k < sizeof(NibbleTables) / 4; k += blockDim.x) dst[k] = src[k];
+  for (uint32_t w = threadIdx.x; w < kByteTabBytes / 4; w += blockDim.x)
+    byte_tab[w] = p.tab.byte[w >> 13][(w >> 5) & 255u];  // table w / 8192, entry (w / 32) % 256, copy w % 32
   __syncthreads();
+  return tab + (threadIdx.x & 31u) * 4u;
 }
 
 // Descriptor checks that need no layer pointers.
@@ -107,9 +148,9 @@ __device__ __forceinline__ void store_header(kv_segment_header* h, uint32_t form
   w[3] = (uint64_t)crc | ((uint64_t)status << 32);
 }
 
-__global__ void __launch_bounds__(kThreads) crc_seal_kernel(const __grid_constant__ CrcParams p) {
-  __shared__ CrcTables t;
-  load_tables(p, t);
+__global__ void __launch_bounds__(kCrcThreads, 1) crc_seal_kernel(const __grid_constant__ CrcParams p) {
+  NibbleTables* t;
+  const uint32_t tb = load_tables(p, t);
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   for (uint32_t i = blockIdx.x * kWarps + warp; i < p.n_segments; i += gridDim.x * kWarps) {
     uint32_t role;
@@ -123,15 +164,15 @@ __global__ void __launch_bounds__(kThreads) crc_seal_kernel(const __grid_constan
     uint32_t crc = 0;
     if (st == KV_SEG_ENCODED && p.codec[role] != KV_CODEC_NONE) {
       stored = p.seg_bytes[role];
-      crc = warp_crc(t, p.buf + off, (uint32_t)stored, p.crc_k[role], lane);
+      crc = warp_crc(*t, tb, p.buf + off, (uint32_t)stored, p.crc_k[role], lane);
     }
     if (lane == 0) store_header(p.headers + i, p.format[role], stored, crc, st, p.orig_bytes);
   }
 }
 
-__global__ void __launch_bounds__(kThreads) crc_verify_kernel(const __grid_constant__ CrcParams p) {
-  __shared__ CrcTables t;
-  load_tables(p, t);
+__global__ void __launch_bounds__(kCrcThreads, 1) crc_verify_kernel(const __grid_constant__ CrcParams p) {
+  NibbleTables* t;
+  const uint32_t tb = load_tables(p, t);
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   for (uint32_t i = blockIdx.x * kWarps + warp; i < p.n_segments; i += gridDim.x * kWarps) {
     uint32_t role;
@@ -150,7 +191,7 @@ __global__ void __launch_bounds__(kThreads) crc_verify_kernel(const __grid_const
               orig == p.orig_bytes && st >= KV_SEG_ENCODED && st <= KV_SEG_BAD_DESC;
     if (ok && st == KV_SEG_ENCODED) {
       ok = stored == p.seg_bytes[role];
-      if (ok) ok = warp_crc(t, p.buf + off, (uint32_t)stored, p.crc_k[role], lane) == (uint32_t)w3;
+      if (ok) ok = warp_crc(*t, tb, p.buf + off, (uint32_t)stored, p.crc_k[role], lane) == (uint32_t)w3;
     } else if (ok) {
       ok = stored == 0;
     }
@@ -163,11 +204,16 @@ __global__ void __launch_bounds__(kThreads) crc_verify_kernel(const __grid_const
 int launch_crc(const CrcParams& p, int seal, void* stream) {
   const void* k = seal ? reinterpret_cast<const void*>(crc_seal_kernel)
                        : reinterpret_cast<const void*>(crc_verify_kernel);
+  // the tables need more than the default 48 KB of dynamic shared memory (set
+  // on every launch: the attribute belongs to the current device's context)
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCrcSmem) != cudaSuccess)
+    return KV_ERR_CUDA;
   unsigned grid = 0;
-  const int rc = grid_for(k, (p.n_segments + kWarps - 1) / kWarps, kCrcCtas, &grid);
+  const int rc = grid_for_threads(k, (p.n_segments + kWarps - 1) / kWarps, 1, kCrcThreads, &grid);
   if (rc != KV_OK || grid == 0) return rc;
   void* args[] = {const_cast<CrcParams*>(&p)};
-  const cudaError_t e = cudaLaunchKernel(k, dim3(grid), dim3(kThreads), args, 0, (cudaStream_t)stream);
+  const cudaError_t e =
+      cudaLaunchKernel(k, dim3(grid), dim3(kCrcThreads), args, kCrcSmem, (cudaStream_t)stream);
   return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 

@@ -185,15 +185,12 @@ uint32_t crc_advance(uint32_t r, uint64_t n) {
 // sits in byte 4 w + k/2 of the chunk (low half for even k) and is followed by
 // 15 - that byte's index bytes of the chunk.
 void build_crc_tables(kvc::CrcTables& t) {
-  for (int i = 0; i < 32; ++i) {
-    const int byte = 4 * (i / 8) + (i % 8) / 2, shift = 4 * (i % 2);
-    for (uint32_t v = 0; v < 16; ++v)
-      t.chunk[i][v] = crc_advance(crc_bit_steps(v << shift, 8), (uint64_t)(15 - byte));
-  }
+  for (int k = 0; k < 4; ++k)
+    for (uint32_t v = 0; v < 256; ++v) t.byte[k][v] = crc_advance(crc_bit_steps(v, 8), (uint64_t)k);
   for (int k = 0; k < 8; ++k)
     for (uint32_t v = 0; v < 16; ++v) {
-      t.row[k][v] = crc_advance(v << (4 * k), 512);
-      for (int b = 0; b < 5; ++b) t.fin[b][k][v] = crc_advance(v << (4 * k), 16ull << b);
+      t.row[k][v] = crc_advance(v << (4 * k), kvc::kCrcRow);
+      for (int b = 0; b < 5; ++b) t.fin[b][k][v] = crc_advance(v << (4 * k), (uint64_t)kvc::kCrcBlock << b);
     }
 }
 

@@ -75,10 +75,12 @@ enum Dir { kEncode = 0, kDecode = 1 };
 // 512 zero bytes per row; the lanes' registers are then advanced by the
 // 16 * (31 - l) bytes that follow their last chunk and xor-combined.  Every
 // step is a GF(2)-linear map of 32 bits, applied as 16-entry nibble tables.
+constexpr uint32_t kCrcBlock = 64;               // bytes a lane folds per row
+constexpr uint32_t kCrcRow = 32 * kCrcBlock;     // one row: a 64-byte block per lane
 struct CrcTables {
-  uint32_t chunk[32][16];   // nibble i of a 16-byte chunk -> its share of the chunk's register
-  uint32_t row[8][16];      // register advanced by 512 zero bytes, per nibble
-  uint32_t fin[5][8][16];   // register advanced by 16 * 2^b zero bytes, b = 0..4
+  uint32_t byte[4][256];    // slicing by 4: register of byte v followed by k zero bytes
+  uint32_t row[8][16];      // register advanced by kCrcRow zero bytes, per nibble
+  uint32_t fin[5][8][16];   // register advanced by kCrcBlock * 2^b zero bytes, b = 0..4
 };
 
 struct CrcParams {
