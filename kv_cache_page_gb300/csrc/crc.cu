@@ -20,8 +20,12 @@
 //
 // The byte tables sit in shared memory in 32 copies, entry e of copy l in bank
 // l, so the 32 lookups of a warp never conflict: 4 x 256 x 32 words (128 KB),
-// one 1024-thread CTA per SM.  The advance maps are 16-entry nibble tables
-// (a table fills 16 distinct banks, so any indices are conflict-free).
+// one 1024-thread CTA per SM.  Tables 2i and 2i + 1 share a 64 KB region on a
+// 64 KB boundary: entry e of copy l of table k at (k >> 1) 64 KB + 256 e +
+// 128 (k & 1) + 4 l, so a lookup address is one byte permute of the register
+// (the index byte into bits 8..15) with the lane's constant (the other bytes).
+// The advance maps are 16-entry nibble tables (a table fills 16 distinct
+// banks, so any indices are conflict-free).
 #include "device_common.cuh"
 
 namespace kvc {
@@ -30,13 +34,13 @@ namespace {
 constexpr int kCrcThreads = 1024;       // one CTA per SM (the tables take 128 KB)
 constexpr int kWarps = kCrcThreads / 32;
 constexpr uint32_t kByteTabBytes = 4u * 256u * 32u * 4u;   // 128 KB
-constexpr uint32_t kTabAlign = 32768u;  // each byte table on a 32 KB boundary
+constexpr uint32_t kTabAlign = 65536u;  // the byte tables start on a 64 KB boundary
 struct NibbleTables {
   uint32_t row[8][16];
   uint32_t fin[5][8][16];
 };
 // dynamic shared memory: the nibble tables, then the byte tables at the next
-// 32 KB boundary of the shared window
+// 64 KB boundary of the shared window
 constexpr uint32_t kCrcSmem = (uint32_t)sizeof(NibbleTables) + kTabAlign + kByteTabBytes;
 
 // Entry at byte offset `off` of nibble table q.
@@ -64,10 +68,11 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 }
 
 // R of one 64-byte block (16 little-endian words) from a zero register.
-// tb = the shared address of this lane's copy of byte table 0: table k copy l
-// entry e is at tb + k * 32 KB + e * 128, and bits 7..14 of tb + k * 32 KB
-// are zero, so the byte shifted to bit 7 is OR-ed in.
+// tb = the shared address of this lane's copy of byte table 0 (bits 8..15
+// zero); table k adds (k >> 1) 64 KB + 128 (k & 1), and byte j of the
+// register goes to bits 8..15: s = T3[b0] ^ T2[b1] ^ T1[b2] ^ T0[b3].
 __device__ __forceinline__ uint32_t fold_block(uint32_t tb, const uint4 (&c)[4]) {
+  const uint32_t t3 = tb + kTabAlign + 128u, t2 = tb + kTabAlign, t1 = tb + 128u, t0 = tb;
   uint32_t s = 0;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -75,8 +80,8 @@ __device__ __forceinline__ uint32_t fold_block(uint32_t tb, const uint4 (&c)[4])
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       s ^= w[k];
-      s = lds32(((s << 7) & 0x7f80u) | (tb + 3u * kTabAlign)) ^ lds32(((s >> 1) & 0x7f80u) | (tb + 2u * kTabAlign)) ^
-          lds32(((s >> 9) & 0x7f80u) | (tb + kTabAlign)) ^ lds32(((s >> 17) & 0x7f80u) | tb);
+      s = lds32(__byte_perm(s, t3, 0x7604)) ^ lds32(__byte_perm(s, t2, 0x7614)) ^
+          lds32(__byte_perm(s, t1, 0x7624)) ^ lds32(__byte_perm(s, t0, 0x7634));
     }
   }
   return s;
@@ -88,14 +93,20 @@ __device__ __forceinline__ uint32_t warp_crc(const NibbleTables& T, uint32_t tb,
                                              uint32_t n, uint32_t crc_k, uint32_t lane) {
   const uint32_t pad = (kCrcRow - n % kCrcRow) % kCrcRow;
   const uint32_t rows = (n + pad) / kCrcRow;
+  const bool al32 = ((uintptr_t)slot & 31u) == 0;  // blocks start on 64-byte offsets of the slot
   uint32_t s = 0;
   for (uint32_t m = 0; m < rows; ++m) {
     const int64_t off = (int64_t)m * kCrcRow + kCrcBlock * lane - pad;
     uint32_t r = 0;
     if (off >= 0) {  // blocks of the front padding are zeros: R = 0
       uint4 c[4];
+      if (al32) {
+        ld_nc32(slot + off, c[0], c[1]);
+        ld_nc32(slot + off + 32, c[2], c[3]);
+      } else {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) c[q] = ld_nc16(slot + off + 16 * q);
+        for (int q = 0; q < 4; ++q) c[q] = ld_nc16(slot + off + 16 * q);
+      }
       r = fold_block(tb, c);
     }
     s = apply8(T.row, s) ^ r;
@@ -122,8 +133,10 @@ __device__ __forceinline__ uint32_t load_tables(const CrcParams& p, NibbleTables
   const uint32_t* src = &p.tab.row[0][0];
   uint32_t* dst = &nt->row[0][0];
   for (uint32_t k = threadIdx.x; k < sizeof(NibbleTables) / 4; k += blockDim.x) dst[k] = src[k];
-  for (uint32_t w = threadIdx.x; w < kByteTabBytes / 4; w += blockDim.x)
-    byte_tab[w] = p.tab.byte[w >> 13][(w >> 5) & 255u];  // table w / 8192, entry (w / 32) % 256, copy w % 32
+  for (uint32_t w = threadIdx.x; w < kByteTabBytes / 4; w += blockDim.x) {
+    // word w: region w >> 14, entry (w >> 6) & 255, table 2 region + ((w >> 5) & 1), copy w & 31
+    byte_tab[w] = p.tab.byte[2u * (w >> 14) + ((w >> 5) & 1u)][(w >> 6) & 255u];
+  }
   __syncthreads();
   return tab + (threadIdx.x & 31u) * 4u;
 }
