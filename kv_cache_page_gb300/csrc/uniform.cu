@@ -298,7 +298,10 @@ __device__ __forceinline__ float small_u2f(uint32_t c) {
   return __fsub_rn(__uint_as_float(0x4b000000u | c), 8388608.0f);
 }
 
-template <int DT, int D, int BITS, int NT>
+// ADJ (segments of 256+ vectors, D >= 64, 2/4/8-bit codes): lane li owns the
+// adjacent chunks 2 li, 2 li + 1 -- one code load and, when every vector is
+// 32-byte aligned, one 32-byte store per vector (as the FP8 decoder).
+template <int DT, int D, int BITS, int NT, bool ADJ>
 __global__ void __launch_bounds__(NT) uniform_decode_kernel(const __grid_constant__ Params p) {
   using M = ChunkMap<D>;
   // 3-bit codes (two dependent word loads per chunk) keep twice as many
@@ -310,6 +313,7 @@ __global__ void __launch_bounds__(NT) uniform_decode_kernel(const __grid_constan
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
   const uint32_t nv = p.nv;
+  const bool vec32 = p.vec32 != 0;
   for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
     const Seg s = plan_segment(p, i, kDecode);
     if (s.action != kProcess) {
@@ -327,15 +331,34 @@ __global__ void __launch_bounds__(NT) uniform_decode_kernel(const __grid_constan
         const uint32_t j = j0 + u * VPW + grp;
         const bool in = j < nv;
         const uint8_t* vc = codes + (uint64_t)j * CB;
-#pragma unroll
-        for (int ch = 0; ch < NC; ++ch) {
-          const uint32_t cidx = li + G * ch;
-          cw[u][ch] = make_uint2(0, 0);
+        if (ADJ && NC == 2) {  // chunks 2 li, 2 li + 1: 2 * BITS bytes at 2 * BITS * li
+          cw[u][0] = cw[u][NC - 1] = make_uint2(0, 0);
           if (in) {
-            if (BITS == 8) cw[u][ch] = ld_nc8(vc + 8 * cidx);
-            else if (BITS == 4) cw[u][ch].x = ld_nc4(vc + 4 * cidx);
-            else if (BITS == 2) cw[u][ch].x = ld_nc2(vc + 2 * cidx);
-            else cw[u][ch].x = load_3bit(vc, cidx);
+            if (BITS == 8) {
+              const uint4 t = ld_nc16(vc + 16 * li);
+              cw[u][0] = make_uint2(t.x, t.y);
+              cw[u][NC - 1] = make_uint2(t.z, t.w);
+            } else if (BITS == 4) {
+              const uint2 t = ld_nc8(vc + 8 * li);
+              cw[u][0].x = t.x;
+              cw[u][NC - 1].x = t.y;
+            } else {
+              const uint32_t t = ld_nc4(vc + 4 * li);
+              cw[u][0].x = t & 0xffffu;
+              cw[u][NC - 1].x = t >> 16;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int ch = 0; ch < NC; ++ch) {
+            const uint32_t cidx = li + G * ch;
+            cw[u][ch] = make_uint2(0, 0);
+            if (in) {
+              if (BITS == 8) cw[u][ch] = ld_nc8(vc + 8 * cidx);
+              else if (BITS == 4) cw[u][ch].x = ld_nc4(vc + 4 * cidx);
+              else if (BITS == 2) cw[u][ch].x = ld_nc2(vc + 2 * cidx);
+              else cw[u][ch].x = load_3bit(vc, cidx);
+            }
           }
         }
         mw[u] = in ? ld_nc4(meta + (uint64_t)j * 4) : 0u;
@@ -347,6 +370,7 @@ __global__ void __launch_bounds__(NT) uniform_decode_kernel(const __grid_constan
         const float sc = __half2float(__ushort_as_half((unsigned short)(mw[u] >> 16)));
         const float2 m2 = make_float2(m, m), s2 = make_float2(sc, sc);
         uint16_t* dst = page + (j < nv ? vec_off(p, j) : 0);
+        uint4 oc[NC];
 #pragma unroll
         for (int ch = 0; ch < NC; ++ch) {
           uint32_t r[4];
@@ -364,7 +388,16 @@ __global__ void __launch_bounds__(NT) uniform_decode_kernel(const __grid_constan
             const float2 y = add2(mul2(make_float2(small_u2f(c0), small_u2f(c1)), s2), m2);
             r[k] = pack2<DT>(y.x, y.y);
           }
-          if (j < nv) st16(dst + 8 * (li + G * ch), make_uint4(r[0], r[1], r[2], r[3]));
+          if (ADJ && NC == 2) oc[ch] = make_uint4(r[0], r[1], r[2], r[3]);
+          else if (j < nv) st16(dst + 8 * (li + G * ch), make_uint4(r[0], r[1], r[2], r[3]));
+        }
+        if (ADJ && NC == 2 && j < nv) {
+          if (vec32) {
+            st32(dst + 16 * li, oc[0], oc[NC - 1]);
+          } else {
+            st16(dst + 16 * li, oc[0]);
+            st16(dst + 16 * li + 8, oc[NC - 1]);
+          }
         }
       }
     }
@@ -395,7 +428,9 @@ int launch_encode(const Params& p, void* stream) {
 // segments.)
 template <int DT, int D, int BITS>
 int launch_decode(const Params& p, void* stream) {
-  return launch_codec_kernel(uniform_decode_kernel<DT, D, BITS, kThreads>, p, stream, kDecodeCtas);
+  if (BITS != 3 && p.nv >= 256)
+    return launch_codec_kernel(uniform_decode_kernel<DT, D, BITS, kThreads, BITS != 3>, p, stream, kDecodeCtas);
+  return launch_codec_kernel(uniform_decode_kernel<DT, D, BITS, kThreads, false>, p, stream, kDecodeCtas);
 }
 
 template <int DT, int D>
