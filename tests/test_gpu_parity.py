@@ -136,6 +136,21 @@ def test_layer_pointers_16_and_32_byte_aligned(kc, vc, D, layout, offset):
     assert ulps == 0 and np.all(st == O.S_ENCODED)
 
 
+@pytest.mark.parametrize("kc,vc", [("fp8_dynamic", "uni8"), ("fp8_fixed", "uni4"), ("fp8_cast", "uni2"),
+                                   ("tq3", "uni3")])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("offset", [16, 32])
+def test_large_ragged_segments(kc, vc, D, dtype, offset):
+    """Segments of 272 vectors (17 heads x 16 tokens): the decoders' mapping
+    for segments of 256+ vectors, with a ragged last step, on layer pointers
+    16 bytes (16-byte stores) and 32 bytes (32-byte stores) past an aligned
+    allocation."""
+    case = custom_case(D=D, H=17, T=16, L=1, B=3, dtype=dtype, layout="separate", seed=D + offset)
+    st, ulps = run_parity(case, synth.Arm("big", kc, vc, (0, 1)), layer_offset=offset)
+    assert ulps == 0 and np.all(st == O.S_ENCODED)
+
+
 @pytest.mark.parametrize("kc,vc", [("int8", "int8"), ("int8", "fp8_dynamic"), ("tq4", "int8"),
                                    ("none", "int8")])
 @pytest.mark.parametrize("D", [32, 64, 128, 256])
