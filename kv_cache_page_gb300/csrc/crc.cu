@@ -133,9 +133,13 @@ __device__ __forceinline__ uint32_t load_tables(const CrcParams& p, NibbleTables
   const uint32_t* src = &p.tab.row[0][0];
   uint32_t* dst = &nt->row[0][0];
   for (uint32_t k = threadIdx.x; k < sizeof(NibbleTables) / 4; k += blockDim.x) dst[k] = src[k];
-  for (uint32_t w = threadIdx.x; w < kByteTabBytes / 4; w += blockDim.x) {
-    // word w: region w >> 14, entry (w >> 6) & 255, table 2 region + ((w >> 5) & 1), copy w & 31
-    byte_tab[w] = p.tab.byte[2u * (w >> 14) + ((w >> 5) & 1u)][(w >> 6) & 255u];
+  // one table word per warp and step (a broadcast read of the parameters),
+  // stored to its 32 copies: copy l of entry e of table k at word
+  // (k >> 1) 16384 + 64 e + 32 (k & 1) + l
+  const uint32_t lane = threadIdx.x & 31u;
+  for (uint32_t t = threadIdx.x >> 5; t < 4u * 256u; t += blockDim.x >> 5) {
+    const uint32_t k = t >> 8, e = t & 255u;
+    byte_tab[(k >> 1) * 16384u + 64u * e + 32u * (k & 1u) + lane] = p.tab.byte[k][e];
   }
   __syncthreads();
   return tab + (threadIdx.x & 31u) * 4u;
