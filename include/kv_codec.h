@@ -52,11 +52,11 @@
  * bytes through its device mapping, i.e. over the CPU-GPU link (NVLink-C2C on
  * GB300), so an encode writes its slots straight into host memory and a decode
  * reads them from there and scatters the result into the engine pages.  This
- * is the restore path of "Q4 KV cache for SGLang HiCache" (section "CPU to GPU:
- * restoration": compressed copy, dequantization and scatter all enqueued on
- * the transfer stream before the layer is marked ready) and the "upload encoded
- * bytes and GPU decode" restore of the OrbitKV docs, with the copy folded into
- * the kernel.  Stream order gives the ordering: the caller records an event on
+ * is the restore path of "Building a quantized HiCache for SGLang" (section
+ * "CPU to GPU: restoration": compressed copy, dequantization and scatter all
+ * enqueued on the transfer stream before the layer is marked ready) and the
+ * "upload encoded bytes and GPU decode" restore of the OrbitKV docs, with the
+ * copy folded into the kernel.  Stream order gives the ordering: the caller records an event on
  * the stream it passes and makes the consuming stream wait on it.  Pageable
  * host memory is refused (KV_ERR_NOT_ACCESSIBLE).  The engine pages
  * (layer_ptrs) are device memory.

@@ -33,6 +33,7 @@ namespace {
 
 constexpr int kCrcThreads = 1024;       // one CTA per SM (the tables take 128 KB)
 constexpr int kWarps = kCrcThreads / 32;
+static_assert(kCrcThreads % 32 == 0 && kCrcThreads >= 32, "the table fill and the slot loop work in whole warps");
 constexpr uint32_t kByteTabBytes = 4u * 256u * 32u * 4u;   // 128 KB
 constexpr uint32_t kTabAlign = 65536u;  // the byte tables start on a 64 KB boundary
 struct NibbleTables {

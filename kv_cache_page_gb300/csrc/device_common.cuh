@@ -311,6 +311,13 @@ __device__ __forceinline__ float vec_absmax(const uint4 (&w)[NC]) {
 // holding chunks li, li + G, ... (NC of them), so one warp load instruction
 // reads G contiguous chunks of each of the warp's 32/G vectors.  G is a
 // multiple of 4 for every head dim (the 3-bit packer combines 4 chunks).
+// Segments of at least this many vectors take the decoders' adjacent-chunk
+// mapping (lane li owns chunks 2li, 2li + 1: one 16-byte code load and one
+// 32-byte page store per vector); shorter segments keep the round-robin
+// chunks, which measured faster on 128-vector segments.  Shared by the FP8 and
+// the uniform decoders so that both switch at the same size.
+constexpr uint32_t kAdjacentChunkMinVectors = 256;
+
 template <int D>
 struct ChunkMap {
   static constexpr int E = D == 32 ? 8 : 16;   // elements per lane

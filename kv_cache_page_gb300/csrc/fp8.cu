@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kThreads) fp8_encode_kernel(const __grid_const
   }
 }
 
-// ADJ (segments of 256+ vectors, D >= 64): lane li owns the adjacent chunks
+// ADJ (segments of kAdjacentChunkMinVectors or more, D >= 64): lane li owns the adjacent chunks
 // 2 li, 2 li + 1 -- one 16-byte code load and, when every vector is 32-byte
 // aligned, one 32-byte store per vector.  Measured on a GB300: FP8 decode of
 // 512-vector segments 0.93-0.97 -> 0.97-0.98 of HBM, of 128-vector segments
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThreads) fp8_decode_kernel(const __grid_const
 
 template <int DT, int D, uint32_t CODEC>
 int decode(const Params& p, void* stream) {
-  if (p.nv >= 256)
+  if (p.nv >= kAdjacentChunkMinVectors)
     return launch_codec_kernel(fp8_decode_kernel<DT, D, CODEC, true>, p, stream, kDecodeCtas);
   return launch_codec_kernel(fp8_decode_kernel<DT, D, CODEC, false>, p, stream, kDecodeCtas);
 }

@@ -298,7 +298,7 @@ __device__ __forceinline__ float small_u2f(uint32_t c) {
   return __fsub_rn(__uint_as_float(0x4b000000u | c), 8388608.0f);
 }
 
-// ADJ (segments of 256+ vectors, D >= 64, 2/4/8-bit codes): lane li owns the
+// ADJ (segments of kAdjacentChunkMinVectors or more, D >= 64, 2/4/8-bit codes): lane li owns the
 // adjacent chunks 2 li, 2 li + 1 -- one code load and, when every vector is
 // 32-byte aligned, one 32-byte store per vector (as the FP8 decoder).
 template <int DT, int D, int BITS, int NT, bool ADJ>
@@ -428,7 +428,7 @@ int launch_encode(const Params& p, void* stream) {
 // segments.)
 template <int DT, int D, int BITS>
 int launch_decode(const Params& p, void* stream) {
-  if (BITS != 3 && p.nv >= 256)
+  if (BITS != 3 && p.nv >= kAdjacentChunkMinVectors)
     return launch_codec_kernel(uniform_decode_kernel<DT, D, BITS, kThreads, BITS != 3>, p, stream, kDecodeCtas);
   return launch_codec_kernel(uniform_decode_kernel<DT, D, BITS, kThreads, false>, p, stream, kDecodeCtas);
 }

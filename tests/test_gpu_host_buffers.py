@@ -2,7 +2,7 @@
 results in pinned host memory, which the kernels read and write through its
 device mapping (over NVLink-C2C on GB300).  Offload writes the slots straight
 into host memory; restore reads them from there and scatters into the engine
-pages ("Q4 KV cache for SGLang HiCache", section "CPU to GPU: restoration";
+pages ("Building a quantized HiCache for SGLang", section "CPU to GPU: restoration";
 OrbitKV docs, "upload encoded bytes and GPU decode").
 
 Same bar as the device-buffer parity tests: statuses, slots and results
