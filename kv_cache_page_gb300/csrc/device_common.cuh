@@ -104,35 +104,52 @@ __device__ __forceinline__ Seg plan_segment(const Params& p, uint32_t i, int dir
 struct SegCursor {
   uint32_t base;   // candidate index of lane 0
   uint32_t mask;   // candidates of this batch still to hand out
+  uint32_t stride; // distance between the owner's segments
 };
 
 __device__ __forceinline__ void cursor_init(SegCursor& c) {
   c.base = blockIdx.x;
   c.mask = 0;
+  c.stride = gridDim.x;
+}
+
+// One warp per segment: warp w of CTA b owns segments g, g + S, g + 2S, ...
+// with g = b * warps_per_cta + w and S the number of warps, made odd (one
+// warp idles when it is even) so that alternating K / V descriptors reach
+// every warp.  Such a cursor is private to its warp, which writes the
+// statuses of the segments it only reports.
+__device__ __forceinline__ void warp_cursor_init(SegCursor& c, uint32_t warps_per_cta) {
+  const uint32_t total = gridDim.x * warps_per_cta;
+  c.stride = (total > 1u && (total & 1u) == 0u) ? total - 1u : total;
+  c.base = blockIdx.x * warps_per_cta + (threadIdx.x >> 5);
+  if (c.base >= c.stride) c.base = 0xffffffffu;  // the idle warp of an even count
+  c.mask = 0;
 }
 
 // Next segment index to code (and its plan in s), or 0xffffffff when done.
-template <int DIR>
+// WARP: the cursor was set up by warp_cursor_init (every warp reports its own
+// candidates); otherwise warp 0 of the CTA reports.
+template <int DIR, bool WARP = false>
 __device__ __forceinline__ uint32_t cursor_next(const Params& p, SegCursor& c, Seg& s) {
   while (c.mask == 0u) {
     if (c.base >= p.n_segments) return 0xffffffffu;
-    const uint32_t i = c.base + (threadIdx.x & 31u) * gridDim.x;
+    const uint32_t i = c.base + (threadIdx.x & 31u) * c.stride;
     bool go = false;
     if (i < p.n_segments) {
       const Seg m = plan_segment(p, i, DIR);
       go = m.action == kProcess;
-      if (m.action == kReport && threadIdx.x < 32u) {
+      if (m.action == kReport && (WARP || threadIdx.x < 32u)) {
         if (DIR == kEncode) p.status[i] = m.status;
         else if (p.result) p.result[i] = m.status;
       }
     }
     c.mask = __ballot_sync(0xffffffffu, go);
-    if (c.mask == 0u) c.base += 32u * gridDim.x;
+    if (c.mask == 0u) c.base += 32u * c.stride;
   }
   const uint32_t k = (uint32_t)(__ffs(c.mask) - 1);
   c.mask &= c.mask - 1u;
-  const uint32_t idx = c.base + k * gridDim.x;
-  if (c.mask == 0u) c.base += 32u * gridDim.x;
+  const uint32_t idx = c.base + k * c.stride;
+  if (c.mask == 0u) c.base += 32u * c.stride;
   s = plan_segment(p, idx, DIR);
   return idx;
 }
@@ -427,9 +444,12 @@ __device__ __forceinline__ uint32_t load_3bit(const uint8_t* src, uint32_t c) {
 // write-heavy decodes stream best with few CTAs per SM, the encodes with more.
 template <typename K>
 inline int launch_codec_kernel(K kernel, const Params& p, void* stream, int max_per_sm,
-                               int threads = kThreads) {
+                               int threads = kThreads, bool warp_segments = false) {
   unsigned grid = 0;
-  const int rc = grid_for_threads(reinterpret_cast<const void*>(kernel), p.n_segments, max_per_sm,
+  // one warp per segment: enough CTAs for every segment to have its warp
+  const uint32_t units = warp_segments ? (p.n_segments + (uint32_t)threads / 32u - 1u) / ((uint32_t)threads / 32u)
+                                       : p.n_segments;
+  const int rc = grid_for_threads(reinterpret_cast<const void*>(kernel), units, max_per_sm,
                                   threads, &grid);
   if (rc != KV_OK || grid == 0) return rc;
   void* args[] = {const_cast<Params*>(&p)};

@@ -118,12 +118,11 @@ float unscaled_threshold(float b, float c) {
   return w;
 }
 
-// Cell table over c = rint(4 w) in [-kLutHalf, kLutHalf]: the code of every w
-// in the cell is lo + (w > thr), thr = the one threshold inside the cell or
-// +inf.  Returns false if a cell would hold two thresholds.
-bool build_index_table(const float* bnd, uint32_t nb, float c, float* thr, uint32_t* lo) {
-  float W[15];
-  for (uint32_t j = 0; j < nb; ++j) W[j] = unscaled_threshold(bnd[j], c);
+// Cell table over c = rint(4 w) in [-kLutHalf, kLutHalf] for the ascending
+// thresholds W[0 .. nb): the number of thresholds below every w of the cell
+// is lo + (w > thr), thr = the one threshold inside the cell or +inf.
+// Returns false if a cell would hold two thresholds.
+bool build_cells(const float* W, uint32_t nb, float* thr, uint32_t* lo) {
   for (int cell = -kvc::kLutHalf; cell <= kvc::kLutHalf; ++cell) {
     // floats w with rint(4 w) == cell (4 w is exact; ties go to the even cell)
     const float a = (float)((cell - 0.5) / 4.0), b = (float)((cell + 0.5) / 4.0);
@@ -140,6 +139,19 @@ bool build_index_table(const float* bnd, uint32_t nb, float c, float* thr, uint3
     lo[cell + kvc::kLutHalf] = below;
   }
   return true;
+}
+
+// The encoder's index tables.  Direct: code(w) = #{j : W_j < w} with
+// W_j = unscaled_threshold(bnd_j).  Mirrored, for lanes that hold v = -w:
+// #{j : W_j >= -v} = #{j : v > -succ(W_j)} (succ = next float up), so the
+// mirrored table over the thresholds -succ(W_j) gives (2^bits - 1) - code(w),
+// the complement of the code's bits.
+bool build_index_table(const float* bnd, uint32_t nb, float c, float* thr, uint32_t* lo,
+                       float* mthr, uint32_t* mlo) {
+  float W[15], M[15];
+  for (uint32_t j = 0; j < nb; ++j) W[j] = unscaled_threshold(bnd[j], c);
+  for (uint32_t j = 0; j < nb; ++j) M[j] = -std::nextafterf(W[nb - 1 - j], INFINITY);
+  return build_cells(W, nb, thr, lo) && build_cells(M, nb, mthr, mlo);
 }
 
 // --- CRC-32 (zlib's: reflected polynomial 0xEDB88320) register maps.  A
@@ -452,6 +464,7 @@ int kv_codec_create(const kv_codec_geometry* g, kv_codec_t* out) {
   p.protect_last = g->protect_last;
   p.reject_abs = reject;
   p.wht_scale = (float)(1.0 / std::sqrt((double)g->head_dim));
+  p.neg_zero = -0.0f;
   const uint64_t raw = nv * g->head_dim * 2;
   // INT8_HEAD token record: H int8 head vectors + H BF16 scales, 128-byte multiple
   p.rec_used = p.H * (p.D + 2);
@@ -484,7 +497,8 @@ int kv_codec_create(const kv_codec_geometry* g, kv_codec_t* out) {
   if (is_tq(g->k_codec)) {
     const uint32_t bits = codec_bits(g->k_codec);
     make_codebook(bits, p.D, p.cent, p.bnd);
-    if (!build_index_table(p.bnd, (1u << bits) - 1u, p.wht_scale, p.lut_thr, p.lut_lo)) {
+    if (!build_index_table(p.bnd, (1u << bits) - 1u, p.wht_scale, p.lut_thr, p.lut_lo, p.lut_mthr,
+                           p.lut_mlo)) {
       delete h;
       return KV_ERR_INVALID_ARG;
     }

@@ -44,6 +44,7 @@ struct Params {
   uint8_t vec32;                        // per call: every vector starts on a 32-byte boundary
   float reject_abs;                     // admission bound
   float wht_scale;                      // fl32(1/sqrt(D))
+  float neg_zero;                       // -0.0f (an FMA addend the compiler cannot fold)
   uint32_t sign_words[8];               // TurboQuant sign bits, bit i = negate element i
   float cent[16];                       // TurboQuant centroids (K codec)
   float bnd[16];                        // TurboQuant boundaries (K codec), bnd[15] unused
@@ -52,6 +53,10 @@ struct Params {
   // W_j = max{w : RN(w * wht_scale) <= bnd[j]}, so that no scale multiply is needed.
   float lut_thr[kLutCells];
   uint32_t lut_lo[kLutCells];
+  // The same for lanes holding negated outputs v = -w: lut_mlo[c] + (v > lut_mthr[c])
+  // = (2^bits - 1) - code(w), c = rint(4 v).
+  float lut_mthr[kLutCells];
+  uint32_t lut_mlo[kLutCells];
   float fixed_scale[kMaxLayers][2];     // FP8_FIXED scale per (layer, role)
   const void* layer_ptr[2 * kMaxLayers];
   // ---- per call ----

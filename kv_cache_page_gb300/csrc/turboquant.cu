@@ -433,36 +433,8 @@ __device__ __forceinline__ uint32_t tq_pack2(uint32_t a, uint32_t b, uint32_t c)
   return d;
 }
 
-// Codes of 32 consecutive elements held in pairs a[P0 .. P0 + 15], element 0
-// in the lowest bits of w[0]; BITS * 32 / 32 words.
-template <int BITS, int P0, int P>
-__device__ __forceinline__ void tq_codes32(const float2 (&a)[P], uint32_t lut_base, uint32_t (&acc)[4]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t c[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float x = (e & 1) ? a[P0 + 4 * q + e / 2].y : a[P0 + 4 * q + e / 2].x;
-      const uint32_t cell = __float_as_uint(__fmaf_rn(x, 4.0f, kCellMagic));
-      uint2 ent;
-      asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(ent.x), "=r"(ent.y) : "r"(cell * 128u + lut_base));
-      c[e] = ent.y + (x > __uint_as_float(ent.x) ? 1u : 0u);
-    }
-    if (BITS == 4 || BITS == 2) {  // element 0 in the lowest bits, two codes per pack
-      uint32_t v = tq_pack2<BITS>(c[7], c[6], 0u);
-      v = tq_pack2<BITS>(c[5], c[4], v);
-      v = tq_pack2<BITS>(c[3], c[2], v);
-      acc[q] = tq_pack2<BITS>(c[1], c[0], v);
-    } else {  // element 0 in the lowest bits, combined as a tree (depth 3, not 8)
-      const uint32_t p0 = c[0] + (c[1] << BITS), p1 = c[2] + (c[3] << BITS);
-      const uint32_t p2 = c[4] + (c[5] << BITS), p3 = c[6] + (c[7] << BITS);
-      acc[q] = (p0 + (p1 << (2 * BITS))) + ((p2 + (p3 << (2 * BITS))) << (4 * BITS));
-    }
-  }
-}
-
-// Store the codes of 32 consecutive elements (acc as from tq_codes32) at
-// byte `dst` (the element index of the first times BITS / 8).
+// Store the codes of 32 consecutive elements (4 words of 8 codes, element 0
+// lowest) at byte `dst` (the element index of the first times BITS / 8).
 template <int BITS>
 __device__ __forceinline__ void tq_store32(uint8_t* dst, const uint32_t (&acc)[4]) {
   if (BITS == 4) {
@@ -476,87 +448,204 @@ __device__ __forceinline__ void tq_store32(uint8_t* dst, const uint32_t (&acc)[4
   }
 }
 
+// Encoder for D >= 64.  Lane li of a vector's G = D/64 lanes owns elements
+// 64 li .. 64 li + 63 ("in-lane index" k = 0..63), held as 32 FP32 pairs
+// a[P] = (element k, element k + 16) with k = (P & 15) | ((P & 16) << 1):
+// the in-lane index bits 0..3 are the pair bits 0..3, bit 4 is the pair's
+// component and bit 5 is pair bit 4.  So the pairwise sum of squares and the
+// transform stages of strides 1, 2, 4, 8 and 32 are packed FP32x2 operations
+// between pairs; only stride 16 works inside the pairs.  The next vector's
+// 128 bytes are loaded into registers while the current one is coded.
+//
+// The odd lane's inputs with k >= 32 are negated through its sign masks, so
+// after the in-lane stages its pair P holds what the even lane's pair P ^ 16
+// holds (see tq64_run_negated): both lanes keep pairs 0..15 and exchange
+// 16..31 for the stride-64 stage.  Negated output runs are coded through the
+// mirrored index table, whose codes are the bitwise complement of the
+// direct ones; the packed words are complemented back.
+// Pairwise sum of squares over pairs [P0, P0 + N), componentwise.  The
+// squares are FMAs with the -0 addend nz2 (see the normalisation in the
+// encoder): a packed product feeding a packed addition would be fused with
+// it, which rounds differently when a square falls below the normal range.
+template <int P0, int N>
+struct PairTree {
+  static __device__ __forceinline__ float2 run(const float2 (&a)[32], float2 nz2) {
+    if constexpr (N == 1) {
+      return fma2(a[P0], a[P0], nz2);
+    } else {
+      return add2(PairTree<P0, N / 2>::run(a, nz2), PairTree<P0 + N / 2, N / 2>::run(a, nz2));
+    }
+  }
+};
+
+// Codes of the 32 elements of run R (pairs 16 R .. 16 R + 15; run element o
+// in pair 16 R + (o & 15), component o >> 4), 8 per word, element 0 lowest;
+// `lut` is the direct or the mirrored table of this lane and run, `cm` the
+// complement that turns the table's codes into the element's.
+template <int BITS, int R>
+__device__ __forceinline__ void tq_run_codes(const float2 (&a)[32], uint32_t lut, uint32_t cm,
+                                             uint32_t (&acc)[4]) {
+  const float2 k4 = make_float2(4.0f, 4.0f), mg = make_float2(kCellMagic, kCellMagic);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {  // pairs 16 R + 8 half .. + 7: words half, half + 2
+    uint32_t cx[8], cy[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float2 v = a[16 * R + 8 * half + e];
+      const float2 cell = fma2(v, k4, mg);
+      uint2 tx, ty;
+      asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(tx.x), "=r"(tx.y) : "r"(__float_as_uint(cell.x) * 128u + lut));
+      asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(ty.x), "=r"(ty.y) : "r"(__float_as_uint(cell.y) * 128u + lut));
+      cx[e] = tx.y + (v.x > __uint_as_float(tx.x) ? 1u : 0u);
+      cy[e] = ty.y + (v.y > __uint_as_float(ty.x) ? 1u : 0u);
+    }
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const uint32_t* c = s ? cy : cx;
+      uint32_t v;
+      if (BITS == 4 || BITS == 2) {
+        v = tq_pack2<BITS>(c[7], c[6], 0u);
+        v = tq_pack2<BITS>(c[5], c[4], v);
+        v = tq_pack2<BITS>(c[3], c[2], v);
+        v = tq_pack2<BITS>(c[1], c[0], v);
+      } else {
+        const uint32_t p0 = c[0] + (c[1] << BITS), p1 = c[2] + (c[3] << BITS);
+        const uint32_t p2 = c[4] + (c[5] << BITS), p3 = c[6] + (c[7] << BITS);
+        v = (p0 + (p1 << (2 * BITS))) + ((p2 + (p3 << (2 * BITS))) << (4 * BITS));
+      }
+      acc[half + 2 * s] = v ^ cm;
+    }
+  }
+}
+
+// 128 bytes of vector j's lane part: 32-byte loads when every vector is
+// 32-byte aligned, else 16-byte loads.
+__device__ __forceinline__ void tq64_load(const uint16_t* src, bool v32, uint4 (&w)[8]) {
+  if (v32) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ld_nc32(src + 16 * k, w[2 * k], w[2 * k + 1]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = ld_nc16(src + 8 * k);
+  }
+}
+
 template <int DT, int D, int BITS>
-__global__ void __launch_bounds__(kTq64Threads, 4) tq_encode64_kernel(const __grid_constant__ Params p) {
-  constexpr int E = 64, NCH = E / 8, G = D / E, VPW = 32 / G, W = kTq64Threads / 32;
+__global__ void __launch_bounds__(kTq64Threads, 3) tq_encode64_kernel(const __grid_constant__ Params p) {
+  constexpr int E = 64, G = D / E, VPW = 32 / G, W = kTq64Threads / 32;
   constexpr int CB = D * BITS / 8;
-  constexpr uint32_t CSTEP = W * VPW;
+  constexpr int NT = G >= 2 ? 2 : 1;           // index tables: direct (+ mirrored)
   static_assert(G >= 1 && G <= 4, "head dim 64 .. 256");
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
-  __shared__ uint2 s_lut[kLutCells * 16];
-  __shared__ uint4 s_sign[4][NCH + 1];
-  // next vector of each lane: 128 bytes, chunk k at slot k ^ (lane & 7) so
-  // that the 8 lanes of a 128-bit shared access hit 8 different bank groups
-  __shared__ uint4 s_stage[W][32][NCH];
-  __shared__ uint32_t s_flag[2];
-  for (int k = threadIdx.x; k < kLutCells * 16; k += blockDim.x)
-    s_lut[k] = make_uint2(__float_as_uint(p.lut_thr[k >> 4]), p.lut_lo[k >> 4]);
-  for (int t = threadIdx.x; t < G * NCH; t += blockDim.x) {
-    const uint32_t l = (uint32_t)t / NCH, c = (uint32_t)t % NCH;
-    const uint32_t e0 = l * E + 8u * c;
-    const uint32_t bits = p.sign_words[e0 >> 5];
-    const int k = (int)((e0 & 31u) >> 1);
-    uint4 m = make_uint4(sign_mask_word(bits, k), sign_mask_word(bits, k + 1), sign_mask_word(bits, k + 2),
-                         sign_mask_word(bits, k + 3));
-    if (G >= 2 && (l & 1u) && c >= NCH / 2) m = xor4(m, 0x80008000u);  // the odd lane's upper half
-    s_sign[l][c] = m;
+  __shared__ uint2 s_lut[NT][kLutCells * 16];
+  // sign masks of source word t (elements 2t, 2t + 1) of lane position l:
+  // BF16: [l][0][t] bit 31 = sign of element 2t, [l][1][t] bit 31 = sign of
+  // element 2t + 1; FP16: [l][0][t] bits 15 and 31.
+  __shared__ uint32_t s_mask[G][2][32];
+  for (int k = threadIdx.x; k < NT * kLutCells * 16; k += blockDim.x) {
+    const int t = k / (kLutCells * 16), c = (k >> 4) % kLutCells;
+    s_lut[t][k % (kLutCells * 16)] =
+        t ? make_uint2(__float_as_uint(p.lut_mthr[c]), p.lut_mlo[c]) : make_uint2(__float_as_uint(p.lut_thr[c]), p.lut_lo[c]);
   }
-  if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
+  for (int k = threadIdx.x; k < G * 32; k += blockDim.x) {
+    const uint32_t l = (uint32_t)k / 32, t = (uint32_t)k % 32;
+    const uint32_t e0 = l * E + 2u * t;
+    uint32_t s0 = (p.sign_words[e0 >> 5] >> (e0 & 31u)) & 1u;
+    uint32_t s1 = (p.sign_words[e0 >> 5] >> ((e0 + 1u) & 31u)) & 1u;
+    if (G >= 2 && (l & 1u) && t >= 16u) {  // the odd lane's inputs 32..63
+      s0 ^= 1u;
+      s1 ^= 1u;
+    }
+    if (DT == 1) {
+      s_mask[l][0][t] = s0 << 31;
+      s_mask[l][1][t] = s1 << 31;
+    } else {
+      s_mask[l][0][t] = (s0 << 15) | (s1 << 31);
+      s_mask[l][1][t] = 0u;
+    }
+  }
   __syncthreads();
-  const uint32_t lut_base = (uint32_t)__cvta_generic_to_shared(s_lut) + (lane & 15u) * 8u +
-                            (uint32_t)(kLutHalf * 128) - kCellMagicBits * 128u;
-  const uint32_t stage = (uint32_t)__cvta_generic_to_shared(&s_stage[warp][lane][0]);
-  const uint32_t swz = lane & 7u;
-  const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&s_sign[li][0]);
+  const uint32_t lane_off = (lane & 15u) * 8u + (uint32_t)(kLutHalf * 128) - kCellMagicBits * 128u;
+  const uint32_t lut_d = (uint32_t)__cvta_generic_to_shared(&s_lut[0][0]) + lane_off;
+  const uint32_t lut_m = (uint32_t)__cvta_generic_to_shared(&s_lut[NT - 1][0]) + lane_off;
+  const bool neg_a = tq64_run_negated<G>(li, 0), neg_b = tq64_run_negated<G>(li, 1);
+  const uint32_t lut_a = neg_a ? lut_m : lut_d, lut_b = neg_b ? lut_m : lut_d;
+  constexpr uint32_t kAll = BITS == 4 ? 0xffffffffu : (1u << (8 * BITS)) - 1u;
+  const uint32_t cm_a = neg_a ? kAll : 0u, cm_b = neg_b ? kAll : 0u;
+  const uint32_t mask_addr = (uint32_t)__cvta_generic_to_shared(&s_mask[li][0][0]);
   const uint32_t run_a = tq64_run_start<G>(li, 0), run_b = tq64_run_start<G>(li, 1);
   const uint32_t nv = p.nv;
-  const uint32_t jw = warp * VPW + grp;
+  const bool v32 = p.vec32 != 0;
   const float admit_ss = p.reject_abs * p.reject_abs * 0.99609375f;
 
-  auto prefetch = [&](const Seg& s, uint32_t j) {
-    if (j < nv) {
-      const uint16_t* src = s.page + vec_off(p, j) + E * li;
-#pragma unroll
-      for (int k = 0; k < NCH; ++k) cp_async16(stage + 16u * ((uint32_t)k ^ swz), src + 8 * k);
-    }
-    cp_async_commit();
+  // lanes past the end of a segment load (and code, without storing) its
+  // last vector, so that every lane works on admitted-or-flagged page data
+  auto src_of = [&](const uint16_t* page, uint32_t j) {
+    return page + vec_off(p, j < nv ? j : nv - 1u) + E * li;
   };
 
+  // each warp codes whole segments: no CTA-wide barrier, so the warps of an
+  // SM drift apart and their table lookups overlap other warps' arithmetic
   SegCursor cursor;
-  cursor_init(cursor);
+  warp_cursor_init(cursor, W);
   Seg cur;
-  uint32_t ci = cursor_next<kEncode>(p, cursor, cur);
-  if (ci != 0xffffffffu) prefetch(cur, jw);
-  int it = 0;
+  uint32_t ci = cursor_next<kEncode, true>(p, cursor, cur);
+  uint4 pw[8];
+  if (ci != 0xffffffffu) tq64_load(src_of(cur.page, grp), v32, pw);
   while (ci != 0xffffffffu) {
-    Seg nxt;
-    const uint32_t ni = cursor_next<kEncode>(p, cursor, nxt);
-    if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
+    const uint16_t* npage;  // the next segment's page: the rest of its plan is redone below
+    uint32_t ni;
+    {
+      Seg nxt;
+      ni = cursor_next<kEncode, true>(p, cursor, nxt);
+      npage = nxt.page;
+    }
     uint8_t* codes = cur.slot;
     uint8_t* meta = cur.slot + (uint64_t)nv * CB;
     uint32_t flags = 0;
-    if (warp * VPW >= nv && ni != 0xffffffffu) prefetch(nxt, jw);  // no work in this segment
-    for (uint32_t j0 = warp * VPW; j0 < nv; j0 += CSTEP) {
+    for (uint32_t j0 = 0; j0 < nv; j0 += VPW) {
       const uint32_t j = j0 + grp;
-      const bool in = j < nv;
-      cp_async_wait_all();
-      uint4 w[NCH];
-#pragma unroll
-      for (int k = 0; k < NCH; ++k)
-        w[k] = in ? lds16(stage + 16u * ((uint32_t)k ^ swz)) : make_uint4(0, 0, 0, 0);
-      // the staged data is in registers now: refill the stage with the next vector
-      if (j0 + CSTEP < nv) prefetch(cur, j + CSTEP);
-      else if (ni != 0xffffffffu) prefetch(nxt, jw);
+      // source words -> pairs, sign flips on the 16-bit values (exact)
       float2 a[32];
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        const uint4 m = lds16(sign_addr + 16u * c);
-        const uint32_t ww[4] = {w[c].x ^ m.x, w[c].y ^ m.y, w[c].z ^ m.z, w[c].w ^ m.w};
+      for (int c = 0; c < 8; ++c) {
+        const uint4 m0 = lds16(mask_addr + 16u * c);
+        uint4 m1 = make_uint4(0, 0, 0, 0);
+        if (DT == 1) m1 = lds16(mask_addr + 128u + 16u * c);
+        const uint32_t ww[4] = {pw[c].x, pw[c].y, pw[c].z, pw[c].w};
+        const uint32_t k0[4] = {m0.x, m0.y, m0.z, m0.w}, k1[4] = {m1.x, m1.y, m1.z, m1.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) a[4 * c + k] = make_float2(lo_f32<DT>(ww[k]), hi_f32<DT>(ww[k]));
+        for (int q = 0; q < 4; ++q) {
+          const int t = 4 * c + q;                    // elements 2t, 2t + 1
+          const int P = ((2 * t) & 15) | ((t >> 4) << 4), comp = (t >> 3) & 1;
+          float lo, hi;
+          if (DT == 1) {
+            lo = __uint_as_float(ww[q] * 65536u + k0[q]);   // + 2^31 flips the sign bit
+            hi = __uint_as_float((ww[q] & 0xffff0000u) ^ k1[q]);
+          } else {
+            const uint32_t v = ww[q] ^ k0[q];
+            lo = lo_f32<0>(v);
+            hi = hi_f32<0>(v);
+          }
+          if (comp) {
+            a[P].y = lo;
+            a[P + 1].y = hi;
+          } else {
+            a[P].x = lo;
+            a[P + 1].x = hi;
+          }
+        }
       }
-      const float ss = vector_sumsq<G>(a);
+      // the page data is in registers now: load the next vector
+      if (j0 + VPW < nv) tq64_load(src_of(cur.page, j + VPW), v32, pw);
+      else if (ni != 0xffffffffu) tq64_load(src_of(npage, grp), v32, pw);
+      // pairwise sum of squares: in-lane index bits 0..3, then 4, then 5
+      const float2 nz2 = make_float2(p.neg_zero, p.neg_zero);
+      const float2 ta = PairTree<0, 16>::run(a, nz2), tb = PairTree<16, 16>::run(a, nz2);
+      float ss = __fadd_rn(__fadd_rn(ta.x, ta.y), __fadd_rn(tb.x, tb.y));
+#pragma unroll
+      for (int o = 1; o < G; o <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
       // Admission.  ss is within 2^-20 (relative) of the exact sum of
       // squares, so ss <= 0.996 reject^2 shows every |x| <= reject; a
       // nonfinite element makes ss NaN or inf.  Otherwise the warp takes the
@@ -584,10 +673,73 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_encode64_kernel(const __gr
       const float n = __fsqrt_rn(ss);
       float r = __frcp_rn(n);
       if (!isfinite(r)) r = 0.0f;
+      // u = x r, rounded on its own.  A packed product whose result feeds
+      // packed additions is fused with them into packed FMAs by the compiler
+      // (measured on sm_103a, with contraction disabled and with an explicit
+      // .rn modifier alike), which changes the roundings of the first
+      // butterfly stage.  An FMA with a -0 addend is the same single
+      // rounding of x r, zero signs included, and cannot be fused further as
+      // long as the compiler cannot see that the addend is -0: it comes from
+      // the launch parameters.
       const float2 r2 = make_float2(r, r);
 #pragma unroll
-      for (int m = 0; m < 32; ++m) a[m] = mul2(a[m], r2);
-      butterflies64<G, true>(a, li);
+      for (int m = 0; m < 32; ++m) a[m] = fma2(a[m], r2, nz2);
+      // Walsh-Hadamard butterflies, ascending stride
+#pragma unroll
+      for (int h = 1; h < 16; h <<= 1) {  // strides 1, 2, 4, 8: pair P with pair P + h
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+          if (m & h) continue;
+          const float2 u = a[m], v = a[m + h];
+          a[m] = add2(u, v);
+          a[m + h] = sub2(u, v);
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < 32; ++m) {  // stride 16: inside each pair
+        const float u = a[m].x, v = a[m].y;
+        a[m] = make_float2(__fadd_rn(u, v), __fsub_rn(u, v));
+      }
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {  // stride 32: pair P with pair P + 16
+        const float2 u = a[m], v = a[m + 16];
+        a[m] = add2(u, v);
+        a[m + 16] = sub2(u, v);
+      }
+      if constexpr (G == 2) {  // stride 64: lanes li, li ^ 1 (split, see above)
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float2 rv = make_float2(__shfl_xor_sync(0xffffffffu, a[16 + m].x, 1),
+                                        __shfl_xor_sync(0xffffffffu, a[16 + m].y, 1));
+          const float2 k = a[m];
+          a[m] = add2(k, rv);
+          a[16 + m] = sub2(k, rv);
+        }
+      }
+      if constexpr (G == 4) {
+        // stride 64 as above, except that lanes 2 and 3 put the differences
+        // in pairs 0..15 and the sums in 16..31 (rv * t + k with t = -1 is the
+        // single rounding of k - rv); stride 128 (lanes li, li ^ 2) then pairs
+        // 0..15 of the lower lane with 16..31 of the upper one, split alike.
+        const float t = (li & 2u) ? -1.0f : 1.0f;
+        const float2 t2 = make_float2(t, t), nt2 = make_float2(-t, -t);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float2 rv = make_float2(__shfl_xor_sync(0xffffffffu, a[16 + m].x, 1),
+                                        __shfl_xor_sync(0xffffffffu, a[16 + m].y, 1));
+          const float2 k = a[m];
+          a[m] = fma2(rv, t2, k);
+          a[16 + m] = fma2(rv, nt2, k);
+        }
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float2 rv = make_float2(__shfl_xor_sync(0xffffffffu, a[16 + m].x, 2),
+                                        __shfl_xor_sync(0xffffffffu, a[16 + m].y, 2));
+          const float2 k = a[m];
+          a[m] = add2(k, rv);
+          a[16 + m] = sub2(k, rv);
+        }
+      }
       if (n < 0x1p-62f) {
         // Norms this small may come from squares that underflowed, so |w|
         // can exceed sqrt(D); clamp into the table (beyond +-17 every code
@@ -597,9 +749,9 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_encode64_kernel(const __gr
           a[m] = make_float2(fminf(fmaxf(a[m].x, -17.0f), 17.0f), fminf(fmaxf(a[m].y, -17.0f), 17.0f));
       }
       uint32_t acc_a[4], acc_b[4];
-      tq_codes32<BITS, 0>(a, lut_base, acc_a);
-      tq_codes32<BITS, 16>(a, lut_base, acc_b);
-      if (in) {
+      tq_run_codes<BITS, 0>(a, lut_a, cm_a, acc_a);
+      tq_run_codes<BITS, 1>(a, lut_b, cm_b, acc_b);
+      if (j < nv) {
         uint8_t* vc = codes + (uint64_t)j * CB;
         tq_store32<BITS>(vc + run_a * BITS / 8, acc_a);
         tq_store32<BITS>(vc + run_b * BITS / 8, acc_b);
@@ -608,15 +760,10 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_encode64_kernel(const __gr
       }
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
-    if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
-    zero_padding(cur.slot, (uint64_t)nv * (CB + 2), p.seg_bytes[cur.role]);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const uint32_t f = s_flag[it & 1];
-      p.status[ci] = (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
-    }
-    ++it;
-    cur = nxt;
+    for (uint64_t b = (uint64_t)nv * (CB + 2) + lane; b < p.seg_bytes[cur.role]; b += 32) cur.slot[b] = 0;
+    if (lane == 0)
+      p.status[ci] = (flags & 1u) ? KV_SEG_RAW_NONFINITE : (flags & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+    if (ni != 0xffffffffu) cur = plan_segment(p, ni, kEncode);
     ci = ni;
   }
 }
@@ -891,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
 template <int DT, int D, int BITS>
 int encode(const Params& p, void* stream) {
   if constexpr (D >= 64)
-    return launch_codec_kernel(tq_encode64_kernel<DT, D, BITS>, p, stream, 8, kTq64Threads);
+    return launch_codec_kernel(tq_encode64_kernel<DT, D, BITS>, p, stream, 8, kTq64Threads, true);
   else
     return launch_codec_kernel(tq_encode_kernel<DT, D, BITS>, p, stream, 8);
 }
