@@ -64,39 +64,8 @@ __device__ __forceinline__ float vector_sumsq(const float2 (&a)[P]) {
   return c;
 }
 
-// Unscaled Walsh-Hadamard butterflies over the vector, strides 1 .. D/2.
-template <int G>
-__device__ __forceinline__ void butterflies(float2 (&a)[16], uint32_t li) {
-#pragma unroll
-  for (int m = 0; m < 16; ++m) {  // stride 1: inside each pair
-    const float u = a[m].x, v = a[m].y;
-    a[m] = make_float2(__fadd_rn(u, v), __fsub_rn(u, v));
-  }
-#pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {  // strides 2, 4, 8, 16: pair m with pair m + h
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      if (m & h) continue;
-      const float2 u = a[m], v = a[m + h];
-      a[m] = add2(u, v);
-      a[m + h] = sub2(u, v);
-    }
-  }
-#pragma unroll
-  for (int o = 1; o < G; o <<= 1) {  // strides 32 o: across lanes
-    const float sg = (li & (uint32_t)o) ? -1.0f : 1.0f;
-    const float2 sg2 = make_float2(sg, sg);
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float2 partner = make_float2(__shfl_xor_sync(0xffffffffu, a[m].x, o),
-                                         __shfl_xor_sync(0xffffffffu, a[m].y, o));
-      a[m] = fma2(a[m], sg2, partner);  // low lane: mine + partner; high lane: partner - mine
-    }
-  }
-}
-
-// Walsh-Hadamard butterflies of the decoder.  Strides 1 .. 16 as in
-// butterflies<G>; a cross-lane stage (lanes l and l ^ o, stride 32 o) is split
+// Walsh-Hadamard butterflies of the 32-element decoder.  Strides 1 .. 16
+// inside the lane (stride 1 inside each pair, 2 .. 16 between pairs); a cross-lane stage (lanes l and l ^ o, stride 32 o) is split
 // between the two lanes instead of doubled: the lower lane computes the sums
 // and differences of slots 0..15, the upper lane those of slots 16..31, so
 // each sends only the half the other needs (16 shuffles per stage, not 32).
@@ -145,23 +114,6 @@ __device__ __forceinline__ uint32_t split_group_start(uint32_t li, int c) {
   return (uint32_t)((8 * c) & 15) | (li << 4) | ((uint32_t)(c >> 1) << (4 + J));
 }
 
-// Shared tables of the TurboQuant kernels, built once per CTA: the encoder's
-// index cells, 16 copies (lanes of a half warp never share a bank), and the
-// sign masks per lane of a vector (rows padded against bank conflicts).
-struct TqShared {
-  uint2 lut[kLutCells * 16];
-  uint4 sign[8][5];
-};
-
-__device__ __forceinline__ void tq_sign_init(const Params& p, uint4 (&sign)[8][5]) {
-  for (int t = threadIdx.x; t < 8 * 4; t += blockDim.x) {
-    const uint32_t bits = p.sign_words[t >> 2];
-    const int k = 4 * (t & 3);
-    sign[t >> 2][t & 3] = make_uint4(sign_mask_word(bits, k), sign_mask_word(bits, k + 1),
-                                     sign_mask_word(bits, k + 2), sign_mask_word(bits, k + 3));
-  }
-}
-
 // Sign masks of the decoder's output layout: row li, group c covers the 8
 // elements from split_group_start<G>(li, c).
 template <int G>
@@ -175,146 +127,6 @@ __device__ __forceinline__ void tq_sign_init_split(const Params& p, uint4 (&sign
   }
 }
 
-__device__ __forceinline__ void tq_shared_init(const Params& p, TqShared& sh, bool lut) {
-  if (lut)
-    for (int k = threadIdx.x; k < kLutCells * 16; k += blockDim.x)
-      sh.lut[k] = make_uint2(__float_as_uint(p.lut_thr[k >> 4]), p.lut_lo[k >> 4]);
-  tq_sign_init(p, sh.sign);
-}
-
-// A CTA codes one segment at a time; warp w takes vectors w*VPW + (0..VPW-1),
-// then + W*VPW, ...  Each warp keeps its next vector in flight while it
-// computes the current one (cp.async into a per-lane stage for encode,
-// register loads for decode), across segment boundaries too.
-template <int DT, int D, int BITS>
-__global__ void __launch_bounds__(kThreads, 3) tq_encode_kernel(const __grid_constant__ Params p) {
-  constexpr int G = D / kTqE, VPW = 32 / G, W = kThreads / 32;
-  constexpr int CB = D * BITS / 8;
-  constexpr uint32_t CSTEP = W * VPW;
-  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-  const uint32_t grp = lane / G, li = lane % G;
-  __shared__ TqShared sh;
-  // next vector of each lane: 64 bytes, chunk k at slot k ^ ((lane >> 1) & 3)
-  // so that the 8 lanes of a 128-bit shared access hit 8 different bank groups
-  __shared__ uint4 s_stage[W][32][4];
-  __shared__ uint32_t s_flag[2];
-  tq_shared_init(p, sh, true);
-  if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
-  __syncthreads();
-  const uint32_t lut_base = (uint32_t)__cvta_generic_to_shared(sh.lut) + (lane & 15u) * 8u +
-                            (uint32_t)(kLutHalf * 128) - kCellMagicBits * 128u;
-  const uint32_t stage = (uint32_t)__cvta_generic_to_shared(&s_stage[warp][lane][0]);
-  const uint32_t swz = (lane >> 1) & 3u;
-  const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&sh.sign[li][0]);
-  const uint32_t nv = p.nv;
-  const uint32_t jw = warp * VPW + grp;  // this lane's first vector in a segment
-
-  auto prefetch = [&](const Seg& s, uint32_t j) {
-    if (j < nv) {
-      const uint16_t* src = s.page + vec_off(p, j) + kTqE * li;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) cp_async16(stage + 16u * ((uint32_t)k ^ swz), src + 8 * k);
-    }
-    cp_async_commit();
-  };
-
-  SegCursor cursor;
-  cursor_init(cursor);
-  Seg cur;
-  uint32_t ci = cursor_next<kEncode>(p, cursor, cur);
-  if (ci != 0xffffffffu) prefetch(cur, jw);
-  int it = 0;
-  while (ci != 0xffffffffu) {
-    Seg nxt;
-    const uint32_t ni = cursor_next<kEncode>(p, cursor, nxt);
-    if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
-    uint8_t* codes = cur.slot;
-    uint8_t* meta = cur.slot + (uint64_t)nv * CB;
-    uint32_t flags = 0;
-    if (warp * VPW >= nv && ni != 0xffffffffu) prefetch(nxt, jw);  // no work in this segment
-    for (uint32_t j0 = warp * VPW; j0 < nv; j0 += CSTEP) {
-      const uint32_t j = j0 + grp;
-      const bool in = j < nv;
-      cp_async_wait_all();
-      uint4 w[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) w[k] = in ? lds16(stage + 16u * ((uint32_t)k ^ swz)) : make_uint4(0, 0, 0, 0);
-      const float amax = vec_absmax<DT, G, 4>(w);
-      // the staged data is in registers now: refill the stage with the next vector
-      if (j0 + CSTEP < nv) prefetch(cur, j + CSTEP);
-      else if (ni != 0xffffffffu) prefetch(nxt, jw);
-      const uint32_t vflags = admission_abs(amax, p.reject_abs);
-      flags |= vflags;
-      if (vflags) {  // keep NaN / inf out of the arithmetic (the segment stays raw)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) w[k] = make_uint4(0, 0, 0, 0);
-      }
-      float2 a[16];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 m = lds16(sign_addr + 16u * c);
-        const uint32_t ww[4] = {w[c].x ^ m.x, w[c].y ^ m.y, w[c].z ^ m.z, w[c].w ^ m.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) a[4 * c + k] = make_float2(lo_f32<DT>(ww[k]), hi_f32<DT>(ww[k]));
-      }
-      const float n = __fsqrt_rn(vector_sumsq<G>(a));
-      float r = __frcp_rn(n);
-      if (!isfinite(r)) r = 0.0f;
-      const float2 r2 = make_float2(r, r);
-#pragma unroll
-      for (int m = 0; m < 16; ++m) a[m] = mul2(a[m], r2);
-      butterflies<G>(a, li);
-      if (n < 0x1p-62f) {
-        // Norms this small may come from squares that underflowed, so |w|
-        // can exceed sqrt(D); clamp into the table (beyond +-17 every code
-        // is already the first or the last).
-#pragma unroll
-        for (int m = 0; m < 16; ++m)
-          a[m] = make_float2(fminf(fmaxf(a[m].x, -17.0f), 17.0f), fminf(fmaxf(a[m].y, -17.0f), 17.0f));
-      }
-      // codes, element 0 in the lowest bits: accumulate from the last element
-      uint32_t acc[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t v = 0;
-#pragma unroll
-        for (int e = 7; e >= 0; --e) {
-          const float x = (e & 1) ? a[4 * q + e / 2].y : a[4 * q + e / 2].x;
-          const uint32_t cell = __float_as_uint(__fmaf_rn(x, 4.0f, kCellMagic));
-          uint2 ent;
-          asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(ent.x), "=r"(ent.y) : "r"(cell * 128u + lut_base));
-          v = (v << BITS) + ent.y + (x > __uint_as_float(ent.x) ? 1u : 0u);
-        }
-        acc[q] = v;
-      }
-      uint8_t* vc = codes + (uint64_t)j * CB;
-      if (in) {
-        if (BITS == 4) {
-          st16(vc + 16 * li, make_uint4(acc[0], acc[1], acc[2], acc[3]));
-        } else if (BITS == 2) {
-          st8(vc + 8 * li, make_uint2(acc[0] | (acc[1] << 16), acc[2] | (acc[3] << 16)));
-        } else {
-          st4(vc + 12 * li, acc[0] | (acc[1] << 24));
-          st4(vc + 12 * li + 4, (acc[1] >> 8) | (acc[2] << 16));
-          st4(vc + 12 * li + 8, (acc[2] >> 16) | (acc[3] << 8));
-        }
-        if (li == 0)
-          *reinterpret_cast<uint16_t*>(meta + (uint64_t)j * 2) = __half_as_ushort(__float2half_rn(n));
-      }
-    }
-    flags = __reduce_or_sync(0xffffffffu, flags);
-    if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
-    zero_padding(cur.slot, (uint64_t)nv * (CB + 2), p.seg_bytes[cur.role]);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const uint32_t f = s_flag[it & 1];
-      p.status[ci] = (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
-    }
-    ++it;
-    cur = nxt;
-    ci = ni;
-  }
-}
 
 // ---------------------------------------------------------------- 64 elements per lane
 // For D >= 64 a lane owns 64 contiguous elements (G = D/64 lanes per vector):
@@ -469,7 +281,8 @@ __device__ __forceinline__ void tq_store32(uint8_t* dst, const uint32_t (&acc)[4
 // it, which rounds differently when a square falls below the normal range.
 template <int P0, int N>
 struct PairTree {
-  static __device__ __forceinline__ float2 run(const float2 (&a)[32], float2 nz2) {
+  template <int NP>
+  static __device__ __forceinline__ float2 run(const float2 (&a)[NP], float2 nz2) {
     if constexpr (N == 1) {
       return fma2(a[P0], a[P0], nz2);
     } else {
@@ -482,8 +295,8 @@ struct PairTree {
 // in pair 16 R + (o & 15), component o >> 4), 8 per word, element 0 lowest;
 // `lut` is the direct or the mirrored table of this lane and run, `cm` the
 // complement that turns the table's codes into the element's.
-template <int BITS, int R>
-__device__ __forceinline__ void tq_run_codes(const float2 (&a)[32], uint32_t lut, uint32_t cm,
+template <int BITS, int R, int NP>
+__device__ __forceinline__ void tq_run_codes(const float2 (&a)[NP], uint32_t lut, uint32_t cm,
                                              uint32_t (&acc)[4]) {
   const float2 k4 = make_float2(4.0f, 4.0f), mg = make_float2(kCellMagic, kCellMagic);
 #pragma unroll
@@ -518,38 +331,43 @@ __device__ __forceinline__ void tq_run_codes(const float2 (&a)[32], uint32_t lut
   }
 }
 
-// 128 bytes of vector j's lane part: 32-byte loads when every vector is
-// 32-byte aligned, else 16-byte loads.
-__device__ __forceinline__ void tq64_load(const uint16_t* src, bool v32, uint4 (&w)[8]) {
+// The lane's part of vector j (16 NC bytes): 32-byte loads when every vector
+// is 32-byte aligned, else 16-byte loads.
+template <int NC>
+__device__ __forceinline__ void tq_lane_load(const uint16_t* src, bool v32, uint4 (&w)[NC]) {
   if (v32) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) ld_nc32(src + 16 * k, w[2 * k], w[2 * k + 1]);
+    for (int k = 0; k < NC / 2; ++k) ld_nc32(src + 16 * k, w[2 * k], w[2 * k + 1]);
   } else {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) w[k] = ld_nc16(src + 8 * k);
+    for (int k = 0; k < NC; ++k) w[k] = ld_nc16(src + 8 * k);
   }
 }
 
-template <int DT, int D, int BITS>
-__global__ void __launch_bounds__(kTq64Threads, 3) tq_encode64_kernel(const __grid_constant__ Params p) {
-  constexpr int E = 64, G = D / E, VPW = 32 / G, W = kTq64Threads / 32;
+// E = 64 elements per lane for head dims 64 .. 256; E = 32 (one lane per
+// vector, pairs (k, k + 16), no stride-32 stage) for head dim 32.
+template <int DT, int D, int BITS, int E>
+__global__ void __launch_bounds__(kTq64Threads, E == 64 ? 3 : 5) tq_encode_lanes_kernel(const __grid_constant__ Params p) {
+  constexpr int G = D / E, VPW = 32 / G, W = kTq64Threads / 32;
+  constexpr int NP = E / 2, NCH = E / 8;       // pairs and 16-byte chunks of a lane
   constexpr int CB = D * BITS / 8;
   constexpr int NT = G >= 2 ? 2 : 1;           // index tables: direct (+ mirrored)
-  static_assert(G >= 1 && G <= 4, "head dim 64 .. 256");
+  static_assert((E == 64 && G >= 1 && G <= 4) || (E == 32 && G == 1), "head dim 32 .. 256");
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
   __shared__ uint2 s_lut[NT][kLutCells * 16];
   // sign masks of source word t (elements 2t, 2t + 1) of lane position l:
   // BF16: [l][0][t] bit 31 = sign of element 2t, [l][1][t] bit 31 = sign of
   // element 2t + 1; FP16: [l][0][t] bits 15 and 31.
-  __shared__ uint32_t s_mask[G][2][32];
+  // rows padded by 8 words: the lanes of a vector read different banks
+  __shared__ uint32_t s_mask[G][2 * NP + 8];
   for (int k = threadIdx.x; k < NT * kLutCells * 16; k += blockDim.x) {
     const int t = k / (kLutCells * 16), c = (k >> 4) % kLutCells;
     s_lut[t][k % (kLutCells * 16)] =
         t ? make_uint2(__float_as_uint(p.lut_mthr[c]), p.lut_mlo[c]) : make_uint2(__float_as_uint(p.lut_thr[c]), p.lut_lo[c]);
   }
-  for (int k = threadIdx.x; k < G * 32; k += blockDim.x) {
-    const uint32_t l = (uint32_t)k / 32, t = (uint32_t)k % 32;
+  for (int k = threadIdx.x; k < G * NP; k += blockDim.x) {
+    const uint32_t l = (uint32_t)k / NP, t = (uint32_t)k % NP;
     const uint32_t e0 = l * E + 2u * t;
     uint32_t s0 = (p.sign_words[e0 >> 5] >> (e0 & 31u)) & 1u;
     uint32_t s1 = (p.sign_words[e0 >> 5] >> ((e0 + 1u) & 31u)) & 1u;
@@ -558,11 +376,11 @@ __global__ void __launch_bounds__(kTq64Threads, 3) tq_encode64_kernel(const __gr
       s1 ^= 1u;
     }
     if (DT == 1) {
-      s_mask[l][0][t] = s0 << 31;
-      s_mask[l][1][t] = s1 << 31;
+      s_mask[l][t] = s0 << 31;
+      s_mask[l][NP + t] = s1 << 31;
     } else {
-      s_mask[l][0][t] = (s0 << 15) | (s1 << 31);
-      s_mask[l][1][t] = 0u;
+      s_mask[l][t] = (s0 << 15) | (s1 << 31);
+      s_mask[l][NP + t] = 0u;
     }
   }
   __syncthreads();
@@ -573,7 +391,7 @@ __global__ void __launch_bounds__(kTq64Threads, 3) tq_encode64_kernel(const __gr
   const uint32_t lut_a = neg_a ? lut_m : lut_d, lut_b = neg_b ? lut_m : lut_d;
   constexpr uint32_t kAll = BITS == 4 ? 0xffffffffu : (1u << (8 * BITS)) - 1u;
   const uint32_t cm_a = neg_a ? kAll : 0u, cm_b = neg_b ? kAll : 0u;
-  const uint32_t mask_addr = (uint32_t)__cvta_generic_to_shared(&s_mask[li][0][0]);
+  const uint32_t mask_addr = (uint32_t)__cvta_generic_to_shared(&s_mask[li][0]);
   const uint32_t run_a = tq64_run_start<G>(li, 0), run_b = tq64_run_start<G>(li, 1);
   const uint32_t nv = p.nv;
   const bool v32 = p.vec32 != 0;
@@ -591,8 +409,8 @@ __global__ void __launch_bounds__(kTq64Threads, 3) tq_encode64_kernel(const __gr
   warp_cursor_init(cursor, W);
   Seg cur;
   uint32_t ci = cursor_next<kEncode, true>(p, cursor, cur);
-  uint4 pw[8];
-  if (ci != 0xffffffffu) tq64_load(src_of(cur.page, grp), v32, pw);
+  uint4 pw[NCH];
+  if (ci != 0xffffffffu) tq_lane_load(src_of(cur.page, grp), v32, pw);
   while (ci != 0xffffffffu) {
     const uint16_t* npage;  // the next segment's page: the rest of its plan is redone below
     uint32_t ni;
@@ -607,12 +425,12 @@ __global__ void __launch_bounds__(kTq64Threads, 3) tq_encode64_kernel(const __gr
     for (uint32_t j0 = 0; j0 < nv; j0 += VPW) {
       const uint32_t j = j0 + grp;
       // source words -> pairs, sign flips on the 16-bit values (exact)
-      float2 a[32];
+      float2 a[NP];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < NCH; ++c) {
         const uint4 m0 = lds16(mask_addr + 16u * c);
         uint4 m1 = make_uint4(0, 0, 0, 0);
-        if (DT == 1) m1 = lds16(mask_addr + 128u + 16u * c);
+        if (DT == 1) m1 = lds16(mask_addr + 4u * NP + 16u * c);
         const uint32_t ww[4] = {pw[c].x, pw[c].y, pw[c].z, pw[c].w};
         const uint32_t k0[4] = {m0.x, m0.y, m0.z, m0.w}, k1[4] = {m1.x, m1.y, m1.z, m1.w};
 #pragma unroll
@@ -638,12 +456,18 @@ __global__ void __launch_bounds__(kTq64Threads, 3) tq_encode64_kernel(const __gr
         }
       }
       // the page data is in registers now: load the next vector
-      if (j0 + VPW < nv) tq64_load(src_of(cur.page, j + VPW), v32, pw);
-      else if (ni != 0xffffffffu) tq64_load(src_of(npage, grp), v32, pw);
+      if (j0 + VPW < nv) tq_lane_load(src_of(cur.page, j + VPW), v32, pw);
+      else if (ni != 0xffffffffu) tq_lane_load(src_of(npage, grp), v32, pw);
       // pairwise sum of squares: in-lane index bits 0..3, then 4, then 5
       const float2 nz2 = make_float2(p.neg_zero, p.neg_zero);
-      const float2 ta = PairTree<0, 16>::run(a, nz2), tb = PairTree<16, 16>::run(a, nz2);
-      float ss = __fadd_rn(__fadd_rn(ta.x, ta.y), __fadd_rn(tb.x, tb.y));
+      float ss;
+      if constexpr (E == 64) {
+        const float2 ta = PairTree<0, 16>::run(a, nz2), tb = PairTree<16, 16>::run(a, nz2);
+        ss = __fadd_rn(__fadd_rn(ta.x, ta.y), __fadd_rn(tb.x, tb.y));
+      } else {
+        const float2 ta = PairTree<0, 16>::run(a, nz2);
+        ss = __fadd_rn(ta.x, ta.y);
+      }
 #pragma unroll
       for (int o = 1; o < G; o <<= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
       // Admission.  ss is within 2^-20 (relative) of the exact sum of
@@ -654,7 +478,7 @@ __global__ void __launch_bounds__(kTq64Threads, 3) tq_encode64_kernel(const __gr
         float amax = 0.0f;
         uint32_t nonfinite = 0;
 #pragma unroll
-        for (int m = 0; m < 32; ++m) {
+        for (int m = 0; m < NP; ++m) {
           nonfinite |= !isfinite(a[m].x) | !isfinite(a[m].y);
           amax = fmaxf(amax, fmaxf(fabsf(a[m].x), fabsf(a[m].y)));
         }
@@ -667,7 +491,7 @@ __global__ void __launch_bounds__(kTq64Threads, 3) tq_encode64_kernel(const __gr
         flags |= vflags;
         if (vflags) {  // keep NaN / inf out of the arithmetic (the segment stays raw)
 #pragma unroll
-          for (int m = 0; m < 32; ++m) a[m] = make_float2(0.0f, 0.0f);
+          for (int m = 0; m < NP; ++m) a[m] = make_float2(0.0f, 0.0f);
         }
       }
       const float n = __fsqrt_rn(ss);
@@ -683,12 +507,12 @@ __global__ void __launch_bounds__(kTq64Threads, 3) tq_encode64_kernel(const __gr
       // the launch parameters.
       const float2 r2 = make_float2(r, r);
 #pragma unroll
-      for (int m = 0; m < 32; ++m) a[m] = fma2(a[m], r2, nz2);
+      for (int m = 0; m < NP; ++m) a[m] = fma2(a[m], r2, nz2);
       // Walsh-Hadamard butterflies, ascending stride
 #pragma unroll
       for (int h = 1; h < 16; h <<= 1) {  // strides 1, 2, 4, 8: pair P with pair P + h
 #pragma unroll
-        for (int m = 0; m < 32; ++m) {
+        for (int m = 0; m < NP; ++m) {
           if (m & h) continue;
           const float2 u = a[m], v = a[m + h];
           a[m] = add2(u, v);
@@ -696,15 +520,17 @@ __global__ void __launch_bounds__(kTq64Threads, 3) tq_encode64_kernel(const __gr
         }
       }
 #pragma unroll
-      for (int m = 0; m < 32; ++m) {  // stride 16: inside each pair
+      for (int m = 0; m < NP; ++m) {  // stride 16: inside each pair
         const float u = a[m].x, v = a[m].y;
         a[m] = make_float2(__fadd_rn(u, v), __fsub_rn(u, v));
       }
+      if constexpr (E == 64) {
 #pragma unroll
-      for (int m = 0; m < 16; ++m) {  // stride 32: pair P with pair P + 16
-        const float2 u = a[m], v = a[m + 16];
-        a[m] = add2(u, v);
-        a[m + 16] = sub2(u, v);
+        for (int m = 0; m < 16; ++m) {  // stride 32: pair P with pair P + 16
+          const float2 u = a[m], v = a[m + 16];
+          a[m] = add2(u, v);
+          a[m + 16] = sub2(u, v);
+        }
       }
       if constexpr (G == 2) {  // stride 64: lanes li, li ^ 1 (split, see above)
 #pragma unroll
@@ -745,16 +571,16 @@ __global__ void __launch_bounds__(kTq64Threads, 3) tq_encode64_kernel(const __gr
         // can exceed sqrt(D); clamp into the table (beyond +-17 every code
         // is already the first or the last).
 #pragma unroll
-        for (int m = 0; m < 32; ++m)
+        for (int m = 0; m < NP; ++m)
           a[m] = make_float2(fminf(fmaxf(a[m].x, -17.0f), 17.0f), fminf(fmaxf(a[m].y, -17.0f), 17.0f));
       }
       uint32_t acc_a[4], acc_b[4];
       tq_run_codes<BITS, 0>(a, lut_a, cm_a, acc_a);
-      tq_run_codes<BITS, 1>(a, lut_b, cm_b, acc_b);
+      if constexpr (E == 64) tq_run_codes<BITS, 1>(a, lut_b, cm_b, acc_b);
       if (j < nv) {
         uint8_t* vc = codes + (uint64_t)j * CB;
         tq_store32<BITS>(vc + run_a * BITS / 8, acc_a);
-        tq_store32<BITS>(vc + run_b * BITS / 8, acc_b);
+        if constexpr (E == 64) tq_store32<BITS>(vc + run_b * BITS / 8, acc_b);
         if (li == 0)
           *reinterpret_cast<uint16_t*>(meta + (uint64_t)j * 2) = __half_as_ushort(__float2half_rn(n));
       }
@@ -1037,10 +863,8 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
 
 template <int DT, int D, int BITS>
 int encode(const Params& p, void* stream) {
-  if constexpr (D >= 64)
-    return launch_codec_kernel(tq_encode64_kernel<DT, D, BITS>, p, stream, 8, kTq64Threads, true);
-  else
-    return launch_codec_kernel(tq_encode_kernel<DT, D, BITS>, p, stream, 8);
+  constexpr int E = D >= 64 ? 64 : 32;
+  return launch_codec_kernel(tq_encode_lanes_kernel<DT, D, BITS, E>, p, stream, 8, kTq64Threads, true);
 }
 
 template <int DT, int D, int BITS>
