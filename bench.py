@@ -9,12 +9,14 @@ Qwen3-8B-shaped KV (36 layers, 8 KV heads, D=128, FP16, 4 x 8192 tokens in
 16-token pages) with the FP8 K16/V8 arm (V only) and the FP8 K8/V8 arm, both
 with dynamic per-token/head scales.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference] [--partition]
 
 N > 1 runs one process per GPU (torchrun): every rank codes its own copy of the
-workload (weak scaling, no data-path collective; a gloo barrier and a max of
-the timings are the only cross-rank operations).  `--impl reference` times the
-plain CPU oracle on a bounded sample of the same workload on the host cores.
+workload (weak scaling), or with --partition its own contiguous range of the
+cache's layers (strong scaling).  There is no data-path collective: a gloo
+barrier, a max of the timings and sums of the work are the only cross-rank
+operations.  `--impl reference` times the plain CPU oracle on a bounded sample
+of the same workload on the host cores.
 """
 from __future__ import annotations
 
@@ -91,7 +93,7 @@ class Arm:
     """One codec arm bound to device buffers: codec handle, descriptors,
     encoded buffer, statuses and restore destinations."""
 
-    def __init__(self, case: synth.Case, arm: synth.Arm, dev_layers, device):
+    def __init__(self, case: synth.Case, arm: synth.Arm, dev_layers, device, part=None):
         self.case, self.arm = case, arm
         self.codec = K.Codec(dtype="fp16" if case.dtype == torch.float16 else "bf16",
                              layout=case.layout, head_dim=case.head_dim,
@@ -103,6 +105,8 @@ class Arm:
         self.seg = [self.codec.segment_bytes(r)[0] for r in (0, 1)]
         raw_seg = self.codec.segment_bytes(0)[1]
         rows, self.total = synth.segment_list(case, arm, self.seg)
+        if part is not None:  # (world, rank): this rank's layers only, slots at their offsets
+            rows = synth.partition_rows(rows, *part)
         self.rows = rows
         self.n = len(rows)
         self.descs = K.descriptors(rows, device)
@@ -111,10 +115,11 @@ class Arm:
         self.status = torch.empty(self.n, dtype=torch.uint8, device=device)
         self.dst = [None if t is None else torch.empty_like(t) for t in dev_layers]
         # which layer tensors this arm touches (separate layout: K/V by role)
+        mine = sorted({r[0] for r in rows})
         if case.layout == "separate":
-            used = {2 * l + r for l in range(case.num_layers) for r in arm.roles}
+            used = {2 * l + r for l in mine for r in arm.roles}
         else:
-            used = set(range(case.num_layers))
+            used = set(mine)
         self.used = sorted(used)
         self.layout = case.layout
         self.src_view = [t if i in used else None for i, t in enumerate(dev_layers)]
@@ -222,7 +227,8 @@ def run_gpu(args, dist, world, rank, local):
     torch.cuda.set_device(device)
     case = synth.make_case(args.workload, device=device, seed=args.seed, num_layers=args.layers,
                            num_blocks=args.pages, head_dim=args.head_dim)
-    arms = [Arm(case, a, case.layers, device) for a in case.arms
+    part = (world, rank) if args.partition else None
+    arms = [Arm(case, a, case.layers, device, part) for a in case.arms
             if args.arm is None or a.name == args.arm]
     stream = torch.cuda.current_stream(device)
 
@@ -243,7 +249,7 @@ def run_gpu(args, dist, world, rank, local):
         step()
     torch.cuda.synchronize()
     statuses = [a.status.cpu() for a in arms]
-    n_encoded = sum(int((s == K.SEG_ENCODED).sum()) for s in statuses)
+    n_encoded = int(sum_over_ranks(dist, sum(int((s == K.SEG_ENCODED).sum()) for s in statuses)))
 
     clocks = ClockSampler(local)
     time.sleep(0.3)
@@ -297,14 +303,15 @@ def run_gpu(args, dist, world, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "scaling": "strong" if args.partition else "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; see kv_cache_page_gb300/synth.py)",
         "config": {"workload": args.workload, "arms": [a.arm.name for a in arms],
                    "source_dtype": "fp16" if case.dtype == torch.float16 else "bf16",
                    "layers": case.num_layers, "pages_per_layer": case.num_blocks,
                    "kv_heads": case.num_heads, "head_dim": case.head_dim,
                    "raw_kv_bytes_per_step": raw_per_step, "segments_encoded": n_encoded,
-                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+                   "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": (f"layer partition x{world}" if args.partition else f"replicas x{world}")},
         "roofline": roofline,
         "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                     for k, v in kernels.items()},
@@ -398,11 +405,53 @@ def run_e2e(args, arms, stream, dist):
     sec = max_over_ranks(dist, time.perf_counter() - t0)
     raw = sum(2 * a.raw_bytes for a in arms)
     value = sum_over_ranks(dist, raw * steps) / sec / GB
+    link = link_ceiling(arms, host, streams)
+    link_raw = raw / link["both_s"] / GB          # raw KV per second if the step were only its copies
     return {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "path": "pages copied H2D/D2H from pinned memory; slots and statuses in pinned host "
                     f"memory, moved by the kernels; chunks of {args.e2e_chunk_layers} layers "
-                    f"pipelined over {args.e2e_streams} streams"}
+                    f"pipelined over {args.e2e_streams} streams",
+            "link_ceiling_gbs": round(link_raw, 2),
+            "frac_of_link": round(value / link_raw, 4),
+            "link": {k: (round(v, 2) if isinstance(v, float) else v) for k, v in link.items()}}
+
+
+def link_ceiling(arms, host, streams):
+    """The host link's own rate for the end-to-end step's bytes: plain
+    cudaMemcpyAsync copies of exactly the bytes a step moves (the pages in and
+    out, the slots and statuses once each way), H2D alone, D2H alone, and
+    both at once on two streams (the link is full duplex).  Best of 3 runs,
+    host clock around a device synchronize."""
+    h2d_pairs, d2h_pairs = [], []
+    for a, (src_h, dst_h, enc_h, st_h) in zip(arms, host):
+        for i in a.used:
+            h2d_pairs.append((a.src[i], src_h[i]))
+            d2h_pairs.append((dst_h[i], a.dst[i]))
+        h2d_pairs += [(a.enc, enc_h), (a.status, st_h)]
+        d2h_pairs += [(enc_h, a.enc), (st_h, a.status)]
+    bi = sum(d.numel() * d.element_size() for d, _ in h2d_pairs)
+    bo = sum(d.numel() * d.element_size() for d, _ in d2h_pairs)
+    s_in, s_out = streams[0], streams[1 % len(streams)]
+
+    def run(pairs_by_stream):
+        best = float("inf")
+        for _ in range(3):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for s, pairs in pairs_by_stream:
+                with torch.cuda.stream(s):
+                    for dst, src in pairs:
+                        dst.copy_(src, non_blocking=True)
+            torch.cuda.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        return best
+
+    t_in = run([(s_in, h2d_pairs)])
+    t_out = run([(s_out, d2h_pairs)])
+    t_both = run([(s_in, h2d_pairs), (s_out, d2h_pairs)])
+    return {"h2d_bytes": bi, "d2h_bytes": bo, "h2d_gbs": bi / t_in / GB, "d2h_gbs": bo / t_out / GB,
+            "both_gbs": (bi + bo) / t_both / GB, "both_s": t_both}
 
 
 def run_host_link(args, arms, stream):
@@ -560,20 +609,31 @@ def run_extra(args, device):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-def _oracle_sample(case_name, blocks, layers):
-    """Host copies of a bounded sample of the workload + per-arm oracle inputs."""
+# One workload per codec family for the per-codec CPU baseline.
+CPU_FAMILIES = (("fp8", "qwen3_8b"), ("turboquant+uniform", "vllm_packed"),
+                ("uniform8", "qwen25_7b_offload"), ("int8_head", "hiq_qwen3_8b"))
+
+
+def _oracle_sample(case_name, blocks):
+    """Host copies of a bounded sample of the workload + per-arm oracle inputs:
+    `blocks` pages of one layer that no arm protects (the workload is built
+    with just enough layers for that)."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     import oracle as O
     from kvcases import host_bits, oracle_descs, oracle_geom
+    probe = synth.make_case(case_name, num_layers=1, num_blocks=1)
+    pf = max(a.protect[0] for a in probe.arms)
+    pl = max(a.protect[1] for a in probe.arms)
+    layers = pf + pl + 1
     case = synth.make_case(case_name, num_layers=layers, num_blocks=blocks)
     bits = [host_bits(t) for t in case.layers]
     work = []
     for arm in case.arms:
         g = oracle_geom(case, arm)
         seg = [O.segment_enc_bytes(g, r) for r in (0, 1)]
-        rows, total = synth.segment_list(case, arm, seg)
+        rows, total = synth.segment_list(case, arm, seg, layers=[pf])
         work.append((g, rows, total, case.raw_segment_bytes))
-    return O, bits, work, oracle_descs
+    return O, bits, work, oracle_descs, pf
 
 
 def _oracle_pass(O, bits, work, oracle_descs, threads):
@@ -591,19 +651,19 @@ def _oracle_pass(O, bits, work, oracle_descs, threads):
         for g, rows, total, raw_seg in work:
             chunk = -(-len(rows) // threads)
             for k in range(0, len(rows), chunk):
-                part = [(l, b, r, off) for (l, b, r, off) in rows[k:k + chunk]]
-                jobs.append(ex.submit(one, g, part, total))
+                jobs.append(ex.submit(one, g, rows[k:k + chunk], total))
             done += 2 * len(rows) * raw_seg
         for j in jobs:
             j.result()
     return done
 
 
-def cpu_baseline(args, case_name, seconds):
-    threads = os.cpu_count() or 1
-    blocks = max(threads * 2, 16)
-    O, bits, work, od = _oracle_sample(case_name, blocks, 1)
-    _oracle_pass(O, bits, work, od, threads)            # warm-up
+def _timed_oracle(case_name, threads, seconds):
+    """GB/s of raw KV of the oracle on `threads` host threads: a warm-up pass,
+    then passes until `seconds` have elapsed (at least one)."""
+    blocks = 4 if threads == 1 else 8 * threads
+    O, bits, work, od, layer = _oracle_sample(case_name, blocks)
+    _oracle_pass(O, bits, work, od, threads)
     t0 = time.perf_counter()
     done, passes = 0, 0
     while True:
@@ -612,15 +672,32 @@ def cpu_baseline(args, case_name, seconds):
         if time.perf_counter() - t0 >= seconds:
             break
     sec = time.perf_counter() - t0
-    return {"value": round(done / sec / GB, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{case_name}: layer 0, pages 0..{blocks - 1}, every arm, encode+decode, "
+    return {"value": round(done / sec / GB, 6), "cores": threads,
+            "sample": f"{case_name}: layer {layer}, pages 0..{blocks - 1}, every arm, encode+decode, "
                       f"{passes} passes in {sec:.1f} s"}
+
+
+def cpu_baseline(args, case_name, seconds):
+    """The oracle as it stands on the host cores: the benchmark's workload on
+    all cores (the reported value) and on one core, and one workload per
+    codec family on one and on all cores."""
+    threads = os.cpu_count() or 1
+    main = _timed_oracle(case_name, threads, seconds)
+    one = _timed_oracle(case_name, 1, seconds / 2)
+    per = {}
+    for fam, name in CPU_FAMILIES:
+        per[fam] = {"workload": name, "all_cores": _timed_oracle(name, threads, seconds / 4),
+                    "one_core": _timed_oracle(name, 1, seconds / 4)}
+    return {"value": main["value"], "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": main["sample"], "nproc": threads,
+            "one_core": {"value": one["value"], "unit": UNIT, "cores": 1, "sample": one["sample"]},
+            "per_codec": per}
 
 
 def run_reference(args):
     threads = os.cpu_count() or 1
     blocks = max(threads, 8)
-    O, bits, work, od = _oracle_sample(args.workload, blocks, 1)
+    O, bits, work, od, layer = _oracle_sample(args.workload, blocks)
     for _ in range(args.warmup):
         _oracle_pass(O, bits, work, od, threads)
     t0 = time.perf_counter()
@@ -629,7 +706,7 @@ def run_reference(args):
         done += _oracle_pass(O, bits, work, od, threads)
     sec = time.perf_counter() - t0
     value = done / sec / GB
-    sample = f"{args.workload}: layer 0, pages 0..{blocks - 1}, every arm, encode+decode per step"
+    sample = f"{args.workload}: layer {layer}, pages 0..{blocks - 1}, every arm, encode+decode per step"
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
             "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(sec * 1e3 / args.steps, 3),
@@ -664,6 +741,9 @@ def main(argv=None):
                     help="skip the host-resident slot offload/restore timings")
     ap.add_argument("--no-integrity", dest="integrity", action="store_false",
                     help="skip the segment header seal/verify timings")
+    ap.add_argument("--partition", action="store_true",
+                    help="N > 1: rank r codes its own contiguous range of layers (strong scaling) "
+                         "instead of a replica of the whole cache")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args(argv)

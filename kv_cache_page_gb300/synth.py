@@ -31,7 +31,7 @@ from typing import List, Optional, Sequence, Tuple
 
 import torch
 
-__all__ = ["Case", "make_case", "CASES"]
+__all__ = ["Case", "make_case", "CASES", "segment_list", "partition_rows"]
 
 
 @dataclasses.dataclass
@@ -213,6 +213,18 @@ def make_case(name: str, *, device="cpu", num_layers: Optional[int] = None,
 
 
 CASES = ("tiny", "qwen3_8b", "vllm_packed", "head_dim_sweep", "qwen25_7b_offload", "hiq_qwen3_8b")
+
+
+def partition_rows(rows, world: int, rank: int):
+    """The rows (layer, block, role, offset) of one rank when `world` GPUs
+    share a cache: rank r takes the layers [L r / world, L (r + 1) / world) of
+    the layers the rows cover, so that each rank codes whole layers of its own
+    pages and the ranks' rows, concatenated in rank order, are the rows in
+    their original (layer-major) order.  Slot offsets are kept."""
+    layers = sorted({r[0] for r in rows})
+    n = len(layers)
+    mine = set(layers[n * rank // world: n * (rank + 1) // world])
+    return [r for r in rows if r[0] in mine]
 
 
 def segment_list(case: Case, arm: Arm, seg_bytes: Sequence[int], layers=None, blocks=None):
