@@ -54,7 +54,7 @@ class Geom(C.Structure):
         ("num_blocks", C.c_int64), ("stride_block", C.c_int64), ("stride_token", C.c_int64),
         ("stride_head", C.c_int64), ("codec", C.c_int32 * 2), ("protect_first", C.c_int32),
         ("protect_last", C.c_int32), ("seed", C.c_uint64), ("reject_abs", C.c_float),
-        ("pad_", C.c_int32), ("fixed_amax", C.POINTER(C.c_float)),
+        ("sign_version", C.c_int32), ("fixed_amax", C.POINTER(C.c_float)),
     ]
 
 
@@ -85,6 +85,9 @@ def lib():
             "kvo_absmax": [_f32, C.c_int],
             "kvo_fp8_encode_many": [_f32, C.c_int64, C.c_int, _f32, _u8],
             "kvo_signs": [C.c_uint64, C.c_int, _u8],
+            "kvo_signs_layer": [C.c_uint64, C.c_int, C.c_int, _u8],
+            "kvo_tq_encode_many_signs": [_f32, C.c_int64, C.c_int, C.c_int, _u8, _u8, _u16],
+            "kvo_tq_decode_many_signs": [_u8, _u16, C.c_int64, C.c_int, C.c_int, _u8, _f32],
             "kvo_splitmix64_next": [C.POINTER(C.c_uint64)],
             "kvo_wht": [_f32, C.c_int],
             "kvo_wht_scale": [C.c_int],
@@ -179,6 +182,13 @@ def signs(seed, D):
     return out
 
 
+def signs_layer(seed, layer, D):
+    """Format version 2: the sign vector of one layer."""
+    out = np.empty(D, dtype=np.uint8)
+    lib().kvo_signs_layer(seed, layer, D, out)
+    return out
+
+
 def splitmix64(seed, n):
     st = C.c_uint64(seed)
     return [lib().kvo_splitmix64_next(C.byref(st)) for _ in range(n)]
@@ -222,6 +232,25 @@ def tq_encode(x, bits, seed):
     norm = np.empty(nvec, dtype=np.uint16)
     lib().kvo_tq_encode_many(x.reshape(-1), nvec, D, bits, seed, codes.reshape(-1), norm)
     return codes, norm
+
+
+def tq_encode_with_signs(x, bits, neg):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    nvec, D = x.shape
+    codes = np.empty((nvec, D), dtype=np.uint8)
+    norm = np.empty(nvec, dtype=np.uint16)
+    lib().kvo_tq_encode_many_signs(x.reshape(-1), nvec, D, bits, np.ascontiguousarray(neg, dtype=np.uint8),
+                                   codes.reshape(-1), norm)
+    return codes, norm
+
+
+def tq_decode_with_signs(codes, norm16, bits, neg):
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    nvec, D = codes.shape
+    out = np.empty((nvec, D), dtype=np.float32)
+    lib().kvo_tq_decode_many_signs(codes.reshape(-1), np.ascontiguousarray(norm16, dtype=np.uint16), nvec,
+                                   D, bits, np.ascontiguousarray(neg, dtype=np.uint8), out.reshape(-1))
+    return out
 
 
 def tq_decode(codes, norm16, bits, seed):
@@ -298,9 +327,12 @@ def unpack_bits(packed, n, bits):
 
 # ---------------------------------------------------------------- segments
 def make_geom(*, dtype, layout, head_dim, num_heads, block_tokens, num_layers, num_blocks,
-              strides, codecs, protect=(0, 0), seed=0, reject_abs=448.0, fixed_amax=None):
+              strides, codecs, protect=(0, 0), seed=0, reject_abs=448.0, fixed_amax=None,
+              sign_version=1):
     """Build the oracle's geometry.  `strides` = (block, token, head) in elements;
-    `fixed_amax` = float32 [num_layers, 2] calibration absmax (FP8 fixed mode)."""
+    `fixed_amax` = float32 [num_layers, 2] calibration absmax (FP8 fixed mode);
+    `sign_version` 1: one TurboQuant sign vector per (seed, head dim), 2: one
+    per layer as well (format version 2)."""
     g = Geom()
     g.dtype, g.layout, g.head_dim = dtype, layout, head_dim
     g.num_heads, g.block_tokens, g.num_layers = num_heads, block_tokens, num_layers
@@ -309,6 +341,7 @@ def make_geom(*, dtype, layout, head_dim, num_heads, block_tokens, num_layers, n
     g.codec[0], g.codec[1] = codecs
     g.protect_first, g.protect_last = protect
     g.seed = seed
+    g.sign_version = sign_version
     g.reject_abs = reject_abs
     if fixed_amax is not None:
         fa = np.ascontiguousarray(fixed_amax, dtype=np.float32).reshape(-1)

@@ -218,6 +218,21 @@ void kvo_signs(uint64_t seed, int D, uint8_t* neg) {
   }
 }
 
+/* Format version 2: one sign vector per (seed, layer, head dim).  READING of
+ * [OKV "FP8 and TurboQuant"] ("versioned sign generator"): layer l takes its
+ * W = ceil(D/64) words from the same SplitMix64 stream, after the W*l words of
+ * the layers below it, so sign i of layer l is bit (i mod 64) of output
+ * l*W + floor(i/64).  Layer 0 is the version-1 vector. */
+void kvo_signs_layer(uint64_t seed, int layer, int D, uint8_t* neg) {
+  const int W = (D + 63) / 64;
+  uint64_t st = seed, w = 0;
+  for (long k = 0; k < (long)layer * W; ++k) kvo_splitmix64_next(&st);  /* the layers below */
+  for (int i = 0; i < D; ++i) {
+    if ((i & 63) == 0) w = kvo_splitmix64_next(&st);
+    neg[i] = (uint8_t)((w >> (i & 63)) & 1u);
+  }
+}
+
 /* 1/sqrt(D) rounded to FP32 (exact for D = 64, 256). */
 float kvo_wht_scale(int D) { return (float)(1.0 / sqrt((double)D)); }
 
@@ -451,9 +466,16 @@ typedef struct {
   int32_t protect_first, protect_last;
   uint64_t seed;
   float reject_abs;
-  int32_t pad_;
+  int32_t sign_version;             /* 0 or 1: one sign vector per (seed, D); 2: per layer too */
   const float* fixed_amax;          /* [num_layers][2] calibration absmax */
 } kvo_geom;
+
+/* The sign vector of a layer under the geometry's format version. */
+static void layer_signs(const kvo_geom* g, int layer, uint8_t* neg) {
+  if (g->sign_version == 2) kvo_signs_layer(g->seed, layer, g->head_dim, neg);
+  else kvo_signs(g->seed, g->head_dim, neg);
+}
+static uint32_t format_version(const kvo_geom* g) { return g->sign_version == 2 ? 2u : 1u; }
 
 typedef struct {
   uint32_t layer, block, role, reserved;
@@ -542,7 +564,7 @@ void kvo_encode(const kvo_geom* g, void* const* ptrs, const kvo_desc* descs, uin
   int nv = H * T;
   uint8_t neg[256];
   float cent[16], bnd[16];
-  kvo_signs(g->seed, D, neg);
+  int neg_layer = -1;               /* layer whose signs neg holds */
   float reject = g->reject_abs > 0.0f ? g->reject_abs : 448.0f;
   float* x = (float*)malloc(sizeof(float) * (size_t)D);
   uint8_t* codes = (uint8_t*)malloc((size_t)D);
@@ -570,6 +592,7 @@ void kvo_encode(const kvo_geom* g, void* const* ptrs, const kvo_desc* descs, uin
     vec_bytes(codec, D, &cbytes, &mbytes);
     int bits = codec_bits(codec);
     if (is_tq(codec) && cb_bits_done != bits) { kvo_codebook(bits, D, cent, bnd); cb_bits_done = bits; }
+    if (is_tq(codec) && neg_layer != (int)d->layer) { layer_signs(g, (int)d->layer, neg); neg_layer = (int)d->layer; }
     uint8_t* slot = out + d->enc_offset;
     int64_t seg_bytes = kvo_segment_enc_bytes(g, (int)d->role);
     memset(slot, 0, (size_t)seg_bytes);
@@ -630,7 +653,7 @@ void kvo_decode(const kvo_geom* g, void* const* ptrs, const kvo_desc* descs, uin
   int nv = H * T;
   uint8_t neg[256];
   float cent[16], bnd[16];
-  kvo_signs(g->seed, D, neg);
+  int neg_layer = -1;               /* layer whose signs neg holds */
   float* y = (float*)malloc(sizeof(float) * (size_t)D);
   uint8_t* codes = (uint8_t*)malloc((size_t)D);
   int cb_bits_done = 0;
@@ -649,6 +672,7 @@ void kvo_decode(const kvo_geom* g, void* const* ptrs, const kvo_desc* descs, uin
     vec_bytes(codec, D, &cbytes, &mbytes);
     int bits = codec_bits(codec);
     if (is_tq(codec) && cb_bits_done != bits) { kvo_codebook(bits, D, cent, bnd); cb_bits_done = bits; }
+    if (is_tq(codec) && neg_layer != (int)d->layer) { layer_signs(g, (int)d->layer, neg); neg_layer = (int)d->layer; }
     const uint8_t* slot = in + d->enc_offset;
     const uint8_t* meta = slot + (size_t)nv * cbytes;
     int64_t rec = kvo_int8_record_bytes(H, D);
@@ -746,7 +770,7 @@ void kvo_seal(const kvo_geom* g, const kvo_desc* descs, uint32_t n, const uint8_
     const kvo_desc* d = &descs[i];
     kvo_header h;
     memset(&h, 0, sizeof h);
-    h.version = 1;
+    h.version = format_version(g);
     h.orig_bytes = (uint64_t)kvo_segment_raw_bytes(g);
     if (!slot_desc_ok(g, d, buf_bytes)) {
       h.status = S_BAD_DESC;
@@ -768,7 +792,7 @@ void kvo_verify(const kvo_geom* g, const kvo_desc* descs, uint32_t n, const uint
     const kvo_desc* d = &descs[i];
     const kvo_header* h = &hdr[i];
     if (!slot_desc_ok(g, d, buf_bytes) || g->codec[d->role] == O_NONE) { result[i] = S_BAD_DESC; continue; }
-    int ok = h->version == 1 && h->format == header_format(g, (int)d->role) &&
+    int ok = h->version == format_version(g) && h->format == header_format(g, (int)d->role) &&
              h->orig_bytes == (uint64_t)kvo_segment_raw_bytes(g) &&
              h->status >= S_ENCODED && h->status <= S_BAD_DESC;
     if (ok && h->status == S_ENCODED)
@@ -819,6 +843,21 @@ void kvo_tq_decode_many(const uint8_t* codes, const uint16_t* norm16, int64_t nv
   uint8_t neg[256];
   float cent[16], bnd[16];
   kvo_signs(seed, D, neg);
+  kvo_codebook(bits, D, cent, bnd);
+  for (int64_t v = 0; v < nvec; ++v)
+    kvo_tq_decode_vec(codes + v * D, norm16[v], D, bits, neg, cent, out + v * D);
+}
+/* The same with the sign vector given (one byte per element, 1 = negate). */
+void kvo_tq_encode_many_signs(const float* x, int64_t nvec, int D, int bits, const uint8_t* neg,
+                              uint8_t* codes, uint16_t* norm16) {
+  float cent[16], bnd[16];
+  kvo_codebook(bits, D, cent, bnd);
+  for (int64_t v = 0; v < nvec; ++v)
+    kvo_tq_encode_vec(x + v * D, D, bits, neg, bnd, codes + v * D, norm16 + v);
+}
+void kvo_tq_decode_many_signs(const uint8_t* codes, const uint16_t* norm16, int64_t nvec, int D,
+                              int bits, const uint8_t* neg, float* out) {
+  float cent[16], bnd[16];
   kvo_codebook(bits, D, cent, bnd);
   for (int64_t v = 0; v < nvec; ++v)
     kvo_tq_decode_vec(codes + v * D, norm16[v], D, bits, neg, cent, out + v * D);
