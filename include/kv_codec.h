@@ -147,7 +147,11 @@ typedef struct kv_codec_geometry {
   uint32_t protect_last;  /* layers [num_layers - protect_last, num_layers) stay raw */
   uint64_t rotation_seed; /* seed of the TurboQuant sign vector */
   float reject_abs;       /* admission bound, 0 < reject_abs <= 448; 0 selects 448 */
-  uint32_t reserved0;     /* must be 0 */
+  uint32_t sign_version;  /* TurboQuant sign vectors ("versioned sign generator", storage-format
+                             page, "FP8 and TurboQuant"): 0 or 1 = one vector per (rotation_seed,
+                             head_dim), segment format version 1; 2 = one per layer as well,
+                             format version 2 (see kv_codec_layer_signs); other values are refused
+                             with KV_ERR_INVALID_ARG */
   const float* fixed_amax; /* host, [num_layers][2] (K, V) calibration absolute maxima,
                               required iff a role uses FP8_FIXED; copied at create */
 } kv_codec_geometry;
@@ -169,9 +173,11 @@ typedef struct kv_segment_desc {
  * "Ownership, storage and GDS": every encoded segment carries a version, its
  * original length, its format, its stored length and a CRC32).  32 bytes,
  * little endian, one per descriptor. */
-#define KV_SEGMENT_FORMAT_VERSION 1u
+#define KV_SEGMENT_FORMAT_VERSION 1u   /* geometry sign_version 0 or 1 */
+#define KV_SEGMENT_FORMAT_VERSION_2 2u /* geometry sign_version 2: per-layer sign vectors */
 typedef struct kv_segment_header {
-  uint32_t version;       /* KV_SEGMENT_FORMAT_VERSION */
+  uint32_t version;       /* the geometry's format version: KV_SEGMENT_FORMAT_VERSION (1) or
+                             KV_SEGMENT_FORMAT_VERSION_2; verify treats any other as a mismatch */
   uint32_t format;        /* codec kind | dtype << 8 | log2(head_dim) << 16 (0 for a bad descriptor) */
   uint64_t orig_bytes;    /* source segment bytes: num_kv_heads * block_tokens * head_dim * 2 */
   uint64_t stored_bytes;  /* encoded slot bytes; 0 when the segment stayed raw */
@@ -259,8 +265,17 @@ const char* kv_codec_strerror(int code);
  * Gaussian Lloyd-Max levels scaled by 1/sqrt(head_dim). */
 int kv_codec_codebook(uint32_t bits, uint32_t head_dim, float* centroids, float* boundaries);
 
-/* The sign vector for (seed, head_dim): one byte per element, 1 = negate. */
+/* The sign vector for (seed, head_dim): one byte per element, 1 = negate.
+ * Sign i is bit (i mod 64) of output floor(i/64) of SplitMix64 seeded with
+ * `seed` (Steele, Lea and Flood, OOPSLA 2014). */
 int kv_codec_signs(uint64_t seed, uint32_t head_dim, uint8_t* negate);
+
+/* Format version 2: the sign vector of `layer` for (seed, head_dim), one byte
+ * per element, 1 = negate.  Layer l takes the W = ceil(head_dim / 64) outputs
+ * l*W .. l*W + W - 1 of the same SplitMix64 stream (sign i is bit (i mod 64)
+ * of output l*W + floor(i/64)), so layer 0 is the kv_codec_signs vector.
+ * layer < KV_CODEC_MAX_LAYERS. */
+int kv_codec_layer_signs(uint64_t seed, uint32_t layer, uint32_t head_dim, uint8_t* negate);
 
 /* ABI version compiled into the library. */
 uint32_t kv_codec_abi_version(void);

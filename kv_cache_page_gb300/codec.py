@@ -34,7 +34,7 @@ DESC_DTYPE = np.dtype([("layer", "<u4"), ("block", "<u4"), ("role", "<u4"),
 
 EXPORTS = ("kv_codec_create", "kv_codec_destroy", "kv_codec_segment_bytes", "kv_codec_encode",
            "kv_codec_decode", "kv_codec_seal", "kv_codec_verify", "kv_codec_strerror",
-           "kv_codec_codebook", "kv_codec_signs",
+           "kv_codec_codebook", "kv_codec_signs", "kv_codec_layer_signs",
            "kv_codec_abi_version")
 
 
@@ -46,7 +46,7 @@ class Geometry(C.Structure):
         ("stride_block", C.c_int64), ("stride_token", C.c_int64), ("stride_head", C.c_int64),
         ("k_codec", C.c_uint32), ("v_codec", C.c_uint32), ("protect_first", C.c_uint32),
         ("protect_last", C.c_uint32), ("rotation_seed", C.c_uint64), ("reject_abs", C.c_float),
-        ("reserved0", C.c_uint32), ("fixed_amax", C.POINTER(C.c_float)),
+        ("sign_version", C.c_uint32), ("fixed_amax", C.POINTER(C.c_float)),
     ]
 
 
@@ -80,10 +80,11 @@ def lib():
         L.kv_codec_strerror.restype = C.c_char_p
         L.kv_codec_codebook.argtypes = [C.c_uint32, C.c_uint32, C.POINTER(C.c_float), C.POINTER(C.c_float)]
         L.kv_codec_signs.argtypes = [C.c_uint64, C.c_uint32, C.POINTER(C.c_uint8)]
+        L.kv_codec_layer_signs.argtypes = [C.c_uint64, C.c_uint32, C.c_uint32, C.POINTER(C.c_uint8)]
         L.kv_codec_abi_version.restype = C.c_uint32
         for f in ("kv_codec_create", "kv_codec_destroy", "kv_codec_segment_bytes", "kv_codec_encode",
                   "kv_codec_decode", "kv_codec_seal", "kv_codec_verify", "kv_codec_codebook",
-                  "kv_codec_signs"):
+                  "kv_codec_signs", "kv_codec_layer_signs"):
             getattr(L, f).restype = C.c_int
         _LIB = L
     return _LIB
@@ -109,6 +110,13 @@ def codebook(bits: int, head_dim: int):
 def signs(seed: int, head_dim: int):
     out = np.zeros(head_dim, np.uint8)
     _check(lib().kv_codec_signs(seed, head_dim, out.ctypes.data_as(C.POINTER(C.c_uint8))), "kv_codec_signs")
+    return out
+
+
+def layer_signs(seed: int, layer: int, head_dim: int):
+    out = np.zeros(head_dim, np.uint8)
+    _check(lib().kv_codec_layer_signs(seed, layer, head_dim, out.ctypes.data_as(C.POINTER(C.c_uint8))),
+           "kv_codec_layer_signs")
     return out
 
 
@@ -146,7 +154,8 @@ class Codec:
     def __init__(self, *, dtype: str, layout: str, head_dim: int, num_kv_heads: int,
                  block_tokens: int, num_layers: int, num_blocks: int, strides: Sequence[int],
                  k_codec: str, v_codec: str, protect=(0, 0), rotation_seed: int = 0,
-                 reject_abs: float = 448.0, fixed_amax=None, geometry_overrides=None):
+                 reject_abs: float = 448.0, fixed_amax=None, sign_version: int = 1,
+                 geometry_overrides=None):
         g = Geometry()
         g.abi_version, g.struct_size = ABI_VERSION, C.sizeof(Geometry)
         g.dtype, g.layout = DT[dtype], LAYOUT[layout]
@@ -156,6 +165,7 @@ class Codec:
         g.k_codec, g.v_codec = CODEC[k_codec], CODEC[v_codec]
         g.protect_first, g.protect_last = protect
         g.rotation_seed, g.reject_abs = rotation_seed, reject_abs
+        g.sign_version = sign_version
         self._amax = None
         if fixed_amax is not None:
             self._amax = np.ascontiguousarray(np.asarray(fixed_amax, dtype=np.float32).reshape(-1))

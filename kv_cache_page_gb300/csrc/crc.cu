@@ -157,10 +157,10 @@ __device__ __forceinline__ bool slot_ok(const CrcParams& p, const kv_segment_des
   return off <= p.buf_bytes && p.seg_bytes[role] <= p.buf_bytes - off;
 }
 
-__device__ __forceinline__ void store_header(kv_segment_header* h, uint32_t format, uint64_t stored,
-                                             uint32_t crc, uint32_t status, uint64_t orig) {
+__device__ __forceinline__ void store_header(kv_segment_header* h, uint32_t version, uint32_t format,
+                                             uint64_t stored, uint32_t crc, uint32_t status, uint64_t orig) {
   uint64_t* w = reinterpret_cast<uint64_t*>(h);
-  w[0] = (uint64_t)KV_SEGMENT_FORMAT_VERSION | ((uint64_t)format << 32);
+  w[0] = (uint64_t)version | ((uint64_t)format << 32);
   w[1] = orig;
   w[2] = stored;
   w[3] = (uint64_t)crc | ((uint64_t)status << 32);
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kCrcThreads, 1) crc_seal_kernel(const __grid_c
     uint32_t role;
     uint64_t off;
     if (!slot_ok(p, p.descs + i, role, off)) {
-      if (lane == 0) store_header(p.headers + i, 0, 0, 0, KV_SEG_BAD_DESC, p.orig_bytes);
+      if (lane == 0) store_header(p.headers + i, p.version, 0, 0, 0, KV_SEG_BAD_DESC, p.orig_bytes);
       continue;
     }
     const uint32_t st = p.status[i];
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kCrcThreads, 1) crc_seal_kernel(const __grid_c
       stored = p.seg_bytes[role];
       crc = warp_crc(*t, tb, p.buf + off, (uint32_t)stored, p.crc_k[role], lane);
     }
-    if (lane == 0) store_header(p.headers + i, p.format[role], stored, crc, st, p.orig_bytes);
+    if (lane == 0) store_header(p.headers + i, p.version, p.format[role], stored, crc, st, p.orig_bytes);
   }
 }
 
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kCrcThreads, 1) crc_verify_kernel(const __grid
     const uint64_t stored = __ldg(reinterpret_cast<const unsigned long long*>(w + 2));
     const uint64_t w3 = __ldg(reinterpret_cast<const unsigned long long*>(w + 3));
     const uint32_t st = (uint32_t)(w3 >> 32);
-    bool ok = (uint32_t)w0 == KV_SEGMENT_FORMAT_VERSION && (uint32_t)(w0 >> 32) == p.format[role] &&
+    bool ok = (uint32_t)w0 == p.version && (uint32_t)(w0 >> 32) == p.format[role] &&
               orig == p.orig_bytes && st >= KV_SEG_ENCODED && st <= KV_SEG_BAD_DESC;
     if (ok && st == KV_SEG_ENCODED) {
       ok = stored == p.seg_bytes[role];

@@ -407,6 +407,19 @@ int kv_codec_signs(uint64_t seed, uint32_t head_dim, uint8_t* negate) {
   return KV_OK;
 }
 
+int kv_codec_layer_signs(uint64_t seed, uint32_t layer, uint32_t head_dim, uint8_t* negate) {
+  if (!negate || layer >= KV_CODEC_MAX_LAYERS) return KV_ERR_INVALID_ARG;
+  if (!supported_dim(head_dim)) return KV_ERR_UNSUPPORTED_HEAD_DIM;
+  const uint32_t W = (head_dim + 63) / 64;
+  uint64_t st = seed, w = 0;
+  for (uint64_t k = 0; k < (uint64_t)layer * W; ++k) splitmix_next(st);  // the layers below
+  for (uint32_t i = 0; i < head_dim; ++i) {
+    if ((i & 63u) == 0) w = splitmix_next(st);
+    negate[i] = (uint8_t)((w >> (i & 63u)) & 1u);
+  }
+  return KV_OK;
+}
+
 int kv_codec_create(const kv_codec_geometry* g, kv_codec_t* out) {
   if (!out) return KV_ERR_INVALID_ARG;
   *out = nullptr;
@@ -417,7 +430,7 @@ int kv_codec_create(const kv_codec_geometry* g, kv_codec_t* out) {
   if (g->layout != KV_LAYOUT_SEPARATE && g->layout != KV_LAYOUT_VLLM_PACKED) return KV_ERR_INVALID_ARG;
   if (!supported_dim(g->head_dim)) return KV_ERR_UNSUPPORTED_HEAD_DIM;
   if (g->num_layers == 0 || g->num_layers > KV_CODEC_MAX_LAYERS) return KV_ERR_TOO_MANY_LAYERS;
-  if (g->num_kv_heads == 0 || g->block_tokens == 0 || g->num_blocks == 0 || g->reserved0 != 0)
+  if (g->num_kv_heads == 0 || g->block_tokens == 0 || g->num_blocks == 0 || g->sign_version > 2)
     return KV_ERR_INVALID_ARG;
   const uint64_t nv = (uint64_t)g->num_kv_heads * g->block_tokens;
   if (nv > (1u << 20) || g->num_kv_heads > 4096) return KV_ERR_INVALID_ARG;
@@ -493,7 +506,8 @@ int kv_codec_create(const kv_codec_geometry* g, kv_codec_t* out) {
     }
     p.static_status[r] = st;
   }
-  sign_words(g->rotation_seed, p.D, p.sign_words);
+  p.sign_seed = g->rotation_seed;
+  p.sign_per_layer = g->sign_version == 2 ? 1u : 0u;
   if (is_tq(g->k_codec)) {
     const uint32_t bits = codec_bits(g->k_codec);
     make_codebook(bits, p.D, p.cent, p.bnd);
@@ -512,6 +526,7 @@ int kv_codec_create(const kv_codec_geometry* g, kv_codec_t* out) {
   c.L = p.L;
   c.num_blocks = p.num_blocks;
   c.orig_bytes = raw;
+  c.version = g->sign_version == 2 ? KV_SEGMENT_FORMAT_VERSION_2 : KV_SEGMENT_FORMAT_VERSION;
   uint32_t lg = 0;
   while ((1u << lg) < p.D) ++lg;
   for (int r = 0; r < 2; ++r) {

@@ -45,7 +45,9 @@ struct Params {
   float reject_abs;                     // admission bound
   float wht_scale;                      // fl32(1/sqrt(D))
   float neg_zero;                       // -0.0f (an FMA addend the compiler cannot fold)
-  uint32_t sign_words[8];               // TurboQuant sign bits, bit i = negate element i
+  uint64_t sign_seed;                   // TurboQuant sign stream (SplitMix64 seed)
+  uint32_t sign_per_layer;              // 1: format version 2, a sign vector per layer
+  uint32_t pad0;
   float cent[16];                       // TurboQuant centroids (K codec)
   float bnd[16];                        // TurboQuant boundaries (K codec), bnd[15] unused
   // Index table of the unscaled WHT output w: code(w) = lut_lo[c] + (w > lut_thr[c]),
@@ -95,6 +97,7 @@ struct CrcParams {
   uint32_t L;
   uint64_t num_blocks;
   uint32_t codec[2];
+  uint32_t version;                     // header version (the geometry's format version)
   uint32_t format[2];                   // header format word per role
   uint64_t seg_bytes[2];
   uint32_t crc_k[2];                    // CRC of a zero slot of seg_bytes[role] (preset and complement)

@@ -36,6 +36,27 @@ __device__ __forceinline__ uint32_t sign_mask_word(uint32_t bits, int k) {
   return (((bits >> (2 * k)) & 1u) << 15) | (((bits >> (2 * k + 1)) & 1u) << 31);
 }
 
+// Output k (k = 0, 1, ...) of the SplitMix64 stream seeded with `seed`
+// (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
+// OOPSLA 2014): the seed advanced by k + 1 golden-gamma increments, through
+// the variant-13 finalizer.
+__device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t k) {
+  uint64_t z = seed + (k + 1u) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Sign bits of elements 32 w .. 32 w + 31 (bit i = negate element 32 w + i)
+// of the TurboQuant sign vector of `layer`: bit i mod 64 of stream output
+// layer * ceil(D / 64) + i / 64 (format version 2), or of layer 0's outputs
+// for every layer (version 1).
+__device__ __forceinline__ uint32_t tq_sign_word(const Params& p, uint32_t layer, uint32_t w) {
+  const uint32_t per_layer = (p.D + 63u) / 64u;
+  const uint64_t z = splitmix64_at(p.sign_seed, (uint64_t)(p.sign_per_layer ? layer : 0u) * per_layer + (w >> 1));
+  return (w & 1u) ? (uint32_t)(z >> 32) : (uint32_t)z;
+}
+
 // Pairwise sum of the squares of pairs [M0, M0 + N) (2N elements), written
 // depth first so that few partial sums are live at a time.
 template <int M0, int N>
@@ -114,18 +135,6 @@ __device__ __forceinline__ uint32_t split_group_start(uint32_t li, int c) {
   return (uint32_t)((8 * c) & 15) | (li << 4) | ((uint32_t)(c >> 1) << (4 + J));
 }
 
-// Sign masks of the decoder's output layout: row li, group c covers the 8
-// elements from split_group_start<G>(li, c).
-template <int G>
-__device__ __forceinline__ void tq_sign_init_split(const Params& p, uint4 (&sign)[8][5]) {
-  for (int t = threadIdx.x; t < 8 * 4; t += blockDim.x) {
-    const uint32_t e0 = split_group_start<G>((uint32_t)(t >> 2), t & 3);
-    const uint32_t bits = e0 < p.D ? p.sign_words[e0 >> 5] : 0u;
-    const int k = (int)((e0 & 31u) >> 1);
-    sign[t >> 2][t & 3] = make_uint4(sign_mask_word(bits, k), sign_mask_word(bits, k + 1),
-                                     sign_mask_word(bits, k + 2), sign_mask_word(bits, k + 3));
-  }
-}
 
 
 // ---------------------------------------------------------------- 64 elements per lane
@@ -356,34 +365,34 @@ __global__ void __launch_bounds__(kTq64Threads, E == 64 ? 3 : 5) tq_encode_lanes
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
   __shared__ uint2 s_lut[NT][kLutCells * 16];
-  // sign masks of source word t (elements 2t, 2t + 1) of lane position l:
-  // BF16: [l][0][t] bit 31 = sign of element 2t, [l][1][t] bit 31 = sign of
-  // element 2t + 1; FP16: [l][0][t] bits 15 and 31.
-  // rows padded by 8 words: the lanes of a vector read different banks
-  __shared__ uint32_t s_mask[G][2 * NP + 8];
+  // each warp's sign masks of its current layer, source word t (elements 2t,
+  // 2t + 1) of lane position l: BF16: [l][t] bit 31 = sign of element 2t,
+  // [l][NP + t] bit 31 = sign of element 2t + 1; FP16: [l][t] bits 15 and 31.
+  // Rows padded by 8 words: the lanes of a vector read different banks.
+  __shared__ uint32_t s_mask[W][G][2 * NP + 8];
   for (int k = threadIdx.x; k < NT * kLutCells * 16; k += blockDim.x) {
     const int t = k / (kLutCells * 16), c = (k >> 4) % kLutCells;
     s_lut[t][k % (kLutCells * 16)] =
         t ? make_uint2(__float_as_uint(p.lut_mthr[c]), p.lut_mlo[c]) : make_uint2(__float_as_uint(p.lut_thr[c]), p.lut_lo[c]);
   }
-  for (int k = threadIdx.x; k < G * NP; k += blockDim.x) {
-    const uint32_t l = (uint32_t)k / NP, t = (uint32_t)k % NP;
-    const uint32_t e0 = l * E + 2u * t;
-    uint32_t s0 = (p.sign_words[e0 >> 5] >> (e0 & 31u)) & 1u;
-    uint32_t s1 = (p.sign_words[e0 >> 5] >> ((e0 + 1u) & 31u)) & 1u;
-    if (G >= 2 && (l & 1u) && t >= 16u) {  // the odd lane's inputs 32..63
-      s0 ^= 1u;
-      s1 ^= 1u;
-    }
-    if (DT == 1) {
-      s_mask[l][t] = s0 << 31;
-      s_mask[l][NP + t] = s1 << 31;
-    } else {
-      s_mask[l][t] = (s0 << 15) | (s1 << 31);
-      s_mask[l][NP + t] = 0u;
-    }
-  }
   __syncthreads();
+  // this warp's masks for `layer` (lanes of position li write row li)
+  auto build_masks = [&](uint32_t layer) {
+    __syncwarp();  // every lane is done with the previous layer's masks
+    for (uint32_t t = grp; t < (uint32_t)NP; t += VPW) {
+      const uint32_t e0 = li * E + 2u * t;
+      const uint32_t bits = tq_sign_word(p, layer, e0 >> 5);
+      uint32_t s0 = (bits >> (e0 & 31u)) & 1u, s1 = (bits >> ((e0 + 1u) & 31u)) & 1u;
+      if (G >= 2 && (li & 1u) && t >= 16u) {  // the odd lane's inputs 32..63
+        s0 ^= 1u;
+        s1 ^= 1u;
+      }
+      s_mask[warp][li][t] = DT == 1 ? s0 << 31 : (s0 << 15) | (s1 << 31);
+      s_mask[warp][li][NP + t] = DT == 1 ? s1 << 31 : 0u;
+    }
+    __syncwarp();
+  };
+  uint32_t mask_layer = 0xffffffffu;
   const uint32_t lane_off = (lane & 15u) * 8u + (uint32_t)(kLutHalf * 128) - kCellMagicBits * 128u;
   const uint32_t lut_d = (uint32_t)__cvta_generic_to_shared(&s_lut[0][0]) + lane_off;
   const uint32_t lut_m = (uint32_t)__cvta_generic_to_shared(&s_lut[NT - 1][0]) + lane_off;
@@ -391,7 +400,7 @@ __global__ void __launch_bounds__(kTq64Threads, E == 64 ? 3 : 5) tq_encode_lanes
   const uint32_t lut_a = neg_a ? lut_m : lut_d, lut_b = neg_b ? lut_m : lut_d;
   constexpr uint32_t kAll = BITS == 4 ? 0xffffffffu : (1u << (8 * BITS)) - 1u;
   const uint32_t cm_a = neg_a ? kAll : 0u, cm_b = neg_b ? kAll : 0u;
-  const uint32_t mask_addr = (uint32_t)__cvta_generic_to_shared(&s_mask[li][0]);
+  const uint32_t mask_addr = (uint32_t)__cvta_generic_to_shared(&s_mask[warp][li][0]);
   const uint32_t run_a = tq64_run_start<G>(li, 0), run_b = tq64_run_start<G>(li, 1);
   const uint32_t nv = p.nv;
   const bool v32 = p.vec32 != 0;
@@ -422,6 +431,11 @@ __global__ void __launch_bounds__(kTq64Threads, E == 64 ? 3 : 5) tq_encode_lanes
     uint8_t* codes = cur.slot;
     uint8_t* meta = cur.slot + (uint64_t)nv * CB;
     uint32_t flags = 0;
+    const uint32_t layer = p.sign_per_layer ? cur.layer : 0u;
+    if (layer != mask_layer) {
+      build_masks(layer);
+      mask_layer = layer;
+    }
     for (uint32_t j0 = 0; j0 < nv; j0 += VPW) {
       const uint32_t j = j0 + grp;
       // source words -> pairs, sign flips on the 16-bit values (exact)
@@ -610,27 +624,30 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
   static_assert(G >= 1 && G <= 4, "head dim 64 .. 256");
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
-  __shared__ uint4 s_sign[4][9];
+  // each warp's output sign masks of its current layer: row l, chunk c
+  __shared__ uint4 s_sign[W][4][9];
   // (centroid[lo code], centroid[hi code]) for every pair of codes, REP copies
   __shared__ float2 s_pair[NPAIR * REP];
-  for (int t = threadIdx.x; t < G * 8; t += blockDim.x) {
-    // output chunk c of lane l: elements A + 8c (c < 4) or B + 8(c - 4)
-    const uint32_t l = (uint32_t)t / 8, c = (uint32_t)t % 8;
-    const uint32_t e0 = tq64_run_start<G>(l, c < 4 ? 0 : 1) + 8u * (c & 3u);
-    const uint32_t bits = p.sign_words[e0 >> 5];
-    const int k = (int)((e0 & 31u) >> 1);
-    uint4 m = make_uint4(sign_mask_word(bits, k), sign_mask_word(bits, k + 1), sign_mask_word(bits, k + 2),
-                         sign_mask_word(bits, k + 3));
-    if (tq64_run_negated<G>(l, c < 4 ? 0 : 1)) m = xor4(m, 0x80008000u);  // negated runs
-    s_sign[l][c] = m;
-  }
+  auto build_signs = [&](uint32_t layer) {
+    __syncwarp();  // every lane is done with the previous layer's masks
+    for (uint32_t q = lane; q < (uint32_t)G * 32u; q += 32u) {
+      // word k4 of output chunk c of lane l: elements A + 8c (c < 4) or B + 8(c - 4), + 2 k4
+      const uint32_t l = q / 32u, c = (q % 32u) / 4u, k4 = q % 4u;
+      const uint32_t e0 = tq64_run_start<G>(l, c < 4 ? 0 : 1) + 8u * (c & 3u) + 2u * k4;
+      uint32_t m = sign_mask_word(tq_sign_word(p, layer, e0 >> 5), (int)((e0 & 31u) >> 1));
+      if (tq64_run_negated<G>(l, c < 4 ? 0 : 1)) m ^= 0x80008000u;  // negated runs
+      reinterpret_cast<uint32_t*>(&s_sign[warp][l][c])[k4] = m;
+    }
+    __syncwarp();
+  };
+  uint32_t sign_layer = 0xffffffffu;
   for (int k = threadIdx.x; k < NPAIR * REP; k += blockDim.x) {
     const int v = k / REP;
     s_pair[k] = make_float2(p.cent[v & ((1 << BITS) - 1)], p.cent[v >> BITS]);
   }
   __syncthreads();
   const uint32_t pair_base = (uint32_t)__cvta_generic_to_shared(s_pair) + (lane % REP) * 8u;
-  const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&s_sign[li][0]);
+  const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&s_sign[warp][li][0]);
   const uint32_t run_a = tq64_run_start<G>(li, 0), run_b = tq64_run_start<G>(li, 1);
   const uint32_t cmask = (G >= 2 && (li & 1u)) ? 0xffffffffu : 0u;  // complement the upper codes
   const bool vec32 = p.vec32 != 0;
@@ -677,6 +694,11 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
     Seg nxt;
     const uint32_t ni = cursor_next<kDecode>(p, cursor, nxt);
     uint16_t* page = const_cast<uint16_t*>(cur.page);
+    const uint32_t layer = p.sign_per_layer ? cur.layer : 0u;
+    if (layer != sign_layer) {
+      build_signs(layer);
+      sign_layer = layer;
+    }
     if (warp * VPW >= nv && ni != 0xffffffffu) fetch(nxt, jw, cwn, nn);
     for (uint32_t j0 = warp * VPW; j0 < nv; j0 += CSTEP) {
       const uint32_t j = j0 + grp;
@@ -756,17 +778,29 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
   constexpr int REP = 16;                       // copies: each lane of a half warp has its own banks
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
-  __shared__ uint4 s_sign[8][5];
+  // each warp's output sign masks of its current layer: row li, group c covers
+  // the 8 elements from split_group_start<G>(li, c)
+  __shared__ uint4 s_sign[W][G][5];
   // (centroid[lo code], centroid[hi code]) for every pair of codes, REP copies
   __shared__ float2 s_pair[NPAIR * REP];
-  tq_sign_init_split<G>(p, s_sign);
+  auto build_signs = [&](uint32_t layer) {
+    __syncwarp();  // every lane is done with the previous layer's masks
+    for (uint32_t q = lane; q < (uint32_t)G * 16u; q += 32u) {
+      const uint32_t l = q / 16u, c = (q % 16u) / 4u, k4 = q % 4u;
+      const uint32_t e0 = split_group_start<G>(l, (int)c) + 2u * k4;
+      reinterpret_cast<uint32_t*>(&s_sign[warp][l][c])[k4] =
+          sign_mask_word(tq_sign_word(p, layer, e0 >> 5), (int)((e0 & 31u) >> 1));
+    }
+    __syncwarp();
+  };
+  uint32_t sign_layer = 0xffffffffu;
   for (int k = threadIdx.x; k < NPAIR * REP; k += blockDim.x) {
     const int v = k / REP;
     s_pair[k] = make_float2(p.cent[v & ((1 << BITS) - 1)], p.cent[v >> BITS]);
   }
   __syncthreads();
   const uint32_t pair_base = (uint32_t)__cvta_generic_to_shared(s_pair) + (lane % REP) * 8u;
-  const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&s_sign[li][0]);
+  const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&s_sign[warp][li][0]);
   const float cD = p.wht_scale;
   const float2 cD2 = make_float2(cD, cD);
   const uint32_t nv = p.nv;
@@ -805,6 +839,11 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
     Seg nxt;
     const uint32_t ni = cursor_next<kDecode>(p, cursor, nxt);
     uint16_t* page = const_cast<uint16_t*>(cur.page);
+    const uint32_t layer = p.sign_per_layer ? cur.layer : 0u;
+    if (layer != sign_layer) {
+      build_signs(layer);
+      sign_layer = layer;
+    }
     if (warp * VPW >= nv && ni != 0xffffffffu) fetch(nxt, jw, cwn, nn);
     for (uint32_t j0 = warp * VPW; j0 < nv; j0 += CSTEP) {
       const uint32_t j = j0 + grp;

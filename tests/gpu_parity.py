@@ -20,13 +20,13 @@ SENTINEL_ENC = 0xAB
 SENTINEL_PAGE = 0x7BCD  # an ordinary finite value, never produced by chance in bulk
 
 
-def make_codec(case: synth.Case, arm: synth.Arm, reject_abs=448.0) -> K.Codec:
+def make_codec(case: synth.Case, arm: synth.Arm, reject_abs=448.0, sign_version=1) -> K.Codec:
     return K.Codec(dtype="fp16" if case.dtype == torch.float16 else "bf16", layout=case.layout,
                    head_dim=case.head_dim, num_kv_heads=case.num_heads,
                    block_tokens=case.block_tokens, num_layers=case.num_layers,
                    num_blocks=case.num_blocks, strides=case.strides, k_codec=arm.k_codec,
                    v_codec=arm.v_codec, protect=arm.protect, rotation_seed=case.seed,
-                   reject_abs=reject_abs,
+                   reject_abs=reject_abs, sign_version=sign_version,
                    fixed_amax=None if case.fixed_amax is None else case.fixed_amax.numpy())
 
 
@@ -73,15 +73,16 @@ def _offset_layer(t: torch.Tensor, device, offset_bytes: int) -> torch.Tensor:
 
 
 def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="cuda",
-               reject_abs=448.0, check_decode=True, buffers="device", layer_offset=0):
+               reject_abs=448.0, check_decode=True, buffers="device", layer_offset=0, sign_version=1):
     """Encode + decode `case` with `arm` on the GPU and in the oracle; assert parity.
     buffers="host" keeps descriptors, slots, statuses and results in pinned host
     memory (the kernels read and write them over the host link).  layer_offset
     places the source and restored layer tensors that many bytes past an aligned
     allocation (16: the 16-byte alignment the library requires, not 32).
+    sign_version 2: TurboQuant sign vectors per layer (format version 2).
     Returns (status array, number of restored elements off by one ulp)."""
-    codec = make_codec(case, arm, reject_abs)
-    g = oracle_geom(case, arm, reject_abs)
+    codec = make_codec(case, arm, reject_abs, sign_version)
+    g = oracle_geom(case, arm, reject_abs, sign_version)
     seg = [codec.segment_bytes(r)[0] for r in (0, 1)]
     assert seg == [0 if c == "none" else O.segment_enc_bytes(g, r)
                    for r, c in enumerate((arm.k_codec, arm.v_codec))]
@@ -132,11 +133,11 @@ def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="
     return st_ref, ulps
 
 
-def run_seal_parity(case: synth.Case, arm: synth.Arm, device="cuda"):
+def run_seal_parity(case: synth.Case, arm: synth.Arm, device="cuda", sign_version=1):
     """Encode on the GPU, seal the slots (CRC-32 headers) and verify them; the
     headers must equal the oracle's bit for bit and verify must pass every
     segment's status through.  Returns the number of sealed ENCODED slots."""
-    codec = make_codec(case, arm)
+    codec = make_codec(case, arm, sign_version=sign_version)
     seg = [codec.segment_bytes(r)[0] for r in (0, 1)]
     rows, total = synth.segment_list(case, arm, seg)
     n = len(rows)
@@ -150,7 +151,7 @@ def run_seal_parity(case: synth.Case, arm: synth.Arm, device="cuda"):
     codec.seal(descs, n, enc, total, st, hdr)
     codec.verify(descs, n, enc, total, hdr, res)
     torch.cuda.synchronize()
-    g = oracle_geom(case, arm)
+    g = oracle_geom(case, arm, sign_version=sign_version)
     st_h = st.cpu().numpy()[:n]
     want = O.seal(g, oracle_descs(rows), enc.cpu().numpy()[:total], st_h)
     assert np.array_equal(hdr.cpu().numpy()[:32 * n], want.view(np.uint8)), "headers differ"

@@ -70,7 +70,7 @@ def _kw(**over):
     (dict(k_codec="fp8_fixed", v_codec="fp8_fixed"), -1),    # fixed scales missing
     (dict(geometry_overrides={"abi_version": 2}), -7),
     (dict(geometry_overrides={"struct_size": 96}), -7),
-    (dict(geometry_overrides={"reserved0": 1}), -1),
+    (dict(sign_version=3), -1),
     (dict(num_kv_heads=0), -1),
     (dict(num_blocks=0), -1),
 ])
@@ -152,6 +152,29 @@ def test_codebook_bitwise_equal_to_oracle(bits, D):
 @pytest.mark.parametrize("seed", [0, 1, 12345, 2**64 - 1])
 def test_signs_equal_to_oracle(D, seed):
     assert np.array_equal(K.signs(seed, D), O.signs(seed, D))
+
+
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+@pytest.mark.parametrize("seed", [0, 99, 2**64 - 1])
+def test_layer_signs_equal_to_oracle(D, seed):
+    for layer in (0, 1, 7, 511):
+        assert np.array_equal(K.layer_signs(seed, layer, D), O.signs_layer(seed, layer, D)), layer
+    assert np.array_equal(K.layer_signs(seed, 0, D), K.signs(seed, D))
+
+
+def test_layer_signs_refuse_bad_arguments():
+    with pytest.raises(K.KvCodecError):
+        K.layer_signs(0, 512, 64)
+    with pytest.raises(K.KvCodecError):
+        K.layer_signs(0, 0, 48)
+
+
+@pytest.mark.parametrize("v", [0, 1, 2])
+def test_sign_versions_accepted(v):
+    c = K.Codec(dtype="bf16", layout="separate", head_dim=128, num_kv_heads=8, block_tokens=16,
+                num_layers=4, num_blocks=2, strides=(16 * 8 * 128, 8 * 128, 128), k_codec="tq4",
+                v_codec="uni4", sign_version=v)
+    c.close()
 
 
 def test_call_argument_checks_need_no_gpu():

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle as O
-from gpu_parity import SENTINEL_PAGE, make_codec
+from gpu_parity import SENTINEL_PAGE, make_codec, run_seal_parity
 from kv_cache_page_gb300 import codec as K
 from kv_cache_page_gb300 import synth
 from kvcases import host_bits, oracle_descs, oracle_geom
@@ -164,3 +164,10 @@ def test_host_resident_slots_and_headers():
     assert np.array_equal(hdr.numpy()[: 32 * n], want.view(np.uint8))
     assert np.all(res.numpy() == O.S_ENCODED)
     codec.close()
+
+
+def test_headers_carry_format_version_2():
+    """Sealed headers of a format-version-2 geometry carry version 2, equal to
+    the oracle's, and verify passes them."""
+    case = synth.make_case("vllm_packed", num_layers=5, num_blocks=3)
+    assert run_seal_parity(case, case.arms[0], sign_version=2) > 0

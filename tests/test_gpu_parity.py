@@ -388,3 +388,29 @@ def test_repeat_calls_are_deterministic():
         a, _ = run_parity(case, arm)
         b, _ = run_parity(case, arm)
         assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("kc,vc", [("tq4", "uni4"), ("tq3", "uni3"), ("tq2", "uni2")])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("layout", ["separate", "packed"])
+def test_per_layer_signs(kc, vc, D, dtype, layout):
+    """Format version 2: every layer codes K with its own sign vector (the
+    kernels generate the layer's words from the seed); 6 layers, ragged
+    segments (H=3, T=11), several segments per warp and layer changes between
+    them."""
+    case = custom_case(D=D, H=3, T=11, L=6, B=7, dtype=dtype, layout=layout,
+                       values="heavy" if dtype == "bf16" else "normal", seed=D + 1)
+    arm = synth.Arm("v2", kc, vc, (0, 1))
+    st, ulps = run_parity(case, arm, sign_version=2)
+    assert np.all(st == O.S_ENCODED) and ulps == 0
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_per_layer_signs_full_pages(D):
+    """Format version 2 on whole 16-token pages of 8 heads across 36 layers."""
+    case = custom_case(D=D, H=8, T=16, L=36, B=3, dtype="fp16", layout="separate", seed=5)
+    for kc, vc in (("tq4", "uni4"), ("tq3", "none")):
+        st, ulps = run_parity(case, synth.Arm("v2", kc, vc, (0, 1) if vc != "none" else (0,)),
+                              sign_version=2)
+        assert np.all(st == O.S_ENCODED) and ulps == 0
