@@ -228,7 +228,12 @@ def run_gpu(args, dist, world, rank, local):
     case = synth.make_case(args.workload, device=device, seed=args.seed, num_layers=args.layers,
                            num_blocks=args.pages, head_dim=args.head_dim)
     part = (world, rank) if args.partition else None
-    arms = [Arm(case, a, case.layers, device, part) for a in case.arms
+    arm_list = case.arms
+    if args.codecs:  # profiling: one arm with the given K and V codecs on this workload's pages
+        kc, vc = args.codecs.split(",")
+        roles = tuple(r for r, c in ((0, kc), (1, vc)) if c != "none")
+        arm_list = [synth.Arm(f"{kc}+{vc}", kc, vc, roles, case.arms[0].protect)]
+    arms = [Arm(case, a, case.layers, device, part) for a in arm_list
             if args.arm is None or a.name == args.arm]
     stream = torch.cuda.current_stream(device)
 
@@ -321,7 +326,7 @@ def run_gpu(args, dist, world, rank, local):
         "host_link": host_link,
         "integrity": integrity,
     }
-    shrunk = args.layers is not None or args.pages is not None or args.arm is not None
+    shrunk = args.layers is not None or args.pages is not None or args.arm is not None or bool(args.codecs)
     if shrunk:
         result["config"]["reduced"] = True
     if args.extra and world == 1 and not shrunk:
@@ -730,6 +735,8 @@ def main(argv=None):
     ap.add_argument("--pages", type=int, default=None, help="pages per layer (profiling)")
     ap.add_argument("--head-dim", type=int, default=None, help="head_dim_sweep point")
     ap.add_argument("--arm", default=None, help="run only this codec arm")
+    ap.add_argument("--codecs", default=None,
+                    help="profiling: replace the workload's arms by one arm 'K,V' (codec names)")
     ap.add_argument("--no-extra", dest="extra", action="store_false")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
