@@ -618,7 +618,6 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
   constexpr int E = 64, G = D / E, VPW = 32 / G, W = kTq64Threads / 32;
   constexpr int CB = D * BITS / 8;
   constexpr int NW = 2 * BITS;                  // code words of a lane (64 codes)
-  constexpr uint32_t CSTEP = W * VPW;
   constexpr int NPAIR = 1 << (2 * BITS);        // table of two consecutive codes
   constexpr int REP = 16;                       // copies: each lane of a half warp has its own banks
   static_assert(G >= 1 && G <= 4, "head dim 64 .. 256");
@@ -654,7 +653,7 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
   const float cD = p.wht_scale;
   const float2 cD2 = make_float2(cD, cD);
   const uint32_t nv = p.nv;
-  const uint32_t jw = warp * VPW + grp;
+  const uint32_t jw = grp;  // one warp per segment: this lane's first vector
 
   // codes and norm of vector j of segment s (registers; issued ahead of use)
   auto fetch = [&](const Seg& s, uint32_t j, uint32_t (&cw)[NW], uint16_t& n16) {
@@ -682,9 +681,9 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
   };
 
   SegCursor cursor;
-  cursor_init(cursor);
+  warp_cursor_init(cursor, W);
   Seg cur;
-  uint32_t ci = cursor_next<kDecode>(p, cursor, cur);
+  uint32_t ci = cursor_next<kDecode, true>(p, cursor, cur);
   uint32_t cwn[NW];
   uint16_t nn = 0;
 #pragma unroll
@@ -692,21 +691,20 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
   if (ci != 0xffffffffu) fetch(cur, jw, cwn, nn);
   while (ci != 0xffffffffu) {
     Seg nxt;
-    const uint32_t ni = cursor_next<kDecode>(p, cursor, nxt);
+    const uint32_t ni = cursor_next<kDecode, true>(p, cursor, nxt);
     uint16_t* page = const_cast<uint16_t*>(cur.page);
     const uint32_t layer = p.sign_per_layer ? cur.layer : 0u;
     if (layer != sign_layer) {
       build_signs(layer);
       sign_layer = layer;
     }
-    if (warp * VPW >= nv && ni != 0xffffffffu) fetch(nxt, jw, cwn, nn);
-    for (uint32_t j0 = warp * VPW; j0 < nv; j0 += CSTEP) {
+    for (uint32_t j0 = 0; j0 < nv; j0 += VPW) {
       const uint32_t j = j0 + grp;
       uint32_t cw[NW];
 #pragma unroll
       for (int k = 0; k < NW; ++k) cw[k] = k < NW / 2 ? cwn[k] : cwn[k] ^ cmask;
       const uint16_t n16 = nn;
-      if (j0 + CSTEP < nv) fetch(cur, j + CSTEP, cwn, nn);
+      if (j0 + VPW < nv) fetch(cur, j + VPW, cwn, nn);
       else if (ni != 0xffffffffu) fetch(nxt, jw, cwn, nn);
       float2 a[32];
 #pragma unroll
@@ -763,7 +761,7 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
         }
       }
     }
-    if (threadIdx.x == 0 && p.result) p.result[ci] = KV_SEG_ENCODED;
+    if (lane == 0 && p.result) p.result[ci] = KV_SEG_ENCODED;
     cur = nxt;
     ci = ni;
   }
@@ -773,7 +771,6 @@ template <int DT, int D, int BITS>
 __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_constant__ Params p) {
   constexpr int G = D / kTqE, VPW = 32 / G, W = kThreads / 32;
   constexpr int CB = D * BITS / 8;
-  constexpr uint32_t CSTEP = W * VPW;
   constexpr int NPAIR = 1 << (2 * BITS);        // table of two consecutive codes
   constexpr int REP = 16;                       // copies: each lane of a half warp has its own banks
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
@@ -804,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
   const float cD = p.wht_scale;
   const float2 cD2 = make_float2(cD, cD);
   const uint32_t nv = p.nv;
-  const uint32_t jw = warp * VPW + grp;
+  const uint32_t jw = grp;  // one warp per segment: this lane's first vector
   const bool vec32 = p.vec32 != 0;
 
   // codes and norm of vector j of segment s (registers; issued ahead of use)
@@ -829,27 +826,26 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
   };
 
   SegCursor cursor;
-  cursor_init(cursor);
+  warp_cursor_init(cursor, W);
   Seg cur;
-  uint32_t ci = cursor_next<kDecode>(p, cursor, cur);
+  uint32_t ci = cursor_next<kDecode, true>(p, cursor, cur);
   uint32_t cwn[4] = {0, 0, 0, 0};
   uint16_t nn = 0;
   if (ci != 0xffffffffu) fetch(cur, jw, cwn, nn);
   while (ci != 0xffffffffu) {
     Seg nxt;
-    const uint32_t ni = cursor_next<kDecode>(p, cursor, nxt);
+    const uint32_t ni = cursor_next<kDecode, true>(p, cursor, nxt);
     uint16_t* page = const_cast<uint16_t*>(cur.page);
     const uint32_t layer = p.sign_per_layer ? cur.layer : 0u;
     if (layer != sign_layer) {
       build_signs(layer);
       sign_layer = layer;
     }
-    if (warp * VPW >= nv && ni != 0xffffffffu) fetch(nxt, jw, cwn, nn);
-    for (uint32_t j0 = warp * VPW; j0 < nv; j0 += CSTEP) {
+    for (uint32_t j0 = 0; j0 < nv; j0 += VPW) {
       const uint32_t j = j0 + grp;
       const uint32_t cw[4] = {cwn[0], cwn[1], cwn[2], cwn[3]};
       const uint16_t n16 = nn;
-      if (j0 + CSTEP < nv) fetch(cur, j + CSTEP, cwn, nn);
+      if (j0 + VPW < nv) fetch(cur, j + VPW, cwn, nn);
       else if (ni != 0xffffffffu) fetch(nxt, jw, cwn, nn);
       float2 a[16];
 #pragma unroll
@@ -894,7 +890,7 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
         }
       }
     }
-    if (threadIdx.x == 0 && p.result) p.result[ci] = KV_SEG_ENCODED;
+    if (lane == 0 && p.result) p.result[ci] = KV_SEG_ENCODED;
     cur = nxt;
     ci = ni;
   }
@@ -909,9 +905,9 @@ int encode(const Params& p, void* stream) {
 template <int DT, int D, int BITS>
 int decode(const Params& p, void* stream) {
   if constexpr (D >= 64)
-    return launch_codec_kernel(tq_decode64_kernel<DT, D, BITS>, p, stream, 8, kTq64Threads);
+    return launch_codec_kernel(tq_decode64_kernel<DT, D, BITS>, p, stream, 8, kTq64Threads, true);
   else
-    return launch_codec_kernel(tq_decode_kernel<DT, D, BITS>, p, stream, 8);
+    return launch_codec_kernel(tq_decode_kernel<DT, D, BITS>, p, stream, 8, kThreads, true);
 }
 
 template <int DT, int D>
