@@ -627,6 +627,9 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
   __shared__ uint4 s_sign[W][4][9];
   // (centroid[lo code], centroid[hi code]) for every pair of codes, REP copies
   __shared__ float2 s_pair[NPAIR * REP];
+  // D = 64 (one lane per vector): 16 restored vectors of each warp at a time,
+  // 128 bytes a row, 16-byte chunk q of row r at position q ^ (r & 7)
+  __shared__ uint4 s_out[G == 1 ? W : 1][G == 1 ? 16 : 1][8];
   auto build_signs = [&](uint32_t layer) {
     __syncwarp();  // every lane is done with the previous layer's masks
     for (uint32_t q = lane; q < (uint32_t)G * 32u; q += 32u) {
@@ -650,6 +653,9 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
   const uint32_t run_a = tq64_run_start<G>(li, 0), run_b = tq64_run_start<G>(li, 1);
   const uint32_t cmask = (G >= 2 && (li & 1u)) ? 0xffffffffu : 0u;  // complement the upper codes
   const bool vec32 = p.vec32 != 0;
+  // one lane per vector and the warp's vectors side by side in the page:
+  // stage them and store 1 KB runs (8 cache lines a store instead of 32)
+  const bool stage_out = G == 1 && vec32 && p.heads_contig != 0 && p.sh == (int64_t)D;
   const float cD = p.wht_scale;
   const float2 cD2 = make_float2(cD, cD);
   const uint32_t nv = p.nv;
@@ -742,7 +748,28 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
           o[4 * c + k] = pack2<DT>(t.x, t.y) ^ mk[k];
         }
       }
-      if (j < nv) {
+      if (G == 1 && stage_out && j0 + VPW <= nv) {
+        uint16_t* base = page + vec_off(p, j0);  // the warp's 32 vectors, 64 elements apart
+#pragma unroll
+        for (uint32_t half = 0; half < 2; ++half) {
+          __syncwarp();  // the previous reads of the stage are done
+          if ((lane >> 4) == half) {
+            const uint32_t r = lane & 15u;
+#pragma unroll
+            for (uint32_t q = 0; q < 8; ++q)
+              s_out[G == 1 ? warp : 0][G == 1 ? r : 0][q ^ (r & 7u)] =
+                  make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          }
+          __syncwarp();
+#pragma unroll
+          for (uint32_t kk = 0; kk < 2; ++kk) {  // rows 8 kk .. 8 kk + 7, four lanes a row
+            const uint32_t r = 8u * kk + (lane >> 2), c = 2u * (lane & 3u);
+            const uint4 lo = s_out[G == 1 ? warp : 0][G == 1 ? r : 0][c ^ (r & 7u)];
+            const uint4 hi = s_out[G == 1 ? warp : 0][G == 1 ? r : 0][(c + 1u) ^ (r & 7u)];
+            st32(base + (uint64_t)(16u * half + r) * D + 8u * c, lo, hi);
+          }
+        }
+      } else if (j < nv) {
         uint16_t* dst = page + vec_off(p, j);
         if (vec32) {  // 32 bytes per store: twice the bytes per line of each warp store
 #pragma unroll
