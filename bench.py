@@ -517,11 +517,31 @@ def run_host_link(args, arms, stream):
     return out
 
 
+def _median_ms(fn, stream, reps):
+    """Median CUDA-event time of fn() on `stream` after two untimed calls."""
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
 def run_integrity(args, arms, stream, peak):
-    """Segment headers (CRC-32 of every encoded slot): seal after encode and
-    verify before decode, per arm.  Median CUDA-event time on the launching
-    stream; GB/s of slot bytes checked and, against the HBM peak, of algorithmic
-    bytes (slots read + 32-byte headers written or read + descriptors)."""
+    """Segment headers (CRC-32 of every encoded slot), per arm.  seal / verify:
+    the standalone passes after encode and before decode -- GB/s of slot bytes
+    checked and, against the HBM peak, of algorithmic bytes (slots read +
+    32-byte headers written or read + descriptors).  one_pass: encode_sealed
+    against plain encode and decode_verified against plain decode on the same
+    buffers (one pass over the slots when every coded role is FP8), with the
+    time each adds.  Median CUDA-event times on the launching stream."""
     out = {}
     reps = max(3, min(args.steps, 20))
     for a in arms:
@@ -533,24 +553,26 @@ def run_integrity(args, arms, stream, peak):
         row = {}
         for tag, fn in (("seal", lambda: a.codec.seal(a.descs, a.n, a.enc, a.total, a.status, hdr, stream)),
                         ("verify", lambda: a.codec.verify(a.descs, a.n, a.enc, a.total, hdr, res, stream))):
-            for _ in range(2):
-                fn()
-            torch.cuda.synchronize()
-            ts = []
-            for _ in range(reps):
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                fn()
-                e1.record(stream)
-                torch.cuda.synchronize()
-                ts.append(e0.elapsed_time(e1))
-            ms = statistics.median(ts)
+            ms = _median_ms(fn, stream, reps)
             row[tag] = {"ms": round(ms, 4), "slot_gbs": round(slot_bytes / (ms / 1e3) / GB, 1),
                         "frac_of_hbm": round(alg / (ms / 1e3) / GB / peak, 4)}
         ok = int((res == K.SEG_ENCODED).sum())
         row["verified_encoded"] = ok
         row["slot_bytes"] = slot_bytes
+        t = {
+            "encode": _median_ms(lambda: a.encode(stream), stream, reps),
+            "encode_sealed": _median_ms(lambda: a.codec.encode_sealed(
+                a.src_view, a.descs, a.n, a.enc, a.total, a.status, hdr, stream), stream, reps),
+            "decode": _median_ms(lambda: a.decode(stream), stream, reps),
+            "decode_verified": _median_ms(lambda: a.codec.decode_verified(
+                a.dst_view, a.descs, a.n, a.enc, a.total, hdr, res, stream), stream, reps),
+        }
+        one = {k + "_ms": round(v, 4) for k, v in t.items()}
+        one["seal_adds"] = round(t["encode_sealed"] / t["encode"] - 1.0, 4)
+        one["verify_adds"] = round(t["decode_verified"] / t["decode"] - 1.0, 4)
+        one["one_pass"] = all(c.startswith("fp8") or c == "none" for c in (a.arm.k_codec, a.arm.v_codec))
+        one["restored"] = int((res == K.SEG_ENCODED).sum())
+        row["one_pass"] = one
         out[a.arm.name] = row
         del hdr, res
     return out

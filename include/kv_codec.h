@@ -75,6 +75,8 @@ extern "C" {
 
 #define KV_CODEC_ABI_VERSION 1u
 #define KV_CODEC_MAX_LAYERS 512u
+/* Largest n_segments of one call (larger counts return KV_ERR_INVALID_ARG). */
+#define KV_CODEC_MAX_SEGMENTS 0x7FFFFFFFu
 
 /* ---- return codes ------------------------------------------------------ */
 #define KV_OK 0
@@ -256,6 +258,33 @@ int kv_codec_seal(kv_codec_t codec, const kv_segment_desc* descs, uint32_t n_seg
 int kv_codec_verify(kv_codec_t codec, const kv_segment_desc* descs, uint32_t n_segments,
                     const void* buf, uint64_t buf_bytes, const kv_segment_header* headers,
                     uint8_t* result, void* stream);
+
+/* Encode and seal in one call (section "Ownership, storage and GDS": a CRC32
+ * per stored segment).  Slots, statuses and headers equal those of
+ * kv_codec_encode followed by kv_codec_seal on the same arguments.  When every
+ * coded role takes an FP8 codec this is one pass: each slot's CRC-32 is taken
+ * by the warp that encoded it, from the bytes it has just written, so HBM
+ * carries the slots once; other codecs run encode, then seal.  Arguments as
+ * for kv_codec_encode, plus headers (n records, 8-byte aligned, device or
+ * pinned host memory). */
+int kv_codec_encode_sealed(kv_codec_t codec, const void* const* layer_ptrs, uint32_t n_layer_ptrs,
+                           const kv_segment_desc* descs, uint32_t n_segments, void* out,
+                           uint64_t out_bytes, uint8_t* status, kv_segment_header* headers,
+                           void* stream);
+
+/* Verify and decode in one call (same section: checksums validated before GPU
+ * decode, a damaged object becomes a miss).  result[i] and the restored pages
+ * equal those of kv_codec_verify into result followed by kv_codec_decode with
+ * status = result and d_result = result: a segment whose header or CRC-32 does
+ * not match is reported KV_SEG_CORRUPT and its page is not written.  When every
+ * coded role takes an FP8 codec this is one pass: the warp that checks a slot
+ * then restores it, re-reading the slot from L2.  Arguments as for
+ * kv_codec_decode, with the headers in place of the statuses and result (n
+ * bytes) required. */
+int kv_codec_decode_verified(kv_codec_t codec, void* const* layer_ptrs, uint32_t n_layer_ptrs,
+                             const kv_segment_desc* descs, uint32_t n_segments, const void* in,
+                             uint64_t in_bytes, const kv_segment_header* headers, uint8_t* result,
+                             void* stream);
 
 /* Static description of an error code. */
 const char* kv_codec_strerror(int code);

@@ -35,7 +35,7 @@ DESC_DTYPE = np.dtype([("layer", "<u4"), ("block", "<u4"), ("role", "<u4"),
 EXPORTS = ("kv_codec_create", "kv_codec_destroy", "kv_codec_segment_bytes", "kv_codec_encode",
            "kv_codec_decode", "kv_codec_seal", "kv_codec_verify", "kv_codec_strerror",
            "kv_codec_codebook", "kv_codec_signs", "kv_codec_layer_signs",
-           "kv_codec_abi_version")
+           "kv_codec_abi_version", "kv_codec_encode_sealed", "kv_codec_decode_verified")
 
 
 class Geometry(C.Structure):
@@ -76,6 +76,10 @@ def lib():
                                       vp, vp]
         L.kv_codec_seal.argtypes = [vp, vp, C.c_uint32, vp, C.c_uint64, vp, vp, vp]
         L.kv_codec_verify.argtypes = [vp, vp, C.c_uint32, vp, C.c_uint64, vp, vp, vp]
+        L.kv_codec_encode_sealed.argtypes = [vp, C.POINTER(vp), C.c_uint32, vp, C.c_uint32, vp, C.c_uint64,
+                                             vp, vp, vp]
+        L.kv_codec_decode_verified.argtypes = [vp, C.POINTER(vp), C.c_uint32, vp, C.c_uint32, vp,
+                                               C.c_uint64, vp, vp, vp]
         L.kv_codec_strerror.argtypes = [C.c_int]
         L.kv_codec_strerror.restype = C.c_char_p
         L.kv_codec_codebook.argtypes = [C.c_uint32, C.c_uint32, C.POINTER(C.c_float), C.POINTER(C.c_float)]
@@ -230,6 +234,25 @@ class Codec:
         Buffers: device or pinned host tensors."""
         _check(lib().kv_codec_seal(self._h, _ptr(descs), n_segments, _ptr(buf), buf_bytes, _ptr(status),
                                    _ptr(headers), _stream_handle(stream)), "kv_codec_seal")
+
+    def encode_sealed(self, layers, descs, n_segments: int, out, out_bytes: int, status, headers,
+                      stream=None):
+        """encode followed by seal, in one pass over the slots when every coded role is
+        FP8 (the encoding warp checksums the slot it has just written)."""
+        arr, n = self._layer_array(layers)
+        _check(lib().kv_codec_encode_sealed(self._h, arr, n, _ptr(descs), n_segments, _ptr(out), out_bytes,
+                                            _ptr(status), _ptr(headers), _stream_handle(stream)),
+               "kv_codec_encode_sealed")
+
+    def decode_verified(self, layers, descs, n_segments: int, enc, enc_bytes: int, headers, result,
+                        stream=None):
+        """verify followed by decode of the verified segments: result[i] as verify gives
+        it (SEG_ENCODED once restored); a segment failing its header or CRC-32 check is
+        SEG_CORRUPT and its page is left untouched.  One pass when every coded role is FP8."""
+        arr, n = self._layer_array(layers)
+        _check(lib().kv_codec_decode_verified(self._h, arr, n, _ptr(descs), n_segments, _ptr(enc),
+                                              enc_bytes, _ptr(headers), _ptr(result), _stream_handle(stream)),
+               "kv_codec_decode_verified")
 
     def verify(self, descs, n_segments: int, buf, buf_bytes: int, headers, result, stream=None):
         """Check slots against their headers: result[i] = the header's status, or

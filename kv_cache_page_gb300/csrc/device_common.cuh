@@ -37,8 +37,16 @@ struct Seg {
 // Ownership: a launch that codes one role (role_sel 0 or 1) owns the
 // descriptors of that role; the first launch also owns descriptors with an
 // invalid role or a role without codec.  Descriptors of the other coded role
-// are skipped after reading just the role field.
-__device__ __forceinline__ Seg plan_segment(const Params& p, uint32_t i, int dir) {
+// are skipped after reading just the role field.  Decode takes the segment's
+// status from `given` when it is not negative, else from p.status (a coherent
+// load when p.status is the result array this launch writes, each entry
+// rewritten only by its owner with a value that leads to the same plan).
+__device__ __forceinline__ bool owns_segment(const Params& p, uint32_t role) {
+  const bool coded_role = role <= 1u && p.codec[role] != KV_CODEC_NONE;
+  return coded_role ? (p.role_sel == 2u || role == p.role_sel) : (p.is_first != 0u);
+}
+
+__device__ __forceinline__ Seg plan_segment(const Params& p, uint32_t i, int dir, int given = -1) {
   Seg s;
   const kv_segment_desc* dp = p.descs + i;
   // all fields in one round trip
@@ -50,8 +58,7 @@ __device__ __forceinline__ Seg plan_segment(const Params& p, uint32_t i, int dir
   s.slot = nullptr;
   s.status = 0;
   const bool coded_role = role <= 1u && p.codec[role] != KV_CODEC_NONE;
-  const bool owner = coded_role ? (p.role_sel == 2u || role == p.role_sel) : (p.is_first != 0u);
-  if (!owner) {
+  if (!owns_segment(p, role)) {
     s.action = kSkip;
     return s;
   }
@@ -81,7 +88,9 @@ __device__ __forceinline__ Seg plan_segment(const Params& p, uint32_t i, int dir
       return s;
     }
   } else {
-    const uint8_t st = __ldg(p.status + i);
+    const uint8_t st = given >= 0          ? (uint8_t)given
+                       : p.status_is_result ? *(const volatile uint8_t*)(p.status + i)
+                                            : __ldg(p.status + i);
     if (st != (uint8_t)KV_SEG_ENCODED) {
       s.status = st;
       return s;
@@ -163,11 +172,19 @@ __device__ __forceinline__ int64_t vec_off(const Params& p, uint32_t j) {
 }
 
 // ---------------------------------------------------------------- memory
+// V: volatile, so that the load stays ahead of later volatile asm (table
+// reads a kernel overlaps with the load's latency)
+template <bool V = false>
 __device__ __forceinline__ uint4 ld_stream16(const void* ptr) {
   uint4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(ptr));
+  if (V)
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr));
+  else
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(ptr));
   return v;
 }
 // read-only 16-byte load that allocates in L1 (for lanes reading 64-byte
@@ -184,6 +201,22 @@ __device__ __forceinline__ void ld_nc32(const void* ptr, uint4& a, uint4& b) {
   asm("ld.global.nc.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
       : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
       : "l"(ptr));
+}
+// coherent 32- and 16-byte loads, for data written earlier in the same launch
+// (ordered after the writers' barrier by the memory clobber)
+__device__ __forceinline__ void ld_plain32(const void* ptr, uint4& a, uint4& b) {
+  asm volatile("ld.global.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+               : "l"(ptr)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_plain16(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr)
+               : "memory");
+  return v;
 }
 __device__ __forceinline__ uint2 ld_nc8(const void* ptr) {
   uint2 v;
@@ -223,9 +256,80 @@ __device__ __forceinline__ void st32(void* ptr, const uint4& a, const uint4& b) 
 __device__ __forceinline__ void st8(void* ptr, uint2 v) { *reinterpret_cast<uint2*>(ptr) = v; }
 __device__ __forceinline__ void st4(void* ptr, uint32_t v) { *reinterpret_cast<uint32_t*>(ptr) = v; }
 
-// Zero the alignment padding [used, seg_bytes) of a slot (whole CTA).
-__device__ __forceinline__ void zero_padding(uint8_t* slot, uint64_t used, uint64_t total) {
-  for (uint64_t k = used + threadIdx.x; k < total; k += blockDim.x) slot[k] = 0;
+// L2 eviction priorities.  A policy from createpolicy rides on a load or a
+// store as a cache hint: evict_last for bytes that are read again soon (a slot
+// checked before it is decoded), evict_first for bytes read or written once.
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// Read-only loads and stores, with the policy when H (else as above).
+template <bool H>
+__device__ __forceinline__ void ld_nc32_h(const void* ptr, uint4& a, uint4& b, uint64_t pol) {
+  if (!H) return ld_nc32(ptr, a, b);
+  asm("ld.global.nc.L2::cache_hint.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], %9;"
+      : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+      : "l"(ptr), "l"(pol));
+}
+template <bool H>
+__device__ __forceinline__ uint4 ld_nc16_h(const void* ptr, uint64_t pol) {
+  if (!H) return ld_nc16(ptr);
+  uint4 v;
+  asm("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(ptr), "l"(pol));
+  return v;
+}
+template <bool H>
+__device__ __forceinline__ uint2 ld_nc8_h(const void* ptr, uint64_t pol) {
+  if (!H) return ld_nc8(ptr);
+  uint2 v;
+  asm("ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;" : "=r"(v.x), "=r"(v.y) : "l"(ptr), "l"(pol));
+  return v;
+}
+template <bool H>
+__device__ __forceinline__ uint32_t ld_nc4_h(const void* ptr, uint64_t pol) {
+  if (!H) return ld_nc4(ptr);
+  uint32_t v;
+  asm("ld.global.nc.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol));
+  return v;
+}
+template <bool H>
+__device__ __forceinline__ void st16_h(void* ptr, uint4 v, uint64_t pol) {
+  if (!H) return st16(ptr, v);
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
+template <bool H>
+__device__ __forceinline__ void st32_h(void* ptr, const uint4& a, const uint4& b, uint64_t pol) {
+  if (!H) return st32(ptr, a, b);
+  asm volatile("st.global.L2::cache_hint.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(ptr),
+               "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w), "l"(pol)
+               : "memory");
+}
+
+// Bring `bytes` (a multiple of 16) at `ptr` (16-byte aligned) into L2 without
+// waiting for them; a plain hint, its completion is never awaited.
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(ptr), "r"(bytes), "l"(pol)
+               : "memory");
+}
+
+// Zero the alignment padding [used, seg_bytes) of a slot: threads first,
+// first + step, ... (the whole CTA: threadIdx.x, blockDim.x; one warp: lane, 32).
+__device__ __forceinline__ void zero_padding(uint8_t* slot, uint64_t used, uint64_t total, uint32_t first,
+                                             uint32_t step) {
+  for (uint64_t k = used + first; k < total; k += step) slot[k] = 0;
 }
 
 // ---------------------------------------------------------------- 16-bit formats
@@ -450,7 +554,7 @@ inline int launch_codec_kernel(K kernel, const Params& p, void* stream, int max_
   const uint32_t units = warp_segments ? (p.n_segments + (uint32_t)threads / 32u - 1u) / ((uint32_t)threads / 32u)
                                        : p.n_segments;
   const int rc = grid_for_threads(reinterpret_cast<const void*>(kernel), units, max_per_sm,
-                                  threads, &grid);
+                                  threads, &grid, !warp_segments);
   if (rc != KV_OK || grid == 0) return rc;
   void* args[] = {const_cast<Params*>(&p)};
   const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(kernel), dim3(grid),

@@ -12,13 +12,21 @@
 // Per element the encoder does one correctly rounded division (reciprocal of
 // the vector's scale + one FMA correction) and the hardware conversion
 // cvt.rn.satfinite.e4m3x2.f32, whose saturation to +-448 is the clip.
-#include "device_common.cuh"
+//
+// Besides the plain kernels (one CTA per segment) there are sealing encoders
+// and verifying decoders (one warp per segment) that give the segment
+// headers' CRC-32 without a second pass over the slots in HBM: section
+// "Ownership, storage and GDS" of the same OrbitKV page asks for a CRC32 per
+// stored segment, checked before GPU decode.
+#include <type_traits>
+
+#include "crc_common.cuh"
 
 namespace kvc {
 namespace {
 
 constexpr float kRecip448 = 1.0f / 448.0f;  // fl32(1/448)
-// Resident CTAs per SM (see launch_codec_kernel), from sweeps of 2-8 on the
+// Resident CTAs per SM (see launch_plain), from sweeps of 2-8 on the
 // GB300: the dynamic-scale encoder (more work per vector) and the head_dim 32
 // encoders want 6, the fixed-scale / cast encoders 4; the decoders 3.
 template <uint32_t CODEC, int D>
@@ -67,32 +75,91 @@ __device__ __forceinline__ uint2 fp8_codes8(const float (&x)[8], float s, float 
                     e4m3x4(q[4], q[5], q[6], q[7]) ^ 0x80808080u);
 }
 
-template <int DT, int D, uint32_t CODEC>
-__global__ void __launch_bounds__(kThreads) fp8_encode_kernel(const __grid_constant__ Params p) {
+template <uint32_t CODEC, int D>
+__device__ __forceinline__ uint64_t fp8_used_bytes(uint32_t nv) {
+  return (uint64_t)nv * (D + (CODEC == KV_CODEC_FP8_DYNAMIC ? 4 : 0));
+}
+
+__device__ __forceinline__ uint8_t status_of_flags(uint32_t f) {
+  return (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+}
+
+// The second kernel parameter selects the variant.  NoSeal: the plain kernel,
+// one CTA of kThreads per segment.  CrcParams: the sealing encoder /
+// verifying decoder, one warp per segment in 1024-thread CTAs (one per SM)
+// holding the CRC lookup tables.  The sealing encoder codes its segment, then
+// -- after __syncwarp, with plain loads, since its lanes have just written the
+// slot and the bytes sit in L2 -- computes the slot's CRC-32 and writes the
+// header kv_codec_seal would write.  The verifying decoder first checks header
+// and CRC-32 exactly as kv_codec_verify does and restores the segment only when
+// they match, re-reading the slot from L2: a damaged slot is never scattered,
+// and HBM carries each slot once either way.  The sealing encoder folds each
+// 2 KB row of codes into its CRC while the loads of its next vectors are in
+// flight, so its warps keep streaming.  (The vector loop is written out
+// in the kernel bodies: moved into a helper function it compiled to half again
+// as many registers, which cost the plain encoder two of its six CTAs per SM.)
+struct NoSeal {};
+template <typename Q>
+struct Variant {
+  static constexpr bool kSeal = !std::is_same<Q, NoSeal>::value;
+  static constexpr int kCtaThreads = kSeal ? crc::kCrcThreads : kThreads;
+};
+
+template <int DT, int D, uint32_t CODEC, typename Q>
+__global__ void __launch_bounds__(Variant<Q>::kCtaThreads)
+    fp8_encode_kernel(const __grid_constant__ Params p, const __grid_constant__ Q q) {
   using M = ChunkMap<D>;
-  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = kThreads / 32;
-  constexpr int STEP = W * VPW * U;
+  constexpr bool SEAL = Variant<Q>::kSeal;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = Variant<Q>::kCtaThreads / 32;
+  // a warp's vector rows: a CTA's warps interleave over the segment; a sealing
+  // warp walks its segment alone
+  constexpr uint32_t STEP = SEAL ? VPW * U : W * VPW * U;
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
+  const uint32_t j_first = SEAL ? 0u : warp * VPW * U;
   __shared__ uint32_t s_flag[2];
-  if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
-  __syncthreads();
+  crc::NibbleTables* t = nullptr;
+  uint32_t tb = 0;
+  uint32_t i = blockIdx.x, i_step = gridDim.x;  // no wrap: n_segments < 2^31
+  if constexpr (SEAL) {
+    tb = crc::load_tables(q, t);
+    SegCursor c;
+    warp_cursor_init(c, W);
+    i = c.base;
+    i_step = c.stride;
+  } else {
+    if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
+    __syncthreads();
+  }
   const uint32_t nv = p.nv;
   int it = 0;
-  for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
+  for (; i < p.n_segments; i += i_step) {
     const Seg s = plan_segment(p, i, kEncode);
     if (s.action != kProcess) {
-      if (s.action == kReport && threadIdx.x == 0) p.status[i] = s.status;
+      if constexpr (SEAL) {
+        if (s.action == kReport) {
+          if (lane == 0) p.status[i] = s.status;
+          crc::seal_segment<true>(q, *t, tb, i, s.status, lane);
+        }
+      } else {
+        if (s.action == kReport && threadIdx.x == 0) p.status[i] = s.status;
+      }
       continue;
     }
-    if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
+    if (!SEAL && threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
     float fixed = 1.0f;
     if (CODEC == KV_CODEC_FP8_FIXED) fixed = p.fixed_scale[s.layer][s.role];
     const float fixed_nr = -__frcp_rn(fixed);
     uint8_t* codes = s.slot;
     uint8_t* meta = s.slot + (uint64_t)nv * D;
     uint32_t flags = 0;
-    for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
+    // sealing: the slot's CRC rows (2 KB) folded so far into this lane's
+    // register; a step writes 1 KB of codes, so row m is complete once step
+    // 2m + 1 is, and is folded during the loads of step 2m + 2
+    static_assert(!SEAL || VPW * U * D == kCrcRow / 2, "a step writes half a CRC row");
+    uint32_t crc_s = 0, crc_m = 0;
+    const bool al32 = ((uintptr_t)s.slot & 31u) == 0;
+    for (uint32_t j0 = j_first, k = 0; j0 < nv; j0 += STEP, ++k) {
       uint4 w[U][NC];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -100,7 +167,17 @@ __global__ void __launch_bounds__(kThreads) fp8_encode_kernel(const __grid_const
         const uint16_t* src = s.page + (j < nv ? vec_off(p, j) : 0);
 #pragma unroll
         for (int c = 0; c < NC; ++c)
-          w[u][c] = j < nv ? ld_stream16(src + 8 * (li + G * c)) : make_uint4(0, 0, 0, 0);
+          w[u][c] = j < nv ? ld_stream16<SEAL>(src + 8 * (li + G * c)) : make_uint4(0, 0, 0, 0);
+      }
+      if constexpr (SEAL) {
+        // the vectors two steps ahead into L2 meanwhile, one per lane
+        const uint32_t jn = j0 + 2u * STEP + lane;
+        if (lane < STEP && jn < nv) prefetch_l2(s.page + vec_off(p, jn), D * 2);
+        if (k >= 2u && (k & 1u) == 0u) {
+          __syncwarp();
+          crc_s = crc::fold_row<false>(*t, tb, s.slot, crc_m, al32, crc_s, lane);
+          ++crc_m;
+        }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -125,44 +202,76 @@ __global__ void __launch_bounds__(kThreads) fp8_encode_kernel(const __grid_const
       }
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
-    if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
-    const uint64_t used = (uint64_t)nv * (D + (CODEC == KV_CODEC_FP8_DYNAMIC ? 4 : 0));
-    zero_padding(s.slot, used, p.seg_bytes[s.role]);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const uint32_t f = s_flag[it & 1];
-      p.status[i] = (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+    if constexpr (SEAL) {
+      zero_padding(s.slot, fp8_used_bytes<CODEC, D>(nv), p.seg_bytes[s.role], lane, 32);
+      const uint32_t st = status_of_flags(flags);
+      __syncwarp();
+      if (lane == 0) p.status[i] = (uint8_t)st;
+      crc::seal_segment<false>(q, *t, tb, i, st, lane, crc_m, crc_s);
+    } else {
+      if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
+      zero_padding(s.slot, fp8_used_bytes<CODEC, D>(nv), p.seg_bytes[s.role], threadIdx.x, blockDim.x);
+      __syncthreads();
+      if (threadIdx.x == 0) p.status[i] = status_of_flags(s_flag[it & 1]);
+      ++it;
     }
-    ++it;
   }
 }
 
-// ADJ (segments of kAdjacentChunkMinVectors or more, D >= 64): lane li owns the adjacent chunks
-// 2 li, 2 li + 1 -- one 16-byte code load and, when every vector is 32-byte
-// aligned, one 32-byte store per vector.  Measured on a GB300: FP8 decode of
-// 512-vector segments 0.93-0.97 -> 0.97-0.98 of HBM, of 128-vector segments
-// 0.968 -> 0.958, so smaller segments keep chunks li, li + G.
-template <int DT, int D, uint32_t CODEC, bool ADJ>
-__global__ void __launch_bounds__(kThreads) fp8_decode_kernel(const __grid_constant__ Params p) {
+// ADJ (segments of kAdjacentChunkMinVectors or more, D >= 64): lane li owns the
+// adjacent chunks 2 li, 2 li + 1 -- one 16-byte code load and, when every vector
+// is 32-byte aligned, one 32-byte store per vector.  Measured on a GB300: FP8
+// decode of 512-vector segments 0.93-0.97 -> 0.97-0.98 of HBM, of 128-vector
+// segments 0.968 -> 0.958, so smaller segments keep chunks li, li + G.
+template <int DT, int D, uint32_t CODEC, bool ADJ, typename Q>
+__global__ void __launch_bounds__(Variant<Q>::kCtaThreads)
+    fp8_decode_kernel(const __grid_constant__ Params p, const __grid_constant__ Q q) {
   using M = ChunkMap<D>;
-  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = kThreads / 32;
-  constexpr int STEP = W * VPW * U;
+  constexpr bool SEAL = Variant<Q>::kSeal;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = Variant<Q>::kCtaThreads / 32;
+  constexpr uint32_t STEP = SEAL ? VPW * U : W * VPW * U;
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
+  const uint32_t j_first = SEAL ? 0u : warp * VPW * U;
   const uint32_t nv = p.nv;
   const bool vec32 = p.vec32 != 0;
-  for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
-    const Seg s = plan_segment(p, i, kDecode);
-    if (s.action != kProcess) {
-      if (s.action == kReport && threadIdx.x == 0 && p.result) p.result[i] = s.status;
-      continue;
+  crc::NibbleTables* t = nullptr;
+  uint32_t tb = 0;
+  uint32_t i = blockIdx.x, i_step = gridDim.x;  // no wrap: n_segments < 2^31
+  // verifying: the check's reads keep the slot in L2 (evict_last) for the
+  // restore's reads right after, which with the page stores go first
+  uint64_t keep = 0, once = 0;
+  if constexpr (SEAL) {
+    tb = crc::load_tables(q, t);
+    SegCursor c;
+    warp_cursor_init(c, W);
+    i = c.base;
+    i_step = c.stride;
+    keep = l2_evict_last();
+    once = l2_evict_first();
+  }
+  for (; i < p.n_segments; i += i_step) {
+    Seg s;
+    if constexpr (SEAL) {
+      if (!owns_segment(p, __ldg(&p.descs[i].role))) continue;  // another launch's: no CRC
+      s = plan_segment(p, i, kDecode, (int)crc::verify_segment<true>(q, *t, tb, i, lane, keep));
+      if (s.action != kProcess) {
+        if (lane == 0) p.result[i] = s.status;
+        continue;
+      }
+    } else {
+      s = plan_segment(p, i, kDecode);
+      if (s.action != kProcess) {
+        if (s.action == kReport && threadIdx.x == 0 && p.result) p.result[i] = s.status;
+        continue;
+      }
     }
     float fixed = 1.0f;
     if (CODEC == KV_CODEC_FP8_FIXED) fixed = p.fixed_scale[s.layer][s.role];
     const uint8_t* codes = s.slot;
     const uint8_t* meta = s.slot + (uint64_t)nv * D;
     uint16_t* page = const_cast<uint16_t*>(s.page);
-    for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
+    for (uint32_t j0 = j_first; j0 < nv; j0 += STEP) {
       uint2 cw[U][NC];
       float sc[U];
 #pragma unroll
@@ -170,16 +279,17 @@ __global__ void __launch_bounds__(kThreads) fp8_decode_kernel(const __grid_const
         const uint32_t j = j0 + u * VPW + grp;
         const bool in = j < nv;
         if (ADJ && NC == 2) {  // lane li owns the adjacent chunks 2 li, 2 li + 1: one 16-byte load
-          const uint4 t = in ? ld_nc16(codes + (uint64_t)j * D + 16 * li) : make_uint4(0, 0, 0, 0);
-          cw[u][0] = make_uint2(t.x, t.y);
-          cw[u][NC - 1] = make_uint2(t.z, t.w);
+          const uint4 tt = in ? ld_nc16_h<SEAL>(codes + (uint64_t)j * D + 16 * li, once) : make_uint4(0, 0, 0, 0);
+          cw[u][0] = make_uint2(tt.x, tt.y);
+          cw[u][NC - 1] = make_uint2(tt.z, tt.w);
         } else {
 #pragma unroll
           for (int c = 0; c < NC; ++c)
-            cw[u][c] = in ? ld_nc8(codes + (uint64_t)j * D + 8 * (li + G * c)) : make_uint2(0, 0);
+            cw[u][c] = in ? ld_nc8_h<SEAL>(codes + (uint64_t)j * D + 8 * (li + G * c), once) : make_uint2(0, 0);
         }
         sc[u] = fixed;
-        if (CODEC == KV_CODEC_FP8_DYNAMIC) sc[u] = in ? __uint_as_float(ld_nc4(meta + (uint64_t)j * 4)) : 0.0f;
+        if (CODEC == KV_CODEC_FP8_DYNAMIC)
+          sc[u] = in ? __uint_as_float(ld_nc4_h<SEAL>(meta + (uint64_t)j * 4, once)) : 0.0f;
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -205,27 +315,90 @@ __global__ void __launch_bounds__(kThreads) fp8_decode_kernel(const __grid_const
             o = make_uint4(r[0], r[1], r[2], r[3]);
           }
           if (ADJ && NC == 2) oc[c] = o;
-          else if (j < nv) st16(dst + 8 * (li + G * c), o);
+          else if (j < nv) st16_h<SEAL>(dst + 8 * (li + G * c), o, once);
         }
         if (ADJ && NC == 2 && j < nv) {
           if (vec32) {
-            st32(dst + 16 * li, oc[0], oc[NC - 1]);
+            st32_h<SEAL>(dst + 16 * li, oc[0], oc[NC - 1], once);
           } else {
-            st16(dst + 16 * li, oc[0]);
-            st16(dst + 16 * li + 8, oc[NC - 1]);
+            st16_h<SEAL>(dst + 16 * li, oc[0], once);
+            st16_h<SEAL>(dst + 16 * li + 8, oc[NC - 1], once);
           }
         }
       }
     }
-    if (threadIdx.x == 0 && p.result) p.result[i] = KV_SEG_ENCODED;
+    if constexpr (SEAL) {
+      if (lane == 0) p.result[i] = KV_SEG_ENCODED;
+    } else {
+      if (threadIdx.x == 0 && p.result) p.result[i] = KV_SEG_ENCODED;
+    }
   }
+}
+
+// Plain kernels: kThreads per CTA, at most max_per_sm CTAs per SM.
+template <typename K>
+int launch_plain(K kernel, const Params& p, void* stream, int max_per_sm) {
+  unsigned grid = 0;
+  const int rc = grid_for_threads(reinterpret_cast<const void*>(kernel), p.n_segments, max_per_sm, kThreads, &grid);
+  if (rc != KV_OK || grid == 0) return rc;
+  NoSeal none;
+  void* args[] = {const_cast<Params*>(&p), &none};
+  const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(kThreads), args, 0,
+                                         (cudaStream_t)stream);
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+template <typename K>
+int launch_sealed(K kernel, const Params& p, const CrcParams& q, void* stream) {
+  const void* k = reinterpret_cast<const void*>(kernel);
+  // the tables need more than the default 48 KB of dynamic shared memory (set
+  // on every launch: the attribute belongs to the current device's context)
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)crc::kCrcSmem) != cudaSuccess)
+    return KV_ERR_CUDA;
+  unsigned grid = 0;
+  const int rc = grid_for_threads(k, (p.n_segments + crc::kCrcWarps - 1) / crc::kCrcWarps, 1,
+                                  crc::kCrcThreads, &grid, false);
+  if (rc != KV_OK || grid == 0) return rc;
+  void* args[] = {const_cast<Params*>(&p), const_cast<CrcParams*>(&q)};
+  const cudaError_t e = cudaLaunchKernel(k, dim3(grid), dim3(crc::kCrcThreads), args, crc::kCrcSmem,
+                                         (cudaStream_t)stream);
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+template <int DT, int D, uint32_t CODEC>
+int sealed_mode(const Params& p, const CrcParams& q, int dir, void* stream) {
+  if (dir == kEncode) return launch_sealed(fp8_encode_kernel<DT, D, CODEC, CrcParams>, p, q, stream);
+  if (p.nv >= kAdjacentChunkMinVectors)
+    return launch_sealed(fp8_decode_kernel<DT, D, CODEC, true, CrcParams>, p, q, stream);
+  return launch_sealed(fp8_decode_kernel<DT, D, CODEC, false, CrcParams>, p, q, stream);
+}
+
+template <int DT, int D>
+int sealed_codec(const Params& p, const CrcParams& q, int dir, uint32_t codec, void* stream) {
+  switch (codec) {
+    case KV_CODEC_FP8_CAST: return sealed_mode<DT, D, KV_CODEC_FP8_CAST>(p, q, dir, stream);
+    case KV_CODEC_FP8_FIXED: return sealed_mode<DT, D, KV_CODEC_FP8_FIXED>(p, q, dir, stream);
+    case KV_CODEC_FP8_DYNAMIC: return sealed_mode<DT, D, KV_CODEC_FP8_DYNAMIC>(p, q, dir, stream);
+  }
+  return KV_ERR_INVALID_ARG;
+}
+
+template <int DT>
+int sealed_dim(const Params& p, const CrcParams& q, int dir, uint32_t codec, void* stream) {
+  switch (p.D) {
+    case 32: return sealed_codec<DT, 32>(p, q, dir, codec, stream);
+    case 64: return sealed_codec<DT, 64>(p, q, dir, codec, stream);
+    case 128: return sealed_codec<DT, 128>(p, q, dir, codec, stream);
+    case 256: return sealed_codec<DT, 256>(p, q, dir, codec, stream);
+  }
+  return KV_ERR_UNSUPPORTED_HEAD_DIM;
 }
 
 template <int DT, int D, uint32_t CODEC>
 int decode(const Params& p, void* stream) {
   if (p.nv >= kAdjacentChunkMinVectors)
-    return launch_codec_kernel(fp8_decode_kernel<DT, D, CODEC, true>, p, stream, kDecodeCtas);
-  return launch_codec_kernel(fp8_decode_kernel<DT, D, CODEC, false>, p, stream, kDecodeCtas);
+    return launch_plain(fp8_decode_kernel<DT, D, CODEC, true, NoSeal>, p, stream, kDecodeCtas);
+  return launch_plain(fp8_decode_kernel<DT, D, CODEC, false, NoSeal>, p, stream, kDecodeCtas);
 }
 
 template <int DT, int D>
@@ -233,13 +406,13 @@ int dispatch_mode(const Params& p, int dir, uint32_t codec, void* stream) {
   if (dir == kEncode) {
     switch (codec) {
       case KV_CODEC_FP8_CAST:
-        return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_CAST>, p, stream,
+        return launch_plain(fp8_encode_kernel<DT, D, KV_CODEC_FP8_CAST, NoSeal>, p, stream,
                                    encode_ctas<KV_CODEC_FP8_CAST, D>());
       case KV_CODEC_FP8_FIXED:
-        return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_FIXED>, p, stream,
+        return launch_plain(fp8_encode_kernel<DT, D, KV_CODEC_FP8_FIXED, NoSeal>, p, stream,
                                    encode_ctas<KV_CODEC_FP8_FIXED, D>());
       case KV_CODEC_FP8_DYNAMIC:
-        return launch_codec_kernel(fp8_encode_kernel<DT, D, KV_CODEC_FP8_DYNAMIC>, p, stream,
+        return launch_plain(fp8_encode_kernel<DT, D, KV_CODEC_FP8_DYNAMIC, NoSeal>, p, stream,
                                    encode_ctas<KV_CODEC_FP8_DYNAMIC, D>());
     }
   } else {
@@ -268,6 +441,11 @@ int dispatch_dim(const Params& p, int dir, uint32_t codec, void* stream) {
 int launch_fp8(const Params& p, int dir, uint32_t codec, void* stream) {
   return p.dtype == KV_DT_FP16 ? dispatch_dim<0>(p, dir, codec, stream)
                                : dispatch_dim<1>(p, dir, codec, stream);
+}
+
+int launch_fp8_sealed(const Params& p, const CrcParams& q, int dir, uint32_t codec, void* stream) {
+  return p.dtype == KV_DT_FP16 ? sealed_dim<0>(p, q, dir, codec, stream)
+                               : sealed_dim<1>(p, q, dir, codec, stream);
 }
 
 }  // namespace kvc

@@ -243,10 +243,14 @@ std::mutex g_mu;
 std::map<int, int> g_sms;
 std::map<std::pair<int, const void*>, int> g_occ;
 
-int launch_all(kv_codec_s* h, int dir, void* stream) {
+// The launches of one encode or decode call: one when both roles share a
+// codec, else one per coded role.  With `seal` (every coded role FP8), the FP8
+// launches also write (encode) or first check (decode) the segment headers.
+int launch_all(kv_codec_s* h, int dir, void* stream, const kvc::CrcParams* seal = nullptr) {
   Params& p = h->p;
   const uint32_t kc = p.codec[0], vc = p.codec[1];
   auto run = [&](uint32_t codec) -> int {
+    if (seal) return kvc::launch_fp8_sealed(p, *seal, dir, codec, stream);
     if (is_fp8(codec)) return kvc::launch_fp8(p, dir, codec, stream);
     if (is_tq(codec)) return kvc::launch_turboquant(p, dir, codec, stream);
     if (codec == KV_CODEC_INT8_HEAD) return kvc::launch_int8(p, dir, codec, stream);
@@ -256,7 +260,8 @@ int launch_all(kv_codec_s* h, int dir, void* stream) {
     p.is_first = 1;
     if (kc == KV_CODEC_NONE) {  // statuses only
       p.role_sel = 3;
-      return kvc::launch_fp8(p, dir, KV_CODEC_FP8_CAST, stream);
+      return seal ? kvc::launch_fp8_sealed(p, *seal, dir, KV_CODEC_FP8_CAST, stream)
+                  : kvc::launch_fp8(p, dir, KV_CODEC_FP8_CAST, stream);
     }
     p.role_sel = 2;
     return run(kc);
@@ -272,6 +277,13 @@ int launch_all(kv_codec_s* h, int dir, void* stream) {
     if (rc != KV_OK) return rc;
   }
   return KV_OK;
+}
+
+// Every coded role takes an FP8 codec (the one-pass sealed / verified kernels).
+bool fp8_roles_only(const Params& p) {
+  for (int r = 0; r < 2; ++r)
+    if (p.codec[r] != KV_CODEC_NONE && !is_fp8(p.codec[r])) return false;
+  return true;
 }
 
 // Address under which the kernels reach a caller buffer: device and managed
@@ -329,6 +341,29 @@ int check_call(kv_codec_s* h, const void* const* layer_ptrs, uint32_t n_layer_pt
   return KV_OK;
 }
 
+// The per-call CRC parameters: device views of descriptors, slots, statuses
+// (seal), headers and result (verify).
+int crc_call(kv_codec_t h, kvc::CrcParams& p, const kv_segment_desc* descs, uint32_t n_segments,
+             const void* buf, uint64_t buf_bytes, const uint8_t* status, const kv_segment_header* headers,
+             uint8_t* result) {
+  p = h->crc;
+  const void* v = nullptr;
+  int rc;
+  if ((rc = device_view(descs, &v)) != KV_OK) return rc;
+  p.descs = static_cast<const kv_segment_desc*>(v);
+  if ((rc = device_view(buf, &v)) != KV_OK) return rc;
+  p.buf = static_cast<const uint8_t*>(v);
+  if ((rc = device_view(status, &v)) != KV_OK) return rc;
+  p.status = static_cast<const uint8_t*>(v);
+  if ((rc = device_view(headers, &v)) != KV_OK) return rc;
+  p.headers = const_cast<kv_segment_header*>(static_cast<const kv_segment_header*>(v));
+  if ((rc = device_view(result, &v)) != KV_OK) return rc;
+  p.result = static_cast<uint8_t*>(const_cast<void*>(v));
+  p.n_segments = n_segments;
+  p.buf_bytes = buf_bytes;
+  return KV_OK;
+}
+
 }  // namespace
 
 namespace kvc {
@@ -336,7 +371,8 @@ int grid_for(const void* kernel, uint32_t n_segments, int max_per_sm, unsigned* 
   return grid_for_threads(kernel, n_segments, max_per_sm, kThreads, grid);
 }
 
-int grid_for_threads(const void* kernel, uint32_t n_segments, int max_per_sm, int threads, unsigned* grid) {
+int grid_for_threads(const void* kernel, uint32_t n_segments, int max_per_sm, int threads, unsigned* grid,
+                     bool odd) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KV_ERR_CUDA;
   int sms = 0, occ = 0;
@@ -363,8 +399,9 @@ int grid_for_threads(const void* kernel, uint32_t n_segments, int max_per_sm, in
   uint64_t g = std::min<uint64_t>((uint64_t)sms * (uint64_t)per_sm, n_segments);
   // An odd stride deals segments of both roles to every CTA when K and V
   // segments alternate in the descriptor list (a launch that codes one role
-  // only skips the other role's segments).
-  if (g > 1 && g < n_segments && (g & 1) == 0) --g;
+  // only skips the other role's segments).  Kernels with a segment per warp
+  // make their warp stride odd themselves (odd = false).
+  if (odd && g > 1 && g < n_segments && (g & 1) == 0) --g;
   *grid = (unsigned)g;
   return KV_OK;
 }
@@ -567,6 +604,7 @@ int kv_codec_encode(kv_codec_t h, const void* const* layer_ptrs, uint32_t n_laye
                     uint64_t out_bytes, uint8_t* d_status, void* stream) {
   if (!h) return KV_ERR_INVALID_ARG;
   if (n_segments == 0) return KV_OK;
+  if (n_segments > KV_CODEC_MAX_SEGMENTS) return KV_ERR_INVALID_ARG;
   const int rc = check_call(h, layer_ptrs, n_layer_ptrs, d_descs, d_out, d_status);
   if (rc != KV_OK) return rc;
   kv_codec_s call = *h;  // per-call copy: the handle stays immutable
@@ -584,24 +622,13 @@ int kv_codec_seal(kv_codec_t h, const kv_segment_desc* descs, uint32_t n_segment
                   uint64_t buf_bytes, const uint8_t* status, kv_segment_header* headers, void* stream) {
   if (!h) return KV_ERR_INVALID_ARG;
   if (n_segments == 0) return KV_OK;
+  if (n_segments > KV_CODEC_MAX_SEGMENTS) return KV_ERR_INVALID_ARG;
   if (!descs || !buf || !status || !headers) return KV_ERR_INVALID_ARG;
   if (((uintptr_t)buf & 15u) || ((uintptr_t)descs & 7u) || ((uintptr_t)headers & 7u))
     return KV_ERR_MISALIGNED;
-  kvc::CrcParams p = h->crc;
-  const void* v = nullptr;
-  int rc;
-  if ((rc = device_view(descs, &v)) != KV_OK) return rc;
-  p.descs = static_cast<const kv_segment_desc*>(v);
-  if ((rc = device_view(buf, &v)) != KV_OK) return rc;
-  p.buf = static_cast<const uint8_t*>(v);
-  if ((rc = device_view(status, &v)) != KV_OK) return rc;
-  p.status = static_cast<const uint8_t*>(v);
-  if ((rc = device_view(headers, &v)) != KV_OK) return rc;
-  p.headers = const_cast<kv_segment_header*>(static_cast<const kv_segment_header*>(v));
-  p.result = nullptr;
-  p.n_segments = n_segments;
-  p.buf_bytes = buf_bytes;
-  return kvc::launch_crc(p, 1, stream);
+  kvc::CrcParams p;
+  const int rc = crc_call(h, p, descs, n_segments, buf, buf_bytes, status, headers, nullptr);
+  return rc != KV_OK ? rc : kvc::launch_crc(p, 1, stream);
 }
 
 int kv_codec_verify(kv_codec_t h, const kv_segment_desc* descs, uint32_t n_segments, const void* buf,
@@ -609,24 +636,66 @@ int kv_codec_verify(kv_codec_t h, const kv_segment_desc* descs, uint32_t n_segme
                     void* stream) {
   if (!h) return KV_ERR_INVALID_ARG;
   if (n_segments == 0) return KV_OK;
+  if (n_segments > KV_CODEC_MAX_SEGMENTS) return KV_ERR_INVALID_ARG;
   if (!descs || !buf || !headers || !result) return KV_ERR_INVALID_ARG;
   if (((uintptr_t)buf & 15u) || ((uintptr_t)descs & 7u) || ((uintptr_t)headers & 7u))
     return KV_ERR_MISALIGNED;
-  kvc::CrcParams p = h->crc;
-  const void* v = nullptr;
-  int rc;
-  if ((rc = device_view(descs, &v)) != KV_OK) return rc;
-  p.descs = static_cast<const kv_segment_desc*>(v);
-  if ((rc = device_view(buf, &v)) != KV_OK) return rc;
-  p.buf = static_cast<const uint8_t*>(v);
-  if ((rc = device_view(headers, &v)) != KV_OK) return rc;
-  p.headers = const_cast<kv_segment_header*>(static_cast<const kv_segment_header*>(v));
-  if ((rc = device_view(result, &v)) != KV_OK) return rc;
-  p.result = const_cast<uint8_t*>(static_cast<const uint8_t*>(v));
-  p.status = nullptr;
+  kvc::CrcParams p;
+  const int rc = crc_call(h, p, descs, n_segments, buf, buf_bytes, nullptr, headers, result);
+  return rc != KV_OK ? rc : kvc::launch_crc(p, 0, stream);
+}
+
+int kv_codec_encode_sealed(kv_codec_t h, const void* const* layer_ptrs, uint32_t n_layer_ptrs,
+                           const kv_segment_desc* descs, uint32_t n_segments, void* out, uint64_t out_bytes,
+                           uint8_t* status, kv_segment_header* headers, void* stream) {
+  if (!h) return KV_ERR_INVALID_ARG;
+  if (n_segments == 0) return KV_OK;
+  if (n_segments > KV_CODEC_MAX_SEGMENTS) return KV_ERR_INVALID_ARG;
+  int rc = check_call(h, layer_ptrs, n_layer_ptrs, descs, out, status);
+  if (rc != KV_OK) return rc;
+  if (!headers) return KV_ERR_INVALID_ARG;
+  if ((uintptr_t)headers & 7u) return KV_ERR_MISALIGNED;
+  kv_codec_s call = *h;
+  Params& p = call.p;
+  for (uint32_t k = 0; k < n_layer_ptrs; ++k) p.layer_ptr[k] = layer_ptrs[k];
+  p.vec32 = vectors_32b_aligned(p);
+  if ((rc = resolve_buffers(p, descs, out, status, nullptr)) != KV_OK) return rc;
   p.n_segments = n_segments;
-  p.buf_bytes = buf_bytes;
-  return kvc::launch_crc(p, 0, stream);
+  p.buf_bytes = out_bytes;
+  kvc::CrcParams q;
+  if ((rc = crc_call(h, q, descs, n_segments, out, out_bytes, status, headers, nullptr)) != KV_OK) return rc;
+  if (fp8_roles_only(p)) return launch_all(&call, kvc::kEncode, stream, &q);
+  // other codecs: encode, then seal the slots in a second pass
+  if ((rc = launch_all(&call, kvc::kEncode, stream)) != KV_OK) return rc;
+  return kvc::launch_crc(q, 1, stream);
+}
+
+int kv_codec_decode_verified(kv_codec_t h, void* const* layer_ptrs, uint32_t n_layer_ptrs,
+                             const kv_segment_desc* descs, uint32_t n_segments, const void* in,
+                             uint64_t in_bytes, const kv_segment_header* headers, uint8_t* result,
+                             void* stream) {
+  if (!h) return KV_ERR_INVALID_ARG;
+  if (n_segments == 0) return KV_OK;
+  if (n_segments > KV_CODEC_MAX_SEGMENTS) return KV_ERR_INVALID_ARG;
+  int rc = check_call(h, layer_ptrs, n_layer_ptrs, descs, in, result);
+  if (rc != KV_OK) return rc;
+  if (!headers) return KV_ERR_INVALID_ARG;
+  if ((uintptr_t)headers & 7u) return KV_ERR_MISALIGNED;
+  kv_codec_s call = *h;
+  Params& p = call.p;
+  for (uint32_t k = 0; k < n_layer_ptrs; ++k) p.layer_ptr[k] = layer_ptrs[k];
+  p.vec32 = vectors_32b_aligned(p);
+  // other codecs decode with the verified results as their statuses, which
+  // they then overwrite with the final results (same array)
+  if ((rc = resolve_buffers(p, descs, in, result, result)) != KV_OK) return rc;
+  p.status_is_result = 1;
+  p.n_segments = n_segments;
+  p.buf_bytes = in_bytes;
+  kvc::CrcParams q;
+  if ((rc = crc_call(h, q, descs, n_segments, in, in_bytes, nullptr, headers, result)) != KV_OK) return rc;
+  if (fp8_roles_only(p)) return launch_all(&call, kvc::kDecode, stream, &q);
+  if ((rc = kvc::launch_crc(q, 0, stream)) != KV_OK) return rc;
+  return launch_all(&call, kvc::kDecode, stream);
 }
 
 int kv_codec_decode(kv_codec_t h, void* const* layer_ptrs, uint32_t n_layer_ptrs,
@@ -634,6 +703,7 @@ int kv_codec_decode(kv_codec_t h, void* const* layer_ptrs, uint32_t n_layer_ptrs
                     uint64_t in_bytes, const uint8_t* d_status, uint8_t* d_result, void* stream) {
   if (!h) return KV_ERR_INVALID_ARG;
   if (n_segments == 0) return KV_OK;
+  if (n_segments > KV_CODEC_MAX_SEGMENTS) return KV_ERR_INVALID_ARG;
   const int rc = check_call(h, layer_ptrs, n_layer_ptrs, d_descs, d_in, d_status);
   if (rc != KV_OK) return rc;
   kv_codec_s call = *h;

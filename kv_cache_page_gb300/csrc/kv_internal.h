@@ -1,7 +1,7 @@
 // kv_internal.h -- launch parameters shared by the host library and the kernels.
 //
 // Everything a kernel needs travels in one __grid_constant__ parameter block
-// (about 13 KB: per-layer pointers, fixed FP8 scales, the TurboQuant codebook
+// (about 15 KB: per-layer pointers, fixed FP8 scales, the TurboQuant codebook
 // and sign bits), so the codec holds no device memory and a launch needs no
 // host-to-device copy.
 #pragma once
@@ -66,7 +66,7 @@ struct Params {
   uint32_t n_segments;
   uint32_t role_sel;                    // 0 / 1: that role only; 2: both roles; 3: none
   uint32_t is_first;                    // this launch reports segments no launch encodes
-  uint32_t pad1;
+  uint32_t status_is_result;            // decode: status and result are the same array
   uint8_t* buf;                         // encode: slots written; decode: slots read
   uint64_t buf_bytes;
   uint8_t* status;                      // encode: written; decode: read
@@ -76,12 +76,12 @@ struct Params {
 enum Dir { kEncode = 0, kDecode = 1 };
 
 // Segment checksums (seal / verify).  CRC-32 over a slot is computed by one
-// warp: lane l reads the 16-byte chunks l, l + 32, ... of the slot (front
-// padded with zeros to a multiple of 512 bytes, which leaves a zero-preset CRC
-// unchanged) and keeps the zero-preset CRC register of its chunks, advanced by
-// 512 zero bytes per row; the lanes' registers are then advanced by the
-// 16 * (31 - l) bytes that follow their last chunk and xor-combined.  Every
-// step is a GF(2)-linear map of 32 bits, applied as 16-entry nibble tables.
+// warp: lane l folds the 64-byte blocks l, l + 32, ... of the slot (rows of
+// 2 KB from the slot's start, the last one possibly short) into a zero-preset
+// CRC register with byte tables, advancing the register by 2 KB of zero bytes
+// per row; the lanes' registers are then advanced by the bytes that follow
+// their last block and xor-combined.  The advances are GF(2)-linear maps of 32
+// bits, applied as 16-entry nibble tables.
 constexpr uint32_t kCrcBlock = 64;               // bytes a lane folds per row
 constexpr uint32_t kCrcRow = 32 * kCrcBlock;     // one row: a 64-byte block per lane
 struct CrcTables {
@@ -114,6 +114,9 @@ int launch_crc(const CrcParams& p, int seal, void* stream);
 // Kernel launchers (one per codec family), defined in the .cu files.  `codec`
 // is the KV_CODEC_* kind the launch runs; grid size is chosen from the device.
 int launch_fp8(const Params& p, int dir, uint32_t codec, void* stream);
+// FP8 encode that also writes the segment headers (q.headers), or decode that
+// first verifies them (result in p.result); one pass over the slots.
+int launch_fp8_sealed(const Params& p, const CrcParams& q, int dir, uint32_t codec, void* stream);
 int launch_uniform(const Params& p, int dir, uint32_t codec, void* stream);
 int launch_turboquant(const Params& p, int dir, uint32_t codec, void* stream);
 int launch_int8(const Params& p, int dir, uint32_t codec, void* stream);
@@ -122,7 +125,9 @@ int launch_int8(const Params& p, int dir, uint32_t codec, void* stream);
 // SM count x resident CTAs per SM, the latter the occupancy limit (cached per
 // device and kernel) capped at `max_per_sm`.  Defined in the host library.
 int grid_for(const void* kernel, uint32_t n_segments, int max_per_sm, unsigned* grid);
-// The same for a kernel launched with `threads` threads per CTA.
-int grid_for_threads(const void* kernel, uint32_t n_segments, int max_per_sm, int threads, unsigned* grid);
+// The same for a kernel launched with `threads` threads per CTA; odd: make the
+// grid odd (CTA-per-segment kernels), else the units are warps' segment groups.
+int grid_for_threads(const void* kernel, uint32_t n_segments, int max_per_sm, int threads, unsigned* grid,
+                     bool odd = true);
 
 }  // namespace kvc

@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(NT) uniform_encode_kernel(const __grid_constan
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
     if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
-    zero_padding(s.slot, (uint64_t)nv * (CB + 4), p.seg_bytes[s.role]);
+    zero_padding(s.slot, (uint64_t)nv * (CB + 4), p.seg_bytes[s.role], threadIdx.x, blockDim.x);
     __syncthreads();
     if (threadIdx.x == 0) {
       const uint32_t f = s_flag[it & 1];
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(NT) uniform_encode_lanes_kernel(const __grid_c
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
     if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
-    zero_padding(s.slot, (uint64_t)nv * (CB + 4), p.seg_bytes[s.role]);
+    zero_padding(s.slot, (uint64_t)nv * (CB + 4), p.seg_bytes[s.role], threadIdx.x, blockDim.x);
     __syncthreads();
     if (threadIdx.x == 0) {
       const uint32_t f = s_flag[it & 1];

@@ -158,3 +158,76 @@ def run_seal_parity(case: synth.Case, arm: synth.Arm, device="cuda", sign_versio
     assert np.array_equal(res.cpu().numpy()[:n], st_h), "verify rejected a sealed slot"
     codec.close()
     return int(np.count_nonzero(st_h == O.S_ENCODED))
+
+
+def run_sealed_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="cuda",
+                      buffers="device", tamper=0, seed=0, sign_version=1):
+    """The one-call paths against the oracle.  encode_sealed: statuses, ENCODED
+    slots and all headers equal the oracle's encode followed by seal.
+    decode_verified, on the oracle's slots and headers with `tamper` ENCODED
+    segments damaged on the host (a slot byte or a header field each): results
+    equal the oracle's verify followed by decode with those results, damaged
+    segments are CORRUPT and their pages keep the sentinel, the rest restore.
+    Returns (statuses, verified results)."""
+    codec = make_codec(case, arm, sign_version=sign_version)
+    g = oracle_geom(case, arm, sign_version=sign_version)
+    seg = [codec.segment_bytes(r)[0] for r in (0, 1)]
+    if rows is None:
+        rows, total = synth.segment_list(case, arm, seg)
+    elif total is None:
+        total = max([r[3] + seg[r[2]] for r in rows if r[2] <= 1 and r[3] < (1 << 32)] + [16])
+    n = len(rows)
+    d = oracle_descs(rows)
+    host_layers = [host_bits(t) for t in case.layers]
+    dev_layers = [t.to(device) for t in case.layers]
+    descs = _buffer(K.descriptors(rows, "cpu"), buffers, device)
+    out = _buffer(torch.full((max(total, 16),), SENTINEL_ENC, dtype=torch.uint8), buffers, device)
+    status = _buffer(torch.full((max(n, 1),), 0xEE, dtype=torch.uint8), buffers, device)
+    hdr = _buffer(torch.full((max(n, 1) * 32,), 0xEE, dtype=torch.uint8), buffers, device)
+    codec.encode_sealed(dev_layers, descs, n, out, total, status, hdr)
+    torch.cuda.synchronize()
+    enc_ref, st_ref = O.encode(g, host_layers, d, total)
+    hdr_ref = O.seal(g, d, enc_ref, st_ref)
+    st_gpu = status[:n].cpu().numpy()
+    assert np.array_equal(st_gpu, st_ref), f"status mismatch at {np.flatnonzero(st_gpu != st_ref)[:10]}"
+    enc_gpu = out[:total].cpu().numpy()
+    for (layer, blk, role, off), s in zip(rows, st_ref):
+        if s == O.S_ENCODED:
+            assert np.array_equal(enc_gpu[off:off + seg[role]], enc_ref[off:off + seg[role]]), \
+                f"slot (layer {layer}, block {blk}, role {role}) differs"
+    got = hdr[:32 * n].cpu().numpy()
+    want = hdr_ref.view(np.uint8)
+    if not np.array_equal(got, want):
+        bad = np.flatnonzero((got.reshape(n, 32) != want.reshape(n, 32)).any(axis=1))
+        raise AssertionError(f"headers differ at segments {bad[:10]}: got {got.view(O.HEADER_DTYPE)[bad[:3]]} "
+                             f"want {hdr_ref[bad[:3]]}")
+    # verify + decode of the oracle's slots and headers, some damaged
+    enc_bad = np.zeros(max(total, 16), dtype=np.uint8)
+    enc_bad[:total] = enc_ref
+    hdr_bad = hdr_ref.copy()
+    coded = np.flatnonzero(st_ref == O.S_ENCODED)
+    victims = np.random.default_rng(seed).choice(coded, size=min(tamper, coded.size), replace=False)
+    for k, i in enumerate(victims):
+        layer, blk, role, off = rows[i]
+        if k % 2 == 0:
+            enc_bad[off + (k * 977) % seg[role]] ^= 1 << (k % 8)
+        else:
+            hdr_bad[i][["crc32", "stored_bytes", "version", "format", "orig_bytes"][(k // 2) % 5]] ^= 1
+    dst_dev = [t.to(device) for t in case.layers]
+    for t in dst_dev:
+        t.view(torch.int16).fill_(SENTINEL_PAGE)
+    dst_host = [np.full_like(h, SENTINEL_PAGE) for h in host_layers]
+    enc_dev = _buffer(torch.from_numpy(enc_bad), buffers, device)
+    hdr_dev = _buffer(torch.from_numpy(hdr_bad.view(np.uint8).copy()), buffers, device)
+    result = _buffer(torch.full((max(n, 1),), 0xEE, dtype=torch.uint8), buffers, device)
+    codec.decode_verified(dst_dev, descs, n, enc_dev, total, hdr_dev, result)
+    torch.cuda.synchronize()
+    ver = O.verify(g, d, enc_bad[:total], hdr_bad)
+    res_ref = O.decode(g, dst_host, d, enc_bad[:total], ver)
+    res = result[:n].cpu().numpy()
+    assert np.array_equal(res, res_ref), f"results differ at {np.flatnonzero(res != res_ref)[:10]}"
+    assert set(np.flatnonzero(res == O.S_CORRUPT).tolist()) == set(victims.tolist())
+    for k, (a, b) in enumerate(zip(dst_dev, dst_host)):
+        assert compare_pages(host_bits(a), b, f"layer tensor {k}") == 0
+    codec.close()
+    return st_ref, res

@@ -32,3 +32,30 @@ def oracle_descs(rows):
         a = np.array(rows, dtype=np.uint64)
         d["layer"], d["block"], d["role"], d["enc_offset"] = a[:, 0], a[:, 1], a[:, 2], a[:, 3]
     return d
+
+
+def custom_case(*, D, H, T, L, B, dtype, layout, values="normal", seed=0):
+    """A seeded synthetic case of any geometry: per-vector log-normal magnitudes
+    ("normal") or Student-t(4) entries ("heavy"), clipped inside the FP8 range."""
+    g = torch.Generator().manual_seed(seed)
+    tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
+
+    def draw(shape):
+        if values == "normal":
+            x = torch.randn(shape, generator=g) * torch.exp(torch.randn(shape[:-1] + (1,), generator=g))
+        elif values == "heavy":
+            z = torch.randn(shape, generator=g)
+            chi = sum(torch.randn(shape, generator=g) ** 2 for _ in range(4))
+            x = z / torch.sqrt(chi / 4)
+        return x.clamp(-440, 440).to(tdt)
+
+    if layout == "separate":
+        layers = []
+        for _ in range(L):
+            layers += [draw((B, T, H, D)), draw((B, T, H, D))]
+        strides = synth._separate_strides(T, H, D)
+    else:
+        layers = [draw((B, H, T, 2 * D)) for _ in range(L)]
+        strides = synth._packed_strides(T, H, D)
+    amax = torch.rand(L, 2, generator=g) * 8 + 0.5
+    return synth.Case("custom", tdt, layout, D, H, T, L, B, strides, layers, [], seed, amax)

@@ -194,6 +194,10 @@ def test_call_argument_checks_need_no_gpu():
     with pytest.raises(K.KvCodecError) as e:     # missing status array
         c.encode([0x1000] * 8, 0x2000, 1, 0x3000, buf, None, stream=0)
     assert e.value.code == -1
+    for call in (c.encode, c.decode):             # more than 2^31 - 1 segments in one call
+        with pytest.raises(K.KvCodecError) as e:
+            call([0x1000] * 8, 0x2000, 1 << 31, 0x3000, buf, 0x4000, stream=0)
+        assert e.value.code == -1
     c.close()
 
 
@@ -214,6 +218,28 @@ def test_seal_verify_argument_checks_need_no_gpu():
     c.seal(0, 0, 0, 0, 0, 0, stream=0)                                 # n = 0: no-op
     c.verify(0, 0, 0, 0, 0, 0, stream=0)
     assert K.HEADER_DTYPE.itemsize == 32 == O.HEADER_DTYPE.itemsize
+    c.close()
+
+
+def test_sealed_and_verified_argument_checks_need_no_gpu():
+    c = K.Codec(**_kw())
+    buf = 16 * 1024
+    c.encode_sealed([None] * 8, 0, 0, 0, 0, 0, 0, stream=0)             # n = 0: no-op
+    c.decode_verified([None] * 8, 0, 0, 0, 0, 0, 0, stream=0)
+    cases = [
+        (lambda: c.encode_sealed([0x1000] * 8, 0x2000, 1, 0x3000, buf, 0x4000, None, stream=0), -1),
+        (lambda: c.encode_sealed([0x1000] * 8, 0x2000, 1, 0x3000, buf, 0x4000, 0x5004, stream=0), -5),
+        (lambda: c.encode_sealed([0x1000] * 8, 0x2000, 1, 0x3008, buf, 0x4000, 0x5000, stream=0), -5),
+        (lambda: c.encode_sealed([0x1000] * 7, 0x2000, 1, 0x3000, buf, 0x4000, 0x5000, stream=0), -1),
+        (lambda: c.decode_verified([0x1000] * 8, 0x2000, 1, 0x3000, buf, 0x5000, None, stream=0), -1),
+        (lambda: c.decode_verified([0x1000] * 8, 0x2000, 1, 0x3000, buf, None, 0x6000, stream=0), -1),
+        (lambda: c.decode_verified([0x1000] * 8, 0x2000, 1, 0x3000, buf, 0x5004, 0x6000, stream=0), -5),
+        (lambda: c.decode_verified([0x1008] * 8, 0x2000, 1, 0x3000, buf, 0x5000, 0x6000, stream=0), -5),
+    ]
+    for call, code in cases:
+        with pytest.raises(K.KvCodecError) as e:
+            call()
+        assert e.value.code == code
     c.close()
 
 

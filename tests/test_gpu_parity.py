@@ -11,6 +11,7 @@ import torch
 
 import oracle as O
 from gpu_parity import run_parity
+from kvcases import custom_case
 from kv_cache_page_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -28,31 +29,6 @@ def built():
 ALL_CODECS = [("fp8_cast", "fp8_cast"), ("fp8_fixed", "fp8_fixed"), ("fp8_dynamic", "fp8_dynamic"),
               ("tq3", "uni3"), ("tq4", "uni4"), ("uni8", "uni8"), ("uni3", "uni4"), ("none", "fp8_dynamic"),
               ("tq4", "none"), ("tq2", "uni2"), ("uni2", "uni8")]
-
-
-def custom_case(*, D, H, T, L, B, dtype, layout, values="normal", seed=0):
-    g = torch.Generator().manual_seed(seed)
-    tdt = torch.float16 if dtype == "fp16" else torch.bfloat16
-
-    def draw(shape):
-        if values == "normal":
-            x = torch.randn(shape, generator=g) * torch.exp(torch.randn(shape[:-1] + (1,), generator=g))
-        elif values == "heavy":
-            z = torch.randn(shape, generator=g)
-            chi = sum(torch.randn(shape, generator=g) ** 2 for _ in range(4))
-            x = z / torch.sqrt(chi / 4)
-        return x.clamp(-440, 440).to(tdt)
-
-    if layout == "separate":
-        layers = []
-        for _ in range(L):
-            layers += [draw((B, T, H, D)), draw((B, T, H, D))]
-        strides = synth._separate_strides(T, H, D)
-    else:
-        layers = [draw((B, H, T, 2 * D)) for _ in range(L)]
-        strides = synth._packed_strides(T, H, D)
-    amax = torch.rand(L, 2, generator=g) * 8 + 0.5
-    return synth.Case("custom", tdt, layout, D, H, T, L, B, strides, layers, [], seed, amax)
 
 
 @pytest.mark.parametrize("name", ["tiny"])
