@@ -153,7 +153,10 @@ __device__ __forceinline__ uint32_t fold_row(const NibbleTables& T, uint32_t tb,
 // rows and a tail row of t = (n mod 2048) / 64 blocks; lane l's last block is
 // then followed by 64 after_l bytes, after_l = t - 1 - l for l < t, else
 // 31 - l + t (at most 62), by which its register is advanced before the xor.
-template <bool NC = true, bool H = false>
+// PAIRS: fold two rows a step (two independent chains), which measured faster
+// for a warp finishing a slot it has just written and slower for the
+// standalone passes, whose 32 warps per SM already hide the chains' latency.
+template <bool NC = true, bool H = false, bool PAIRS = false>
 __device__ __forceinline__ uint32_t crc_rows(const NibbleTables& T, uint32_t tb, const uint8_t* slot, uint32_t n,
                                              uint32_t m0, uint32_t s, uint32_t crc_k, uint32_t lane,
                                              uint64_t pol = 0) {
@@ -161,7 +164,7 @@ __device__ __forceinline__ uint32_t crc_rows(const NibbleTables& T, uint32_t tb,
   const bool al32 = ((uintptr_t)slot & 31u) == 0;  // blocks start on 64-byte offsets of the slot
   uint32_t m = m0;
   // two rows a step: s = F_row(F_row(s) ^ R(block of row m)) ^ R(block of row m + 1)
-  for (; m + 2u <= rows; m += 2u) {
+  for (; PAIRS && m + 2u <= rows; m += 2u) {
     const uint8_t* src = slot + (uint64_t)m * kCrcRow + kCrcBlock * lane;
     uint4 c[4], d[4];
     load_block<NC, H>(src, al32, c, pol);
@@ -170,7 +173,7 @@ __device__ __forceinline__ uint32_t crc_rows(const NibbleTables& T, uint32_t tb,
     fold_block2(tb, c, d, rc, rd);
     s = apply8(T.row, apply8(T.row, s) ^ rc) ^ rd;
   }
-  if (m < rows) s = fold_row<NC, H>(T, tb, slot, m, al32, s, lane, pol);
+  for (; m < rows; ++m) s = fold_row<NC, H>(T, tb, slot, m, al32, s, lane, pol);
   uint32_t after = 31u - lane + tail;
   if (lane < tail) {
     s = fold_row<NC, H>(T, tb, slot, rows, al32, s, lane, pol);
@@ -256,7 +259,7 @@ __device__ __forceinline__ void seal_segment(const CrcParams& p, const NibbleTab
   uint32_t crc = 0;
   if (st == KV_SEG_ENCODED && p.codec[role] != KV_CODEC_NONE) {
     stored = p.seg_bytes[role];
-    crc = crc_rows<NC>(T, tb, p.buf + off, (uint32_t)stored, m0, s0, p.crc_k[role], lane);
+    crc = crc_rows<NC, false, !NC>(T, tb, p.buf + off, (uint32_t)stored, m0, s0, p.crc_k[role], lane);
   }
   if (lane == 0) store_header(p.headers + i, p.version, p.format[role], stored, crc, st, p.orig_bytes);
 }
