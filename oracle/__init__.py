@@ -55,6 +55,7 @@ class Geom(C.Structure):
         ("stride_head", C.c_int64), ("codec", C.c_int32 * 2), ("protect_first", C.c_int32),
         ("protect_last", C.c_int32), ("seed", C.c_uint64), ("reject_abs", C.c_float),
         ("sign_version", C.c_int32), ("fixed_amax", C.POINTER(C.c_float)),
+        ("fixed_overflow", C.c_int32), ("reserved", C.c_int32),
     ]
 
 
@@ -328,11 +329,12 @@ def unpack_bits(packed, n, bits):
 # ---------------------------------------------------------------- segments
 def make_geom(*, dtype, layout, head_dim, num_heads, block_tokens, num_layers, num_blocks,
               strides, codecs, protect=(0, 0), seed=0, reject_abs=448.0, fixed_amax=None,
-              sign_version=1):
+              sign_version=1, fixed_overflow=0):
     """Build the oracle's geometry.  `strides` = (block, token, head) in elements;
     `fixed_amax` = float32 [num_layers, 2] calibration absmax (FP8 fixed mode);
     `sign_version` 1: one TurboQuant sign vector per (seed, head dim), 2: one
-    per layer as well (format version 2)."""
+    per layer as well (format version 2); `fixed_overflow` 0: FP8 fixed-scale
+    quotients beyond +-448 are clipped, 1: such a segment stays raw."""
     g = Geom()
     g.dtype, g.layout, g.head_dim = dtype, layout, head_dim
     g.num_heads, g.block_tokens, g.num_layers = num_heads, block_tokens, num_layers
@@ -342,6 +344,7 @@ def make_geom(*, dtype, layout, head_dim, num_heads, block_tokens, num_layers, n
     g.protect_first, g.protect_last = protect
     g.seed = seed
     g.sign_version = sign_version
+    g.fixed_overflow = fixed_overflow
     g.reject_abs = reject_abs
     if fixed_amax is not None:
         fa = np.ascontiguousarray(fixed_amax, dtype=np.float32).reshape(-1)

@@ -468,6 +468,8 @@ typedef struct {
   float reject_abs;
   int32_t sign_version;             /* 0 or 1: one sign vector per (seed, D); 2: per layer too */
   const float* fixed_amax;          /* [num_layers][2] calibration absmax */
+  int32_t fixed_overflow;           /* FP8_FIXED: 0 = clip quotients to +-448, 1 = keep the segment raw */
+  int32_t reserved;
 } kvo_geom;
 
 /* The sign vector of a layer under the geometry's format version. */
@@ -622,6 +624,14 @@ void kvo_encode(const kvo_geom* g, void* const* ptrs, const kvo_desc* descs, uin
             s = kvo_fp8_scale_from_amax(kvo_absmax(x, D));
             memcpy(meta + (size_t)v * 4, &s, 4);
           }
+          /* READING: [OKV "FP8 and TurboQuant"] keeps values outside the
+           * range raw rather than clipping them; [ASYM "Precision and scaling
+           * reference"] clips quotients to +-448.  The clip is the default;
+           * with fixed_overflow = 1 a fixed-scale segment in which some FP32
+           * quotient x / s lies beyond +-448 stays raw (out of range). */
+          if (codec == O_FP8_FIXED && g->fixed_overflow == 1)
+            for (int e = 0; e < D; ++e)
+              if (fabsf(x[e] / s) > 448.0f) meta_overflow = 1;
           kvo_fp8_encode_vec(x, D, s, vc);
         } else if (is_tq(codec)) {
           uint16_t n16;

@@ -278,3 +278,104 @@ def test_restore_of_every_code_exact(dtype):
             if codes[t, d] == 0x80:
                 assert np.signbit(got[t, d])
     assert rounded_in_fp32 > 0
+
+
+def _fp16_values_near(t: Fraction, span: int):
+    """The FP16 values within `span` FP16 steps of t (t > 0 in the normal range)."""
+    c = int(np.array([float(t)], np.float16).view(np.uint16)[0])
+    return [float(np.array([c + k], np.uint16).view(np.float16)[0]) for k in range(-span, span + 1)]
+
+
+def _boundary_cases(pred, n):
+    """(calibration amax, FP16 x) pairs, found by a deterministic search over FP16
+    x and FP32 scales s within three steps of x / 448 that the fixed-scale rule
+    reaches (s = dynamic_scale(amax) for some FP32 amax), with pred(x, s) true."""
+    r448 = fl32(F(1, 448))
+    out = []
+    for bits in range(0x1800, 0x5C00):          # FP16 2^-9 .. 256, increasing
+        x = F(float(np.array([bits], np.uint16).view(np.float16)[0]))
+        s0 = np.float32(float(x / 448))
+        for k in range(-3, 4):
+            sv = s0
+            for _ in range(abs(k)):
+                sv = np.nextafter(sv, np.float32(np.inf if k > 0 else -np.inf), dtype=np.float32)
+            sf = F(float(sv))
+            if not pred(x, sf):
+                continue
+            a0 = np.float32(float(sf / r448))
+            for j in range(-4, 5):
+                av = a0
+                for _ in range(abs(j)):
+                    av = np.nextafter(av, np.float32(np.inf if j > 0 else -np.inf), dtype=np.float32)
+                if F(dynamic_scale(float(av))) == sf:
+                    out.append((float(av), float(x)))
+                    break
+            if len(out) == n:
+                return out
+            break
+    raise AssertionError("no boundary case found")
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_fixed_overflow_boundary(mode):
+    """FP8 fixed scales and quotients beyond +-448 ("KV precision and storage
+    encoding", section "FP8 and TurboQuant": values outside the range stay raw
+    rather than being clipped; "Asymmetric KV", section "Precision and scaling
+    reference": clipped to +-448).  Mode 0 clips (every segment encodes, the
+    largest codes 0x7E / 0xFE); mode 1 keeps a segment raw exactly when one of
+    its FP32 quotients fl32(x / s) lies beyond +-448.  Each segment holds one
+    FP16 value within a few steps of 448 s, for scales whose quotients straddle
+    the boundary, plus values where the FP32 quotient and two plausible slips
+    disagree: the exact quotient (beyond 448 while fl32(x / s) = 448) and the
+    product test |x| > fl32(448 s)."""
+    D, T = 64, 4                                 # 4 vectors: the slot saves half the bytes
+    amaxes = [0.37, 2.75, 19.0, 333.0]
+    cases = []                                   # (scale index, x)
+    for k, a in enumerate(amaxes):
+        s = dynamic_scale(a)
+        for x in _fp16_values_near(F(448) * F(s), 3):
+            cases.append((k, x))
+            cases.append((k, -x))
+    # exact quotient beyond 448 but its FP32 value 448 (encodes), and FP32
+    # quotient beyond 448 while x <= fl32(448 s) (stays raw)
+    for pred in (lambda x, s: x / s > 448 and fl32(x / s) == 448,
+                 lambda x, s: (fl32(x / s) > 448) != (x > fl32(448 * s))):
+        for a, x in _boundary_cases(pred, 3):
+            amaxes.append(a)
+            cases += [(len(amaxes) - 1, x), (len(amaxes) - 1, -x)]
+    B = len(cases)
+    L = len(amaxes)
+    fixed = np.array([[a, a] for a in amaxes], np.float32)
+    g = O.make_geom(dtype=O.FP16, layout=O.SEPARATE, head_dim=D, num_heads=1, block_tokens=T,
+                    num_layers=L, num_blocks=B, strides=(T * D, D, D), codecs=(O.FP8_FIXED, O.FP8_FIXED),
+                    fixed_amax=fixed, fixed_overflow=mode)
+    layers = []
+    for l in range(L):
+        for r in range(2):
+            x = np.zeros((B, T, D), np.float32)
+            for b, (k, v) in enumerate(cases):
+                if k == l:
+                    x[b, 2, 5] = v                  # token 2
+                    x[b, 0, 9] = -0.5 * v            # inside the range
+            layers.append(O.f32_to_f16(x.reshape(-1)))
+    seg = O.segment_enc_bytes(g, 0)
+    rows = [(k, b, r, (2 * b + r) * seg) for b, (k, _) in enumerate(cases) for r in range(2)]
+    enc, st = O.encode(g, layers, oracle_descs(rows), len(rows) * seg)
+    over = 0
+    for j, (k, b, r, off) in enumerate(rows):
+        s = dynamic_scale(amaxes[k])
+        q = fl32(F(cases[b][1]) / F(s))
+        beyond = abs(q) > 448
+        over += beyond
+        if mode == 1 and beyond:
+            assert st[j] == O.S_RAW_RANGE, (cases[b], s, q)
+        else:
+            assert st[j] == O.S_ENCODED, (cases[b], s, q)
+            assert enc[off + 2 * D + 5] == expected_code(cases[b][1], s)
+            if beyond:
+                assert enc[off + 2 * D + 5] in (0x7E, 0xFE)
+    # both sides of the boundary are present, including exact quotients above
+    # 448 that round to 448 in FP32 (encoded in both modes)
+    assert 0 < over < len(rows)
+    assert any(F(v) / F(dynamic_scale(amaxes[k])) > 448 and fl32(F(v) / F(dynamic_scale(amaxes[k]))) == 448
+               for k, v in cases)
