@@ -114,7 +114,8 @@ extern "C" {
 /* ---- per-segment status bytes (written by encode, read by decode) ------- */
 #define KV_SEG_ENCODED 1u       /* slot holds the encoding */
 #define KV_SEG_RAW_NONFINITE 2u /* an element is inf or NaN: keep raw */
-#define KV_SEG_RAW_RANGE 3u     /* an element has |x| > reject_abs: keep raw, no clipping */
+#define KV_SEG_RAW_RANGE 3u     /* an element has |x| > reject_abs (or, under KV_FIXED_OVERFLOW_REJECT,
+                                   an FP8 fixed-scale quotient beyond +-448): keep raw, no clipping */
 #define KV_SEG_RAW_PROTECTED 4u /* layer is in the protected first/last range */
 #define KV_SEG_RAW_POLICY 5u    /* the role's codec is KV_CODEC_NONE */
 #define KV_SEG_RAW_OVERSIZE 6u  /* source segment larger than 16 MiB */
@@ -156,7 +157,20 @@ typedef struct kv_codec_geometry {
                              with KV_ERR_INVALID_ARG */
   const float* fixed_amax; /* host, [num_layers][2] (K, V) calibration absolute maxima,
                               required iff a role uses FP8_FIXED; copied at create */
+  uint32_t fixed_overflow; /* FP8_FIXED quotients x / s beyond +-448 (calibration below the
+                              data's range): KV_FIXED_OVERFLOW_CLIP (0) clips them to +-448
+                              ("Asymmetric KV: methods and results", "Precision and scaling
+                              reference"); KV_FIXED_OVERFLOW_REJECT (1) keeps such a segment
+                              raw, status KV_SEG_RAW_RANGE ("KV precision and storage
+                              encoding", "FP8 and TurboQuant": out-of-range values stay raw
+                              rather than being clipped); other values are refused */
+  uint32_t reserved;       /* 0 */
 } kv_codec_geometry;
+/* struct_size: sizeof(kv_codec_geometry) (112 bytes), or 104 for the layout
+ * without fixed_overflow and reserved (taken as 0). */
+#define KV_CODEC_GEOMETRY_SIZE_V1 104u
+#define KV_FIXED_OVERFLOW_CLIP 0u
+#define KV_FIXED_OVERFLOW_REJECT 1u
 
 /* One segment to encode or decode.  Device-resident array, 24 bytes each.
  * A descriptor is invalid (status KV_SEG_BAD_DESC, nothing read or written) when

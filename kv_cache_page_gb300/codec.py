@@ -47,7 +47,10 @@ class Geometry(C.Structure):
         ("k_codec", C.c_uint32), ("v_codec", C.c_uint32), ("protect_first", C.c_uint32),
         ("protect_last", C.c_uint32), ("rotation_seed", C.c_uint64), ("reject_abs", C.c_float),
         ("sign_version", C.c_uint32), ("fixed_amax", C.POINTER(C.c_float)),
+        ("fixed_overflow", C.c_uint32), ("reserved", C.c_uint32),
     ]
+
+FIXED_OVERFLOW = {"clip": 0, "reject": 1}
 
 
 class KvCodecError(RuntimeError):
@@ -159,7 +162,7 @@ class Codec:
                  block_tokens: int, num_layers: int, num_blocks: int, strides: Sequence[int],
                  k_codec: str, v_codec: str, protect=(0, 0), rotation_seed: int = 0,
                  reject_abs: float = 448.0, fixed_amax=None, sign_version: int = 1,
-                 geometry_overrides=None):
+                 fixed_overflow: str = "clip", geometry_overrides=None):
         g = Geometry()
         g.abi_version, g.struct_size = ABI_VERSION, C.sizeof(Geometry)
         g.dtype, g.layout = DT[dtype], LAYOUT[layout]
@@ -170,6 +173,7 @@ class Codec:
         g.protect_first, g.protect_last = protect
         g.rotation_seed, g.reject_abs = rotation_seed, reject_abs
         g.sign_version = sign_version
+        g.fixed_overflow = FIXED_OVERFLOW[fixed_overflow]
         self._amax = None
         if fixed_amax is not None:
             self._amax = np.ascontiguousarray(np.asarray(fixed_amax, dtype=np.float32).reshape(-1))

@@ -189,6 +189,14 @@ __global__ void __launch_bounds__(Variant<Q>::kCtaThreads)
           sc = __fmul_rn(fmaxf(amax, 1e-12f), kRecip448);
           nr = -__frcp_rn(sc);
         }
+        if (CODEC == KV_CODEC_FP8_FIXED && p.fixed_reject) {
+          // the vector's largest |x / s| is RN(amax / s) (correctly rounded
+          // division is monotonic), formed as -RN(amax / s) by the steps of
+          // fp8_codes8; beyond 448 the segment stays raw (out of range)
+          const float q0 = __fmul_rn(amax, nr);
+          const float qn = __fmaf_rn(__fmaf_rn(q0, sc, amax), nr, q0);
+          if (qn < -448.0f) flags |= 2u;
+        }
         const bool in = j < nv;
 #pragma unroll
         for (int c = 0; c < NC; ++c) {

@@ -17,6 +17,8 @@
 #include <new>
 #include <utility>
 
+#include <cstddef>
+
 #include "kv_codec.h"
 #include "kv_internal.h"
 
@@ -457,12 +459,20 @@ int kv_codec_layer_signs(uint64_t seed, uint32_t layer, uint32_t head_dim, uint8
   return KV_OK;
 }
 
+static_assert(sizeof(kv_codec_geometry) == 112 && offsetof(kv_codec_geometry, fixed_overflow) == KV_CODEC_GEOMETRY_SIZE_V1,
+              "the geometry grows at its end only");
+
 int kv_codec_create(const kv_codec_geometry* g, kv_codec_t* out) {
   if (!out) return KV_ERR_INVALID_ARG;
   *out = nullptr;
   if (!g) return KV_ERR_INVALID_ARG;
-  if (g->abi_version != KV_CODEC_ABI_VERSION || g->struct_size != sizeof(kv_codec_geometry))
+  if (g->abi_version != KV_CODEC_ABI_VERSION ||
+      (g->struct_size != sizeof(kv_codec_geometry) && g->struct_size != KV_CODEC_GEOMETRY_SIZE_V1))
     return KV_ERR_ABI;
+  // fields past the earlier 104-byte layout are read only when the caller has them
+  const bool ext = g->struct_size >= sizeof(kv_codec_geometry);
+  const uint32_t fixed_overflow = ext ? g->fixed_overflow : KV_FIXED_OVERFLOW_CLIP;
+  if (fixed_overflow > KV_FIXED_OVERFLOW_REJECT || (ext && g->reserved != 0)) return KV_ERR_INVALID_ARG;
   if (g->dtype != KV_DT_FP16 && g->dtype != KV_DT_BF16) return KV_ERR_INVALID_ARG;
   if (g->layout != KV_LAYOUT_SEPARATE && g->layout != KV_LAYOUT_VLLM_PACKED) return KV_ERR_INVALID_ARG;
   if (!supported_dim(g->head_dim)) return KV_ERR_UNSUPPORTED_HEAD_DIM;
@@ -545,6 +555,7 @@ int kv_codec_create(const kv_codec_geometry* g, kv_codec_t* out) {
   }
   p.sign_seed = g->rotation_seed;
   p.sign_per_layer = g->sign_version == 2 ? 1u : 0u;
+  p.fixed_reject = fixed_overflow == KV_FIXED_OVERFLOW_REJECT ? 1u : 0u;
   if (is_tq(g->k_codec)) {
     const uint32_t bits = codec_bits(g->k_codec);
     make_codebook(bits, p.D, p.cent, p.bnd);

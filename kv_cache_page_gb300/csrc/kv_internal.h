@@ -47,7 +47,7 @@ struct Params {
   float neg_zero;                       // -0.0f (an FMA addend the compiler cannot fold)
   uint64_t sign_seed;                   // TurboQuant sign stream (SplitMix64 seed)
   uint32_t sign_per_layer;              // 1: format version 2, a sign vector per layer
-  uint32_t pad0;
+  uint32_t fixed_reject;                // FP8_FIXED: a quotient beyond +-448 keeps the segment raw
   float cent[16];                       // TurboQuant centroids (K codec)
   float bnd[16];                        // TurboQuant boundaries (K codec), bnd[15] unused
   // Index table of the unscaled WHT output w: code(w) = lut_lo[c] + (w > lut_thr[c]),

@@ -20,13 +20,14 @@ SENTINEL_ENC = 0xAB
 SENTINEL_PAGE = 0x7BCD  # an ordinary finite value, never produced by chance in bulk
 
 
-def make_codec(case: synth.Case, arm: synth.Arm, reject_abs=448.0, sign_version=1) -> K.Codec:
+def make_codec(case: synth.Case, arm: synth.Arm, reject_abs=448.0, sign_version=1,
+               fixed_overflow="clip") -> K.Codec:
     return K.Codec(dtype="fp16" if case.dtype == torch.float16 else "bf16", layout=case.layout,
                    head_dim=case.head_dim, num_kv_heads=case.num_heads,
                    block_tokens=case.block_tokens, num_layers=case.num_layers,
                    num_blocks=case.num_blocks, strides=case.strides, k_codec=arm.k_codec,
                    v_codec=arm.v_codec, protect=arm.protect, rotation_seed=case.seed,
-                   reject_abs=reject_abs, sign_version=sign_version,
+                   reject_abs=reject_abs, sign_version=sign_version, fixed_overflow=fixed_overflow,
                    fixed_amax=None if case.fixed_amax is None else case.fixed_amax.numpy())
 
 
@@ -73,16 +74,19 @@ def _offset_layer(t: torch.Tensor, device, offset_bytes: int) -> torch.Tensor:
 
 
 def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="cuda",
-               reject_abs=448.0, check_decode=True, buffers="device", layer_offset=0, sign_version=1):
+               reject_abs=448.0, check_decode=True, buffers="device", layer_offset=0, sign_version=1,
+               fixed_overflow="clip"):
     """Encode + decode `case` with `arm` on the GPU and in the oracle; assert parity.
     buffers="host" keeps descriptors, slots, statuses and results in pinned host
     memory (the kernels read and write them over the host link).  layer_offset
     places the source and restored layer tensors that many bytes past an aligned
     allocation (16: the 16-byte alignment the library requires, not 32).
     sign_version 2: TurboQuant sign vectors per layer (format version 2).
-    Returns (status array, number of restored elements off by one ulp)."""
-    codec = make_codec(case, arm, reject_abs, sign_version)
-    g = oracle_geom(case, arm, reject_abs, sign_version)
+    fixed_overflow "reject": FP8 fixed-scale segments with a quotient beyond
+    +-448 stay raw.  Returns (status array, number of restored elements off by
+    one ulp)."""
+    codec = make_codec(case, arm, reject_abs, sign_version, fixed_overflow)
+    g = oracle_geom(case, arm, reject_abs, sign_version, fixed_overflow)
     seg = [codec.segment_bytes(r)[0] for r in (0, 1)]
     assert seg == [0 if c == "none" else O.segment_enc_bytes(g, r)
                    for r, c in enumerate((arm.k_codec, arm.v_codec))]
@@ -161,7 +165,7 @@ def run_seal_parity(case: synth.Case, arm: synth.Arm, device="cuda", sign_versio
 
 
 def run_sealed_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="cuda",
-                      buffers="device", tamper=0, seed=0, sign_version=1):
+                      buffers="device", tamper=0, seed=0, sign_version=1, fixed_overflow="clip"):
     """The one-call paths against the oracle.  encode_sealed: statuses, ENCODED
     slots and all headers equal the oracle's encode followed by seal.
     decode_verified, on the oracle's slots and headers with `tamper` ENCODED
@@ -169,8 +173,8 @@ def run_sealed_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, d
     equal the oracle's verify followed by decode with those results, damaged
     segments are CORRUPT and their pages keep the sentinel, the rest restore.
     Returns (statuses, verified results)."""
-    codec = make_codec(case, arm, sign_version=sign_version)
-    g = oracle_geom(case, arm, sign_version=sign_version)
+    codec = make_codec(case, arm, sign_version=sign_version, fixed_overflow=fixed_overflow)
+    g = oracle_geom(case, arm, sign_version=sign_version, fixed_overflow=fixed_overflow)
     seg = [codec.segment_bytes(r)[0] for r in (0, 1)]
     if rows is None:
         rows, total = synth.segment_list(case, arm, seg)

@@ -15,7 +15,7 @@ def host_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16).reshape(-1).copy()
 
 
-def oracle_geom(case: synth.Case, arm: synth.Arm, reject_abs=448.0, sign_version=1):
+def oracle_geom(case: synth.Case, arm: synth.Arm, reject_abs=448.0, sign_version=1, fixed_overflow="clip"):
     return O.make_geom(
         dtype=O.FP16 if case.dtype == torch.float16 else O.BF16,
         layout=O.SEPARATE if case.layout == "separate" else O.PACKED,
@@ -23,6 +23,7 @@ def oracle_geom(case: synth.Case, arm: synth.Arm, reject_abs=448.0, sign_version
         num_layers=case.num_layers, num_blocks=case.num_blocks, strides=case.strides,
         codecs=(CODEC_IDS[arm.k_codec], CODEC_IDS[arm.v_codec]), protect=arm.protect,
         seed=case.seed, reject_abs=reject_abs, sign_version=sign_version,
+        fixed_overflow={"clip": 0, "reject": 1}[fixed_overflow],
         fixed_amax=None if case.fixed_amax is None else case.fixed_amax.numpy())
 
 

@@ -37,7 +37,21 @@ def test_exports_every_declared_symbol():
 
 def test_abi_version_and_struct_size():
     assert K.lib().kv_codec_abi_version() == K.ABI_VERSION
-    assert C.sizeof(K.Geometry) == 104
+    assert C.sizeof(K.Geometry) == 112
+
+
+def test_fixed_overflow_field_and_earlier_struct_size():
+    """fixed_overflow: clip (0) or reject (1), reserved must be 0; a geometry of
+    the earlier 104-byte layout (no fixed_overflow) is still accepted."""
+    kw = _kw(k_codec="fp8_fixed", v_codec="fp8_fixed", fixed_amax=np.ones((4, 2)))
+    for mode in ("clip", "reject"):
+        K.Codec(**kw, fixed_overflow=mode).close()
+    for over in ({"fixed_overflow": 2}, {"reserved": 1}, {"struct_size": 108}, {"struct_size": 96}):
+        with pytest.raises(K.KvCodecError) as e:
+            K.Codec(**kw, geometry_overrides=over)
+        assert e.value.code == (-7 if "struct_size" in over else -1)
+    # 104 bytes: the trailing fields are not read (a nonzero reserved is ignored)
+    K.Codec(**kw, geometry_overrides={"struct_size": 104, "fixed_overflow": 7, "reserved": 3}).close()
 
 
 def _kw(**over):

@@ -390,3 +390,45 @@ def test_per_layer_signs_full_pages(D):
         st, ulps = run_parity(case, synth.Arm("v2", kc, vc, (0, 1) if vc != "none" else (0,)),
                               sign_version=2)
         assert np.all(st == O.S_ENCODED) and ulps == 0
+
+
+def _calibrate_around_data(case):
+    """Calibration maxima per (layer, role) set against the data: layer 0 half
+    the largest |x| (most segments' quotients exceed 448), layer 1 above it
+    (none do), the rest at the median of the pages' maxima (about half do)."""
+    amax = torch.zeros(case.num_layers, 2)
+    for l in range(case.num_layers):
+        for r in range(2):
+            t = case.layers[2 * l + r] if case.layout == "separate" else \
+                case.layers[l][..., r * case.head_dim:(r + 1) * case.head_dim]
+            per_page = t.float().abs().flatten(1).amax(dim=1)
+            amax[l, r] = {0: 0.5 * per_page.max(), 1: 1.01 * per_page.max()}.get(l, per_page.median())
+    case.fixed_amax = amax
+
+
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+@pytest.mark.parametrize("dtype,layout", [("fp16", "separate"), ("bf16", "packed")])
+def test_fixed_overflow_reject(D, dtype, layout):
+    """FP8 fixed scales below the data's range ("KV precision and storage
+    encoding", "FP8 and TurboQuant": out-of-range values stay raw rather than
+    being clipped).  Under reject, a segment with a quotient beyond +-448 is
+    RAW_RANGE and the others encode, statuses and slots bit-exact against the
+    oracle; under the default clip every segment encodes."""
+    case = custom_case(D=D, H=4, T=16, L=4, B=8, dtype=dtype, layout=layout, seed=D + 3)
+    _calibrate_around_data(case)
+    arm = synth.Arm("fx", "fp8_fixed", "fp8_fixed", (0, 1))
+    st, ulps = run_parity(case, arm, fixed_overflow="reject")
+    assert ulps == 0
+    assert np.any(st == O.S_RAW_RANGE) and np.any(st == O.S_ENCODED)
+    st_clip, ulps = run_parity(case, arm)
+    assert ulps == 0 and np.all(st_clip == O.S_ENCODED)
+
+
+def test_fixed_overflow_reject_sealed():
+    """The same through the one-pass sealing encoder and verifying decoder."""
+    from gpu_parity import run_sealed_parity
+    case = custom_case(D=128, H=8, T=16, L=4, B=8, dtype="fp16", layout="separate", seed=77)
+    _calibrate_around_data(case)
+    st, res = run_sealed_parity(case, synth.Arm("fx", "fp8_fixed", "fp8_dynamic", (0, 1)),
+                                fixed_overflow="reject", tamper=2)
+    assert np.any(st == O.S_RAW_RANGE) and np.any(st == O.S_ENCODED)
