@@ -4,7 +4,10 @@ on the same bits, and compare.  Used by the GPU tests and the smoke check.
 Comparison rules: statuses bit-exact; ENCODED slots byte-exact (codes,
 metadata and zero padding); restored pages within one unit in the last place
 of the 16-bit format (+0 and -0 equal), which the kernels in fact meet
-exactly; restore results byte-exact.
+exactly; restore results byte-exact.  Bounds: every buffer a call may write
+sits between guard zones that must stay untouched, slot-buffer bytes outside
+the accepted descriptors' slots keep their sentinel, and encode leaves its
+source pages unchanged.
 """
 from __future__ import annotations
 
@@ -59,18 +62,47 @@ def _buffer(t: torch.Tensor, where: str, device) -> torch.Tensor:
     return t.to(device)
 
 
-def _offset_layer(t: torch.Tensor, device, offset_bytes: int) -> torch.Tensor:
-    """A device copy of the contiguous tensor `t` whose first element sits
-    `offset_bytes` past the start of its allocation (which is 256-byte aligned)."""
-    if offset_bytes == 0:
-        return t.to(device)
-    assert t.is_contiguous() and offset_bytes % t.element_size() == 0
-    k = offset_bytes // t.element_size()
-    base = torch.empty(t.numel() + k, dtype=t.dtype, device=device)
-    v = base[k:].view(t.shape)
-    v.copy_(t.to(device))
-    assert v.data_ptr() % 32 == offset_bytes % 32
-    return v
+GUARD = 4096           # sentinel bytes on each side of every buffer a call may write
+SENTINEL_GUARD = 0x5A
+
+
+class Guarded:
+    """A copy of `t` placed GUARD + offset_bytes bytes into an allocation filled
+    with SENTINEL_GUARD and followed by GUARD more sentinel bytes, in device or
+    pinned host memory (`where`).  The kernels get `.t`; `check()` asserts that
+    nothing outside it was written (a write past either end of a caller buffer,
+    e.g. from a wrong index in a ragged last step, lands in a guard).  With
+    offset_bytes = 16 the copy is 16- but not 32-byte aligned."""
+
+    def __init__(self, t: torch.Tensor, where: str, device, offset_bytes: int = 0):
+        t = t.contiguous()
+        nbytes = t.numel() * t.element_size()
+        self.lead, self.nbytes = GUARD + offset_bytes, nbytes
+        raw = torch.full((self.lead + nbytes + GUARD,), SENTINEL_GUARD, dtype=torch.uint8)
+        self.raw = raw.pin_memory() if where == "host" else raw.to(device)
+        self.t = self.raw[self.lead:self.lead + nbytes].view(t.dtype).view(t.shape)
+        self.t.copy_(t.to(self.t.device))
+        assert self.t.data_ptr() % 32 == offset_bytes % 32
+
+    def check(self, what: str):
+        r = self.raw.cpu().numpy()
+        bad = np.flatnonzero(np.concatenate([r[:self.lead], r[self.lead + self.nbytes:]]) != SENTINEL_GUARD)
+        assert bad.size == 0, f"{what}: {bad.size} guard bytes written"
+
+
+def guarded_layers(case: synth.Case, device, offset_bytes: int = 0):
+    return [Guarded(t, "device", device, offset_bytes) for t in case.layers]
+
+
+def check_slot_gaps(enc: np.ndarray, rows, seg, status, what: str):
+    """Bytes of the slot buffer outside the slot of every descriptor the call
+    accepted (status other than BAD_DESC) still hold SENTINEL_ENC."""
+    free = np.ones(enc.size, bool)
+    for (layer, blk, role, off), st in zip(rows, status):
+        if st != O.S_BAD_DESC and role <= 1:
+            free[off:off + seg[role]] = False
+    bad = np.flatnonzero(free & (enc != SENTINEL_ENC))
+    assert bad.size == 0, f"{what}: {bad.size} bytes written outside the slots, first at {bad[:5]}"
 
 
 def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="cuda",
@@ -95,17 +127,25 @@ def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="
     elif total is None:
         total = max([r[3] + seg[r[2]] for r in rows if r[2] <= 1 and r[3] < (1 << 32)] + [16])
     n = len(rows)
-    dev_layers = [_offset_layer(t, device, layer_offset) for t in case.layers]
+    src = guarded_layers(case, device, layer_offset)
+    dev_layers = [x.t for x in src]
     host_layers = [host_bits(t) for t in case.layers]
     descs = _buffer(K.descriptors(rows, "cpu"), buffers, device)
-    out = _buffer(torch.full((max(total, 16),), SENTINEL_ENC, dtype=torch.uint8), buffers, device)
-    status = _buffer(torch.full((max(n, 1),), 0xEE, dtype=torch.uint8), buffers, device)
+    out_g = Guarded(torch.full((max(total, 16),), SENTINEL_ENC, dtype=torch.uint8), buffers, device)
+    status_g = Guarded(torch.full((max(n, 1),), 0xEE, dtype=torch.uint8), buffers, device)
+    out, status = out_g.t, status_g.t
     codec.encode(dev_layers, descs, n, out, total, status)
     torch.cuda.synchronize()
+    for k, x in enumerate(src):
+        x.check(f"source layer {k}")
+        assert np.array_equal(host_bits(x.t), host_layers[k]), f"encode wrote source layer {k}"
+    out_g.check("slot buffer")
+    status_g.check("status array")
     enc_ref, st_ref = O.encode(g, host_layers, oracle_descs(rows), total)
     st_gpu = status[:n].cpu().numpy()
     assert np.array_equal(st_gpu, st_ref), f"status mismatch at {np.flatnonzero(st_gpu != st_ref)[:10]}"
     enc_gpu = out[:total].cpu().numpy()
+    check_slot_gaps(enc_gpu, rows, seg, st_ref, "encode")
     for (layer, blk, role, off), s in zip(rows, st_ref):
         if s == O.S_ENCODED:
             a, b = enc_gpu[off:off + seg[role]], enc_ref[off:off + seg[role]]
@@ -118,7 +158,8 @@ def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="
     ulps = 0
     if check_decode:
         # decode the oracle's encoding on the GPU into sentinel-filled pages
-        dst_dev = [_offset_layer(t, device, layer_offset) for t in case.layers]
+        dst_g = guarded_layers(case, device, layer_offset)
+        dst_dev = [x.t for x in dst_g]
         for t in dst_dev:
             t.view(torch.int16).fill_(SENTINEL_PAGE)
         dst_host = [np.full_like(h, SENTINEL_PAGE) for h in host_layers]
@@ -126,9 +167,14 @@ def run_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, device="
         enc_h[:total] = torch.from_numpy(enc_ref)
         enc_dev = _buffer(enc_h, buffers, device)
         st_dev = _buffer(torch.from_numpy(st_ref), buffers, device)
-        result = _buffer(torch.full((max(n, 1),), 0xEE, dtype=torch.uint8), buffers, device)
+        result_g = Guarded(torch.full((max(n, 1),), 0xEE, dtype=torch.uint8), buffers, device)
+        result = result_g.t
         codec.decode(dst_dev, descs, n, enc_dev, total, st_dev, result)
         torch.cuda.synchronize()
+        for k, x in enumerate(dst_g):
+            x.check(f"restored layer {k}")
+        result_g.check("result array")
+        assert np.array_equal(enc_dev.cpu().numpy(), enc_h.numpy()), "decode wrote the slot buffer"
         res_ref = O.decode(g, dst_host, oracle_descs(rows), enc_ref, st_ref)
         assert np.array_equal(result[:n].cpu().numpy(), res_ref)
         for k, (d_dev, d_host) in enumerate(zip(dst_dev, dst_host)):
@@ -149,12 +195,17 @@ def run_seal_parity(case: synth.Case, arm: synth.Arm, device="cuda", sign_versio
     descs = K.descriptors(rows, device)
     enc = torch.zeros(max(total, 16), dtype=torch.uint8, device=device)
     st = torch.zeros(max(n, 1), dtype=torch.uint8, device=device)
-    hdr = torch.zeros(max(n, 1) * 32, dtype=torch.uint8, device=device)
-    res = torch.zeros(max(n, 1), dtype=torch.uint8, device=device)
+    hdr_g = Guarded(torch.zeros(max(n, 1) * 32, dtype=torch.uint8), "device", device)
+    res_g = Guarded(torch.zeros(max(n, 1), dtype=torch.uint8), "device", device)
+    hdr, res = hdr_g.t, res_g.t
     codec.encode(layers, descs, n, enc, total, st)
+    enc_before = enc.cpu().numpy()
     codec.seal(descs, n, enc, total, st, hdr)
     codec.verify(descs, n, enc, total, hdr, res)
     torch.cuda.synchronize()
+    hdr_g.check("header array")
+    res_g.check("result array")
+    assert np.array_equal(enc.cpu().numpy(), enc_before), "seal or verify wrote the slot buffer"
     g = oracle_geom(case, arm, sign_version=sign_version)
     st_h = st.cpu().numpy()[:n]
     want = O.seal(g, oracle_descs(rows), enc.cpu().numpy()[:total], st_h)
@@ -183,18 +234,26 @@ def run_sealed_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, d
     n = len(rows)
     d = oracle_descs(rows)
     host_layers = [host_bits(t) for t in case.layers]
-    dev_layers = [t.to(device) for t in case.layers]
+    src = guarded_layers(case, device)
+    dev_layers = [x.t for x in src]
     descs = _buffer(K.descriptors(rows, "cpu"), buffers, device)
-    out = _buffer(torch.full((max(total, 16),), SENTINEL_ENC, dtype=torch.uint8), buffers, device)
-    status = _buffer(torch.full((max(n, 1),), 0xEE, dtype=torch.uint8), buffers, device)
-    hdr = _buffer(torch.full((max(n, 1) * 32,), 0xEE, dtype=torch.uint8), buffers, device)
+    bufs = [Guarded(torch.full((max(total, 16),), SENTINEL_ENC, dtype=torch.uint8), buffers, device),
+            Guarded(torch.full((max(n, 1),), 0xEE, dtype=torch.uint8), buffers, device),
+            Guarded(torch.full((max(n, 1) * 32,), 0xEE, dtype=torch.uint8), buffers, device)]
+    out, status, hdr = (x.t for x in bufs)
     codec.encode_sealed(dev_layers, descs, n, out, total, status, hdr)
     torch.cuda.synchronize()
+    for k, x in enumerate(src):
+        x.check(f"source layer {k}")
+        assert np.array_equal(host_bits(x.t), host_layers[k]), f"encode wrote source layer {k}"
+    for x, what in zip(bufs, ("slot buffer", "status array", "header array")):
+        x.check(what)
     enc_ref, st_ref = O.encode(g, host_layers, d, total)
     hdr_ref = O.seal(g, d, enc_ref, st_ref)
     st_gpu = status[:n].cpu().numpy()
     assert np.array_equal(st_gpu, st_ref), f"status mismatch at {np.flatnonzero(st_gpu != st_ref)[:10]}"
     enc_gpu = out[:total].cpu().numpy()
+    check_slot_gaps(enc_gpu, rows, seg, st_ref, "encode_sealed")
     for (layer, blk, role, off), s in zip(rows, st_ref):
         if s == O.S_ENCODED:
             assert np.array_equal(enc_gpu[off:off + seg[role]], enc_ref[off:off + seg[role]]), \
@@ -217,15 +276,21 @@ def run_sealed_parity(case: synth.Case, arm: synth.Arm, rows=None, total=None, d
             enc_bad[off + (k * 977) % seg[role]] ^= 1 << (k % 8)
         else:
             hdr_bad[i][["crc32", "stored_bytes", "version", "format", "orig_bytes"][(k // 2) % 5]] ^= 1
-    dst_dev = [t.to(device) for t in case.layers]
+    dst_g = guarded_layers(case, device)
+    dst_dev = [x.t for x in dst_g]
     for t in dst_dev:
         t.view(torch.int16).fill_(SENTINEL_PAGE)
     dst_host = [np.full_like(h, SENTINEL_PAGE) for h in host_layers]
     enc_dev = _buffer(torch.from_numpy(enc_bad), buffers, device)
     hdr_dev = _buffer(torch.from_numpy(hdr_bad.view(np.uint8).copy()), buffers, device)
-    result = _buffer(torch.full((max(n, 1),), 0xEE, dtype=torch.uint8), buffers, device)
+    result_g = Guarded(torch.full((max(n, 1),), 0xEE, dtype=torch.uint8), buffers, device)
+    result = result_g.t
     codec.decode_verified(dst_dev, descs, n, enc_dev, total, hdr_dev, result)
     torch.cuda.synchronize()
+    for k, x in enumerate(dst_g):
+        x.check(f"restored layer {k}")
+    result_g.check("result array")
+    assert np.array_equal(enc_dev.cpu().numpy(), enc_bad), "decode wrote the slot buffer"
     ver = O.verify(g, d, enc_bad[:total], hdr_bad)
     res_ref = O.decode(g, dst_host, d, enc_bad[:total], ver)
     res = result[:n].cpu().numpy()
