@@ -124,3 +124,39 @@ def test_format_version_2_headers():
     case = synth.make_case("tiny")
     run_sealed_parity(case, case.arms[0], sign_version=2, tamper=2)
     run_sealed_parity(case, case.arms[1], sign_version=2, tamper=2)
+
+
+@pytest.mark.parametrize("T,coded", [(512, True), (513, False)])
+def test_maximum_segment_size(T, coded):
+    """A 16 MiB source segment (64 heads x 512 tokens x 256 dims, FP16) is sealed
+    and verified in one pass by a single warp; one token more and it stays raw
+    (OVERSIZE), its header saying so."""
+    case = custom_case(D=256, H=64, T=T, L=1, B=1, dtype="fp16", layout="separate")
+    st, res = run_sealed_parity(case, synth.Arm("max", "fp8_dynamic", "fp8_fixed", (0, 1)),
+                                tamper=1 if coded else 0)
+    want = O.S_ENCODED if coded else O.S_RAW_OVERSIZE
+    assert list(st) == [want, want]
+    if coded:
+        assert sorted(res.tolist()) == [O.S_ENCODED, O.S_CORRUPT]
+
+
+def test_every_16bit_pattern():
+    """All 65,536 FP16 patterns through the sealing encoder and the verifying
+    decoder: in-range values fill admitted pages, each nonfinite or out-of-range
+    pattern sits alone in a page of its own (raw, header status included)."""
+    allp = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f = O.src_to_f32(allp, O.FP16)
+    ok = np.isfinite(f) & (np.abs(f) <= 448)
+    good, bad = allp[ok], allp[~ok]
+    per = 128 * 8 * 16
+    ng = -(-good.size // per)
+    buf = np.zeros((ng + bad.size) * per, np.uint16)
+    buf[: good.size] = good
+    for i, b in enumerate(bad):
+        buf[(ng + i) * per + 37] = b
+    B = ng + bad.size
+    t = torch.from_numpy(buf.view(np.int16)).view(torch.float16).reshape(B, 16, 8, 128)
+    case = synth.Case("all16", torch.float16, "separate", 128, 8, 16, 1, B,
+                      synth._separate_strides(16, 8, 128), [t, t.clone()], [], 0, torch.ones(1, 2))
+    st, res = run_sealed_parity(case, synth.Arm("all", "fp8_dynamic", "fp8_cast", (0, 1)), tamper=4)
+    assert np.any(st == O.S_ENCODED) and np.any(st == O.S_RAW_NONFINITE) and np.any(st == O.S_RAW_RANGE)
