@@ -625,8 +625,12 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
   const uint32_t grp = lane / G, li = lane % G;
   // each warp's output sign masks of its current layer: row l, chunk c
   __shared__ uint4 s_sign[W][4][9];
-  // (centroid[lo code], centroid[hi code]) for every pair of codes, REP copies
-  __shared__ float2 s_pair[NPAIR * REP];
+  // (centroid[lo code], centroid[hi code]) for every pair of codes, REP copies;
+  // 2-bit codes: the four centroids of every code byte instead, REPQ copies
+  // (a quarter warp's eight 16-byte reads then fall in distinct banks)
+  constexpr int REPQ = 8;
+  __shared__ float2 s_pair[BITS == 2 ? 1 : NPAIR * REP];
+  __shared__ float4 s_quad[BITS == 2 ? 256 * REPQ : 1];
   // D = 64 (one lane per vector): 16 restored vectors of each warp at a time,
   // 128 bytes a row, 16-byte chunk q of row r at position q ^ (r & 7)
   __shared__ uint4 s_out[G == 1 ? W : 1][G == 1 ? 16 : 1][8];
@@ -643,12 +647,20 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
     __syncwarp();
   };
   uint32_t sign_layer = 0xffffffffu;
-  for (int k = threadIdx.x; k < NPAIR * REP; k += blockDim.x) {
-    const int v = k / REP;
-    s_pair[k] = make_float2(p.cent[v & ((1 << BITS) - 1)], p.cent[v >> BITS]);
+  if (BITS == 2) {
+    for (int k = threadIdx.x; k < 256 * REPQ; k += blockDim.x) {
+      const int v = k / REPQ;
+      s_quad[k] = make_float4(p.cent[v & 3], p.cent[(v >> 2) & 3], p.cent[(v >> 4) & 3], p.cent[v >> 6]);
+    }
+  } else {
+    for (int k = threadIdx.x; k < NPAIR * REP; k += blockDim.x) {
+      const int v = k / REP;
+      s_pair[k] = make_float2(p.cent[v & ((1 << BITS) - 1)], p.cent[v >> BITS]);
+    }
   }
   __syncthreads();
-  const uint32_t pair_base = (uint32_t)__cvta_generic_to_shared(s_pair) + (lane % REP) * 8u;
+  const uint32_t pair_base = BITS == 2 ? (uint32_t)__cvta_generic_to_shared(s_quad) + (lane % REPQ) * 16u
+                                       : (uint32_t)__cvta_generic_to_shared(s_pair) + (lane % REP) * 8u;
   const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&s_sign[warp][li][0]);
   const uint32_t run_a = tq64_run_start<G>(li, 0), run_b = tq64_run_start<G>(li, 1);
   const uint32_t cmask = (G >= 2 && (li & 1u)) ? 0xffffffffu : 0u;  // complement the upper codes
@@ -713,19 +725,27 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
       if (j0 + VPW < nv) fetch(cur, j + VPW, cwn, nn);
       else if (ni != 0xffffffffu) fetch(nxt, jw, cwn, nn);
       float2 a[32];
+      if (BITS == 2) {  // code byte q: elements 4q .. 4q + 3
 #pragma unroll
-      for (int m = 0; m < 32; ++m) {
-        uint32_t v;
-        if (BITS == 4) {
-          v = __byte_perm(cw[m >> 2], 0, 0x4440 | (m & 3));
-        } else if (BITS == 2) {
-          v = (cw[m >> 3] >> (4 * (m & 7))) & 15u;
-        } else {
-          const int bit = 6 * m;
-          v = (bit & 31) <= 26 ? (cw[bit >> 5] >> (bit & 31)) & 63u
-                               : __funnelshift_r(cw[bit >> 5], cw[(bit >> 5) + 1], bit & 31) & 63u;
+        for (int q = 0; q < 16; ++q) {
+          const uint32_t v = __byte_perm(cw[q >> 2], 0, 0x4440 | (q & 3));
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(a[2 * q].x), "=f"(a[2 * q].y), "=f"(a[2 * q + 1].x), "=f"(a[2 * q + 1].y)
+                       : "r"(v * (16u * REPQ) + pair_base));
         }
-        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(a[m].x), "=f"(a[m].y) : "r"(v * (8u * REP) + pair_base));
+      } else {
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+          uint32_t v;
+          if (BITS == 4) {
+            v = __byte_perm(cw[m >> 2], 0, 0x4440 | (m & 3));
+          } else {
+            const int bit = 6 * m;
+            v = (bit & 31) <= 26 ? (cw[bit >> 5] >> (bit & 31)) & 63u
+                                 : __funnelshift_r(cw[bit >> 5], cw[(bit >> 5) + 1], bit & 31) & 63u;
+          }
+          asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(a[m].x), "=f"(a[m].y) : "r"(v * (8u * REP) + pair_base));
+        }
       }
       const float nc = __fsqrt_rn(vector_sumsq<G>(a));
       const float g = __fdiv_rn(__half2float(__ushort_as_half(n16)), nc);
@@ -805,8 +825,12 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
   // each warp's output sign masks of its current layer: row li, group c covers
   // the 8 elements from split_group_start<G>(li, c)
   __shared__ uint4 s_sign[W][G][5];
-  // (centroid[lo code], centroid[hi code]) for every pair of codes, REP copies
-  __shared__ float2 s_pair[NPAIR * REP];
+  // (centroid[lo code], centroid[hi code]) for every pair of codes, REP copies;
+  // 2-bit codes: the four centroids of every code byte instead, REPQ copies
+  // (a quarter warp's eight 16-byte reads then fall in distinct banks)
+  constexpr int REPQ = 8;
+  __shared__ float2 s_pair[BITS == 2 ? 1 : NPAIR * REP];
+  __shared__ float4 s_quad[BITS == 2 ? 256 * REPQ : 1];
   auto build_signs = [&](uint32_t layer) {
     __syncwarp();  // every lane is done with the previous layer's masks
     for (uint32_t q = lane; q < (uint32_t)G * 16u; q += 32u) {
@@ -818,12 +842,20 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
     __syncwarp();
   };
   uint32_t sign_layer = 0xffffffffu;
-  for (int k = threadIdx.x; k < NPAIR * REP; k += blockDim.x) {
-    const int v = k / REP;
-    s_pair[k] = make_float2(p.cent[v & ((1 << BITS) - 1)], p.cent[v >> BITS]);
+  if (BITS == 2) {
+    for (int k = threadIdx.x; k < 256 * REPQ; k += blockDim.x) {
+      const int v = k / REPQ;
+      s_quad[k] = make_float4(p.cent[v & 3], p.cent[(v >> 2) & 3], p.cent[(v >> 4) & 3], p.cent[v >> 6]);
+    }
+  } else {
+    for (int k = threadIdx.x; k < NPAIR * REP; k += blockDim.x) {
+      const int v = k / REP;
+      s_pair[k] = make_float2(p.cent[v & ((1 << BITS) - 1)], p.cent[v >> BITS]);
+    }
   }
   __syncthreads();
-  const uint32_t pair_base = (uint32_t)__cvta_generic_to_shared(s_pair) + (lane % REP) * 8u;
+  const uint32_t pair_base = BITS == 2 ? (uint32_t)__cvta_generic_to_shared(s_quad) + (lane % REPQ) * 16u
+                                       : (uint32_t)__cvta_generic_to_shared(s_pair) + (lane % REP) * 8u;
   const uint32_t sign_addr = (uint32_t)__cvta_generic_to_shared(&s_sign[warp][li][0]);
   const float cD = p.wht_scale;
   const float2 cD2 = make_float2(cD, cD);
