@@ -907,18 +907,26 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
       if (j0 + VPW < nv) fetch(cur, j + VPW, cwn, nn);
       else if (ni != 0xffffffffu) fetch(nxt, jw, cwn, nn);
       float2 a[16];
+      if (BITS == 2) {  // code byte q: elements 4q .. 4q + 3
 #pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        uint32_t v;
-        if (BITS == 4) {
-          v = __byte_perm(cw[m >> 2], 0, 0x4440 | (m & 3));
-        } else if (BITS == 2) {
-          v = (cw[m >> 3] >> (4 * (m & 7))) & 15u;
-        } else {
-          const int bit = 6 * m;
-          v = __funnelshift_r(cw[bit >> 5], cw[(bit >> 5) + 1], bit & 31) & 63u;
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t v = __byte_perm(cw[q >> 2], 0, 0x4440 | (q & 3));
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(a[2 * q].x), "=f"(a[2 * q].y), "=f"(a[2 * q + 1].x), "=f"(a[2 * q + 1].y)
+                       : "r"(v * (16u * REPQ) + pair_base));
         }
-        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(a[m].x), "=f"(a[m].y) : "r"(v * (8u * REP) + pair_base));
+      } else {
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          uint32_t v;
+          if (BITS == 4) {
+            v = __byte_perm(cw[m >> 2], 0, 0x4440 | (m & 3));
+          } else {
+            const int bit = 6 * m;
+            v = __funnelshift_r(cw[bit >> 5], cw[(bit >> 5) + 1], bit & 31) & 63u;
+          }
+          asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(a[m].x), "=f"(a[m].y) : "r"(v * (8u * REP) + pair_base));
+        }
       }
       const float nc = __fsqrt_rn(vector_sumsq<G>(a));
       const float g = __fdiv_rn(__half2float(__ushort_as_half(n16)), nc);
