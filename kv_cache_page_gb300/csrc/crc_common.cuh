@@ -191,12 +191,6 @@ __device__ __forceinline__ uint32_t crc_rows(const NibbleTables& T, uint32_t tb,
   return s ^ crc_k;
 }
 
-template <bool NC = true>
-__device__ __forceinline__ uint32_t warp_crc(const NibbleTables& T, uint32_t tb, const uint8_t* slot, uint32_t n,
-                                             uint32_t crc_k, uint32_t lane) {
-  return crc_rows<NC>(T, tb, slot, n, 0, 0, crc_k, lane);
-}
-
 // Fill the shared tables; returns the shared address of this lane's copy of
 // byte table 0.
 __device__ __forceinline__ uint32_t load_tables(const CrcParams& p, NibbleTables*& nt) {

@@ -320,10 +320,6 @@ __device__ __forceinline__ void st32_h(void* ptr, const uint4& a, const uint4& b
 __device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes, uint64_t pol) {
-  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(ptr), "r"(bytes), "l"(pol)
-               : "memory");
-}
 
 // Zero the alignment padding [used, seg_bytes) of a slot: threads first,
 // first + step, ... (the whole CTA: threadIdx.x, blockDim.x; one warp: lane, 32).
