@@ -191,6 +191,44 @@ __device__ __forceinline__ uint32_t crc_rows(const NibbleTables& T, uint32_t tb,
   return s ^ crc_k;
 }
 
+// The same by one half warp, the other half coding another slot at the same
+// time: rows of 1 KB (16 blocks of 64 bytes), so a slot is rounded up to a
+// whole number of 1 KB rows rather than 2 KB (FP8 dynamic slots of 16,896
+// bytes: 17 half rows for 16.5, against 9 rows for 8.25).  Lane h = lane & 15
+// folds block h of every row; its register is advanced by 1 KB per row
+// (fin[4], 64 * 16 bytes) and at the end by the at most 30 blocks after its
+// last block.  Every lane of the warp calls it (the final xor is a half-warp
+// shuffle); n = 0 gives crc_k.  Every lane of a half returns its slot's CRC.
+template <bool NC = true>
+__device__ __forceinline__ uint32_t crc_rows_half(const NibbleTables& T, uint32_t tb, const uint8_t* slot,
+                                                  uint32_t n, uint32_t crc_k, uint32_t lane) {
+  constexpr uint32_t kHalfRow = kCrcRow / 2;
+  const uint32_t h = lane & 15u;
+  const uint32_t rows = n / kHalfRow, tail = (n % kHalfRow) / kCrcBlock;
+  const bool al32 = ((uintptr_t)slot & 31u) == 0;
+  uint32_t s = 0;
+  for (uint32_t m = 0; m < rows; ++m) {
+    uint4 c[4];
+    load_block<NC>(slot + (uint64_t)m * kHalfRow + kCrcBlock * h, al32, c);
+    s = apply8(T.fin[4], s) ^ fold_block(tb, c);
+  }
+  uint32_t after = 15u - h + tail;
+  if (h < tail) {
+    uint4 c[4];
+    load_block<NC>(slot + (uint64_t)rows * kHalfRow + kCrcBlock * h, al32, c);
+    s = apply8(T.fin[4], s) ^ fold_block(tb, c);
+    after = tail - 1u - h;
+  }
+#pragma unroll
+  for (int b = 0; b < 5; ++b) {
+    const uint32_t t = apply8(T.fin[b], s);
+    s = ((after >> b) & 1u) ? t : s;
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) s ^= __shfl_xor_sync(0xffffffffu, s, o);
+  return s ^ crc_k;
+}
+
 // Fill the shared tables; returns the shared address of this lane's copy of
 // byte table 0.
 __device__ __forceinline__ uint32_t load_tables(const CrcParams& p, NibbleTables*& nt) {
