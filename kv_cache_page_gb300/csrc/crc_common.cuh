@@ -1,6 +1,6 @@
-// crc_common.cuh -- CRC-32 of encoded slots by one warp, shared by the seal /
-// verify kernels and the codec kernels that seal or verify a slot in the same
-// pass as they encode or decode it.
+// crc_common.cuh -- CRC-32 of encoded slots by a warp (or a half warp), shared
+// by the seal / verify kernels and the codec kernels that seal or verify a
+// slot in the same pass as they encode or decode it.
 //
 // "KV precision and storage encoding" (OrbitKV docs), section "Ownership,
 // storage and GDS": each encoded segment carries a version, its original
@@ -18,7 +18,8 @@
 // and keeps s = F_2048(s) ^ R(block).  Finally it advances s by the bytes that
 // follow its last block (a multiple of 64, below 4 KB); the xor of the lanes is
 // R(M).  Rows can be folded as soon as they are written, which lets an encoder
-// checksum its slot while it is still producing it.
+// checksum its slot while it is still producing it.  The standalone passes
+// give each half warp a slot of its own, with 1 KB rows (crc_rows_half).
 //
 // The byte tables sit in shared memory in 32 copies, entry e of copy l in bank
 // l, so the 32 lookups of a warp never conflict: 4 x 256 x 32 words (128 KB),

@@ -85,19 +85,21 @@ __device__ __forceinline__ uint8_t status_of_flags(uint32_t f) {
 }
 
 // The second kernel parameter selects the variant.  NoSeal: the plain kernel,
-// one CTA of kThreads per segment.  CrcParams: the sealing encoder /
-// verifying decoder, one warp per segment in 1024-thread CTAs (one per SM)
-// holding the CRC lookup tables.  The sealing encoder codes its segment, then
-// -- after __syncwarp, with plain loads, since its lanes have just written the
-// slot and the bytes sit in L2 -- computes the slot's CRC-32 and writes the
-// header kv_codec_seal would write.  The verifying decoder first checks header
-// and CRC-32 exactly as kv_codec_verify does and restores the segment only when
-// they match, re-reading the slot from L2: a damaged slot is never scattered,
-// and HBM carries each slot once either way.  The sealing encoder folds each
-// 2 KB row of codes into its CRC while the loads of its next vectors are in
-// flight, so its warps keep streaming.  (The vector loop is written out
-// in the kernel bodies: moved into a helper function it compiled to half again
-// as many registers, which cost the plain encoder two of its six CTAs per SM.)
+// one CTA of kThreads per segment.  CrcParams: one warp per segment, in
+// 1024-thread CTAs (one per SM) holding the CRC lookup tables.
+//  * Sealing encoder: every encode step writes 1 KB of codes.  At the start of
+//    every second step, with that step's loads in flight, the warp folds the
+//    2 KB CRC row its last two steps wrote (after __syncwarp, with plain loads:
+//    the bytes were just written and sit in L2) and prefetches the vectors two
+//    steps ahead into L2.  The rows left after the last step follow, then the
+//    header kv_codec_seal would write.
+//  * Verifying decoder: checks header and CRC-32 exactly as kv_codec_verify
+//    does (loads with an L2 evict_last policy) and restores the segment only
+//    when they match, re-reading the slot from L2 (evict_first, like the page
+//    stores): a damaged slot is never scattered.
+// (The vector loop is written out in the kernel bodies: moved into a helper
+// function it compiled to half again as many registers, which cost the plain
+// encoder two of its six CTAs per SM.)
 struct NoSeal {};
 template <typename Q>
 struct Variant {
