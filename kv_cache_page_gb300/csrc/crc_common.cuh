@@ -30,6 +30,8 @@
 // The advance maps are 16-entry nibble tables (a table fills 16 distinct
 // banks, so any indices are conflict-free).
 #pragma once
+#include <type_traits>
+
 #include "device_common.cuh"
 
 namespace kvc {
@@ -326,4 +328,55 @@ __device__ __forceinline__ uint32_t verify_segment(const CrcParams& p, const Nib
 }
 
 }  // namespace crc
+
+// The codec kernels' second parameter selects their variant.  NoSeal: the
+// plain kernel, a CTA of NT threads per segment.  CrcParams: one warp per
+// segment in kCrcThreads-thread CTAs (one per SM) that hold the CRC tables;
+// the encoder seals each slot as it writes it, the decoder verifies each slot
+// before it restores it.
+struct NoSeal {};
+template <typename Q, int NT = kThreads>
+struct Variant {
+  static constexpr bool kSeal = !std::is_same<Q, NoSeal>::value;
+  static constexpr int kCtaThreads = kSeal ? crc::kCrcThreads : NT;
+};
+
+// Status of an encoded segment from its admission flags (bit 0: a nonfinite
+// value, bit 1: a value beyond the admission bound).
+__device__ __forceinline__ uint8_t status_of_flags(uint32_t f) {
+  return (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+}
+
+// Plain launch of a codec kernel's NoSeal variant: `threads` per CTA, at most
+// max_per_sm CTAs per SM.
+inline int launch_plain(void (*kernel)(Params, NoSeal), const Params& p, void* stream, int max_per_sm,
+                        int threads = kThreads) {
+  const void* k = reinterpret_cast<const void*>(kernel);
+  unsigned grid = 0;
+  const int rc = grid_for_threads(k, p.n_segments, max_per_sm, threads, &grid);
+  if (rc != KV_OK || grid == 0) return rc;
+  NoSeal none;
+  void* args[] = {const_cast<Params*>(&p), &none};
+  const cudaError_t e = cudaLaunchKernel(k, dim3(grid), dim3(threads), args, 0, (cudaStream_t)stream);
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
+// Launch of a codec kernel's CrcParams variant: one CTA of kCrcThreads per SM
+// at most, kCrcSmem bytes of dynamic shared memory for the tables.
+inline int launch_sealed(void (*kernel)(Params, CrcParams), const Params& p, const CrcParams& q, void* stream) {
+  const void* k = reinterpret_cast<const void*>(kernel);
+  // the tables need more than the default 48 KB of dynamic shared memory (set
+  // on every launch: the attribute belongs to the current device's context)
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)crc::kCrcSmem) != cudaSuccess)
+    return KV_ERR_CUDA;
+  unsigned grid = 0;
+  const int rc = grid_for_threads(k, (p.n_segments + crc::kCrcWarps - 1) / crc::kCrcWarps, 1,
+                                  crc::kCrcThreads, &grid, false);
+  if (rc != KV_OK || grid == 0) return rc;
+  void* args[] = {const_cast<Params*>(&p), const_cast<CrcParams*>(&q)};
+  const cudaError_t e = cudaLaunchKernel(k, dim3(grid), dim3(crc::kCrcThreads), args, crc::kCrcSmem,
+                                         (cudaStream_t)stream);
+  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+
 }  // namespace kvc

@@ -18,8 +18,6 @@
 // headers' CRC-32 without a second pass over the slots in HBM: section
 // "Ownership, storage and GDS" of the same OrbitKV page asks for a CRC32 per
 // stored segment, checked before GPU decode.
-#include <type_traits>
-
 #include "crc_common.cuh"
 
 namespace kvc {
@@ -80,13 +78,8 @@ __device__ __forceinline__ uint64_t fp8_used_bytes(uint32_t nv) {
   return (uint64_t)nv * (D + (CODEC == KV_CODEC_FP8_DYNAMIC ? 4 : 0));
 }
 
-__device__ __forceinline__ uint8_t status_of_flags(uint32_t f) {
-  return (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
-}
-
-// The second kernel parameter selects the variant.  NoSeal: the plain kernel,
-// one CTA of kThreads per segment.  CrcParams: one warp per segment, in
-// 1024-thread CTAs (one per SM) holding the CRC lookup tables.
+// Variants (NoSeal: the plain kernel, one CTA of kThreads per segment;
+// CrcParams: one warp per segment):
 //  * Sealing encoder: every encode step writes 1 KB of codes.  At the start of
 //    every second step, with that step's loads in flight, the warp folds the
 //    2 KB CRC row its last two steps wrote (after __syncwarp, with plain loads:
@@ -96,16 +89,10 @@ __device__ __forceinline__ uint8_t status_of_flags(uint32_t f) {
 //  * Verifying decoder: checks header and CRC-32 exactly as kv_codec_verify
 //    does (loads with an L2 evict_last policy) and restores the segment only
 //    when they match, re-reading the slot from L2 (evict_first, like the page
-//    stores): a damaged slot is never scattered.
+//    stores) last vectors first: a damaged slot is never scattered.
 // (The vector loop is written out in the kernel bodies: moved into a helper
 // function it compiled to half again as many registers, which cost the plain
 // encoder two of its six CTAs per SM.)
-struct NoSeal {};
-template <typename Q>
-struct Variant {
-  static constexpr bool kSeal = !std::is_same<Q, NoSeal>::value;
-  static constexpr int kCtaThreads = kSeal ? crc::kCrcThreads : kThreads;
-};
 
 template <int DT, int D, uint32_t CODEC, typename Q>
 __global__ void __launch_bounds__(Variant<Q>::kCtaThreads)
@@ -281,7 +268,11 @@ __global__ void __launch_bounds__(Variant<Q>::kCtaThreads)
     const uint8_t* codes = s.slot;
     const uint8_t* meta = s.slot + (uint64_t)nv * D;
     uint16_t* page = const_cast<uint16_t*>(s.page);
-    for (uint32_t j0 = j_first; j0 < nv; j0 += STEP) {
+    // verifying: the restore walks the steps last to first, so that it starts
+    // on the rows the check read last (the likeliest still in L2)
+    const uint32_t n_steps = SEAL ? (nv + STEP - 1u) / STEP : 0u;
+    for (uint32_t kk = 0, j0 = SEAL ? (n_steps - 1u) * STEP : j_first; SEAL ? kk < n_steps : j0 < nv;
+         ++kk, j0 = SEAL ? (n_steps - 1u - kk) * STEP : j0 + STEP) {
       uint2 cw[U][NC];
       float sc[U];
 #pragma unroll
@@ -343,36 +334,6 @@ __global__ void __launch_bounds__(Variant<Q>::kCtaThreads)
       if (threadIdx.x == 0 && p.result) p.result[i] = KV_SEG_ENCODED;
     }
   }
-}
-
-// Plain kernels: kThreads per CTA, at most max_per_sm CTAs per SM.
-template <typename K>
-int launch_plain(K kernel, const Params& p, void* stream, int max_per_sm) {
-  unsigned grid = 0;
-  const int rc = grid_for_threads(reinterpret_cast<const void*>(kernel), p.n_segments, max_per_sm, kThreads, &grid);
-  if (rc != KV_OK || grid == 0) return rc;
-  NoSeal none;
-  void* args[] = {const_cast<Params*>(&p), &none};
-  const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(kThreads), args, 0,
-                                         (cudaStream_t)stream);
-  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
-}
-
-template <typename K>
-int launch_sealed(K kernel, const Params& p, const CrcParams& q, void* stream) {
-  const void* k = reinterpret_cast<const void*>(kernel);
-  // the tables need more than the default 48 KB of dynamic shared memory (set
-  // on every launch: the attribute belongs to the current device's context)
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)crc::kCrcSmem) != cudaSuccess)
-    return KV_ERR_CUDA;
-  unsigned grid = 0;
-  const int rc = grid_for_threads(k, (p.n_segments + crc::kCrcWarps - 1) / crc::kCrcWarps, 1,
-                                  crc::kCrcThreads, &grid, false);
-  if (rc != KV_OK || grid == 0) return rc;
-  void* args[] = {const_cast<Params*>(&p), const_cast<CrcParams*>(&q)};
-  const cudaError_t e = cudaLaunchKernel(k, dim3(grid), dim3(crc::kCrcThreads), args, crc::kCrcSmem,
-                                         (cudaStream_t)stream);
-  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
 }
 
 template <int DT, int D, uint32_t CODEC>

@@ -246,13 +246,16 @@ std::map<int, int> g_sms;
 std::map<std::pair<int, const void*>, int> g_occ;
 
 // The launches of one encode or decode call: one when both roles share a
-// codec, else one per coded role.  With `seal` (every coded role FP8), the FP8
-// launches also write (encode) or first check (decode) the segment headers.
+// codec, else one per coded role.  With `seal` (one_pass: every coded role FP8
+// or uniform-8), the launches also write (encode) or first check (decode) the
+// segment headers.
 int launch_all(kv_codec_s* h, int dir, void* stream, const kvc::CrcParams* seal = nullptr) {
   Params& p = h->p;
   const uint32_t kc = p.codec[0], vc = p.codec[1];
   auto run = [&](uint32_t codec) -> int {
-    if (seal) return kvc::launch_fp8_sealed(p, *seal, dir, codec, stream);
+    if (seal)
+      return is_fp8(codec) ? kvc::launch_fp8_sealed(p, *seal, dir, codec, stream)
+                           : kvc::launch_uniform_sealed(p, *seal, dir, codec, stream);
     if (is_fp8(codec)) return kvc::launch_fp8(p, dir, codec, stream);
     if (is_tq(codec)) return kvc::launch_turboquant(p, dir, codec, stream);
     if (codec == KV_CODEC_INT8_HEAD) return kvc::launch_int8(p, dir, codec, stream);
@@ -281,10 +284,11 @@ int launch_all(kv_codec_s* h, int dir, void* stream, const kvc::CrcParams* seal 
   return KV_OK;
 }
 
-// Every coded role takes an FP8 codec (the one-pass sealed / verified kernels).
-bool fp8_roles_only(const Params& p) {
+// Every coded role takes a codec with sealing / verifying kernels (FP8 and
+// uniform-8): the headers are written or checked in the codec's own pass.
+bool one_pass(const Params& p) {
   for (int r = 0; r < 2; ++r)
-    if (p.codec[r] != KV_CODEC_NONE && !is_fp8(p.codec[r])) return false;
+    if (p.codec[r] != KV_CODEC_NONE && !is_fp8(p.codec[r]) && p.codec[r] != KV_CODEC_UNIFORM8) return false;
   return true;
 }
 
@@ -675,7 +679,7 @@ int kv_codec_encode_sealed(kv_codec_t h, const void* const* layer_ptrs, uint32_t
   p.buf_bytes = out_bytes;
   kvc::CrcParams q;
   if ((rc = crc_call(h, q, descs, n_segments, out, out_bytes, status, headers, nullptr)) != KV_OK) return rc;
-  if (fp8_roles_only(p)) return launch_all(&call, kvc::kEncode, stream, &q);
+  if (one_pass(p)) return launch_all(&call, kvc::kEncode, stream, &q);
   // other codecs: encode, then seal the slots in a second pass
   if ((rc = launch_all(&call, kvc::kEncode, stream)) != KV_OK) return rc;
   return kvc::launch_crc(q, 1, stream);
@@ -704,7 +708,7 @@ int kv_codec_decode_verified(kv_codec_t h, void* const* layer_ptrs, uint32_t n_l
   p.buf_bytes = in_bytes;
   kvc::CrcParams q;
   if ((rc = crc_call(h, q, descs, n_segments, in, in_bytes, nullptr, headers, result)) != KV_OK) return rc;
-  if (fp8_roles_only(p)) return launch_all(&call, kvc::kDecode, stream, &q);
+  if (one_pass(p)) return launch_all(&call, kvc::kDecode, stream, &q);
   if ((rc = kvc::launch_crc(q, 0, stream)) != KV_OK) return rc;
   return launch_all(&call, kvc::kDecode, stream);
 }

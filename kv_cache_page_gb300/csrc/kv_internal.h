@@ -118,6 +118,8 @@ int launch_fp8(const Params& p, int dir, uint32_t codec, void* stream);
 // first verifies them (result in p.result); one pass over the slots.
 int launch_fp8_sealed(const Params& p, const CrcParams& q, int dir, uint32_t codec, void* stream);
 int launch_uniform(const Params& p, int dir, uint32_t codec, void* stream);
+// The same for KV_CODEC_UNIFORM8 (KV_ERR_INVALID_ARG for another codec).
+int launch_uniform_sealed(const Params& p, const CrcParams& q, int dir, uint32_t codec, void* stream);
 int launch_turboquant(const Params& p, int dir, uint32_t codec, void* stream);
 int launch_int8(const Params& p, int dir, uint32_t codec, void* stream);
 

@@ -7,7 +7,7 @@
 // clamp(rint((x - m) / s), 0, 2^b - 1) against the stored (rounded) m and s,
 // code 0 when s == 0; restore code * s + m.  Codes are a little-endian bit
 // stream (b = 2, 3, 4) or one byte each (b = 8); metadata is (m, s) as two FP16.
-#include "device_common.cuh"
+#include "crc_common.cuh"
 
 namespace kvc {
 namespace {
@@ -123,32 +123,61 @@ __device__ __forceinline__ void store_codes32(uint8_t* dst, const uint2 (&v)[4])
 
 // 8-bit codes: the chunk layout of the FP8 kernels (G lanes of a vector take
 // its 16-byte chunks round-robin), so each lane's 8-byte code stores and each
-// warp's loads stay coalesced.
-template <int DT, int D, int BITS, int NT>
-__global__ void __launch_bounds__(NT) uniform_encode_kernel(const __grid_constant__ Params p) {
+// warp's loads stay coalesced.  Q selects the variant (NoSeal / CrcParams, as
+// for the FP8 kernels).  The sealing encoder is the FP8 one's scheme: a step
+// of one warp writes 1 KB of codes, and at the start of every second step,
+// with that step's loads in flight, the warp folds the 2 KB CRC row its last
+// two steps wrote (re-read from L2) and prefetches the vectors two steps
+// ahead into L2; the rows left after the last step and the header follow.
+template <int DT, int D, int BITS, int NT, typename Q>
+__global__ void __launch_bounds__(Variant<Q, NT>::kCtaThreads)
+    uniform_encode_kernel(const __grid_constant__ Params p, const __grid_constant__ Q q) {
   using M = ChunkMap<D>;
-  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = NT / 32;
-  constexpr int STEP = W * VPW * U;
+  constexpr bool SEAL = Variant<Q, NT>::kSeal;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = Variant<Q, NT>::kCtaThreads / 32;
+  constexpr uint32_t STEP = SEAL ? VPW * U : W * VPW * U;
   constexpr uint32_t LEVELS = (1u << BITS) - 1u;
   constexpr int CB = D * BITS / 8;  // code bytes per vector
+  static_assert(!SEAL || (BITS == 8 && VPW * U * CB == kCrcRow / 2), "a sealing step writes half a CRC row");
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
+  const uint32_t j_first = SEAL ? 0u : warp * VPW * U;
   __shared__ uint32_t s_flag[2];
-  if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
-  __syncthreads();
+  crc::NibbleTables* t = nullptr;
+  uint32_t tb = 0;
+  uint32_t i = blockIdx.x, i_step = gridDim.x;  // no wrap: n_segments < 2^31
+  if constexpr (SEAL) {
+    tb = crc::load_tables(q, t);
+    SegCursor c;
+    warp_cursor_init(c, W);
+    i = c.base;
+    i_step = c.stride;
+  } else {
+    if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
+    __syncthreads();
+  }
   const uint32_t nv = p.nv;
   int it = 0;
-  for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
+  for (; i < p.n_segments; i += i_step) {
     const Seg s = plan_segment(p, i, kEncode);
     if (s.action != kProcess) {
-      if (s.action == kReport && threadIdx.x == 0) p.status[i] = s.status;
+      if constexpr (SEAL) {
+        if (s.action == kReport) {
+          if (lane == 0) p.status[i] = s.status;
+          crc::seal_segment<true>(q, *t, tb, i, s.status, lane);
+        }
+      } else {
+        if (s.action == kReport && threadIdx.x == 0) p.status[i] = s.status;
+      }
       continue;
     }
-    if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
+    if (!SEAL && threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
     uint8_t* codes = s.slot;
     uint8_t* meta = s.slot + (uint64_t)nv * CB;
     uint32_t flags = 0;
-    for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
+    uint32_t crc_s = 0, crc_m = 0;  // sealing: rows folded so far, and their register
+    const bool al32 = ((uintptr_t)s.slot & 31u) == 0;
+    for (uint32_t j0 = j_first, k = 0; j0 < nv; j0 += STEP, ++k) {
       uint4 w[U][NC];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -156,7 +185,16 @@ __global__ void __launch_bounds__(NT) uniform_encode_kernel(const __grid_constan
         const uint16_t* src = s.page + (j < nv ? vec_off(p, j) : 0);
 #pragma unroll
         for (int c = 0; c < NC; ++c)
-          w[u][c] = j < nv ? ld_stream16(src + 8 * (li + G * c)) : make_uint4(0, 0, 0, 0);
+          w[u][c] = j < nv ? ld_stream16<SEAL>(src + 8 * (li + G * c)) : make_uint4(0, 0, 0, 0);
+      }
+      if constexpr (SEAL) {
+        const uint32_t jn = j0 + 2u * STEP + lane;
+        if (lane < STEP && jn < nv) prefetch_l2(s.page + vec_off(p, jn), D * 2);
+        if (k >= 2u && (k & 1u) == 0u) {
+          __syncwarp();
+          crc_s = crc::fold_row<false>(*t, tb, s.slot, crc_m, al32, crc_s, lane);
+          ++crc_m;
+        }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -196,14 +234,19 @@ __global__ void __launch_bounds__(NT) uniform_encode_kernel(const __grid_constan
       }
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
-    if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
-    zero_padding(s.slot, (uint64_t)nv * (CB + 4), p.seg_bytes[s.role], threadIdx.x, blockDim.x);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const uint32_t f = s_flag[it & 1];
-      p.status[i] = (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+    if constexpr (SEAL) {
+      zero_padding(s.slot, (uint64_t)nv * (CB + 4), p.seg_bytes[s.role], lane, 32);
+      const uint32_t st = status_of_flags(flags);
+      __syncwarp();
+      if (lane == 0) p.status[i] = (uint8_t)st;
+      crc::seal_segment<false>(q, *t, tb, i, st, lane, crc_m, crc_s);
+    } else {
+      if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
+      zero_padding(s.slot, (uint64_t)nv * (CB + 4), p.seg_bytes[s.role], threadIdx.x, blockDim.x);
+      __syncthreads();
+      if (threadIdx.x == 0) p.status[i] = status_of_flags(s_flag[it & 1]);
+      ++it;
     }
-    ++it;
   }
 }
 
@@ -301,29 +344,66 @@ __device__ __forceinline__ float small_u2f(uint32_t c) {
 // ADJ (segments of kAdjacentChunkMinVectors or more, D >= 64, 2/4/8-bit codes): lane li owns the
 // adjacent chunks 2 li, 2 li + 1 -- one code load and, when every vector is
 // 32-byte aligned, one 32-byte store per vector (as the FP8 decoder).
-template <int DT, int D, int BITS, int NT, bool ADJ>
-__global__ void __launch_bounds__(NT) uniform_decode_kernel(const __grid_constant__ Params p) {
+//
+// Q selects the variant (NoSeal / CrcParams).  The verifying decoder (8-bit
+// codes) is the FP8 one's scheme: one warp per segment checks the header and
+// the CRC-32 as kv_codec_verify does (loads with an L2 evict_last policy) and
+// only then restores the segment, re-reading the slot from L2 last vectors
+// first (loads and page stores with evict_first).
+template <int DT, int D, int BITS, int NT, bool ADJ, typename Q>
+__global__ void __launch_bounds__(Variant<Q, NT>::kCtaThreads)
+    uniform_decode_kernel(const __grid_constant__ Params p, const __grid_constant__ Q q) {
   using M = ChunkMap<D>;
+  constexpr bool SEAL = Variant<Q, NT>::kSeal;
+  static_assert(!SEAL || BITS == 8, "verifying decoders for 8-bit codes");
   // 3-bit codes (two dependent word loads per chunk) keep twice as many
   // vectors in flight per step at D >= 64: uniform-3 decode 0.82 -> 0.84 of
   // HBM on a GB300, while 2/4/8 bits lose 1-11% that way.
-  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = (BITS == 3 && D >= 64 ? 2 : 1) * M::U, W = NT / 32;
-  constexpr int STEP = W * VPW * U;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = (BITS == 3 && D >= 64 ? 2 : 1) * M::U;
+  constexpr int W = Variant<Q, NT>::kCtaThreads / 32;
+  constexpr uint32_t STEP = SEAL ? VPW * U : W * VPW * U;
   constexpr int CB = D * BITS / 8;
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
+  const uint32_t j_first = SEAL ? 0u : warp * VPW * U;
   const uint32_t nv = p.nv;
   const bool vec32 = p.vec32 != 0;
-  for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
-    const Seg s = plan_segment(p, i, kDecode);
-    if (s.action != kProcess) {
-      if (s.action == kReport && threadIdx.x == 0 && p.result) p.result[i] = s.status;
-      continue;
+  crc::NibbleTables* t = nullptr;
+  uint32_t tb = 0;
+  uint32_t i = blockIdx.x, i_step = gridDim.x;  // no wrap: n_segments < 2^31
+  uint64_t keep = 0, once = 0;
+  if constexpr (SEAL) {
+    tb = crc::load_tables(q, t);
+    SegCursor c;
+    warp_cursor_init(c, W);
+    i = c.base;
+    i_step = c.stride;
+    keep = l2_evict_last();
+    once = l2_evict_first();
+  }
+  for (; i < p.n_segments; i += i_step) {
+    Seg s;
+    if constexpr (SEAL) {
+      if (!owns_segment(p, __ldg(&p.descs[i].role))) continue;  // another launch's: no CRC
+      s = plan_segment(p, i, kDecode, (int)crc::verify_segment<true>(q, *t, tb, i, lane, keep));
+      if (s.action != kProcess) {
+        if (lane == 0) p.result[i] = s.status;
+        continue;
+      }
+    } else {
+      s = plan_segment(p, i, kDecode);
+      if (s.action != kProcess) {
+        if (s.action == kReport && threadIdx.x == 0 && p.result) p.result[i] = s.status;
+        continue;
+      }
     }
     const uint8_t* codes = s.slot;
     const uint8_t* meta = s.slot + (uint64_t)nv * CB;
     uint16_t* page = const_cast<uint16_t*>(s.page);
-    for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
+    // verifying: the steps last to first (the rows the check read last first)
+    const uint32_t n_steps = SEAL ? (nv + STEP - 1u) / STEP : 0u;
+    for (uint32_t kk = 0, j0 = SEAL ? (n_steps - 1u) * STEP : j_first; SEAL ? kk < n_steps : j0 < nv;
+         ++kk, j0 = SEAL ? (n_steps - 1u - kk) * STEP : j0 + STEP) {
       uint2 cw[U][NC];
       uint32_t mw[U];
 #pragma unroll
@@ -335,7 +415,7 @@ __global__ void __launch_bounds__(NT) uniform_decode_kernel(const __grid_constan
           cw[u][0] = cw[u][NC - 1] = make_uint2(0, 0);
           if (in) {
             if (BITS == 8) {
-              const uint4 t = ld_nc16(vc + 16 * li);
+              const uint4 t = ld_nc16_h<SEAL>(vc + 16 * li, once);
               cw[u][0] = make_uint2(t.x, t.y);
               cw[u][NC - 1] = make_uint2(t.z, t.w);
             } else if (BITS == 4) {
@@ -354,14 +434,14 @@ __global__ void __launch_bounds__(NT) uniform_decode_kernel(const __grid_constan
             const uint32_t cidx = li + G * ch;
             cw[u][ch] = make_uint2(0, 0);
             if (in) {
-              if (BITS == 8) cw[u][ch] = ld_nc8(vc + 8 * cidx);
+              if (BITS == 8) cw[u][ch] = ld_nc8_h<SEAL>(vc + 8 * cidx, once);
               else if (BITS == 4) cw[u][ch].x = ld_nc4(vc + 4 * cidx);
               else if (BITS == 2) cw[u][ch].x = ld_nc2(vc + 2 * cidx);
               else cw[u][ch].x = load_3bit(vc, cidx);
             }
           }
         }
-        mw[u] = in ? ld_nc4(meta + (uint64_t)j * 4) : 0u;
+        mw[u] = in ? ld_nc4_h<SEAL>(meta + (uint64_t)j * 4, once) : 0u;
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -389,19 +469,23 @@ __global__ void __launch_bounds__(NT) uniform_decode_kernel(const __grid_constan
             r[k] = pack2<DT>(y.x, y.y);
           }
           if (ADJ && NC == 2) oc[ch] = make_uint4(r[0], r[1], r[2], r[3]);
-          else if (j < nv) st16(dst + 8 * (li + G * ch), make_uint4(r[0], r[1], r[2], r[3]));
+          else if (j < nv) st16_h<SEAL>(dst + 8 * (li + G * ch), make_uint4(r[0], r[1], r[2], r[3]), once);
         }
         if (ADJ && NC == 2 && j < nv) {
           if (vec32) {
-            st32(dst + 16 * li, oc[0], oc[NC - 1]);
+            st32_h<SEAL>(dst + 16 * li, oc[0], oc[NC - 1], once);
           } else {
-            st16(dst + 16 * li, oc[0]);
-            st16(dst + 16 * li + 8, oc[NC - 1]);
+            st16_h<SEAL>(dst + 16 * li, oc[0], once);
+            st16_h<SEAL>(dst + 16 * li + 8, oc[NC - 1], once);
           }
         }
       }
     }
-    if (threadIdx.x == 0 && p.result) p.result[i] = KV_SEG_ENCODED;
+    if constexpr (SEAL) {
+      if (lane == 0) p.result[i] = KV_SEG_ENCODED;
+    } else {
+      if (threadIdx.x == 0 && p.result) p.result[i] = KV_SEG_ENCODED;
+    }
   }
 }
 
@@ -414,8 +498,8 @@ int launch_encode(const Params& p, void* stream) {
   if constexpr (BITS == 8) {
     constexpr uint32_t step = 8u * ChunkMap<D>::VPW * ChunkMap<D>::U;
     if (p.nv <= step)
-      return launch_codec_kernel(uniform_encode_kernel<DT, D, 8, 128>, p, stream, 2 * kEncodeCtas, 128);
-    return launch_codec_kernel(uniform_encode_kernel<DT, D, 8, kThreads>, p, stream, kEncodeCtas);
+      return launch_plain(uniform_encode_kernel<DT, D, 8, 128, NoSeal>, p, stream, 2 * kEncodeCtas, 128);
+    return launch_plain(uniform_encode_kernel<DT, D, 8, kThreads, NoSeal>, p, stream, kEncodeCtas);
   } else {
     constexpr uint32_t step = 8u * (32 / (D / kUniE)) * 2;
     if (p.nv <= step)
@@ -429,8 +513,28 @@ int launch_encode(const Params& p, void* stream) {
 template <int DT, int D, int BITS>
 int launch_decode(const Params& p, void* stream) {
   if (BITS != 3 && p.nv >= kAdjacentChunkMinVectors)
-    return launch_codec_kernel(uniform_decode_kernel<DT, D, BITS, kThreads, BITS != 3>, p, stream, kDecodeCtas);
-  return launch_codec_kernel(uniform_decode_kernel<DT, D, BITS, kThreads, false>, p, stream, kDecodeCtas);
+    return launch_plain(uniform_decode_kernel<DT, D, BITS, kThreads, BITS != 3, NoSeal>, p, stream, kDecodeCtas);
+  return launch_plain(uniform_decode_kernel<DT, D, BITS, kThreads, false, NoSeal>, p, stream, kDecodeCtas);
+}
+
+// Uniform-8 with segment headers: the sealing encoder / verifying decoder.
+template <int DT, int D>
+int launch_sealed8(const Params& p, const CrcParams& q, int dir, void* stream) {
+  if (dir == kEncode) return launch_sealed(uniform_encode_kernel<DT, D, 8, kThreads, CrcParams>, p, q, stream);
+  if (p.nv >= kAdjacentChunkMinVectors)
+    return launch_sealed(uniform_decode_kernel<DT, D, 8, kThreads, true, CrcParams>, p, q, stream);
+  return launch_sealed(uniform_decode_kernel<DT, D, 8, kThreads, false, CrcParams>, p, q, stream);
+}
+
+template <int DT>
+int sealed_dim(const Params& p, const CrcParams& q, int dir, void* stream) {
+  switch (p.D) {
+    case 32: return launch_sealed8<DT, 32>(p, q, dir, stream);
+    case 64: return launch_sealed8<DT, 64>(p, q, dir, stream);
+    case 128: return launch_sealed8<DT, 128>(p, q, dir, stream);
+    case 256: return launch_sealed8<DT, 256>(p, q, dir, stream);
+  }
+  return KV_ERR_UNSUPPORTED_HEAD_DIM;
 }
 
 template <int DT, int D>
@@ -461,6 +565,11 @@ int dispatch_dim(const Params& p, int dir, uint32_t codec, void* stream) {
 int launch_uniform(const Params& p, int dir, uint32_t codec, void* stream) {
   return p.dtype == KV_DT_FP16 ? dispatch_dim<0>(p, dir, codec, stream)
                                : dispatch_dim<1>(p, dir, codec, stream);
+}
+
+int launch_uniform_sealed(const Params& p, const CrcParams& q, int dir, uint32_t codec, void* stream) {
+  if (codec != KV_CODEC_UNIFORM8) return KV_ERR_INVALID_ARG;
+  return p.dtype == KV_DT_FP16 ? sealed_dim<0>(p, q, dir, stream) : sealed_dim<1>(p, q, dir, stream);
 }
 
 }  // namespace kvc
