@@ -90,6 +90,8 @@ extern "C" {
 #define KV_ERR_TOO_MANY_LAYERS -8      /* num_layers = 0 or > KV_CODEC_MAX_LAYERS */
 #define KV_ERR_NOT_ACCESSIBLE -9       /* a buffer is pageable host memory (not pinned) */
 #define KV_ERR_UNSUPPORTED_DTYPE -10   /* codec not defined for the source dtype (INT8_HEAD: BF16) */
+#define KV_ERR_INTERNAL -11            /* bounds-checked debug library only: a kernel access fell outside
+                                          the call's buffers (skipped, not performed) */
 
 /* ---- enums ------------------------------------------------------------- */
 #define KV_DT_FP16 1u

@@ -14,7 +14,9 @@ from typing import Optional, Sequence
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libkvcodec.so")
+# KV_CODEC_DEBUG=1 loads the bounds-checked build (build(debug=True)) instead
+LIB_PATH = os.path.join(_PKG, "libkvcodec_debug.so" if os.environ.get("KV_CODEC_DEBUG") == "1"
+                        else "libkvcodec.so")
 ABI_VERSION = 1
 MAX_LAYERS = 512
 

@@ -8,9 +8,9 @@
 //
 // The standalone passes: two slots per warp at a time (one per half warp),
 // one 1024-thread CTA per SM holding the lookup tables (the CRC itself is in
-// crc_common.cuh).  The FP8 codec
-// kernels also seal while they encode and verify before they decode, without
-// this second pass over the slots (fp8.cu).
+// crc_common.cuh).  The FP8 and uniform-8
+// codec kernels also seal while they encode and verify before they decode,
+// without this second pass over the slots (fp8.cu, uniform.cu).
 #include "crc_common.cuh"
 
 namespace kvc {
@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(kCrcThreads, 1) crc_seal_kernel(const __grid_c
     uint32_t role = 0;
     uint64_t off = 0;
     const bool ok = have && slot_ok(p, p.descs + i, role, off);
-    const uint32_t st = have ? p.status[i] : 0u;
+    const uint32_t st = have ? ld_u8(p.status + i) : 0u;
     const bool coded = ok && st == KV_SEG_ENCODED && p.codec[role] != KV_CODEC_NONE;
     const uint32_t n = coded ? (uint32_t)p.seg_bytes[role] : 0u;
     const uint32_t crc = crc_rows_half<true>(*t, tb, p.buf + (coded ? off : 0), n, coded ? p.crc_k[role] : 0u, lane);
@@ -56,10 +56,10 @@ __global__ void __launch_bounds__(kCrcThreads, 1) crc_verify_kernel(const __grid
     uint64_t w0 = 0, orig = 0, stored = 0, w3 = 0;
     if (desc) {
       const uint64_t* hw = reinterpret_cast<const uint64_t*>(p.headers + i);
-      w0 = __ldg(reinterpret_cast<const unsigned long long*>(hw));
-      orig = __ldg(reinterpret_cast<const unsigned long long*>(hw + 1));
-      stored = __ldg(reinterpret_cast<const unsigned long long*>(hw + 2));
-      w3 = __ldg(reinterpret_cast<const unsigned long long*>(hw + 3));
+      w0 = ldg_u64(hw);
+      orig = ldg_u64(hw + 1);
+      stored = ldg_u64(hw + 2);
+      w3 = ldg_u64(hw + 3);
     }
     const uint32_t st = (uint32_t)(w3 >> 32);
     bool ok = desc && (uint32_t)w0 == p.version && (uint32_t)(w0 >> 32) == p.format[role] &&
@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kCrcThreads, 1) crc_verify_kernel(const __grid
     const uint32_t crc = crc_rows_half<true>(*t, tb, p.buf + (check ? off : 0), n, check ? p.crc_k[role] : 0u, lane);
     if (ok) ok = st == KV_SEG_ENCODED ? (check && crc == (uint32_t)w3) : stored == 0;
     if (have && (lane & 15u) == 0u)
-      p.result[i] = !desc ? (uint8_t)KV_SEG_BAD_DESC : ok ? (uint8_t)st : (uint8_t)KV_SEG_CORRUPT;
+      st_u8(p.result + i, !desc ? (uint8_t)KV_SEG_BAD_DESC : ok ? (uint8_t)st : (uint8_t)KV_SEG_CORRUPT);
   }
 }
 
@@ -87,9 +87,9 @@ int launch_crc(const CrcParams& p, int seal, void* stream) {
                                   false);
   if (rc != KV_OK || grid == 0) return rc;
   void* args[] = {const_cast<CrcParams*>(&p)};
-  const cudaError_t e =
-      cudaLaunchKernel(k, dim3(grid), dim3(kCrcThreads), args, kCrcSmem, (cudaStream_t)stream);
-  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  return dbg_launch(stream, [&] {
+    return cudaLaunchKernel(k, dim3(grid), dim3(kCrcThreads), args, kCrcSmem, (cudaStream_t)stream);
+  }, p);
 }
 
 }  // namespace kvc

@@ -258,9 +258,9 @@ __device__ __forceinline__ uint32_t load_tables(const CrcParams& p, NibbleTables
 // Descriptor checks that need no layer pointers.
 __device__ __forceinline__ bool slot_ok(const CrcParams& p, const kv_segment_desc* dp, uint32_t& role,
                                         uint64_t& off) {
-  const uint32_t layer = __ldg(&dp->layer), block = __ldg(&dp->block);
-  role = __ldg(&dp->role);
-  off = __ldg(reinterpret_cast<const unsigned long long*>(&dp->enc_offset));
+  const uint32_t layer = ldg_u32(&dp->layer), block = ldg_u32(&dp->block);
+  role = ldg_u32(&dp->role);
+  off = ldg_u64(&dp->enc_offset);
   if (layer >= p.L || role > 1u || (uint64_t)block >= p.num_blocks || (off & 15u)) return false;
   if (p.codec[role] == KV_CODEC_NONE) return true;
   return off <= p.buf_bytes && p.seg_bytes[role] <= p.buf_bytes - off;
@@ -269,10 +269,10 @@ __device__ __forceinline__ bool slot_ok(const CrcParams& p, const kv_segment_des
 __device__ __forceinline__ void store_header(kv_segment_header* h, uint32_t version, uint32_t format,
                                              uint64_t stored, uint32_t crc, uint32_t status, uint64_t orig) {
   uint64_t* w = reinterpret_cast<uint64_t*>(h);
-  w[0] = (uint64_t)version | ((uint64_t)format << 32);
-  w[1] = orig;
-  w[2] = stored;
-  w[3] = (uint64_t)crc | ((uint64_t)status << 32);
+  st_u64(w, (uint64_t)version | ((uint64_t)format << 32));
+  st_u64(w + 1, orig);
+  st_u64(w + 2, stored);
+  st_u64(w + 3, (uint64_t)crc | ((uint64_t)status << 32));
 }
 
 
@@ -311,10 +311,7 @@ __device__ __forceinline__ uint32_t verify_segment(const CrcParams& p, const Nib
   uint64_t off;
   if (!slot_ok(p, p.descs + i, role, off) || p.codec[role] == KV_CODEC_NONE) return KV_SEG_BAD_DESC;
   const uint64_t* w = reinterpret_cast<const uint64_t*>(p.headers + i);
-  const uint64_t w0 = __ldg(reinterpret_cast<const unsigned long long*>(w));
-  const uint64_t orig = __ldg(reinterpret_cast<const unsigned long long*>(w + 1));
-  const uint64_t stored = __ldg(reinterpret_cast<const unsigned long long*>(w + 2));
-  const uint64_t w3 = __ldg(reinterpret_cast<const unsigned long long*>(w + 3));
+  const uint64_t w0 = ldg_u64(w), orig = ldg_u64(w + 1), stored = ldg_u64(w + 2), w3 = ldg_u64(w + 3);
   const uint32_t st = (uint32_t)(w3 >> 32);
   bool ok = (uint32_t)w0 == p.version && (uint32_t)(w0 >> 32) == p.format[role] && orig == p.orig_bytes &&
             st >= KV_SEG_ENCODED && st <= KV_SEG_BAD_DESC;
@@ -348,8 +345,9 @@ __device__ __forceinline__ uint8_t status_of_flags(uint32_t f) {
 }
 
 // Plain launch of a codec kernel's NoSeal variant: `threads` per CTA, at most
-// max_per_sm CTAs per SM.
-inline int launch_plain(void (*kernel)(Params, NoSeal), const Params& p, void* stream, int max_per_sm,
+// max_per_sm CTAs per SM.  (The launch helpers are static: in the debug build
+// each translation unit arms its own bounds-check state.)
+static int launch_plain(void (*kernel)(Params, NoSeal), const Params& p, void* stream, int max_per_sm,
                         int threads = kThreads) {
   const void* k = reinterpret_cast<const void*>(kernel);
   unsigned grid = 0;
@@ -357,13 +355,13 @@ inline int launch_plain(void (*kernel)(Params, NoSeal), const Params& p, void* s
   if (rc != KV_OK || grid == 0) return rc;
   NoSeal none;
   void* args[] = {const_cast<Params*>(&p), &none};
-  const cudaError_t e = cudaLaunchKernel(k, dim3(grid), dim3(threads), args, 0, (cudaStream_t)stream);
-  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  return dbg_launch(stream, [&] { return cudaLaunchKernel(k, dim3(grid), dim3(threads), args, 0, (cudaStream_t)stream); },
+                    p);
 }
 
 // Launch of a codec kernel's CrcParams variant: one CTA of kCrcThreads per SM
 // at most, kCrcSmem bytes of dynamic shared memory for the tables.
-inline int launch_sealed(void (*kernel)(Params, CrcParams), const Params& p, const CrcParams& q, void* stream) {
+static int launch_sealed(void (*kernel)(Params, CrcParams), const Params& p, const CrcParams& q, void* stream) {
   const void* k = reinterpret_cast<const void*>(kernel);
   // the tables need more than the default 48 KB of dynamic shared memory (set
   // on every launch: the attribute belongs to the current device's context)
@@ -374,9 +372,9 @@ inline int launch_sealed(void (*kernel)(Params, CrcParams), const Params& p, con
                                   crc::kCrcThreads, &grid, false);
   if (rc != KV_OK || grid == 0) return rc;
   void* args[] = {const_cast<Params*>(&p), const_cast<CrcParams*>(&q)};
-  const cudaError_t e = cudaLaunchKernel(k, dim3(grid), dim3(crc::kCrcThreads), args, crc::kCrcSmem,
-                                         (cudaStream_t)stream);
-  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  return dbg_launch(stream, [&] {
+    return cudaLaunchKernel(k, dim3(grid), dim3(crc::kCrcThreads), args, crc::kCrcSmem, (cudaStream_t)stream);
+  }, p, q);
 }
 
 }  // namespace kvc

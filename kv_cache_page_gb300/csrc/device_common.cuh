@@ -18,8 +18,163 @@
 #include <stdint.h>
 
 #include "kv_internal.h"
+#ifdef KVC_BOUNDS_CHECK
+#include <cstdlib>
+#include <mutex>
+#endif
 
 namespace kvc {
+
+// ---------------------------------------------------------------- bounds check
+// The debug build (-DKVC_BOUNDS_CHECK: libkvcodec_debug.so) checks every
+// global load and store of the kernels.  Its bytes must lie inside one of the
+// buffers the call was given: a layer tensor (from its first element to the
+// last one the registered strides reach), the slot buffer, the descriptors,
+// statuses, results or headers.  The launcher writes these ranges into this
+// translation unit's g_dbg before each launch.  An access outside them is
+// skipped (a load gives zeros) and counted, with the first such address, and
+// the call returns KV_ERR_INTERNAL.  The release build compiles every check
+// away.
+#ifdef KVC_BOUNDS_CHECK
+constexpr int kDbgMaxRanges = 2 * kMaxLayers + 8;
+struct DbgRanges {
+  uint32_t n;
+  uint64_t lo[kDbgMaxRanges];
+  uint64_t hi[kDbgMaxRanges];  // exclusive
+};
+static __constant__ DbgRanges g_dbg;
+static __device__ unsigned int g_dbg_count;
+static __device__ unsigned long long g_dbg_first;
+
+static __device__ __noinline__ bool dbg_ok(const void* ptr, uint32_t bytes) {
+  const uint64_t a = reinterpret_cast<uint64_t>(ptr), e = a + bytes;
+  for (uint32_t k = 0; k < g_dbg.n; ++k)
+    if (a >= g_dbg.lo[k] && e <= g_dbg.hi[k]) return true;
+  if (atomicAdd(&g_dbg_count, 1u) == 0u) g_dbg_first = a;
+  return false;
+}
+// On an access outside the call's buffers: the statements after `bytes`
+// (typically a return) instead of the access.
+#define KVC_GUARD(ptr, bytes, ...)                  \
+  do {                                              \
+    if (!::kvc::dbg_ok((ptr), (bytes))) {           \
+      __VA_ARGS__;                                  \
+    }                                               \
+  } while (0)
+
+inline void dbg_add(DbgRanges& r, const void* base, uint64_t bytes) {
+  if (base && bytes && r.n < (uint32_t)kDbgMaxRanges) {
+    r.lo[r.n] = reinterpret_cast<uint64_t>(base);
+    r.hi[r.n] = r.lo[r.n] + bytes;
+    ++r.n;
+  }
+}
+// Slot-buffer bytes the check accepts.  KVC_DEBUG_SLOT_MARGIN (bytes) holds
+// back the end of the buffer, so that a test can see the check fire on
+// accesses that are in fact in bounds.
+inline uint64_t dbg_slot_bytes(uint64_t buf_bytes) {
+  const char* m = std::getenv("KVC_DEBUG_SLOT_MARGIN");
+  const uint64_t cut = m ? std::strtoull(m, nullptr, 10) : 0u;
+  return cut < buf_bytes ? buf_bytes - cut : 0u;
+}
+inline void dbg_ranges(DbgRanges& r, const Params& p) {
+  const uint64_t row = p.layout == KV_LAYOUT_VLLM_PACKED ? 2ull * p.D : p.D;
+  const uint64_t last = (uint64_t)p.sb * (p.num_blocks - 1u) + (uint64_t)p.st * (p.T - 1u) +
+                        (uint64_t)p.sh * (p.H - 1u);
+  const uint32_t nptr = p.layout == KV_LAYOUT_SEPARATE ? 2u * p.L : p.L;
+  for (uint32_t k = 0; k < nptr; ++k) dbg_add(r, p.layer_ptr[k], 2u * (last + row));
+  dbg_add(r, p.buf, dbg_slot_bytes(p.buf_bytes));
+  dbg_add(r, p.descs, (uint64_t)p.n_segments * sizeof(kv_segment_desc));
+  dbg_add(r, p.status, p.n_segments);
+  dbg_add(r, p.result, p.n_segments);
+}
+inline void dbg_ranges(DbgRanges& r, const CrcParams& q) {
+  dbg_add(r, q.buf, dbg_slot_bytes(q.buf_bytes));
+  dbg_add(r, q.descs, (uint64_t)q.n_segments * sizeof(kv_segment_desc));
+  dbg_add(r, q.status, q.n_segments);
+  dbg_add(r, q.result, q.n_segments);
+  dbg_add(r, q.headers, (uint64_t)q.n_segments * sizeof(kv_segment_header));
+}
+// One checked launch at a time per translation unit (the ranges and the
+// counter are the unit's own); the launch is waited for.
+static std::mutex& dbg_mutex() {
+  static std::mutex m;
+  return m;
+}
+static int dbg_begin(const DbgRanges& r, void* stream) {
+  const unsigned int zero = 0;
+  if (cudaMemcpyToSymbolAsync(g_dbg, &r, sizeof r, 0, cudaMemcpyHostToDevice, (cudaStream_t)stream) !=
+          cudaSuccess ||
+      cudaMemcpyToSymbolAsync(g_dbg_count, &zero, sizeof zero, 0, cudaMemcpyHostToDevice,
+                              (cudaStream_t)stream) != cudaSuccess)
+    return KV_ERR_CUDA;
+  return KV_OK;
+}
+static int dbg_end(void* stream) {
+  unsigned int n = 0;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess ||
+      cudaMemcpyFromSymbol(&n, g_dbg_count, sizeof n) != cudaSuccess)
+    return KV_ERR_CUDA;
+  return n ? KV_ERR_INTERNAL : KV_OK;
+}
+// Launch `launch` (a callable returning a cudaError_t) with the check armed
+// for the ranges of the given parameter blocks.
+template <typename F, typename... Ps>
+static int dbg_launch(void* stream, F launch, const Ps&... ps) {
+  DbgRanges r;
+  r.n = 0;
+  (dbg_ranges(r, ps), ...);
+  std::lock_guard<std::mutex> g(dbg_mutex());
+  if (dbg_begin(r, stream) != KV_OK) return KV_ERR_CUDA;
+  if (launch() != cudaSuccess) return KV_ERR_CUDA;
+  return dbg_end(stream);
+}
+#else
+#define KVC_GUARD(ptr, bytes, ...) \
+  do {                             \
+  } while (0)
+// Release: launch `launch` and map its status.
+template <typename F, typename... Ps>
+inline int dbg_launch(void*, F launch, const Ps&...) {
+  return launch() == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+}
+#endif
+
+// Scalar global loads and stores of the kernels (every one bounds-checked in
+// the debug build).
+__device__ __forceinline__ uint32_t ldg_u32(const uint32_t* ptr) {
+  KVC_GUARD(ptr, 4, return 0u);
+  return __ldg(ptr);
+}
+__device__ __forceinline__ uint64_t ldg_u64(const void* ptr) {
+  KVC_GUARD(ptr, 8, return 0u);
+  return __ldg(reinterpret_cast<const unsigned long long*>(ptr));
+}
+__device__ __forceinline__ uint8_t ldg_u8(const uint8_t* ptr) {
+  KVC_GUARD(ptr, 1, return 0u);
+  return __ldg(ptr);
+}
+// coherent byte load (an array this launch also writes)
+__device__ __forceinline__ uint8_t ld_volatile_u8(const uint8_t* ptr) {
+  KVC_GUARD(ptr, 1, return 0u);
+  return *(const volatile uint8_t*)ptr;
+}
+__device__ __forceinline__ uint8_t ld_u8(const uint8_t* ptr) {
+  KVC_GUARD(ptr, 1, return 0u);
+  return *ptr;
+}
+__device__ __forceinline__ void st_u8(uint8_t* ptr, uint8_t v) {
+  KVC_GUARD(ptr, 1, return);
+  *ptr = v;
+}
+__device__ __forceinline__ void st_u16(void* ptr, uint16_t v) {
+  KVC_GUARD(ptr, 2, return);
+  *reinterpret_cast<uint16_t*>(ptr) = v;
+}
+__device__ __forceinline__ void st_u64(void* ptr, uint64_t v) {
+  KVC_GUARD(ptr, 8, return);
+  *reinterpret_cast<uint64_t*>(ptr) = v;
+}
 
 // ---------------------------------------------------------------- planning
 enum Action { kProcess = 0, kReport = 1, kSkip = 2 };
@@ -50,8 +205,8 @@ __device__ __forceinline__ Seg plan_segment(const Params& p, uint32_t i, int dir
   Seg s;
   const kv_segment_desc* dp = p.descs + i;
   // all fields in one round trip
-  const uint32_t layer = __ldg(&dp->layer), block = __ldg(&dp->block), role = __ldg(&dp->role);
-  const uint64_t off = __ldg(reinterpret_cast<const unsigned long long*>(&dp->enc_offset));
+  const uint32_t layer = ldg_u32(&dp->layer), block = ldg_u32(&dp->block), role = ldg_u32(&dp->role);
+  const uint64_t off = ldg_u64(&dp->enc_offset);
   s.role = role;
   s.layer = layer;
   s.page = nullptr;
@@ -89,8 +244,8 @@ __device__ __forceinline__ Seg plan_segment(const Params& p, uint32_t i, int dir
     }
   } else {
     const uint8_t st = given >= 0          ? (uint8_t)given
-                       : p.status_is_result ? *(const volatile uint8_t*)(p.status + i)
-                                            : __ldg(p.status + i);
+                       : p.status_is_result ? ld_volatile_u8(p.status + i)
+                                            : ldg_u8(p.status + i);
     if (st != (uint8_t)KV_SEG_ENCODED) {
       s.status = st;
       return s;
@@ -148,8 +303,8 @@ __device__ __forceinline__ uint32_t cursor_next(const Params& p, SegCursor& c, S
       const Seg m = plan_segment(p, i, DIR);
       go = m.action == kProcess;
       if (m.action == kReport && (WARP || threadIdx.x < 32u)) {
-        if (DIR == kEncode) p.status[i] = m.status;
-        else if (p.result) p.result[i] = m.status;
+        if (DIR == kEncode) st_u8(p.status + i, m.status);
+        else if (p.result) st_u8(p.result + i, m.status);
       }
     }
     c.mask = __ballot_sync(0xffffffffu, go);
@@ -176,6 +331,7 @@ __device__ __forceinline__ int64_t vec_off(const Params& p, uint32_t j) {
 // reads a kernel overlaps with the load's latency)
 template <bool V = false>
 __device__ __forceinline__ uint4 ld_stream16(const void* ptr) {
+  KVC_GUARD(ptr, 16, return make_uint4(0, 0, 0, 0));
   uint4 v;
   if (V)
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -190,6 +346,7 @@ __device__ __forceinline__ uint4 ld_stream16(const void* ptr) {
 // read-only 16-byte load that allocates in L1 (for lanes reading 64-byte
 // blocks, whose second half-sector is then served from L1)
 __device__ __forceinline__ uint4 ld_nc16(const void* ptr) {
+  KVC_GUARD(ptr, 16, return make_uint4(0, 0, 0, 0));
   uint4 v;
   asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
@@ -198,6 +355,7 @@ __device__ __forceinline__ uint4 ld_nc16(const void* ptr) {
 }
 // read-only 32-byte load (sm_100+); ptr must be 32-byte aligned
 __device__ __forceinline__ void ld_nc32(const void* ptr, uint4& a, uint4& b) {
+  KVC_GUARD(ptr, 32, a = b = make_uint4(0, 0, 0, 0); return);
   asm("ld.global.nc.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
       : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
       : "l"(ptr));
@@ -205,12 +363,14 @@ __device__ __forceinline__ void ld_nc32(const void* ptr, uint4& a, uint4& b) {
 // coherent 32- and 16-byte loads, for data written earlier in the same launch
 // (ordered after the writers' barrier by the memory clobber)
 __device__ __forceinline__ void ld_plain32(const void* ptr, uint4& a, uint4& b) {
+  KVC_GUARD(ptr, 32, a = b = make_uint4(0, 0, 0, 0); return);
   asm volatile("ld.global.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
                : "l"(ptr)
                : "memory");
 }
 __device__ __forceinline__ uint4 ld_plain16(const void* ptr) {
+  KVC_GUARD(ptr, 16, return make_uint4(0, 0, 0, 0));
   uint4 v;
   asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
@@ -219,26 +379,23 @@ __device__ __forceinline__ uint4 ld_plain16(const void* ptr) {
   return v;
 }
 __device__ __forceinline__ uint2 ld_nc8(const void* ptr) {
+  KVC_GUARD(ptr, 8, return make_uint2(0, 0));
   uint2 v;
   asm("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(ptr));
   return v;
 }
 __device__ __forceinline__ uint32_t ld_nc4(const void* ptr) {
+  KVC_GUARD(ptr, 4, return 0u);
   uint32_t v;
   asm("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(ptr));
   return v;
 }
 __device__ __forceinline__ uint16_t ld_nc2(const void* ptr) {
+  KVC_GUARD(ptr, 2, return (uint16_t)0);
   uint16_t v;
   asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(ptr));
   return v;
 }
-// asynchronous 16-byte global -> shared copy (bypasses L1), its commit and wait
-__device__ __forceinline__ void cp_async16(uint32_t smem, const void* gptr) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(gptr) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ uint4 lds16(uint32_t smem) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -246,15 +403,25 @@ __device__ __forceinline__ uint4 lds16(uint32_t smem) {
                : "r"(smem));
   return v;
 }
-__device__ __forceinline__ void st16(void* ptr, uint4 v) { *reinterpret_cast<uint4*>(ptr) = v; }
+__device__ __forceinline__ void st16(void* ptr, uint4 v) {
+  KVC_GUARD(ptr, 16, return);
+  *reinterpret_cast<uint4*>(ptr) = v;
+}
 // 32-byte store (sm_100+); ptr must be 32-byte aligned
 __device__ __forceinline__ void st32(void* ptr, const uint4& a, const uint4& b) {
+  KVC_GUARD(ptr, 32, return);
   asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(a.x), "r"(a.y),
                "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
                : "memory");
 }
-__device__ __forceinline__ void st8(void* ptr, uint2 v) { *reinterpret_cast<uint2*>(ptr) = v; }
-__device__ __forceinline__ void st4(void* ptr, uint32_t v) { *reinterpret_cast<uint32_t*>(ptr) = v; }
+__device__ __forceinline__ void st8(void* ptr, uint2 v) {
+  KVC_GUARD(ptr, 8, return);
+  *reinterpret_cast<uint2*>(ptr) = v;
+}
+__device__ __forceinline__ void st4(void* ptr, uint32_t v) {
+  KVC_GUARD(ptr, 4, return);
+  *reinterpret_cast<uint32_t*>(ptr) = v;
+}
 
 // L2 eviction priorities.  A policy from createpolicy rides on a load or a
 // store as a cache hint: evict_last for bytes that are read again soon (a slot
@@ -273,6 +440,7 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
 template <bool H>
 __device__ __forceinline__ void ld_nc32_h(const void* ptr, uint4& a, uint4& b, uint64_t pol) {
   if (!H) return ld_nc32(ptr, a, b);
+  KVC_GUARD(ptr, 32, a = b = make_uint4(0, 0, 0, 0); return);
   asm("ld.global.nc.L2::cache_hint.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], %9;"
       : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
       : "l"(ptr), "l"(pol));
@@ -280,6 +448,7 @@ __device__ __forceinline__ void ld_nc32_h(const void* ptr, uint4& a, uint4& b, u
 template <bool H>
 __device__ __forceinline__ uint4 ld_nc16_h(const void* ptr, uint64_t pol) {
   if (!H) return ld_nc16(ptr);
+  KVC_GUARD(ptr, 16, return make_uint4(0, 0, 0, 0));
   uint4 v;
   asm("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
@@ -289,6 +458,7 @@ __device__ __forceinline__ uint4 ld_nc16_h(const void* ptr, uint64_t pol) {
 template <bool H>
 __device__ __forceinline__ uint2 ld_nc8_h(const void* ptr, uint64_t pol) {
   if (!H) return ld_nc8(ptr);
+  KVC_GUARD(ptr, 8, return make_uint2(0, 0));
   uint2 v;
   asm("ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;" : "=r"(v.x), "=r"(v.y) : "l"(ptr), "l"(pol));
   return v;
@@ -296,6 +466,7 @@ __device__ __forceinline__ uint2 ld_nc8_h(const void* ptr, uint64_t pol) {
 template <bool H>
 __device__ __forceinline__ uint32_t ld_nc4_h(const void* ptr, uint64_t pol) {
   if (!H) return ld_nc4(ptr);
+  KVC_GUARD(ptr, 4, return 0u);
   uint32_t v;
   asm("ld.global.nc.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol));
   return v;
@@ -303,6 +474,7 @@ __device__ __forceinline__ uint32_t ld_nc4_h(const void* ptr, uint64_t pol) {
 template <bool H>
 __device__ __forceinline__ void st16_h(void* ptr, uint4 v, uint64_t pol) {
   if (!H) return st16(ptr, v);
+  KVC_GUARD(ptr, 16, return);
   asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w), "l"(pol)
                : "memory");
@@ -310,6 +482,7 @@ __device__ __forceinline__ void st16_h(void* ptr, uint4 v, uint64_t pol) {
 template <bool H>
 __device__ __forceinline__ void st32_h(void* ptr, const uint4& a, const uint4& b, uint64_t pol) {
   if (!H) return st32(ptr, a, b);
+  KVC_GUARD(ptr, 32, return);
   asm volatile("st.global.L2::cache_hint.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(ptr),
                "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w), "l"(pol)
                : "memory");
@@ -318,6 +491,7 @@ __device__ __forceinline__ void st32_h(void* ptr, const uint4& a, const uint4& b
 // Bring `bytes` (a multiple of 16) at `ptr` (16-byte aligned) into L2 without
 // waiting for them; a plain hint, its completion is never awaited.
 __device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+  KVC_GUARD(ptr, bytes, return);
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
@@ -325,7 +499,7 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
 // first + step, ... (the whole CTA: threadIdx.x, blockDim.x; one warp: lane, 32).
 __device__ __forceinline__ void zero_padding(uint8_t* slot, uint64_t used, uint64_t total, uint32_t first,
                                              uint32_t step) {
-  for (uint64_t k = used + first; k < total; k += step) slot[k] = 0;
+  for (uint64_t k = used + first; k < total; k += step) st_u8(slot + k, 0);
 }
 
 // ---------------------------------------------------------------- 16-bit formats
@@ -542,8 +716,10 @@ __device__ __forceinline__ uint32_t load_3bit(const uint8_t* src, uint32_t c) {
 // `threads` threads per CTA and at most `max_per_sm` resident CTAs per SM.
 // The caps come from sweeps on a GB300 (one CTA codes one segment): the
 // write-heavy decodes stream best with few CTAs per SM, the encodes with more.
+// (static: in the debug build each translation unit arms its own
+// bounds-check state)
 template <typename K>
-inline int launch_codec_kernel(K kernel, const Params& p, void* stream, int max_per_sm,
+static int launch_codec_kernel(K kernel, const Params& p, void* stream, int max_per_sm,
                                int threads = kThreads, bool warp_segments = false) {
   unsigned grid = 0;
   // one warp per segment: enough CTAs for every segment to have its warp
@@ -553,9 +729,10 @@ inline int launch_codec_kernel(K kernel, const Params& p, void* stream, int max_
                                   threads, &grid, !warp_segments);
   if (rc != KV_OK || grid == 0) return rc;
   void* args[] = {const_cast<Params*>(&p)};
-  const cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(kernel), dim3(grid),
-                                         dim3(threads), args, 0, (cudaStream_t)stream);
-  return e == cudaSuccess ? KV_OK : KV_ERR_CUDA;
+  return dbg_launch(stream, [&] {
+    return cudaLaunchKernel(reinterpret_cast<const void*>(kernel), dim3(grid), dim3(threads), args, 0,
+                            (cudaStream_t)stream);
+  }, p);
 }
 
 }  // namespace kvc

@@ -127,11 +127,11 @@ __global__ void __launch_bounds__(Variant<Q>::kCtaThreads)
     if (s.action != kProcess) {
       if constexpr (SEAL) {
         if (s.action == kReport) {
-          if (lane == 0) p.status[i] = s.status;
+          if (lane == 0) st_u8(p.status + i, s.status);
           crc::seal_segment<true>(q, *t, tb, i, s.status, lane);
         }
       } else {
-        if (s.action == kReport && threadIdx.x == 0) p.status[i] = s.status;
+        if (s.action == kReport && threadIdx.x == 0) st_u8(p.status + i, s.status);
       }
       continue;
     }
@@ -203,13 +203,13 @@ __global__ void __launch_bounds__(Variant<Q>::kCtaThreads)
       zero_padding(s.slot, fp8_used_bytes<CODEC, D>(nv), p.seg_bytes[s.role], lane, 32);
       const uint32_t st = status_of_flags(flags);
       __syncwarp();
-      if (lane == 0) p.status[i] = (uint8_t)st;
+      if (lane == 0) st_u8(p.status + i, (uint8_t)st);
       crc::seal_segment<false>(q, *t, tb, i, st, lane, crc_m, crc_s);
     } else {
       if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
       zero_padding(s.slot, fp8_used_bytes<CODEC, D>(nv), p.seg_bytes[s.role], threadIdx.x, blockDim.x);
       __syncthreads();
-      if (threadIdx.x == 0) p.status[i] = status_of_flags(s_flag[it & 1]);
+      if (threadIdx.x == 0) st_u8(p.status + i, status_of_flags(s_flag[it & 1]));
       ++it;
     }
   }
@@ -250,16 +250,16 @@ __global__ void __launch_bounds__(Variant<Q>::kCtaThreads)
   for (; i < p.n_segments; i += i_step) {
     Seg s;
     if constexpr (SEAL) {
-      if (!owns_segment(p, __ldg(&p.descs[i].role))) continue;  // another launch's: no CRC
+      if (!owns_segment(p, ldg_u32(&p.descs[i].role))) continue;  // another launch's: no CRC
       s = plan_segment(p, i, kDecode, (int)crc::verify_segment<true>(q, *t, tb, i, lane, keep));
       if (s.action != kProcess) {
-        if (lane == 0) p.result[i] = s.status;
+        if (lane == 0) st_u8(p.result + i, s.status);
         continue;
       }
     } else {
       s = plan_segment(p, i, kDecode);
       if (s.action != kProcess) {
-        if (s.action == kReport && threadIdx.x == 0 && p.result) p.result[i] = s.status;
+        if (s.action == kReport && threadIdx.x == 0 && p.result) st_u8(p.result + i, s.status);
         continue;
       }
     }
@@ -329,9 +329,9 @@ __global__ void __launch_bounds__(Variant<Q>::kCtaThreads)
       }
     }
     if constexpr (SEAL) {
-      if (lane == 0) p.result[i] = KV_SEG_ENCODED;
+      if (lane == 0) st_u8(p.result + i, KV_SEG_ENCODED);
     } else {
-      if (threadIdx.x == 0 && p.result) p.result[i] = KV_SEG_ENCODED;
+      if (threadIdx.x == 0 && p.result) st_u8(p.result + i, KV_SEG_ENCODED);
     }
   }
 }

@@ -77,7 +77,7 @@ __device__ __forceinline__ void zero_record_padding(const Params& p, uint8_t* sl
   const uint32_t total = p.T * pad16;
   for (uint32_t k = threadIdx.x; k < total; k += blockDim.x) {
     const uint32_t t = k / pad16, o = k - t * pad16;
-    *reinterpret_cast<uint16_t*>(slot + (uint64_t)t * p.rec_bytes + p.rec_used + 2u * o) = 0;
+    st_u16(slot + (uint64_t)t * p.rec_bytes + p.rec_used + 2u * o, 0);
   }
 }
 
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kThreads) int8_encode_kernel(const __grid_cons
   for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
     const Seg s = plan_segment(p, i, kEncode);
     if (s.action != kProcess) {
-      if (s.action == kReport && threadIdx.x == 0) p.status[i] = s.status;
+      if (s.action == kReport && threadIdx.x == 0) st_u8(p.status + i, s.status);
       continue;
     }
     if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads) int8_encode_kernel(const __grid_cons
           if (in) st8(s.slot + code_off + 8 * (li + G * c), out);
         }
         if (in && li == 0)
-          *reinterpret_cast<uint16_t*>(s.slot + scale_off) = __bfloat16_as_ushort(s16);
+          st_u16(s.slot + scale_off, __bfloat16_as_ushort(s16));
       }
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kThreads) int8_encode_kernel(const __grid_cons
     __syncthreads();
     if (threadIdx.x == 0) {
       const uint32_t f = s_flag[it & 1];
-      p.status[i] = (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+      st_u8(p.status + i, (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED);
     }
     ++it;
   }
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreads) int8_decode_kernel(const __grid_cons
   for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
     const Seg s = plan_segment(p, i, kDecode);
     if (s.action != kProcess) {
-      if (s.action == kReport && threadIdx.x == 0 && p.result) p.result[i] = s.status;
+      if (s.action == kReport && threadIdx.x == 0 && p.result) st_u8(p.result + i, s.status);
       continue;
     }
     uint16_t* page = const_cast<uint16_t*>(s.page);
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kThreads) int8_decode_kernel(const __grid_cons
         }
       }
     }
-    if (threadIdx.x == 0 && p.result) p.result[i] = KV_SEG_ENCODED;
+    if (threadIdx.x == 0 && p.result) st_u8(p.result + i, KV_SEG_ENCODED);
   }
 }
 

@@ -427,6 +427,7 @@ const char* kv_codec_strerror(int code) {
     case KV_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
     case KV_ERR_NOT_ACCESSIBLE: return "buffer is pageable host memory (pin it or use device memory)";
     case KV_ERR_UNSUPPORTED_DTYPE: return "codec not defined for this source dtype (INT8_HEAD needs BF16)";
+    case KV_ERR_INTERNAL: return "a kernel access fell outside the call's buffers (bounds-checked build)";
     case KV_ERR_CUDA: return "CUDA runtime error";
     case KV_ERR_ABI: return "geometry ABI version or size mismatch";
     case KV_ERR_TOO_MANY_LAYERS: return "num_layers must be 1..KV_CODEC_MAX_LAYERS";

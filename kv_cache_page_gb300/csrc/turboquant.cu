@@ -596,13 +596,13 @@ __global__ void __launch_bounds__(kTq64Threads, E == 64 ? 3 : 5) tq_encode_lanes
         tq_store32<BITS>(vc + run_a * BITS / 8, acc_a);
         if constexpr (E == 64) tq_store32<BITS>(vc + run_b * BITS / 8, acc_b);
         if (li == 0)
-          *reinterpret_cast<uint16_t*>(meta + (uint64_t)j * 2) = __half_as_ushort(__float2half_rn(n));
+          st_u16(meta + (uint64_t)j * 2, __half_as_ushort(__float2half_rn(n)));
       }
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
-    for (uint64_t b = (uint64_t)nv * (CB + 2) + lane; b < p.seg_bytes[cur.role]; b += 32) cur.slot[b] = 0;
+    for (uint64_t b = (uint64_t)nv * (CB + 2) + lane; b < p.seg_bytes[cur.role]; b += 32) st_u8(cur.slot + b, 0);
     if (lane == 0)
-      p.status[ci] = (flags & 1u) ? KV_SEG_RAW_NONFINITE : (flags & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+      st_u8(p.status + ci, (flags & 1u) ? KV_SEG_RAW_NONFINITE : (flags & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED);
     if (ni != 0xffffffffu) cur = plan_segment(p, ni, kEncode);
     ci = ni;
   }
@@ -808,7 +808,7 @@ __global__ void __launch_bounds__(kTq64Threads, 4) tq_decode64_kernel(const __gr
         }
       }
     }
-    if (lane == 0 && p.result) p.result[ci] = KV_SEG_ENCODED;
+    if (lane == 0 && p.result) st_u8(p.result + ci, KV_SEG_ENCODED);
     cur = nxt;
     ci = ni;
   }
@@ -957,7 +957,7 @@ __global__ void __launch_bounds__(kThreads, 3) tq_decode_kernel(const __grid_con
         }
       }
     }
-    if (lane == 0 && p.result) p.result[ci] = KV_SEG_ENCODED;
+    if (lane == 0 && p.result) st_u8(p.result + ci, KV_SEG_ENCODED);
     cur = nxt;
     ci = ni;
   }

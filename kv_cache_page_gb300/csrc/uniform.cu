@@ -163,11 +163,11 @@ __global__ void __launch_bounds__(Variant<Q, NT>::kCtaThreads)
     if (s.action != kProcess) {
       if constexpr (SEAL) {
         if (s.action == kReport) {
-          if (lane == 0) p.status[i] = s.status;
+          if (lane == 0) st_u8(p.status + i, s.status);
           crc::seal_segment<true>(q, *t, tb, i, s.status, lane);
         }
       } else {
-        if (s.action == kReport && threadIdx.x == 0) p.status[i] = s.status;
+        if (s.action == kReport && threadIdx.x == 0) st_u8(p.status + i, s.status);
       }
       continue;
     }
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(Variant<Q, NT>::kCtaThreads)
           } else if (BITS == 4) {
             if (in) st4(vc + 4 * cidx, v.x);
           } else if (BITS == 2) {
-            if (in) *reinterpret_cast<uint16_t*>(vc + 2 * cidx) = (uint16_t)v.x;
+            if (in) st_u16(vc + 2 * cidx, (uint16_t)v.x);
           } else {
             store_3bit(vc, v.x, cidx, in);
           }
@@ -238,13 +238,13 @@ __global__ void __launch_bounds__(Variant<Q, NT>::kCtaThreads)
       zero_padding(s.slot, (uint64_t)nv * (CB + 4), p.seg_bytes[s.role], lane, 32);
       const uint32_t st = status_of_flags(flags);
       __syncwarp();
-      if (lane == 0) p.status[i] = (uint8_t)st;
+      if (lane == 0) st_u8(p.status + i, (uint8_t)st);
       crc::seal_segment<false>(q, *t, tb, i, st, lane, crc_m, crc_s);
     } else {
       if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
       zero_padding(s.slot, (uint64_t)nv * (CB + 4), p.seg_bytes[s.role], threadIdx.x, blockDim.x);
       __syncthreads();
-      if (threadIdx.x == 0) p.status[i] = status_of_flags(s_flag[it & 1]);
+      if (threadIdx.x == 0) st_u8(p.status + i, status_of_flags(s_flag[it & 1]));
       ++it;
     }
   }
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(NT) uniform_encode_lanes_kernel(const __grid_c
   for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
     const Seg s = plan_segment(p, i, kEncode);
     if (s.action != kProcess) {
-      if (s.action == kReport && threadIdx.x == 0) p.status[i] = s.status;
+      if (s.action == kReport && threadIdx.x == 0) st_u8(p.status + i, s.status);
       continue;
     }
     if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(NT) uniform_encode_lanes_kernel(const __grid_c
     __syncthreads();
     if (threadIdx.x == 0) {
       const uint32_t f = s_flag[it & 1];
-      p.status[i] = (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED;
+      st_u8(p.status + i, (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED);
     }
     ++it;
   }
@@ -384,16 +384,16 @@ __global__ void __launch_bounds__(Variant<Q, NT>::kCtaThreads)
   for (; i < p.n_segments; i += i_step) {
     Seg s;
     if constexpr (SEAL) {
-      if (!owns_segment(p, __ldg(&p.descs[i].role))) continue;  // another launch's: no CRC
+      if (!owns_segment(p, ldg_u32(&p.descs[i].role))) continue;  // another launch's: no CRC
       s = plan_segment(p, i, kDecode, (int)crc::verify_segment<true>(q, *t, tb, i, lane, keep));
       if (s.action != kProcess) {
-        if (lane == 0) p.result[i] = s.status;
+        if (lane == 0) st_u8(p.result + i, s.status);
         continue;
       }
     } else {
       s = plan_segment(p, i, kDecode);
       if (s.action != kProcess) {
-        if (s.action == kReport && threadIdx.x == 0 && p.result) p.result[i] = s.status;
+        if (s.action == kReport && threadIdx.x == 0 && p.result) st_u8(p.result + i, s.status);
         continue;
       }
     }
@@ -482,9 +482,9 @@ __global__ void __launch_bounds__(Variant<Q, NT>::kCtaThreads)
       }
     }
     if constexpr (SEAL) {
-      if (lane == 0) p.result[i] = KV_SEG_ENCODED;
+      if (lane == 0) st_u8(p.result + i, KV_SEG_ENCODED);
     } else {
-      if (threadIdx.x == 0 && p.result) p.result[i] = KV_SEG_ENCODED;
+      if (threadIdx.x == 0 && p.result) st_u8(p.result + i, KV_SEG_ENCODED);
     }
   }
 }

@@ -35,6 +35,16 @@ def test_exports_every_declared_symbol():
         assert hasattr(L, n), n
 
 
+def test_bounds_checked_build_exports_every_declared_symbol():
+    """The debug library (every kernel access checked against the call's
+    buffers) builds from the same sources and has the same entry points."""
+    L = C.CDLL(kbuild.build(debug=True))
+    for n in declared_functions():
+        assert hasattr(L, n), n
+    L.kv_codec_strerror.restype = C.c_char_p
+    assert b"outside the call's buffers" in L.kv_codec_strerror(-11)
+
+
 def test_abi_version_and_struct_size():
     assert K.lib().kv_codec_abi_version() == K.ABI_VERSION
     assert C.sizeof(K.Geometry) == 112
