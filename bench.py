@@ -547,7 +547,7 @@ def run_integrity(args, arms, stream, peak):
     checked and, against the HBM peak, of algorithmic bytes (slots read +
     32-byte headers written or read + descriptors).  one_pass: encode_sealed
     against plain encode and decode_verified against plain decode on the same
-    buffers (one pass over the slots when every coded role is FP8 or uniform-8), with the
+    buffers (one pass over the slots when every coded role is FP8, uniform-8 or INT8), with the
     time each adds.  Median CUDA-event times on the launching stream."""
     out = {}
     reps = max(3, min(args.steps, 20))
@@ -577,7 +577,8 @@ def run_integrity(args, arms, stream, peak):
         one = {k + "_ms": round(v, 4) for k, v in t.items()}
         one["seal_adds"] = round(t["encode_sealed"] / t["encode"] - 1.0, 4)
         one["verify_adds"] = round(t["decode_verified"] / t["decode"] - 1.0, 4)
-        one["one_pass"] = all(c.startswith("fp8") or c in ("uni8", "none") for c in (a.arm.k_codec, a.arm.v_codec))
+        one["one_pass"] = all(c.startswith("fp8") or c in ("uni8", "int8", "none")
+                              for c in (a.arm.k_codec, a.arm.v_codec))
         one["restored"] = int((res == K.SEG_ENCODED).sum())
         row["one_pass"] = one
         out[a.arm.name] = row

@@ -278,10 +278,10 @@ int kv_codec_verify(kv_codec_t codec, const kv_segment_desc* descs, uint32_t n_s
 /* Encode and seal in one call (section "Ownership, storage and GDS": a CRC32
  * per stored segment).  Slots, statuses and headers equal those of
  * kv_codec_encode followed by kv_codec_seal on the same arguments.  When every
- * coded role takes an FP8 codec or KV_CODEC_UNIFORM8 this is one pass: each
- * slot's CRC-32 is taken by the warp that encoded it, from the bytes it has
- * just written, so HBM carries the slots once; other codecs run encode, then
- * seal.  Arguments as
+ * coded role takes an FP8 codec, KV_CODEC_UNIFORM8 or KV_CODEC_INT8_HEAD this
+ * is one pass: each slot's CRC-32 is taken by the warp that encoded it, from
+ * the bytes it has just written, so HBM carries the slots once; other codecs
+ * run encode, then seal.  Arguments as
  * for kv_codec_encode, plus headers (n records, 8-byte aligned, device or
  * pinned host memory). */
 int kv_codec_encode_sealed(kv_codec_t codec, const void* const* layer_ptrs, uint32_t n_layer_ptrs,
@@ -294,8 +294,9 @@ int kv_codec_encode_sealed(kv_codec_t codec, const void* const* layer_ptrs, uint
  * equal those of kv_codec_verify into result followed by kv_codec_decode with
  * status = result and d_result = result: a segment whose header or CRC-32 does
  * not match is reported KV_SEG_CORRUPT and its page is not written.  When every
- * coded role takes an FP8 codec or KV_CODEC_UNIFORM8 this is one pass: the warp
- * that checks a slot then restores it, re-reading the slot from L2.  Arguments as for
+ * coded role takes an FP8 codec, KV_CODEC_UNIFORM8 or KV_CODEC_INT8_HEAD this is
+ * one pass: the warp that checks a slot then restores it, re-reading the slot
+ * from L2.  Arguments as for
  * kv_codec_decode, with the headers in place of the statuses and result (n
  * bytes) required. */
 int kv_codec_decode_verified(kv_codec_t codec, void* const* layer_ptrs, uint32_t n_layer_ptrs,

@@ -244,7 +244,7 @@ class Codec:
     def encode_sealed(self, layers, descs, n_segments: int, out, out_bytes: int, status, headers,
                       stream=None):
         """encode followed by seal, in one pass over the slots when every coded role is
-        FP8 or uniform-8 (the encoding warp checksums the slot it has just written)."""
+        FP8, uniform-8 or INT8 (the encoding warp checksums the slot it has just written)."""
         arr, n = self._layer_array(layers)
         _check(lib().kv_codec_encode_sealed(self._h, arr, n, _ptr(descs), n_segments, _ptr(out), out_bytes,
                                             _ptr(status), _ptr(headers), _stream_handle(stream)),
@@ -254,8 +254,8 @@ class Codec:
                         stream=None):
         """verify followed by decode of the verified segments: result[i] as verify gives
         it (SEG_ENCODED once restored); a segment failing its header or CRC-32 check is
-        SEG_CORRUPT and its page is left untouched.  One pass when every coded role is FP8
-        or uniform-8."""
+        SEG_CORRUPT and its page is left untouched.  One pass when every coded role is FP8,
+        uniform-8 or INT8."""
         arr, n = self._layer_array(layers)
         _check(lib().kv_codec_decode_verified(self._h, arr, n, _ptr(descs), n_segments, _ptr(enc),
                                               enc_bytes, _ptr(headers), _ptr(result), _stream_handle(stream)),

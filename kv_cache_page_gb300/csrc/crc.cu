@@ -8,9 +8,10 @@
 //
 // The standalone passes: two slots per warp at a time (one per half warp),
 // one 1024-thread CTA per SM holding the lookup tables (the CRC itself is in
-// crc_common.cuh).  The FP8 and uniform-8
-// codec kernels also seal while they encode and verify before they decode,
-// without this second pass over the slots (fp8.cu, uniform.cu).
+// crc_common.cuh).  The FP8, uniform-8 and
+// INT8 codec kernels also seal while they encode and verify before they
+// decode, without this second pass over the slots (fp8.cu, uniform.cu,
+// int8.cu).
 #include "crc_common.cuh"
 
 namespace kvc {

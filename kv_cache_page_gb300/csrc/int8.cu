@@ -15,7 +15,7 @@
 // the two's-complement code.  The clamp to [-127, 127] is implied for BF16
 // sources: over every BF16 maximum a (floored), a / scale <= 127.33 < 127.5,
 // and |x| <= a, so every rounded quotient is already in range.
-#include "device_common.cuh"
+#include "crc_common.cuh"
 
 namespace kvc {
 namespace {
@@ -81,27 +81,59 @@ __device__ __forceinline__ void zero_record_padding(const Params& p, uint8_t* sl
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads) int8_encode_kernel(const __grid_constant__ Params p) {
+// Q selects the variant (NoSeal: a CTA of kThreads per segment; CrcParams: one
+// warp per segment, as for the FP8 kernels).  The sealing encoder writes the
+// slot's records in token order: the step that completes a token's record
+// also zeroes its padding, and at the start of a step, with its loads in
+// flight, the warp folds the next 2 KB CRC row if the records completed by
+// the earlier steps cover it (re-read from L2).  The rows left after the last
+// step and the header follow.
+template <int D, typename Q>
+__global__ void __launch_bounds__(Variant<Q>::kCtaThreads)
+    int8_encode_kernel(const __grid_constant__ Params p, const __grid_constant__ Q q) {
   using M = ChunkMap<D>;
-  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = kThreads / 32;
-  constexpr int STEP = W * VPW * U;
+  constexpr bool SEAL = Variant<Q>::kSeal;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = Variant<Q>::kCtaThreads / 32;
+  constexpr uint32_t STEP = SEAL ? VPW * U : W * VPW * U;
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
+  const uint32_t j_first = SEAL ? 0u : warp * VPW * U;
   __shared__ uint32_t s_flag[2];
-  if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
-  __syncthreads();
+  crc::NibbleTables* t = nullptr;
+  uint32_t tb = 0;
+  uint32_t i = blockIdx.x, i_step = gridDim.x;  // no wrap: n_segments < 2^31
+  if constexpr (SEAL) {
+    tb = crc::load_tables(q, t);
+    SegCursor c;
+    warp_cursor_init(c, W);
+    i = c.base;
+    i_step = c.stride;
+  } else {
+    if (threadIdx.x < 2) s_flag[threadIdx.x] = 0;
+    __syncthreads();
+  }
   const uint32_t nv = p.nv;
   int it = 0;
-  for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
+  for (; i < p.n_segments; i += i_step) {
     const Seg s = plan_segment(p, i, kEncode);
     if (s.action != kProcess) {
-      if (s.action == kReport && threadIdx.x == 0) st_u8(p.status + i, s.status);
+      if constexpr (SEAL) {
+        if (s.action == kReport) {
+          if (lane == 0) st_u8(p.status + i, s.status);
+          crc::seal_segment<true>(q, *t, tb, i, s.status, lane);
+        }
+      } else {
+        if (s.action == kReport && threadIdx.x == 0) st_u8(p.status + i, s.status);
+      }
       continue;
     }
-    if (threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
+    if (!SEAL && threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
     uint32_t flags = 0;
-    for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
+    // sealing: records [0, rec_done) complete (codes, scales, zeroed padding),
+    // rows [0, crc_m) of the slot folded into crc_s
+    uint32_t rec_done = 0, crc_s = 0, crc_m = 0;
+    const bool al32 = ((uintptr_t)s.slot & 31u) == 0;
+    for (uint32_t j0 = j_first; j0 < nv; j0 += STEP) {
       uint4 w[U][NC];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -109,7 +141,17 @@ __global__ void __launch_bounds__(kThreads) int8_encode_kernel(const __grid_cons
         const uint16_t* src = s.page + (j < nv ? vec_off(p, j) : 0);
 #pragma unroll
         for (int c = 0; c < NC; ++c)
-          w[u][c] = j < nv ? ld_stream16(src + 8 * (li + G * c)) : make_uint4(0, 0, 0, 0);
+          w[u][c] = j < nv ? ld_stream16<SEAL>(src + 8 * (li + G * c)) : make_uint4(0, 0, 0, 0);
+      }
+      if constexpr (SEAL) {
+        // the vectors two steps ahead into L2 meanwhile, one per lane
+        const uint32_t jn = j0 + 2u * STEP + lane;
+        if (lane < STEP && jn < nv) prefetch_l2(s.page + vec_off(p, jn), D * 2);
+        if ((crc_m + 1u) * kCrcRow <= rec_done * p.rec_bytes) {
+          __syncwarp();
+          crc_s = crc::fold_row<false>(*t, tb, s.slot, crc_m, al32, crc_s, lane);
+          ++crc_m;
+        }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -133,38 +175,94 @@ __global__ void __launch_bounds__(kThreads) int8_encode_kernel(const __grid_cons
         if (in && li == 0)
           st_u16(s.slot + scale_off, __bfloat16_as_ushort(s16));
       }
+      if constexpr (SEAL) {
+        // zero the padding of the records this step completed, with the widest
+        // stores the used part's size allows (16, 4 or 2 bytes; the record
+        // size is a multiple of 128)
+        const uint32_t end = min(nv, j0 + STEP), n = p.rec_bytes - p.rec_used;
+        for (; (rec_done + 1u) * p.H <= end; ++rec_done) {
+          uint8_t* pad = s.slot + (uint64_t)rec_done * p.rec_bytes + p.rec_used;
+          if ((p.rec_used & 15u) == 0u) {
+            for (uint32_t o = 16u * lane; o < n; o += 512u) st16(pad + o, make_uint4(0, 0, 0, 0));
+          } else if ((p.rec_used & 3u) == 0u) {
+            for (uint32_t o = 4u * lane; o < n; o += 128u) st4(pad + o, 0u);
+          } else {
+            for (uint32_t o = 2u * lane; o < n; o += 64u) st_u16(pad + o, 0);
+          }
+        }
+      }
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
-    if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
-    zero_record_padding(p, s.slot);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const uint32_t f = s_flag[it & 1];
-      st_u8(p.status + i, (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED);
+    if constexpr (SEAL) {
+      const uint32_t st = status_of_flags(flags);
+      __syncwarp();
+      if (lane == 0) st_u8(p.status + i, (uint8_t)st);
+      crc::seal_segment<false>(q, *t, tb, i, st, lane, crc_m, crc_s);
+    } else {
+      if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
+      zero_record_padding(p, s.slot);
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const uint32_t f = s_flag[it & 1];
+        st_u8(p.status + i, (f & 1u) ? KV_SEG_RAW_NONFINITE : (f & 2u) ? KV_SEG_RAW_RANGE : KV_SEG_ENCODED);
+      }
+      ++it;
     }
-    ++it;
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads) int8_decode_kernel(const __grid_constant__ Params p) {
+// Verifying variant (CrcParams): one warp per segment checks the header and
+// the CRC-32 as kv_codec_verify does (loads with an L2 evict_last policy) and
+// only then restores the segment, re-reading the slot from L2 last vectors
+// first (code loads and page stores with evict_first).
+template <int D, typename Q>
+__global__ void __launch_bounds__(Variant<Q>::kCtaThreads)
+    int8_decode_kernel(const __grid_constant__ Params p, const __grid_constant__ Q q) {
   using M = ChunkMap<D>;
-  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = kThreads / 32;
-  constexpr int STEP = W * VPW * U;
+  constexpr bool SEAL = Variant<Q>::kSeal;
+  constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = Variant<Q>::kCtaThreads / 32;
+  constexpr uint32_t STEP = SEAL ? VPW * U : W * VPW * U;
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
+  const uint32_t j_first = SEAL ? 0u : warp * VPW * U;
   const uint32_t nv = p.nv;
   // float(c) for a two's-complement byte c: the word 0x4B0000(c ^ 0x80) is
   // 2^23 + c + 128 exactly
   const float2 bias2 = make_float2(-8388736.0f, -8388736.0f);
-  for (uint32_t i = blockIdx.x; i < p.n_segments; i += gridDim.x) {
-    const Seg s = plan_segment(p, i, kDecode);
-    if (s.action != kProcess) {
-      if (s.action == kReport && threadIdx.x == 0 && p.result) st_u8(p.result + i, s.status);
-      continue;
+  crc::NibbleTables* t = nullptr;
+  uint32_t tb = 0;
+  uint32_t i = blockIdx.x, i_step = gridDim.x;  // no wrap: n_segments < 2^31
+  uint64_t keep = 0, once = 0;
+  if constexpr (SEAL) {
+    tb = crc::load_tables(q, t);
+    SegCursor c;
+    warp_cursor_init(c, W);
+    i = c.base;
+    i_step = c.stride;
+    keep = l2_evict_last();
+    once = l2_evict_first();
+  }
+  for (; i < p.n_segments; i += i_step) {
+    Seg s;
+    if constexpr (SEAL) {
+      if (!owns_segment(p, ldg_u32(&p.descs[i].role))) continue;  // another launch's: no CRC
+      s = plan_segment(p, i, kDecode, (int)crc::verify_segment<true>(q, *t, tb, i, lane, keep));
+      if (s.action != kProcess) {
+        if (lane == 0) st_u8(p.result + i, s.status);
+        continue;
+      }
+    } else {
+      s = plan_segment(p, i, kDecode);
+      if (s.action != kProcess) {
+        if (s.action == kReport && threadIdx.x == 0 && p.result) st_u8(p.result + i, s.status);
+        continue;
+      }
     }
     uint16_t* page = const_cast<uint16_t*>(s.page);
-    for (uint32_t j0 = warp * VPW * U; j0 < nv; j0 += STEP) {
+    // verifying: the steps last to first (the rows the check read last first)
+    const uint32_t n_steps = SEAL ? (nv + STEP - 1u) / STEP : 0u;
+    for (uint32_t kk = 0, j0 = SEAL ? (n_steps - 1u) * STEP : j_first; SEAL ? kk < n_steps : j0 < nv;
+         ++kk, j0 = SEAL ? (n_steps - 1u - kk) * STEP : j0 + STEP) {
       uint2 cw[U][NC];
       float sc[U];
 #pragma unroll
@@ -175,7 +273,7 @@ __global__ void __launch_bounds__(kThreads) int8_decode_kernel(const __grid_cons
         if (in) record_offsets(p, j, code_off, scale_off);
 #pragma unroll
         for (int c = 0; c < NC; ++c)
-          cw[u][c] = in ? ld_nc8(s.slot + code_off + 8 * (li + G * c)) : make_uint2(0, 0);
+          cw[u][c] = in ? ld_nc8_h<SEAL>(s.slot + code_off + 8 * (li + G * c), once) : make_uint2(0, 0);
         sc[u] = in ? __uint_as_float((uint32_t)ld_nc2(s.slot + scale_off) << 16) : 0.0f;
       }
 #pragma unroll
@@ -195,30 +293,46 @@ __global__ void __launch_bounds__(kThreads) int8_decode_kernel(const __grid_cons
             const float2 y = mul2(add2(f, bias2), s2);
             r[k] = pack2<1>(y.x, y.y);
           }
-          if (j < nv) st16(dst + 8 * (li + G * c), make_uint4(r[0], r[1], r[2], r[3]));
+          if (j < nv) st16_h<SEAL>(dst + 8 * (li + G * c), make_uint4(r[0], r[1], r[2], r[3]), once);
         }
       }
     }
-    if (threadIdx.x == 0 && p.result) st_u8(p.result + i, KV_SEG_ENCODED);
+    if constexpr (SEAL) {
+      if (lane == 0) st_u8(p.result + i, KV_SEG_ENCODED);
+    } else {
+      if (threadIdx.x == 0 && p.result) st_u8(p.result + i, KV_SEG_ENCODED);
+    }
   }
+}
+
+template <int D>
+int launch_dim(const Params& p, const CrcParams* q, int dir, void* stream) {
+  if (q)
+    return dir == kEncode ? launch_sealed(int8_encode_kernel<D, CrcParams>, p, *q, stream)
+                          : launch_sealed(int8_decode_kernel<D, CrcParams>, p, *q, stream);
+  return dir == kEncode ? launch_plain(int8_encode_kernel<D, NoSeal>, p, stream, kEncodeCtas)
+                        : launch_plain(int8_decode_kernel<D, NoSeal>, p, stream, kDecodeCtas);
+}
+
+int launch_any(const Params& p, const CrcParams* q, int dir, uint32_t codec, void* stream) {
+  if (codec != KV_CODEC_INT8_HEAD || p.dtype != KV_DT_BF16) return KV_ERR_INVALID_ARG;
+  switch (p.D) {
+    case 32: return launch_dim<32>(p, q, dir, stream);
+    case 64: return launch_dim<64>(p, q, dir, stream);
+    case 128: return launch_dim<128>(p, q, dir, stream);
+    case 256: return launch_dim<256>(p, q, dir, stream);
+  }
+  return KV_ERR_UNSUPPORTED_HEAD_DIM;
 }
 
 }  // namespace
 
 int launch_int8(const Params& p, int dir, uint32_t codec, void* stream) {
-  if (codec != KV_CODEC_INT8_HEAD || p.dtype != KV_DT_BF16) return KV_ERR_INVALID_ARG;
-  const bool enc = dir == kEncode;
-  switch (p.D) {
-    case 32: return enc ? launch_codec_kernel(int8_encode_kernel<32>, p, stream, kEncodeCtas)
-                        : launch_codec_kernel(int8_decode_kernel<32>, p, stream, kDecodeCtas);
-    case 64: return enc ? launch_codec_kernel(int8_encode_kernel<64>, p, stream, kEncodeCtas)
-                        : launch_codec_kernel(int8_decode_kernel<64>, p, stream, kDecodeCtas);
-    case 128: return enc ? launch_codec_kernel(int8_encode_kernel<128>, p, stream, kEncodeCtas)
-                         : launch_codec_kernel(int8_decode_kernel<128>, p, stream, kDecodeCtas);
-    case 256: return enc ? launch_codec_kernel(int8_encode_kernel<256>, p, stream, kEncodeCtas)
-                         : launch_codec_kernel(int8_decode_kernel<256>, p, stream, kDecodeCtas);
-  }
-  return KV_ERR_UNSUPPORTED_HEAD_DIM;
+  return launch_any(p, nullptr, dir, codec, stream);
+}
+
+int launch_int8_sealed(const Params& p, const CrcParams& q, int dir, uint32_t codec, void* stream) {
+  return launch_any(p, &q, dir, codec, stream);
 }
 
 }  // namespace kvc

@@ -246,16 +246,17 @@ std::map<int, int> g_sms;
 std::map<std::pair<int, const void*>, int> g_occ;
 
 // The launches of one encode or decode call: one when both roles share a
-// codec, else one per coded role.  With `seal` (one_pass: every coded role FP8
-// or uniform-8), the launches also write (encode) or first check (decode) the
-// segment headers.
+// codec, else one per coded role.  With `seal` (one_pass: every coded role FP8,
+// uniform-8 or INT8), the launches also write (encode) or first check (decode)
+// the segment headers.
 int launch_all(kv_codec_s* h, int dir, void* stream, const kvc::CrcParams* seal = nullptr) {
   Params& p = h->p;
   const uint32_t kc = p.codec[0], vc = p.codec[1];
   auto run = [&](uint32_t codec) -> int {
     if (seal)
-      return is_fp8(codec) ? kvc::launch_fp8_sealed(p, *seal, dir, codec, stream)
-                           : kvc::launch_uniform_sealed(p, *seal, dir, codec, stream);
+      return is_fp8(codec)                    ? kvc::launch_fp8_sealed(p, *seal, dir, codec, stream)
+             : codec == KV_CODEC_INT8_HEAD ? kvc::launch_int8_sealed(p, *seal, dir, codec, stream)
+                                            : kvc::launch_uniform_sealed(p, *seal, dir, codec, stream);
     if (is_fp8(codec)) return kvc::launch_fp8(p, dir, codec, stream);
     if (is_tq(codec)) return kvc::launch_turboquant(p, dir, codec, stream);
     if (codec == KV_CODEC_INT8_HEAD) return kvc::launch_int8(p, dir, codec, stream);
@@ -284,11 +285,14 @@ int launch_all(kv_codec_s* h, int dir, void* stream, const kvc::CrcParams* seal 
   return KV_OK;
 }
 
-// Every coded role takes a codec with sealing / verifying kernels (FP8 and
-// uniform-8): the headers are written or checked in the codec's own pass.
+// Every coded role takes a codec with sealing / verifying kernels (FP8,
+// uniform-8 and HiQ INT8): the headers are written or checked in the codec's
+// own pass.
 bool one_pass(const Params& p) {
-  for (int r = 0; r < 2; ++r)
-    if (p.codec[r] != KV_CODEC_NONE && !is_fp8(p.codec[r]) && p.codec[r] != KV_CODEC_UNIFORM8) return false;
+  for (int r = 0; r < 2; ++r) {
+    const uint32_t c = p.codec[r];
+    if (c != KV_CODEC_NONE && !is_fp8(c) && c != KV_CODEC_UNIFORM8 && c != KV_CODEC_INT8_HEAD) return false;
+  }
   return true;
 }
 

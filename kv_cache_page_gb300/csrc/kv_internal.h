@@ -122,6 +122,8 @@ int launch_uniform(const Params& p, int dir, uint32_t codec, void* stream);
 int launch_uniform_sealed(const Params& p, const CrcParams& q, int dir, uint32_t codec, void* stream);
 int launch_turboquant(const Params& p, int dir, uint32_t codec, void* stream);
 int launch_int8(const Params& p, int dir, uint32_t codec, void* stream);
+// The same for KV_CODEC_INT8_HEAD.
+int launch_int8_sealed(const Params& p, const CrcParams& q, int dir, uint32_t codec, void* stream);
 
 // Grid size for a codec kernel over n segments: one CTA per segment up to
 // SM count x resident CTAs per SM, the latter the occupancy limit (cached per

@@ -101,8 +101,8 @@ def test_parity_cases_stay_inside_their_buffers():
     c = synth.make_case("tiny")
     run_seal_parity(c, c.arms[0])
     for arm in (synth.Arm("s8", "fp8_dynamic", "fp8_cast", (0, 1)), synth.Arm("su", "uni8", "uni8", (0, 1)),
-                synth.Arm("s2", "tq3", "fp8_cast", (0, 1))):
-        case = custom_case(D=128, H=4, T=16, L=3, B=4, dtype="fp16", layout="separate", seed=5)
+                synth.Arm("si", "int8", "int8", (0, 1)), synth.Arm("s2", "tq3", "fp8_cast", (0, 1))):
+        case = custom_case(D=128, H=4, T=16, L=3, B=4, dtype="bf16", layout="separate", seed=5)
         run_sealed_parity(case, arm, tamper=2)
         n += 3
     print("cases", n)
