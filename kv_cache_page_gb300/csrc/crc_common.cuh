@@ -330,11 +330,15 @@ __device__ __forceinline__ uint32_t verify_segment(const CrcParams& p, const Nib
 // plain kernel, a CTA of NT threads per segment.  CrcParams: one warp per
 // segment in kCrcThreads-thread CTAs (one per SM) that hold the CRC tables;
 // the encoder seals each slot as it writes it, the decoder verifies each slot
-// before it restores it.
+// before it restores it.  WarpSeg (kernels that offer it): one warp per
+// segment in CTAs of NT threads, without the CRC -- no CTA barrier per
+// segment, for segments too short to keep a CTA's warps busy.
 struct NoSeal {};
+struct WarpSeg {};
 template <typename Q, int NT = kThreads>
 struct Variant {
-  static constexpr bool kSeal = !std::is_same<Q, NoSeal>::value;
+  static constexpr bool kSeal = std::is_same<Q, CrcParams>::value;
+  static constexpr bool kWarp = !std::is_same<Q, NoSeal>::value;  // one warp per segment
   static constexpr int kCtaThreads = kSeal ? crc::kCrcThreads : NT;
 };
 
@@ -356,6 +360,20 @@ static int launch_plain(void (*kernel)(Params, NoSeal), const Params& p, void* s
   NoSeal none;
   void* args[] = {const_cast<Params*>(&p), &none};
   return dbg_launch(stream, [&] { return cudaLaunchKernel(k, dim3(grid), dim3(threads), args, 0, (cudaStream_t)stream); },
+                    p);
+}
+
+// Launch of a codec kernel's WarpSeg variant: kThreads per CTA, at most
+// max_per_sm CTAs per SM, a warp for every segment up to that.
+static int launch_warp(void (*kernel)(Params, WarpSeg), const Params& p, void* stream, int max_per_sm) {
+  const void* k = reinterpret_cast<const void*>(kernel);
+  constexpr uint32_t kWarps = kThreads / 32;
+  unsigned grid = 0;
+  const int rc = grid_for_threads(k, (p.n_segments + kWarps - 1u) / kWarps, max_per_sm, kThreads, &grid, false);
+  if (rc != KV_OK || grid == 0) return rc;
+  WarpSeg none;
+  void* args[] = {const_cast<Params*>(&p), &none};
+  return dbg_launch(stream, [&] { return cudaLaunchKernel(k, dim3(grid), dim3(kThreads), args, 0, (cudaStream_t)stream); },
                     p);
 }
 

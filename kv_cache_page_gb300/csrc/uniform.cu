@@ -123,8 +123,8 @@ __device__ __forceinline__ void store_codes32(uint8_t* dst, const uint2 (&v)[4])
 
 // 8-bit codes: the chunk layout of the FP8 kernels (G lanes of a vector take
 // its 16-byte chunks round-robin), so each lane's 8-byte code stores and each
-// warp's loads stay coalesced.  Q selects the variant (NoSeal / CrcParams, as
-// for the FP8 kernels).  The sealing encoder is the FP8 one's scheme: a step
+// warp's loads stay coalesced.  Q selects the variant (NoSeal / WarpSeg /
+// CrcParams).  The sealing encoder is the FP8 one's scheme: a step
 // of one warp writes 1 KB of codes, and at the start of every second step,
 // with that step's loads in flight, the warp folds the 2 KB CRC row its last
 // two steps wrote (re-read from L2) and prefetches the vectors two steps
@@ -133,21 +133,21 @@ template <int DT, int D, int BITS, int NT, typename Q>
 __global__ void __launch_bounds__(Variant<Q, NT>::kCtaThreads)
     uniform_encode_kernel(const __grid_constant__ Params p, const __grid_constant__ Q q) {
   using M = ChunkMap<D>;
-  constexpr bool SEAL = Variant<Q, NT>::kSeal;
+  constexpr bool SEAL = Variant<Q, NT>::kSeal, WARP = Variant<Q, NT>::kWarp;
   constexpr int G = M::G, NC = M::NC, VPW = M::VPW, U = M::U, W = Variant<Q, NT>::kCtaThreads / 32;
-  constexpr uint32_t STEP = SEAL ? VPW * U : W * VPW * U;
+  constexpr uint32_t STEP = WARP ? VPW * U : W * VPW * U;
   constexpr uint32_t LEVELS = (1u << BITS) - 1u;
   constexpr int CB = D * BITS / 8;  // code bytes per vector
   static_assert(!SEAL || (BITS == 8 && VPW * U * CB == kCrcRow / 2), "a sealing step writes half a CRC row");
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t grp = lane / G, li = lane % G;
-  const uint32_t j_first = SEAL ? 0u : warp * VPW * U;
+  const uint32_t j_first = WARP ? 0u : warp * VPW * U;
   __shared__ uint32_t s_flag[2];
   crc::NibbleTables* t = nullptr;
   uint32_t tb = 0;
   uint32_t i = blockIdx.x, i_step = gridDim.x;  // no wrap: n_segments < 2^31
-  if constexpr (SEAL) {
-    tb = crc::load_tables(q, t);
+  if constexpr (WARP) {
+    if constexpr (SEAL) tb = crc::load_tables(q, t);
     SegCursor c;
     warp_cursor_init(c, W);
     i = c.base;
@@ -161,17 +161,17 @@ __global__ void __launch_bounds__(Variant<Q, NT>::kCtaThreads)
   for (; i < p.n_segments; i += i_step) {
     const Seg s = plan_segment(p, i, kEncode);
     if (s.action != kProcess) {
-      if constexpr (SEAL) {
+      if constexpr (WARP) {
         if (s.action == kReport) {
           if (lane == 0) st_u8(p.status + i, s.status);
-          crc::seal_segment<true>(q, *t, tb, i, s.status, lane);
+          if constexpr (SEAL) crc::seal_segment<true>(q, *t, tb, i, s.status, lane);
         }
       } else {
         if (s.action == kReport && threadIdx.x == 0) st_u8(p.status + i, s.status);
       }
       continue;
     }
-    if (!SEAL && threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
+    if (!WARP && threadIdx.x == 0) s_flag[(it + 1) & 1] = 0;
     uint8_t* codes = s.slot;
     uint8_t* meta = s.slot + (uint64_t)nv * CB;
     uint32_t flags = 0;
@@ -234,12 +234,12 @@ __global__ void __launch_bounds__(Variant<Q, NT>::kCtaThreads)
       }
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
-    if constexpr (SEAL) {
+    if constexpr (WARP) {
       zero_padding(s.slot, (uint64_t)nv * (CB + 4), p.seg_bytes[s.role], lane, 32);
       const uint32_t st = status_of_flags(flags);
       __syncwarp();
       if (lane == 0) st_u8(p.status + i, (uint8_t)st);
-      crc::seal_segment<false>(q, *t, tb, i, st, lane, crc_m, crc_s);
+      if constexpr (SEAL) crc::seal_segment<false>(q, *t, tb, i, st, lane, crc_m, crc_s);
     } else {
       if (lane == 0 && flags) atomicOr(&s_flag[it & 1], flags);
       zero_padding(s.slot, (uint64_t)nv * (CB + 4), p.seg_bytes[s.role], threadIdx.x, blockDim.x);
@@ -489,16 +489,18 @@ __global__ void __launch_bounds__(Variant<Q, NT>::kCtaThreads)
   }
 }
 
-// Encoder segments that fit in one step of a 256-thread CTA run on 128-thread
-// CTAs, twice as many per SM, so that more segments are in flight (each CTA
-// codes one segment at a time; measured on the GB300 for 64- and 128-vector
-// segments: uniform-8 0.70 -> 0.81 of HBM).
+// Encoder segments that fit in one step of a 256-thread CTA are too short to
+// keep a CTA's warps busy between its per-segment barriers.  For the lanes
+// encoders they run on 128-thread CTAs, twice as many per SM (measured on the
+// GB300: uniform-3/2 packed 0.64/0.62 -> 0.74/0.72 of HBM); the 8-bit encoder
+// gives each such segment a warp of its own (WarpSeg, 4 CTAs of 256 threads
+// per SM at its 55 registers): uniform-8 on 64-vector segments 0.70 with
+// 256-thread CTAs, 0.87 with 128-thread CTAs, 0.92 with a warp per segment.
 template <int DT, int D, int BITS>
 int launch_encode(const Params& p, void* stream) {
   if constexpr (BITS == 8) {
     constexpr uint32_t step = 8u * ChunkMap<D>::VPW * ChunkMap<D>::U;
-    if (p.nv <= step)
-      return launch_plain(uniform_encode_kernel<DT, D, 8, 128, NoSeal>, p, stream, 2 * kEncodeCtas, 128);
+    if (p.nv <= step) return launch_warp(uniform_encode_kernel<DT, D, 8, kThreads, WarpSeg>, p, stream, 4);
     return launch_plain(uniform_encode_kernel<DT, D, 8, kThreads, NoSeal>, p, stream, kEncodeCtas);
   } else {
     constexpr uint32_t step = 8u * (32 / (D / kUniE)) * 2;
