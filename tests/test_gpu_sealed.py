@@ -180,3 +180,15 @@ def test_every_16bit_pattern(kv):
                       synth._separate_strides(16, 8, 128), [t, t.clone()], [], 0, torch.ones(1, 2))
     st, res = run_sealed_parity(case, synth.Arm("all", kv[0], kv[1], (0, 1)), tamper=4)
     assert np.any(st == O.S_ENCODED) and np.any(st == O.S_RAW_NONFINITE) and np.any(st == O.S_RAW_RANGE)
+
+
+@pytest.mark.parametrize("kv", [("int8", "int8"), ("uni8", "uni8")])
+@pytest.mark.parametrize("D", [32, 256])
+@pytest.mark.parametrize("H,T", [(1, 37), (2, 9), (5, 7)])
+def test_record_and_step_geometries(kv, D, H, T):
+    """Few heads per token: INT8 records complete faster than one CRC row per
+    step at H = 1 (the in-loop folding lags and the final rows catch up), and
+    record padding takes 2-, 4- and 16-byte stores; uniform-8 segments of one
+    warp step or less take the warp-per-segment encoder."""
+    case = custom_case(D=D, H=H, T=T, L=2, B=5, dtype="bf16", layout="separate", seed=D + H)
+    run_sealed_parity(case, synth.Arm("geo", kv[0], kv[1], (0, 1)), tamper=2, seed=H)
